@@ -1,0 +1,402 @@
+"""Pins of the oracle to facts outside itself (CPU only).
+
+Each test checks the oracle against something it does not compute itself: values
+printed on the pages (``tests/golden``), exact rational arithmetic, brute-force
+enumeration on tiny inputs, a library attention routine
+(``torch.nn.functional.scaled_dot_product_attention`` in fp64), ``numpy.mean``, and
+invariances the method must have (physical page order, prefix sharing).
+"""
+import itertools
+import json
+import math
+import os
+from fractions import Fraction
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from block_sparse_retrieval_gb300 import synth
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+# ---- helpers that restate the pages' definitions in another form ------------------------
+
+def widen(a: np.ndarray) -> np.ndarray:
+    """bf16 bit patterns (uint16) or float32 -> float64, exactly."""
+    if a.dtype == np.uint16:
+        return (a.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    return a.astype(np.float64)
+
+
+def logical_kv(arr, r: int, h: int, S: int):
+    """Keys and values of request r, kv head h, gathered in token order."""
+    bt, L = arr["block_table"], int(arr["seq_lens"][r])
+    K = np.stack([widen(arr["k_cache"][bt[r, t // S], h, t % S]) for t in range(L)]) \
+        if L else np.zeros((0, arr["k_cache"].shape[-1]))
+    V = np.stack([widen(arr["v_cache"][bt[r, t // S], h, t % S]) for t in range(L)]) \
+        if L else np.zeros((0, arr["v_cache"].shape[-1]))
+    return K, V
+
+
+def sdpa(qv: np.ndarray, K: np.ndarray, V: np.ndarray, tokens) -> np.ndarray:
+    """Library softmax attention of one query over the listed tokens."""
+    idx = sorted(tokens)
+    q_t = torch.from_numpy(qv).reshape(1, 1, 1, -1)
+    k_t = torch.from_numpy(K[idx]).reshape(1, 1, len(idx), -1)
+    v_t = torch.from_numpy(V[idx]).reshape(1, 1, len(idx), -1)
+    return torch.nn.functional.scaled_dot_product_attention(q_t, k_t, v_t).reshape(-1).numpy()
+
+
+def exact_k(n: int, p: float) -> int:
+    """Smallest integer >= p*n, with p read as the decimal it was written as."""
+    return min(n, math.ceil(Fraction(repr(p)) * n)) if n > 0 else 0
+
+
+def offload_blocks(L: int, S: int, INIT: int, LOCAL: int) -> list[int]:
+    """Blocks that hold at least one offload token, by enumerating the tokens."""
+    return sorted({t // S for t in range(max(INIT, 0), L - LOCAL)})
+
+
+def attended_set(L: int, S: int, INIT: int, LOCAL: int, selected) -> set[int]:
+    """initial_tokens, plus the offload tokens of the selected blocks, plus the window."""
+    W = L - LOCAL
+    tokens = set(range(0, min(INIT, L)))
+    for b in selected:
+        tokens |= {t for t in range(b * S, min(b * S + S, L)) if INIT <= t < W}
+    tokens |= set(range(max(W, 0), L))
+    return tokens
+
+
+def small_case(seed, **kw):
+    base = dict(seq_lens=[700], num_q_heads=4, num_kv_heads=2, head_dim=16, dtype=synth.F32,
+                block_size=32, init_tokens=64, local_tokens=96, topk_percent=0.3,
+                dense_boundary=0, seed=seed)
+    base.update(kw)
+    return synth.make_case(**base)
+
+
+# ---- closed forms printed on the pages ------------------------------------------------------
+
+def test_footprint_matches_survey_table():
+    g = json.load(open(os.path.join(GOLDEN, "kv_footprint.json")))["kvs_gpt3_table"]
+    for row in g["rows"]:
+        b = oracle.kv_cache_bytes(row["batch"], g["layers"], g["tokens"], g["hidden"],
+                                  g["bytes_per_value"])
+        gib = b / 2**30
+        printed = row["kv_gb"]
+        half_unit = 0.05 if printed != int(printed) else 0.5
+        assert abs(gib - printed) <= half_unit, (row, gib)
+        assert round(gib / g["weights_gb"], 2) == pytest.approx(row["kv_over_weight"], abs=0.011)
+
+
+def test_footprint_atb_example_and_its_printed_slip():
+    g = json.load(open(os.path.join(GOLDEN, "kv_footprint.json")))["atb_llama2_70b"]
+    b = oracle.kv_cache_bytes(1, g["layers"], g["seq_len"], g["hidden"], g["bytes_per_value"])
+    assert b == g["formula_bytes"] == 2 * 80 * 2048 * 8192 * 2
+    # The page's 10.7 GB is twice the product of its own factors.
+    assert abs(2 * b / 1e9 - g["printed_gb"]) < 0.05
+
+
+# ---- k and the candidate range --------------------------------------------------------------
+
+@pytest.mark.parametrize("n,p,k", [(448, 0.2, 90), (445, 0.2, 89), (26, 0.2, 6), (960, 0.1, 96),
+                                   (960, 0.2, 192), (960, 0.4, 384), (960, 1.0, 960),
+                                   (0, 0.2, 0), (100, 0.0, 0), (5, 0.01, 1), (1, 0.2, 1)])
+def test_topk_count_worked_values(n, p, k):
+    assert oracle.topk_count(n, p) == k
+
+
+def test_topk_count_equals_exact_rational_ceiling():
+    for p in (0.05, 0.1, 0.15, 0.2, 0.25, 0.3, 1 / 3, 0.4, 0.5, 0.7, 0.9, 1.0):
+        for n in range(0, 2049):
+            assert oracle.topk_count(n, p) == exact_k(n, p), (n, p)
+
+
+def test_candidate_count_by_token_enumeration():
+    rng = np.random.default_rng(0)
+    for _ in range(300):
+        S = int(rng.choice([1, 4, 16, 128]))
+        L = int(rng.integers(0, 3000))
+        INIT = int(rng.integers(0, 700))
+        LOCAL = int(rng.integers(0, 900))
+        assert oracle.num_candidates(L, S, INIT, LOCAL) == len(offload_blocks(L, S, INIT, LOCAL))
+    # The workloads' defaults: 65536 tokens -> 448 candidates; 131072 -> 960; tiny -> 26.
+    assert oracle.num_candidates(65536, 128, 1024, 7192) == 448
+    assert oracle.num_candidates(131072, 128, 1024, 7192) == 960
+    assert oracle.num_candidates(4096, 128, 256, 512) == 26
+
+
+# ---- representation vectors -------------------------------------------------------------------
+
+@pytest.mark.parametrize("dtype", [synth.BF16, synth.F32])
+def test_block_reps_equal_numpy_mean(dtype):
+    case = small_case(3, dtype=dtype, seq_lens=[300, 257, 64], head_dim=32)
+    arr = synth.to_oracle_arrays(case)
+    reps = oracle.block_reps(case.cfg, arr["k_cache"], arr["page_ids"], arr["page_valid"])
+    K = widen(arr["k_cache"])
+    for i, (p, v) in enumerate(zip(arr["page_ids"], arr["page_valid"])):
+        np.testing.assert_allclose(reps[i], K[p, :, :v, :].mean(axis=1), rtol=0, atol=1e-13)
+
+
+def test_block_rep_of_equal_keys_is_that_key():
+    case = small_case(4, dtype=synth.BF16)
+    arr = synth.to_oracle_arrays(case)
+    k = arr["k_cache"].copy()
+    k[5, 1, :, :] = k[5, 1, 0, :]
+    reps = oracle.block_reps(case.cfg, k, [5], [32])
+    assert np.array_equal(reps[0, 1], widen(k[5, 1, 0]))
+
+
+# ---- attention against a library routine -------------------------------------------------------
+
+def check_against_sdpa(case, token_sets):
+    """token_sets(r, L) -> set of attended tokens, for every unit of the case."""
+    arr = synth.to_oracle_arrays(case)
+    res = oracle.decode(case.cfg, **{k: arr[k] for k in ("q", "k_cache", "v_cache",
+                                                         "block_table", "seq_lens",
+                                                         "prompt_lens")})
+    c = case.cfg
+    G = c["num_q_heads"] // c["num_kv_heads"]
+    for r in range(case.batch):
+        L = int(arr["seq_lens"][r])
+        for h in range(c["num_kv_heads"]):
+            K, V = logical_kv(arr, r, h, c["block_size"])
+            toks = token_sets(r, h, L, res)
+            for j in range(G):
+                want = sdpa(widen(arr["q"][r, h * G + j]), K, V, toks)
+                np.testing.assert_allclose(res["out"][r, h * G + j], want, rtol=1e-12,
+                                           atol=1e-12)
+    return res
+
+
+@pytest.mark.parametrize("dtype", [synth.BF16, synth.F32])
+def test_ratio_one_is_dense_attention(dtype):
+    case = small_case(5, dtype=dtype, topk_percent=1.0, seq_lens=[700, 333, 1024])
+    check_against_sdpa(case, lambda r, h, L, res: set(range(L)))
+
+
+def test_short_prompt_is_dense_attention():
+    case = small_case(6, topk_percent=0.2, dense_boundary=800, seq_lens=[700, 799],
+                      prompt_lens=[700, 799])
+    res = check_against_sdpa(case, lambda r, h, L, res: set(range(L)))
+    # Every candidate is selected for a dense request.
+    for r, L in enumerate((700, 799)):
+        assert res["nsel"][r, 0] == len(offload_blocks(L, 32, 64, 96))
+
+
+def test_prompt_at_boundary_is_sparse():
+    case = small_case(6, topk_percent=0.2, dense_boundary=700, seq_lens=[700])
+    res = oracle.decode(case.cfg, **{k: v for k, v in synth.to_oracle_arrays(case).items()
+                                     if k not in ("page_ids", "page_valid")})
+    n = len(offload_blocks(700, 32, 64, 96))
+    assert res["nsel"][0, 0] == exact_k(n, 0.2) < n
+
+
+def test_ratio_zero_is_sinks_plus_window():
+    case = small_case(7, topk_percent=0.0, seq_lens=[700, 190, 40])
+    check_against_sdpa(case, lambda r, h, L, res: attended_set(L, 32, 64, 96, []))
+
+
+def test_softmax_weights_sum_to_one_and_vanish_off_the_set():
+    case = small_case(8, seq_lens=[900])
+    arr = synth.to_oracle_arrays(case)
+    args = {k: arr[k] for k in ("q", "k_cache", "v_cache", "block_table", "seq_lens",
+                                "prompt_lens")}
+    res = oracle.decode(case.cfg, **args)
+    for h in range(2):
+        w, _ = oracle.unit_weights(case.cfg, **args, r=0, h=h)
+        toks = attended_set(900, 32, 64, 96, res["sel"][0, h, :res["nsel"][0, h]])
+        off = [t for t in range(900) if t not in toks]
+        assert np.all(np.abs(w.sum(axis=1) - 1.0) < 1e-12)
+        assert np.all(w >= 0) and np.all(w[:, off] == 0)
+    ones = dict(args, v_cache=np.ones_like(arr["v_cache"]))
+    out = oracle.decode(case.cfg, **ones)["out"]
+    np.testing.assert_allclose(out, 1.0, rtol=0, atol=1e-12)
+
+
+# ---- selection by brute force ---------------------------------------------------------------------
+
+def brute_force_unit(arr, cfg, r, h):
+    """Best k-subset by total score (ties: lexicographically smallest), enumerated."""
+    S, INIT, LOCAL = cfg["block_size"], cfg["init_tokens"], cfg["local_tokens"]
+    G = cfg["num_q_heads"] // cfg["num_kv_heads"]
+    L = int(arr["seq_lens"][r])
+    K, V = logical_kv(arr, r, h, S)
+    cands = offload_blocks(L, S, INIT, LOCAL)
+    k = exact_k(len(cands), cfg["topk_percent"])
+    qs = [widen(arr["q"][r, h * G + j]) for j in range(G)]
+    score = {b: sum(float(qj @ K[b * S:min(b * S + S, L)].mean(axis=0)) for qj in qs)
+             for b in cands}
+    best, best_sum = None, -math.inf
+    for sub in itertools.combinations(cands, k):     # ascending tuples, lexicographic order
+        s = sum(score[b] for b in sub)
+        if best is None or s > best_sum + 1e-9 * (1 + abs(best_sum)):
+            best, best_sum = sub, s
+    toks = attended_set(L, S, INIT, LOCAL, best or ())
+    outs = [sdpa(qj, K, V, toks) for qj in qs]
+    return list(best or ()), outs
+
+
+def test_selection_and_output_match_brute_force():
+    rng = np.random.default_rng(11)
+    for trial in range(40):
+        S = int(rng.choice([8, 16, 32]))
+        INIT = int(rng.integers(0, 3 * S))
+        LOCAL = int(rng.integers(0, 4 * S))
+        L = int(rng.integers(1, INIT + LOCAL + 12 * S))
+        case = small_case(100 + trial, seq_lens=[L], block_size=S, init_tokens=INIT,
+                          local_tokens=LOCAL, topk_percent=float(rng.choice([0.2, 0.34, 0.5])),
+                          dtype=int(rng.integers(0, 2)), head_dim=8)
+        arr = synth.to_oracle_arrays(case)
+        res = oracle.decode(case.cfg, **{k: arr[k] for k in ("q", "k_cache", "v_cache",
+                                                             "block_table", "seq_lens",
+                                                             "prompt_lens")})
+        for h in range(2):
+            sel, outs = brute_force_unit(arr, case.cfg, 0, h)
+            got = res["sel"][0, h, :res["nsel"][0, h]].tolist()
+            assert got == sel, (trial, h, L, S, INIT, LOCAL)
+            for j in range(2):
+                np.testing.assert_allclose(res["out"][0, h * 2 + j], outs[j], rtol=1e-12,
+                                           atol=1e-12)
+
+
+def test_exact_ties_go_to_the_lower_block():
+    # Every offload block gets identical keys, so every score ties exactly.
+    case = small_case(12, seq_lens=[600], topk_percent=0.25)
+    arr = synth.to_oracle_arrays(case)
+    k = arr["k_cache"].copy()
+    bt = arr["block_table"][0]
+    for b in offload_blocks(600, 32, 64, 96):
+        k[bt[b]] = k[bt[offload_blocks(600, 32, 64, 96)[0]]]
+    arr["k_cache"] = k
+    res = oracle.decode(case.cfg, **{x: arr[x] for x in ("q", "k_cache", "v_cache",
+                                                         "block_table", "seq_lens",
+                                                         "prompt_lens")})
+    cands = offload_blocks(600, 32, 64, 96)
+    kk = exact_k(len(cands), 0.25)
+    for h in range(2):
+        assert res["sel"][0, h, :res["nsel"][0, h]].tolist() == cands[:kk]
+        assert brute_force_unit(arr, case.cfg, 0, h)[0] == cands[:kk]
+
+
+def test_block_size_one_is_token_level_topk():
+    case = small_case(13, seq_lens=[260], block_size=1, init_tokens=20, local_tokens=30,
+                      topk_percent=0.1)
+    arr = synth.to_oracle_arrays(case)
+    res = oracle.decode(case.cfg, **{x: arr[x] for x in ("q", "k_cache", "v_cache",
+                                                         "block_table", "seq_lens",
+                                                         "prompt_lens")})
+    for h in range(2):
+        K, V = logical_kv(arr, 0, h, 1)
+        qs = [widen(arr["q"][0, 2 * h + j]) for j in range(2)]
+        qsum = qs[0] + qs[1]
+        offload = np.arange(20, 230)
+        s = K[offload] @ qsum
+        order = np.lexsort((offload, -s))                 # score desc, then token asc
+        chosen = sorted(offload[order[:exact_k(210, 0.1)]].tolist())
+        assert res["sel"][0, h, :res["nsel"][0, h]].tolist() == chosen
+        toks = set(range(20)) | set(chosen) | set(range(230, 260))
+        for j in range(2):
+            np.testing.assert_allclose(res["out"][0, 2 * h + j], sdpa(qs[j], K, V, toks),
+                                       rtol=1e-12, atol=1e-12)
+
+
+# ---- invariances ------------------------------------------------------------------------------------
+
+def decode_all(case_cfg, arr):
+    return oracle.decode(case_cfg, **{x: arr[x] for x in ("q", "k_cache", "v_cache",
+                                                          "block_table", "seq_lens",
+                                                          "prompt_lens")})
+
+
+def test_physical_page_permutation_changes_nothing():
+    case = small_case(14, seq_lens=[700, 450], shuffle=False)
+    arr = synth.to_oracle_arrays(case)
+    base = decode_all(case.cfg, arr)
+    rng = np.random.default_rng(1)
+    perm = rng.permutation(arr["k_cache"].shape[0])
+    moved = dict(arr)
+    moved["k_cache"] = np.empty_like(arr["k_cache"])
+    moved["v_cache"] = np.empty_like(arr["v_cache"])
+    moved["k_cache"][perm] = arr["k_cache"]
+    moved["v_cache"][perm] = arr["v_cache"]
+    bt = arr["block_table"].copy()
+    bt[bt >= 0] = perm[bt[bt >= 0]]
+    moved["block_table"] = bt
+    other = decode_all(case.cfg, moved)
+    for key in ("out", "sel", "nsel"):
+        assert np.array_equal(base[key], other[key])
+
+
+def test_prefix_sharing_changes_nothing():
+    shared = small_case(15, seq_lens=[500, 640, 590], shared_prefix_tokens=256)
+    arr = synth.to_oracle_arrays(shared)
+    base = decode_all(shared.cfg, arr)
+    # Give every request its own copy of the shared pages.
+    bt = arr["block_table"].copy()
+    k, v = [arr["k_cache"]], [arr["v_cache"]]
+    nxt = arr["k_cache"].shape[0]
+    for r in range(1, 3):
+        for b in range(256 // 32):
+            k.append(arr["k_cache"][bt[r, b]][None])
+            v.append(arr["v_cache"][bt[r, b]][None])
+            bt[r, b] = nxt
+            nxt += 1
+    copied = dict(arr, k_cache=np.concatenate(k), v_cache=np.concatenate(v), block_table=bt)
+    other = decode_all(shared.cfg, copied)
+    for key in ("out", "sel", "nsel"):
+        assert np.array_equal(base[key], other[key])
+
+
+def test_planted_blocks_are_selected():
+    case = synth.llama8b_layer(seq_len=12288, init_tokens=1024, local_tokens=2048,
+                               plant_fraction=0.05, seed=21)
+    arr = synth.to_oracle_arrays(case)
+    res = decode_all(case.cfg, arr)
+    # A planted block: its keys were moved along the group's query direction.
+    bt = arr["block_table"][0]
+    K = widen(arr["k_cache"])
+    G = 4
+    for h in range(8):
+        qd = sum(widen(arr["q"][0, h * G + j]) for j in range(G))
+        qd /= np.linalg.norm(qd)
+        planted = [b for b in offload_blocks(12288, 128, 1024, 2048)
+                   if K[bt[b], h].mean(axis=0) @ qd > 0.35]
+        assert planted, h
+        assert set(planted) <= set(res["sel"][0, h, :res["nsel"][0, h]].tolist())
+
+
+def test_empty_sequence_gives_zero_output():
+    case = small_case(16, seq_lens=[0, 100])
+    res = decode_all(case.cfg, synth.to_oracle_arrays(case))
+    assert np.all(res["out"][0] == 0) and np.all(res["nsel"][0] == 0)
+
+
+def test_candidate_scores_match_enumeration():
+    # LOCAL below the block size makes the partially filled last block a candidate.
+    rng = np.random.default_rng(17)
+    for trial in range(30):
+        S = int(rng.choice([8, 16, 32]))
+        L = int(rng.integers(S + 1, 20 * S))
+        if L % S == 0:
+            L += 1
+        INIT, LOCAL = int(rng.integers(0, 2 * S)), int(rng.integers(0, L % S))
+        case = small_case(300 + trial, seq_lens=[L], block_size=S, init_tokens=INIT,
+                          local_tokens=LOCAL, head_dim=8, dtype=int(rng.integers(0, 2)))
+        arr = synth.to_oracle_arrays(case)
+        res = decode_all(case.cfg, arr)
+        cands = offload_blocks(L, S, INIT, LOCAL)
+        assert cands[-1] == (L - 1) // S            # the partial block is a candidate
+        for h in range(2):
+            K, _ = logical_kv(arr, 0, h, S)
+            qsum = widen(arr["q"][0, 2 * h]) + widen(arr["q"][0, 2 * h + 1])
+            for b in range(case.max_blocks):
+                got = res["scores"][0, h, b]
+                if b in cands:
+                    want = float(qsum @ K[b * S:min(b * S + S, L)].mean(axis=0))
+                    assert abs(got - want) <= 1e-12 * (1 + abs(want)), (trial, b)
+                else:
+                    assert math.isnan(got)
