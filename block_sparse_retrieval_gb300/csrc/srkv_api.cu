@@ -1,0 +1,223 @@
+// srkv_api.cu -- the extern "C" entry points of libsrkv: argument checks and dispatch.
+//
+// Nothing here allocates, frees or synchronises: every entry point validates its
+// arguments on the host, launches on the caller's stream and returns.
+#include <math.h>
+#include <stdint.h>
+
+#include "srkv_internal.cuh"
+
+namespace srkv {
+namespace {
+
+// Upper bound on the split grid of any kernel on any device this library targets; the
+// workspace is sized for it so that its size does not depend on the device.
+constexpr int32_t kMaxCtas = 1024;
+constexpr int32_t kMaxBlocks = 16777215;  // max_blocks * 128 must fit in int32
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+bool config_ok(const srkv_config* c) {
+  if (!c) return false;
+  if (c->num_kv_heads <= 0 || c->num_q_heads <= 0 || c->num_q_heads % c->num_kv_heads) return false;
+  if (c->head_dim != 64 && c->head_dim != 128) return false;
+  if (c->block_size != kBlock) return false;
+  if (c->init_tokens < 0 || c->local_tokens < 0 || c->dense_boundary < 0) return false;
+  if (!(c->topk_percent >= 0.0 && c->topk_percent <= 1.0)) return false;
+  if (c->dtype != SRKV_BF16 && c->dtype != SRKV_F32) return false;
+  return true;
+}
+
+size_t elem_bytes(const srkv_config& c) { return c.dtype == SRKV_BF16 ? 2 : 4; }
+
+int32_t sm_count() {
+  static int32_t cache[128] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 128) return -1;
+  if (cache[dev] == 0) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+      return -1;
+    cache[dev] = n;
+  }
+  return cache[dev];
+}
+
+srkv_status cuda_status(cudaError_t e) { return e == cudaSuccess ? SRKV_OK : SRKV_ERR_CUDA; }
+
+int64_t host_topk_count(int64_t n, double p) {
+  if (n <= 0) return 0;
+  volatile double prod = p * (double)n;  // rounded on its own, as on the device
+  const double x = ceil(prod - 1e-9);
+  if (!(x > 0.0)) return 0;
+  if (x > (double)n) return n;
+  return (int64_t)x;
+}
+
+int64_t host_num_candidates(const srkv_config& c, int64_t L) {
+  const int64_t W = L - c.local_tokens;
+  if (W <= c.init_tokens) return 0;
+  return (W + kBlock - 1) / kBlock - c.init_tokens / kBlock;
+}
+
+}  // namespace
+}  // namespace srkv
+
+using namespace srkv;
+
+extern "C" {
+
+void srkv_default_config(srkv_config* cfg) {
+  if (!cfg) return;
+  cfg->num_q_heads = 32;
+  cfg->num_kv_heads = 8;
+  cfg->head_dim = 128;
+  cfg->block_size = kBlock;
+  cfg->init_tokens = 1024;
+  cfg->local_tokens = 7192;
+  cfg->topk_percent = 0.2;
+  cfg->dense_boundary = 32768;
+  cfg->dtype = SRKV_BF16;
+}
+
+const char* srkv_status_string(srkv_status s) {
+  switch (s) {
+    case SRKV_OK: return "ok";
+    case SRKV_ERR_INVALID_ARG: return "invalid argument";
+    case SRKV_ERR_UNSUPPORTED: return "unsupported configuration";
+    case SRKV_ERR_WORKSPACE: return "workspace missing or too small";
+    case SRKV_ERR_CUDA: return "CUDA error";
+  }
+  return "unknown status";
+}
+
+int64_t srkv_topk_count(int64_t n_candidates, double topk_percent) {
+  return host_topk_count(n_candidates, topk_percent);
+}
+
+int64_t srkv_num_candidates(const srkv_config* cfg, int64_t seq_len) {
+  if (!config_ok(cfg) || seq_len <= 0) return 0;
+  return host_num_candidates(*cfg, seq_len);
+}
+
+int32_t srkv_kmax_bound(const srkv_config* cfg, int32_t max_blocks) {
+  if (!config_ok(cfg) || max_blocks <= 0) return 0;
+  const int64_t n = host_num_candidates(*cfg, (int64_t)max_blocks * kBlock);
+  return (int32_t)(cfg->dense_boundary > 0 ? n : host_topk_count(n, cfg->topk_percent));
+}
+
+srkv_status srkv_build_block_reps(const srkv_config* cfg, const void* k_cache,
+                                  int64_t num_pages, const int32_t* page_ids,
+                                  const int32_t* page_valid_tokens, int32_t n_pages,
+                                  float* reps, int32_t* error_flags, srkv_stream stream) {
+  if (!config_ok(cfg) || n_pages < 0 || num_pages < 0) return SRKV_ERR_INVALID_ARG;
+  if (n_pages == 0) return SRKV_OK;
+  if (!k_cache || !page_ids || !page_valid_tokens || !reps || num_pages == 0)
+    return SRKV_ERR_INVALID_ARG;
+  if (!aligned(k_cache, 16) || !aligned(reps, 16)) return SRKV_ERR_INVALID_ARG;
+  if ((int64_t)n_pages * cfg->num_kv_heads > INT32_MAX) return SRKV_ERR_UNSUPPORTED;
+  return cuda_status(launch_block_reps(*cfg, k_cache, num_pages, page_ids, page_valid_tokens,
+                                       n_pages, reps, error_flags, (cudaStream_t)stream));
+}
+
+srkv_status srkv_score_topk(const srkv_config* cfg, const void* q, const float* reps,
+                            int64_t num_pages, const int32_t* block_table, int32_t max_blocks,
+                            const int32_t* seq_lens, const int32_t* prompt_lens, int32_t batch,
+                            int32_t* sel, int32_t kmax, int32_t* nsel, int32_t* error_flags,
+                            srkv_stream stream) {
+  if (!config_ok(cfg) || batch < 0 || max_blocks <= 0 || max_blocks > kMaxBlocks || kmax < 0 ||
+      num_pages < 0)
+    return SRKV_ERR_INVALID_ARG;
+  if (batch == 0) return SRKV_OK;
+  if (!q || !reps || !block_table || !seq_lens || !sel || !nsel || num_pages == 0)
+    return SRKV_ERR_INVALID_ARG;
+  if (!aligned(q, 16) || !aligned(reps, 16)) return SRKV_ERR_INVALID_ARG;
+  if (kmax < srkv_kmax_bound(cfg, max_blocks)) return SRKV_ERR_INVALID_ARG;
+  if ((int64_t)batch * cfg->num_kv_heads > INT32_MAX) return SRKV_ERR_UNSUPPORTED;
+  if ((size_t)max_blocks * 8 > 200 * 1024) return SRKV_ERR_UNSUPPORTED;  // keys + pages on chip
+  return cuda_status(launch_score_topk(*cfg, q, reps, num_pages, block_table, max_blocks,
+                                       seq_lens, prompt_lens, batch, sel, kmax, nsel,
+                                       error_flags, (cudaStream_t)stream));
+}
+
+size_t srkv_decode_workspace_size(const srkv_config* cfg, int32_t batch) {
+  if (!config_ok(cfg) || batch < 0) return 0;
+  const int64_t units = (int64_t)batch * cfg->num_kv_heads;
+  if (units > INT32_MAX - kMaxCtas) return 0;
+  const int32_t G = cfg->num_q_heads / cfg->num_kv_heads;
+  return ws_layout((int32_t)units, kMaxCtas, G, cfg->head_dim).total;
+}
+
+srkv_status srkv_sparse_paged_decode(const srkv_config* cfg, const void* q, const void* k_cache,
+                                     const void* v_cache, int64_t num_pages,
+                                     const int32_t* block_table, int32_t max_blocks,
+                                     const int32_t* seq_lens, int32_t batch,
+                                     const int32_t* sel, int32_t kmax, const int32_t* nsel,
+                                     void* out, void* workspace, size_t workspace_bytes,
+                                     int32_t* error_flags, srkv_stream stream) {
+  if (!config_ok(cfg) || batch < 0 || max_blocks <= 0 || max_blocks > kMaxBlocks || kmax < 0 ||
+      num_pages < 0)
+    return SRKV_ERR_INVALID_ARG;
+  if (batch == 0) return SRKV_OK;
+  if (!q || !k_cache || !v_cache || !block_table || !seq_lens || !nsel || !out || num_pages == 0)
+    return SRKV_ERR_INVALID_ARG;
+  if (kmax > 0 && !sel) return SRKV_ERR_INVALID_ARG;
+  if (!aligned(q, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) || !aligned(out, 16))
+    return SRKV_ERR_INVALID_ARG;
+  const int32_t G = cfg->num_q_heads / cfg->num_kv_heads;
+  const bool mma = mma_split_supported(*cfg);
+  if (!mma && G > 16) return SRKV_ERR_UNSUPPORTED;
+  const size_t need = srkv_decode_workspace_size(cfg, batch);
+  if (need == 0) return SRKV_ERR_UNSUPPORTED;
+  if (!workspace || workspace_bytes < need || !aligned(workspace, 256)) return SRKV_ERR_WORKSPACE;
+  const int32_t sms = sm_count();
+  if (sms <= 0) return SRKV_ERR_CUDA;
+
+  DecodeArgs a;
+  a.q = q;
+  a.k_cache = k_cache;
+  a.v_cache = v_cache;
+  a.num_pages = num_pages;
+  a.block_table = block_table;
+  a.max_blocks = max_blocks;
+  a.seq_lens = seq_lens;
+  a.batch = batch;
+  a.sel = sel;
+  a.kmax = kmax;
+  a.nsel = nsel;
+  a.out = out;
+  a.ws = static_cast<char*>(workspace);
+  a.error_flags = error_flags;
+  a.Hq = cfg->num_q_heads;
+  a.Hkv = cfg->num_kv_heads;
+  a.G = G;
+  a.d = cfg->head_dim;
+  a.init_tokens = cfg->init_tokens;
+  a.local_tokens = cfg->local_tokens;
+  a.scale_log2 = kLog2e / sqrtf((float)cfg->head_dim);
+  a.ctas = mma ? mma_split_ctas(sms) : simt_split_ctas(sms);
+  if (a.ctas > kMaxCtas) a.ctas = kMaxCtas;
+  a.lay = ws_layout(batch * cfg->num_kv_heads, kMaxCtas, G, cfg->head_dim);
+
+  cudaStream_t s = (cudaStream_t)stream;
+  cudaError_t e = mma ? launch_split_mma(a, s) : launch_split_simt(a, cfg->dtype, s);
+  if (e != cudaSuccess) return SRKV_ERR_CUDA;
+  return cuda_status(launch_combine(a, cfg->dtype, s));
+}
+
+srkv_status srkv_retrieval_decode(const srkv_config* cfg, const void* q, const void* k_cache,
+                                  const void* v_cache, const float* reps, int64_t num_pages,
+                                  const int32_t* block_table, int32_t max_blocks,
+                                  const int32_t* seq_lens, const int32_t* prompt_lens,
+                                  int32_t batch, int32_t* sel, int32_t kmax, int32_t* nsel,
+                                  void* out, void* workspace, size_t workspace_bytes,
+                                  int32_t* error_flags, srkv_stream stream) {
+  srkv_status st = srkv_score_topk(cfg, q, reps, num_pages, block_table, max_blocks, seq_lens,
+                                   prompt_lens, batch, sel, kmax, nsel, error_flags, stream);
+  if (st != SRKV_OK) return st;
+  return srkv_sparse_paged_decode(cfg, q, k_cache, v_cache, num_pages, block_table, max_blocks,
+                                  seq_lens, batch, sel, kmax, nsel, out, workspace,
+                                  workspace_bytes, error_flags, stream);
+}
+
+}  // extern "C"

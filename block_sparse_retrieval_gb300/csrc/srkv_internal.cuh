@@ -1,0 +1,331 @@
+// srkv_internal.cuh -- device helpers and the per-unit page list shared by the decode
+// kernels of libsrkv (sm_103a).  Not part of the public interface.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "srkv.h"
+
+namespace srkv {
+
+constexpr int kBlock = 128;               // tokens per page (the pages' block size)
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr uint64_t kWaitLimitNs = 2000000000ull;  // bounded on-chip waits: 2 s
+
+// ---- error flags -----------------------------------------------------------------------
+
+__device__ __forceinline__ void raise_flags(int32_t* flags, uint32_t bits) {
+  if (flags && bits) atomicOr(reinterpret_cast<unsigned int*>(flags), bits);
+}
+
+// ---- PTX wrappers ------------------------------------------------------------------------
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ uint64_t global_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count)
+               : "memory");
+}
+
+__device__ __forceinline__ void fence_mbar_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)),
+               "r"(bytes)
+               : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t done;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(done)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return done != 0;
+}
+
+// Waits for the phase with the given parity to complete; gives up after kWaitLimitNs.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = global_ns();
+  for (;;) {
+    for (int i = 0; i < 32; ++i)
+      if (mbar_try_wait(bar, parity)) return true;
+    if (global_ns() - t0 > kWaitLimitNs) return false;
+  }
+}
+
+// One-dimensional bulk copy global -> shared (TMA engine), completing on an mbarrier.
+// dst, src and bytes must be multiples of 16.
+__device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes,
+                                          uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+      ::"r"(smem_u32(dst)), "l"(src), "r"(bytes), "r"(smem_u32(bar))
+      : "memory");
+}
+
+__device__ __forceinline__ void named_bar_sync(int id, int threads) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
+}
+
+__device__ __forceinline__ float fast_exp2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// D += A * B, m16n8k16, bf16 inputs, fp32 accumulate.
+__device__ __forceinline__ void mma_16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
+                                          uint32_t a3, uint32_t b0, uint32_t b1) {
+  asm("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+      "{%8,%9}, {%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// Transpose of an 8x8 matrix of 16-bit values held one row per four lanes.
+__device__ __forceinline__ uint32_t movmatrix_trans(uint32_t x) {
+  uint32_t y;
+  asm("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(y) : "r"(x));
+  return y;
+}
+
+__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
+  __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&v);
+}
+
+__device__ __forceinline__ float bf16_lo(uint32_t v) { return __uint_as_float(v << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t v) { return __uint_as_float(v & 0xffff0000u); }
+
+// 16-byte shared-memory load (plain C++, so that the compiler orders it after the
+// mbarrier waits, whose inline assembly clobbers memory).
+__device__ __forceinline__ int4 lds128(const void* p) {
+  return *reinterpret_cast<const int4*>(p);
+}
+
+// ---- the page list of one (request, kv head) unit --------------------------------------
+//
+// The attended set of a unit is init blocks [0, a), the selected blocks, and window
+// blocks [wstart, nb).  The list has a + ns + (nb - wstart) positions; a selected block
+// that is also an init or a window block (only possible at the two boundaries, when
+// init_tokens or the window start is not a multiple of 128) keeps its list slot but is
+// skipped, and the init/window copy carries its "selected" mark instead.  This makes the
+// position count a function of (seq_len, nsel) alone.
+
+struct Geom {
+  int32_t L;       // clamped length
+  int32_t nb;      // blocks holding tokens
+  int32_t ie;      // end of the initial tokens: min(INIT, L)
+  int32_t ws;      // window start: max(L - LOCAL, 0)
+  int32_t W;       // L - LOCAL (may be negative)
+  int32_t a;       // init blocks [0, a)
+  int32_t wstart;  // window blocks [wstart, nb) that are not init blocks
+  int32_t ns;      // clamped selection count
+  __device__ __forceinline__ int32_t npos() const { return a + ns + (nb - wstart); }
+};
+
+__device__ __forceinline__ Geom make_geom(int32_t seq_len, int32_t nsel, int32_t max_blocks,
+                                          int32_t kmax, int32_t INIT, int32_t LOCAL,
+                                          uint32_t& eflags) {
+  Geom g;
+  int32_t L = seq_len;
+  const int32_t Lmax = max_blocks * kBlock;
+  if (L < 0 || L > Lmax) {
+    eflags |= SRKV_EFLAG_SEQ_LEN;
+    L = L < 0 ? 0 : Lmax;
+  }
+  int32_t ns = nsel;
+  if (ns < 0 || ns > kmax) {
+    eflags |= SRKV_EFLAG_SELECTION;
+    ns = ns < 0 ? 0 : kmax;
+  }
+  g.L = L;
+  g.nb = (L + kBlock - 1) / kBlock;
+  g.ie = INIT < L ? INIT : L;
+  g.W = L - LOCAL;
+  g.ws = g.W > 0 ? g.W : 0;
+  g.a = (g.ie + kBlock - 1) / kBlock;
+  const int32_t wb = g.ws < L ? g.ws / kBlock : g.nb;
+  g.wstart = wb > g.a ? wb : g.a;
+  g.ns = ns;
+  return g;
+}
+
+// Does logical block b meet the offload range [INIT, W)?
+__device__ __forceinline__ bool is_candidate(int32_t b, int32_t INIT, int32_t W) {
+  const int64_t lo = max((int64_t)b * kBlock, (int64_t)INIT);
+  const int64_t hi = min((int64_t)b * kBlock + kBlock, (int64_t)W);
+  return b >= 0 && lo < hi;
+}
+
+// What one list position loads.  rows [lo, hi) of the page are read; row r is attended iff
+// lo <= r < hi and (r < ie or r >= ws) (a selected block has ie = hi).
+struct PageTask {
+  int32_t page;  // physical page, -1 = nothing to load
+  int32_t block;
+  int32_t lo, hi, ie, ws;
+};
+
+__device__ __forceinline__ PageTask resolve_position(const Geom& g, int32_t j,
+                                                     const int32_t* sel_u,
+                                                     const int32_t* bt_r, int64_t num_pages,
+                                                     int32_t INIT, uint32_t& eflags) {
+  PageTask t;
+  t.page = -1;
+  t.block = -1;
+  t.lo = t.hi = t.ie = t.ws = 0;
+  int32_t b;
+  bool selected;
+  if (j < g.a) {
+    b = j;
+    selected = g.ns > 0 && sel_u[0] == b;
+  } else if (j < g.a + g.ns) {
+    const int32_t i = j - g.a;
+    b = sel_u[i];
+    const bool ok = is_candidate(b, INIT, g.W) && (i == 0 || sel_u[i - 1] < b);
+    if (!ok) {
+      eflags |= SRKV_EFLAG_SELECTION;
+      return t;
+    }
+    if (b < g.a || b >= g.wstart) return t;  // carried by the init / window slot
+    selected = true;
+  } else {
+    b = g.wstart + (j - g.a - g.ns);
+    selected = g.ns > 0 && sel_u[g.ns - 1] == b;
+  }
+  const int32_t base = b * kBlock;
+  const int32_t cnt = min(kBlock, g.L - base);
+  int32_t lo, hi, ie, ws;
+  if (selected) {
+    lo = 0;
+    hi = cnt;
+    ie = cnt;
+    ws = cnt;
+  } else {
+    ie = min(max(g.ie - base, 0), cnt);
+    ws = min(max(g.ws - base, 0), cnt);
+    lo = ie > 0 ? 0 : ws;
+    hi = ws < cnt ? cnt : ie;
+  }
+  if (lo >= hi) return t;
+  const int32_t page = bt_r[b];
+  if (page < 0 || (int64_t)page >= num_pages) {
+    eflags |= SRKV_EFLAG_PAGE_RANGE;
+    return t;
+  }
+  t.page = page;
+  t.block = b;
+  t.lo = lo;
+  t.hi = hi;
+  t.ie = ie;
+  t.ws = ws;
+  return t;
+}
+
+// CTA c of C owns list positions [c*T/C, (c+1)*T/C) of the concatenated unit lists.
+__device__ __forceinline__ int64_t cta_begin(int64_t c, int64_t T, int64_t C) {
+  return c * T / C;
+}
+// The CTA whose range holds position p (0 <= p < T).
+__device__ __forceinline__ int64_t cta_of(int64_t p, int64_t T, int64_t C) {
+  return ((p + 1) * C - 1) / T;
+}
+
+// Workspace layout of the decode (all offsets 256-byte aligned).
+struct WsLayout {
+  size_t unit_n;    // int32[U]: list positions of each unit
+  size_t unit_off;  // int64[U+1]: exclusive prefix of unit_n; [U] = total
+  size_t acc;       // float[slots][G][d]: unnormalised partial outputs
+  size_t ml;        // float[slots][G][2]: running max (log2 domain) and sum
+  size_t total;
+  int32_t slots;
+};
+
+__host__ __device__ inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+__host__ __device__ inline WsLayout ws_layout(int32_t units, int32_t ctas, int32_t G,
+                                              int32_t d) {
+  WsLayout w;
+  w.slots = units + ctas;
+  size_t off = 0;
+  w.unit_n = off;
+  off = align256(off + sizeof(int32_t) * (size_t)units);
+  w.unit_off = off;
+  off = align256(off + sizeof(int64_t) * ((size_t)units + 1));
+  w.acc = off;
+  off = align256(off + sizeof(float) * (size_t)w.slots * G * d);
+  w.ml = off;
+  off = align256(off + sizeof(float) * 2 * (size_t)w.slots * G);
+  w.total = off;
+  return w;
+}
+
+// Arguments shared by the split-phase decode kernels and the combine kernel.
+struct DecodeArgs {
+  const void* q;
+  const void* k_cache;
+  const void* v_cache;
+  int64_t num_pages;
+  const int32_t* block_table;
+  int32_t max_blocks;
+  const int32_t* seq_lens;
+  int32_t batch;
+  const int32_t* sel;
+  int32_t kmax;
+  const int32_t* nsel;
+  void* out;
+  char* ws;
+  WsLayout lay;
+  int32_t* error_flags;
+  int32_t Hq, Hkv, G, d;
+  int32_t init_tokens, local_tokens;
+  float scale_log2;  // log2(e) / sqrt(d)
+  int32_t ctas;      // C, the split grid
+};
+
+// ---- launchers (defined in the kernel files) ---------------------------------------------
+
+cudaError_t launch_block_reps(const srkv_config& cfg, const void* k_cache, int64_t num_pages,
+                              const int32_t* page_ids, const int32_t* valid, int32_t n,
+                              float* reps, int32_t* error_flags, cudaStream_t stream);
+
+cudaError_t launch_score_topk(const srkv_config& cfg, const void* q, const float* reps,
+                              int64_t num_pages, const int32_t* block_table,
+                              int32_t max_blocks, const int32_t* seq_lens,
+                              const int32_t* prompt_lens, int32_t batch, int32_t* sel,
+                              int32_t kmax, int32_t* nsel, int32_t* error_flags,
+                              cudaStream_t stream);
+
+// Split phase on tensor cores (bf16, G <= 8, d in {64, 128}); grid = SM count.
+bool mma_split_supported(const srkv_config& cfg);
+int32_t mma_split_ctas(int32_t sm_count);
+cudaError_t launch_split_mma(const DecodeArgs& a, cudaStream_t stream);
+
+// Split phase on CUDA cores (any supported dtype / group).
+int32_t simt_split_ctas(int32_t sm_count);
+cudaError_t launch_split_simt(const DecodeArgs& a, int32_t dtype, cudaStream_t stream);
+
+cudaError_t launch_combine(const DecodeArgs& a, int32_t dtype, cudaStream_t stream);
+
+}  // namespace srkv

@@ -1,0 +1,231 @@
+"""Python binding of libsrkv (ctypes): the same entry points as ``include/srkv.h``.
+
+Argument marshalling only: every step of the method runs in the library's CUDA
+kernels.  Tensors are torch CUDA tensors owned by the caller; streams default to
+torch's current stream.  There is no fallback: if ``libsrkv.so`` has not been built
+(``python -m block_sparse_retrieval_gb300.build``), :func:`load` raises.
+
+A configuration is a mapping with the keys of :data:`CFG_KEYS` (``dtype`` 0 = bf16,
+1 = fp32), e.g. :func:`default_config`.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Mapping
+
+import torch
+
+from .build import LIB_PATH
+
+CFG_KEYS = ("num_q_heads", "num_kv_heads", "head_dim", "block_size", "init_tokens",
+            "local_tokens", "topk_percent", "dense_boundary", "dtype")
+BF16, F32 = 0, 1
+EFLAG_PAGE_RANGE, EFLAG_SEQ_LEN, EFLAG_SELECTION, EFLAG_TIMEOUT = 1, 2, 4, 8
+STATUS = {0: "ok", 1: "invalid argument", 2: "unsupported configuration",
+          3: "workspace missing or too small", 4: "CUDA error"}
+EXPORTS = ("srkv_default_config", "srkv_status_string", "srkv_topk_count",
+           "srkv_num_candidates", "srkv_kmax_bound", "srkv_build_block_reps",
+           "srkv_score_topk", "srkv_decode_workspace_size", "srkv_sparse_paged_decode",
+           "srkv_retrieval_decode")
+
+
+class SrkvError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        super().__init__(f"{where}: {STATUS.get(status, status)}")
+        self.status = status
+
+
+class Config(ctypes.Structure):
+    _fields_ = [("num_q_heads", ctypes.c_int32), ("num_kv_heads", ctypes.c_int32),
+                ("head_dim", ctypes.c_int32), ("block_size", ctypes.c_int32),
+                ("init_tokens", ctypes.c_int32), ("local_tokens", ctypes.c_int32),
+                ("topk_percent", ctypes.c_double), ("dense_boundary", ctypes.c_int32),
+                ("dtype", ctypes.c_int32)]
+
+
+_lib: ctypes.CDLL | None = None
+_P = ctypes.c_void_p
+_I32, _I64, _SZ = ctypes.c_int32, ctypes.c_int64, ctypes.c_size_t
+
+
+def load() -> ctypes.CDLL:
+    """Loads the in-tree libsrkv.so; raises if it has not been built."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(LIB_PATH):
+        raise RuntimeError(f"{LIB_PATH} is missing: run python -m block_sparse_retrieval_gb300.build")
+    lib = ctypes.CDLL(LIB_PATH)
+    lib.srkv_default_config.argtypes = [ctypes.POINTER(Config)]
+    lib.srkv_default_config.restype = None
+    lib.srkv_status_string.argtypes = [ctypes.c_int]
+    lib.srkv_status_string.restype = ctypes.c_char_p
+    lib.srkv_topk_count.argtypes = [_I64, ctypes.c_double]
+    lib.srkv_topk_count.restype = _I64
+    lib.srkv_num_candidates.argtypes = [ctypes.POINTER(Config), _I64]
+    lib.srkv_num_candidates.restype = _I64
+    lib.srkv_kmax_bound.argtypes = [ctypes.POINTER(Config), _I32]
+    lib.srkv_kmax_bound.restype = _I32
+    lib.srkv_build_block_reps.argtypes = [ctypes.POINTER(Config), _P, _I64, _P, _P, _I32, _P,
+                                          _P, _P]
+    lib.srkv_score_topk.argtypes = [ctypes.POINTER(Config), _P, _P, _I64, _P, _I32, _P, _P,
+                                    _I32, _P, _I32, _P, _P, _P]
+    lib.srkv_decode_workspace_size.argtypes = [ctypes.POINTER(Config), _I32]
+    lib.srkv_decode_workspace_size.restype = _SZ
+    lib.srkv_sparse_paged_decode.argtypes = [ctypes.POINTER(Config), _P, _P, _P, _I64, _P, _I32,
+                                             _P, _I32, _P, _I32, _P, _P, _P, _SZ, _P, _P]
+    lib.srkv_retrieval_decode.argtypes = [ctypes.POINTER(Config), _P, _P, _P, _P, _I64, _P,
+                                          _I32, _P, _P, _I32, _P, _I32, _P, _P, _P, _SZ, _P, _P]
+    for name in ("srkv_build_block_reps", "srkv_score_topk", "srkv_sparse_paged_decode",
+                 "srkv_retrieval_decode"):
+        getattr(lib, name).restype = ctypes.c_int
+    _lib = lib
+    return lib
+
+
+def config(cfg: Mapping) -> Config:
+    return Config(*[cfg[k] for k in CFG_KEYS])
+
+
+def default_config() -> dict:
+    c = Config()
+    load().srkv_default_config(ctypes.byref(c))
+    return {k: getattr(c, k) for k in CFG_KEYS}
+
+
+def status_string(status: int) -> str:
+    return load().srkv_status_string(status).decode()
+
+
+def topk_count(n: int, p: float) -> int:
+    return int(load().srkv_topk_count(n, p))
+
+
+def num_candidates(cfg: Mapping, seq_len: int) -> int:
+    c = config(cfg)
+    return int(load().srkv_num_candidates(ctypes.byref(c), seq_len))
+
+
+def kmax_bound(cfg: Mapping, max_blocks: int) -> int:
+    c = config(cfg)
+    return int(load().srkv_kmax_bound(ctypes.byref(c), max_blocks))
+
+
+def decode_workspace_size(cfg: Mapping, batch: int) -> int:
+    c = config(cfg)
+    return int(load().srkv_decode_workspace_size(ctypes.byref(c), batch))
+
+
+# ---- marshalling helpers ----------------------------------------------------------------
+
+def _dev(t: torch.Tensor | None, name: str, dtype: torch.dtype | None = None):
+    if t is None:
+        return None
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if dtype is not None and t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _store_dtype(cfg: Mapping) -> torch.dtype:
+    return torch.bfloat16 if cfg["dtype"] == BF16 else torch.float32
+
+
+def _stream(stream) -> ctypes.c_void_p:
+    s = torch.cuda.current_stream() if stream is None else stream
+    return ctypes.c_void_p(s.cuda_stream if hasattr(s, "cuda_stream") else int(s))
+
+
+def _check(status: int, where: str) -> None:
+    if status != 0:
+        raise SrkvError(status, where)
+
+
+# ---- entry points --------------------------------------------------------------------------
+
+def build_block_reps(cfg: Mapping, k_cache: torch.Tensor, page_ids: torch.Tensor,
+                     page_valid_tokens: torch.Tensor, reps: torch.Tensor,
+                     error_flags: torch.Tensor | None = None, stream=None) -> None:
+    c = config(cfg)
+    _check(load().srkv_build_block_reps(
+        ctypes.byref(c), _dev(k_cache, "k_cache", _store_dtype(cfg)), k_cache.shape[0],
+        _dev(page_ids, "page_ids", torch.int32), _dev(page_valid_tokens, "page_valid_tokens",
+                                                      torch.int32),
+        page_ids.numel(), _dev(reps, "reps", torch.float32),
+        _dev(error_flags, "error_flags", torch.int32), _stream(stream)), "srkv_build_block_reps")
+
+
+def score_topk(cfg: Mapping, q: torch.Tensor, reps: torch.Tensor, block_table: torch.Tensor,
+               seq_lens: torch.Tensor, prompt_lens: torch.Tensor | None, sel: torch.Tensor,
+               nsel: torch.Tensor, error_flags: torch.Tensor | None = None,
+               stream=None) -> None:
+    c = config(cfg)
+    B, max_blocks = block_table.shape
+    _check(load().srkv_score_topk(
+        ctypes.byref(c), _dev(q, "q", _store_dtype(cfg)), _dev(reps, "reps", torch.float32),
+        reps.shape[0], _dev(block_table, "block_table", torch.int32), max_blocks,
+        _dev(seq_lens, "seq_lens", torch.int32), _dev(prompt_lens, "prompt_lens", torch.int32),
+        B, _dev(sel, "sel", torch.int32), sel.shape[-1], _dev(nsel, "nsel", torch.int32),
+        _dev(error_flags, "error_flags", torch.int32), _stream(stream)), "srkv_score_topk")
+
+
+def sparse_paged_decode(cfg: Mapping, q: torch.Tensor, k_cache: torch.Tensor,
+                        v_cache: torch.Tensor, block_table: torch.Tensor,
+                        seq_lens: torch.Tensor, sel: torch.Tensor, nsel: torch.Tensor,
+                        out: torch.Tensor, workspace: torch.Tensor,
+                        error_flags: torch.Tensor | None = None, stream=None) -> None:
+    c = config(cfg)
+    dt = _store_dtype(cfg)
+    B, max_blocks = block_table.shape
+    _check(load().srkv_sparse_paged_decode(
+        ctypes.byref(c), _dev(q, "q", dt), _dev(k_cache, "k_cache", dt),
+        _dev(v_cache, "v_cache", dt), k_cache.shape[0],
+        _dev(block_table, "block_table", torch.int32), max_blocks,
+        _dev(seq_lens, "seq_lens", torch.int32), B, _dev(sel, "sel", torch.int32),
+        sel.shape[-1], _dev(nsel, "nsel", torch.int32), _dev(out, "out", dt),
+        _dev(workspace, "workspace"), workspace.numel() * workspace.element_size(),
+        _dev(error_flags, "error_flags", torch.int32), _stream(stream)),
+        "srkv_sparse_paged_decode")
+
+
+def retrieval_decode(cfg: Mapping, q: torch.Tensor, k_cache: torch.Tensor,
+                     v_cache: torch.Tensor, reps: torch.Tensor, block_table: torch.Tensor,
+                     seq_lens: torch.Tensor, prompt_lens: torch.Tensor | None,
+                     sel: torch.Tensor, nsel: torch.Tensor, out: torch.Tensor,
+                     workspace: torch.Tensor, error_flags: torch.Tensor | None = None,
+                     stream=None) -> None:
+    c = config(cfg)
+    dt = _store_dtype(cfg)
+    B, max_blocks = block_table.shape
+    _check(load().srkv_retrieval_decode(
+        ctypes.byref(c), _dev(q, "q", dt), _dev(k_cache, "k_cache", dt),
+        _dev(v_cache, "v_cache", dt), _dev(reps, "reps", torch.float32), k_cache.shape[0],
+        _dev(block_table, "block_table", torch.int32), max_blocks,
+        _dev(seq_lens, "seq_lens", torch.int32), _dev(prompt_lens, "prompt_lens", torch.int32),
+        B, _dev(sel, "sel", torch.int32), sel.shape[-1], _dev(nsel, "nsel", torch.int32),
+        _dev(out, "out", dt), _dev(workspace, "workspace"),
+        workspace.numel() * workspace.element_size(),
+        _dev(error_flags, "error_flags", torch.int32), _stream(stream)), "srkv_retrieval_decode")
+
+
+# ---- buffers for a step --------------------------------------------------------------------
+
+class DecodeBuffers:
+    """Device buffers one decode step needs besides the cache: reps, selection, output,
+    workspace and the error word.  Allocated once by torch (the library allocates none)."""
+
+    def __init__(self, cfg: Mapping, batch: int, max_blocks: int, num_pages: int,
+                 device="cuda"):
+        Hq, Hkv, d = cfg["num_q_heads"], cfg["num_kv_heads"], cfg["head_dim"]
+        self.kmax = max(1, kmax_bound(cfg, max_blocks))
+        self.reps = torch.zeros(num_pages, Hkv, d, dtype=torch.float32, device=device)
+        self.sel = torch.full((batch, Hkv, self.kmax), -1, dtype=torch.int32, device=device)
+        self.nsel = torch.zeros(batch, Hkv, dtype=torch.int32, device=device)
+        self.out = torch.zeros(batch, Hq, d, dtype=_store_dtype(cfg), device=device)
+        nbytes = decode_workspace_size(cfg, batch)
+        self.workspace = torch.empty(max(nbytes, 256), dtype=torch.uint8, device=device)
+        self.error_flags = torch.zeros(1, dtype=torch.int32, device=device)

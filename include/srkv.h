@@ -1,0 +1,184 @@
+/*
+ * srkv.h -- C ABI of libsrkv: block-sparse retrieval decode attention over a paged
+ * KV cache, for one GB300 GPU (sm_103a).
+ *
+ * The method (openGauss 7.0.0 DataVec, "KV Cache Query-Based Computation Inference
+ * Acceleration"):
+ *   - "Feature Description": at prefill, one representation vector is extracted for
+ *     every KV block;
+ *   - "Overall Solution": the cache of a sequence is split into initial_tokens, the
+ *     sliding_window and the offload_tokens between them; at each decode step the
+ *     current query is scored by inner product against the representation vector of
+ *     every offload block, the topK blocks are kept, and attention runs over the
+ *     initial tokens, the kept blocks and the window together;
+ *   - "Configuration Parameters": INIT_TOKENS_NUM (1024), LOCAL_TOKENS_NUM (7192),
+ *     TOPK_PERCENT (0.2), block size 128, DENSE_BOUNDARY (32K: a prompt shorter than
+ *     this is attended densely).
+ * Attention itself is softmax(q K^T / sqrt(d)) V (rkmt.cn ATB KV-cache reuse article,
+ * §1.1), read through a page table of physical pages (same article, §2.2); a group of
+ * query heads shares one K/V head (KV-cache survey "大模型推理百倍加速之KV cache篇",
+ * section "Share--KV cache共享").
+ *
+ * Definitions used by every entry point (S = block_size = 128 tokens per page):
+ *   L      = seq_lens[r], the tokens in request r's cache, the current token included;
+ *   W      = L - local_tokens, the first token of the sliding window;
+ *   candidate blocks of r = logical blocks b whose tokens [bS, bS+S) meet [init_tokens, W);
+ *   rep[p][h][:] = fp32 mean of the keys of physical page p, kv head h, over its valid
+ *            tokens (the representation vector);
+ *   score of block b for (r, h) = (sum of the query vectors of h's group) . rep[bt[r][b]][h];
+ *   k = min(n, ceil(topk_percent * n - 1e-9)) of n candidates (0 if n = 0), or n when
+ *       prompt_lens[r] < dense_boundary;
+ *   selection = the k candidates of highest score, ties to the lower block index;
+ *   attended tokens = [0, init_tokens) u (selected blocks n [init_tokens, W)) u [W, L),
+ *       as a set; out = softmax over them of q.K/sqrt(d), times V; L = 0 gives 0.
+ *
+ * Layouts (all row-major, all device memory unless stated):
+ *   q, out          [B][Hq][d]        dtype of the config (bf16 or fp32)
+ *   k_cache,v_cache [P][Hkv][S][d]    dtype of the config; one (page, kv head) slab of
+ *                                     S*d elements is contiguous
+ *   reps            [P][Hkv][d]       fp32
+ *   block_table     [B][max_blocks]   int32 physical page of logical block b; entries for
+ *                                     b >= ceil(L/S) are never read
+ *   seq_lens, prompt_lens [B]         int32
+ *   sel             [B][Hkv][kmax]    int32 selected logical blocks, ascending
+ *   nsel            [B][Hkv]          int32
+ * Ownership: the caller owns every buffer.  The library allocates nothing, frees
+ * nothing and never synchronises; every call is asynchronous on `stream` (a
+ * cudaStream_t; NULL is the legacy default stream) and returns after launching.
+ * Errors: the return value reports host-side argument checks and launch failures.
+ * Problems only visible on the device (a page id outside [0, num_pages), a sequence
+ * longer than max_blocks*S, a malformed selection, a bounded wait that ran out) make
+ * the kernels skip the offending work, never fault, and set SRKV_EFLAG_* bits in the
+ * optional device word `error_flags` (may be NULL; the caller clears it).
+ * No C++ exception crosses this interface.
+ */
+#ifndef SRKV_H
+#define SRKV_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st* srkv_stream; /* identical to cudaStream_t */
+
+typedef enum {
+  SRKV_OK = 0,
+  SRKV_ERR_INVALID_ARG = 1, /* null pointer, bad size, bad alignment, bad config value */
+  SRKV_ERR_UNSUPPORTED = 2, /* a valid configuration that this build does not implement */
+  SRKV_ERR_WORKSPACE = 3,   /* workspace missing or smaller than srkv_decode_workspace_size */
+  SRKV_ERR_CUDA = 4         /* a CUDA call or kernel launch failed */
+} srkv_status;
+
+typedef enum { SRKV_BF16 = 0, SRKV_F32 = 1 } srkv_dtype;
+
+/* Device-side error bits, OR-ed into *error_flags. */
+#define SRKV_EFLAG_PAGE_RANGE 1u /* a block-table entry outside [0, num_pages) was skipped */
+#define SRKV_EFLAG_SEQ_LEN 2u    /* seq_len < 0 or > max_blocks*S; clamped into range */
+#define SRKV_EFLAG_SELECTION 4u  /* nsel outside [0, kmax], or a sel entry that is not a
+                                    candidate or not ascending; such entries were skipped */
+#define SRKV_EFLAG_TIMEOUT 8u    /* a bounded on-chip wait ran out; the kernel returned early */
+
+/* Configuration: the method's knobs ("Configuration Parameters") and the head layout. */
+typedef struct {
+  int32_t num_q_heads;    /* Hq, a multiple of num_kv_heads */
+  int32_t num_kv_heads;   /* Hkv */
+  int32_t head_dim;       /* d: 64 or 128 */
+  int32_t block_size;     /* S: must be 128 (the pages' recommended block size) */
+  int32_t init_tokens;    /* INIT_TOKENS_NUM, >= 0, default 1024 */
+  int32_t local_tokens;   /* LOCAL_TOKENS_NUM, >= 0, default 7192 */
+  double topk_percent;    /* TOPK_PERCENT in [0, 1], default 0.2 */
+  int32_t dense_boundary; /* DENSE_BOUNDARY, >= 0, default 32768; 0 disables dense mode */
+  int32_t dtype;          /* srkv_dtype of q, caches and out */
+} srkv_config;
+
+/* Fills the pages' defaults: Hq 32, Hkv 8, d 128, S 128, 1024 / 7192 / 0.2 / 32768, bf16. */
+void srkv_default_config(srkv_config* cfg);
+
+/* Human-readable name of a status; never NULL. */
+const char* srkv_status_string(srkv_status status);
+
+/* k for n candidates at ratio p (definition above); 0 for n <= 0. */
+int64_t srkv_topk_count(int64_t n_candidates, double topk_percent);
+
+/* Number of candidate blocks of a sequence of seq_len tokens under cfg; 0 if cfg is NULL. */
+int64_t srkv_num_candidates(const srkv_config* cfg, int64_t seq_len);
+
+/* The sel capacity (kmax) that srkv_score_topk needs for any request of at most
+ * max_blocks*S tokens: all candidates when dense mode can occur, else k of them. */
+int32_t srkv_kmax_bound(const srkv_config* cfg, int32_t max_blocks);
+
+/*
+ * Representation vectors ("Feature Description": extracted block by block at prefill).
+ * For i < n_pages: reps[page_ids[i]][h][:] = mean over t < page_valid_tokens[i] of
+ * k_cache[page_ids[i]][h][t][:], accumulated in fp32, for every kv head h.  Pages not
+ * listed are left untouched.  page_valid_tokens[i] = 0 writes zeros.
+ *   k_cache: [num_pages][Hkv][S][d], 16-byte aligned.   reps: [num_pages][Hkv][d] fp32.
+ *   page_ids, page_valid_tokens: device int32 [n_pages]; an id outside [0, num_pages) or a
+ *   count outside [0, S] is skipped and flagged (SRKV_EFLAG_PAGE_RANGE).
+ */
+srkv_status srkv_build_block_reps(const srkv_config* cfg, const void* k_cache,
+                                  int64_t num_pages, const int32_t* page_ids,
+                                  const int32_t* page_valid_tokens, int32_t n_pages,
+                                  float* reps, int32_t* error_flags, srkv_stream stream);
+
+/*
+ * Scoring and top-k ("Overall Solution": inner product of the current query with each
+ * representation vector, keep the topK closest).  For every request r and kv head h:
+ * sel[r][h][0..nsel[r][h]) = the selected candidate blocks of (r, h), ascending; dense
+ * requests (prompt_lens[r] < dense_boundary) select every candidate.
+ *   q: [B][Hq][d] (cfg dtype, 16-byte aligned); reps: [num_pages][Hkv][d] fp32 as written
+ *   by srkv_build_block_reps for every page a candidate block maps to;
+ *   prompt_lens may be NULL (then prompt = seq_len);
+ *   kmax >= srkv_kmax_bound(cfg, max_blocks), else SRKV_ERR_INVALID_ARG.
+ */
+srkv_status srkv_score_topk(const srkv_config* cfg, const void* q, const float* reps,
+                            int64_t num_pages, const int32_t* block_table, int32_t max_blocks,
+                            const int32_t* seq_lens, const int32_t* prompt_lens, int32_t batch,
+                            int32_t* sel, int32_t kmax, int32_t* nsel, int32_t* error_flags,
+                            srkv_stream stream);
+
+/* Bytes of device workspace srkv_sparse_paged_decode needs for `batch` requests on the
+ * current device; 0 if cfg is invalid. */
+size_t srkv_decode_workspace_size(const srkv_config* cfg, int32_t batch);
+
+/*
+ * Sparse paged decode attention ("Overall Solution": the kept blocks are concatenated
+ * with the initial and window KV and take part in attention; flash-decoding split and
+ * merge as in the survey's "Share--KV cache共享" section).  For every request r and query
+ * head j of kv head h = j / G:
+ *   out[r][j][:] = softmax over the attended tokens of q[r][j].K_t / sqrt(d), times V_t,
+ * with the attended set built from sel/nsel (as written by srkv_score_topk, or any
+ * ascending list of candidate blocks).  Accumulation is fp32; out has the cfg dtype.
+ *   k_cache, v_cache: [num_pages][Hkv][S][d], 16-byte aligned;
+ *   workspace: >= srkv_decode_workspace_size(cfg, batch) bytes, 256-byte aligned, contents
+ *   need not be initialised; it is scratch owned by this call until the stream reaches
+ *   the end of the call.
+ */
+srkv_status srkv_sparse_paged_decode(const srkv_config* cfg, const void* q, const void* k_cache,
+                                     const void* v_cache, int64_t num_pages,
+                                     const int32_t* block_table, int32_t max_blocks,
+                                     const int32_t* seq_lens, int32_t batch,
+                                     const int32_t* sel, int32_t kmax, const int32_t* nsel,
+                                     void* out, void* workspace, size_t workspace_bytes,
+                                     int32_t* error_flags, srkv_stream stream);
+
+/*
+ * One whole decode step: srkv_score_topk followed by srkv_sparse_paged_decode on the same
+ * stream, with the selection written to the caller's sel/nsel buffers.
+ */
+srkv_status srkv_retrieval_decode(const srkv_config* cfg, const void* q, const void* k_cache,
+                                  const void* v_cache, const float* reps, int64_t num_pages,
+                                  const int32_t* block_table, int32_t max_blocks,
+                                  const int32_t* seq_lens, const int32_t* prompt_lens,
+                                  int32_t batch, int32_t* sel, int32_t kmax, int32_t* nsel,
+                                  void* out, void* workspace, size_t workspace_bytes,
+                                  int32_t* error_flags, srkv_stream stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SRKV_H */

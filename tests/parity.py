@@ -1,0 +1,98 @@
+"""Helpers for the GPU parity tests: run the library on a synthetic case and compare with
+the oracle under the rules of the method's statement:
+
+  * selected block ids equal the oracle's exactly wherever the top-k boundary gap
+    (s_(k) - s_(k+1)) / max_b |s_b| exceeds 1e-4; inside that band any selection that is a
+    valid top-k within the band is accepted (scores are fp32 on the GPU, fp64 in the oracle);
+  * attention outputs are compared with the oracle's own selection fed to the GPU decode:
+    |gpu - oracle| <= 2e-2 + 1e-2 |oracle| for bf16 inputs, 1e-5 + 1e-5 |oracle| for fp32.
+"""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+import oracle
+from block_sparse_retrieval_gb300 import srkv, synth
+
+GAP = 1e-4
+TOL = {synth.BF16: (2e-2, 1e-2), synth.F32: (1e-5, 1e-5)}
+ORACLE_KEYS = ("q", "k_cache", "v_cache", "block_table", "seq_lens", "prompt_lens")
+
+
+def gpu_select(case, buf=None):
+    cfg = case.cfg
+    buf = buf or srkv.DecodeBuffers(cfg, case.batch, case.max_blocks, case.num_pages,
+                                    device=case.q.device)
+    srkv.build_block_reps(cfg, case.k_cache, case.page_ids, case.page_valid, buf.reps,
+                          buf.error_flags)
+    srkv.score_topk(cfg, case.q, buf.reps, case.block_table, case.seq_lens, case.prompt_lens,
+                    buf.sel, buf.nsel, buf.error_flags)
+    torch.cuda.synchronize()
+    return buf
+
+
+def gpu_decode(case, buf, sel: np.ndarray, nsel: np.ndarray) -> np.ndarray:
+    dev = case.q.device
+    kmax = buf.kmax
+    s = np.full((case.batch, case.cfg["num_kv_heads"], kmax), -1, np.int32)
+    s[:, :, :min(kmax, sel.shape[2])] = sel[:, :, :kmax]
+    srkv.sparse_paged_decode(case.cfg, case.q, case.k_cache, case.v_cache, case.block_table,
+                             case.seq_lens, torch.from_numpy(s).to(dev),
+                             torch.from_numpy(np.ascontiguousarray(nsel)).to(dev), buf.out,
+                             buf.workspace, buf.error_flags)
+    torch.cuda.synchronize()
+    return buf.out.float().cpu().numpy()
+
+
+def oracle_ref(case, arr=None, units=None, kmax=None, threads=8):
+    arr = arr or synth.to_oracle_arrays(case)
+    return oracle.decode(case.cfg, *[arr[k] for k in ORACLE_KEYS], units=units, kmax=kmax,
+                         threads=threads)
+
+
+def check_selection(case, gpu_sel: np.ndarray, gpu_nsel: np.ndarray, ref: dict, units=None):
+    """Returns the number of units compared exactly (gap above the threshold)."""
+    B, Hkv = gpu_nsel.shape
+    units = units or [(r, h) for r in range(B) for h in range(Hkv)]
+    exact = 0
+    for r, h in units:
+        k = int(ref["nsel"][r, h])
+        assert int(gpu_nsel[r, h]) == k, (r, h, int(gpu_nsel[r, h]), k)
+        want = ref["sel"][r, h, :k]
+        got = gpu_sel[r, h, :k]
+        scores = ref["scores"][r, h]
+        cand = np.flatnonzero(~np.isnan(scores))
+        n = cand.size
+        if k == 0 or k == n:
+            assert np.array_equal(got, want), (r, h)
+            exact += 1
+            continue
+        s_sorted = np.sort(scores[cand])[::-1]
+        scale = max(np.abs(scores[cand]).max(), 1e-300)
+        gap = (s_sorted[k - 1] - s_sorted[k]) / scale
+        if gap > GAP:
+            assert np.array_equal(got, want), (r, h, gap)
+            exact += 1
+        else:
+            assert np.all(np.diff(got) > 0), (r, h)
+            assert np.all(~np.isnan(scores[got])), (r, h)
+            band = GAP * scale
+            assert scores[got].min() >= s_sorted[k - 1] - band, (r, h)
+            assert np.all(np.isin(cand[scores[cand] > s_sorted[k - 1] + band], got)), (r, h)
+    return exact
+
+
+def check_out(case, got: np.ndarray, want: np.ndarray, units=None):
+    atol, rtol = TOL[case.cfg["dtype"]]
+    G = case.cfg["num_q_heads"] // case.cfg["num_kv_heads"]
+    if units is None:
+        g, w = got, want
+    else:
+        heads = [(r, h * G + j) for r, h in units for j in range(G)]
+        g = np.stack([got[r, qh] for r, qh in heads])
+        w = np.stack([want[r, qh] for r, qh in heads])
+    err = np.abs(g - w)
+    bad = err > atol + rtol * np.abs(w)
+    assert not bad.any(), f"{bad.sum()} elements off, max err {err.max():.3e}"
+    return float(err.max())
