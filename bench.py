@@ -1,0 +1,454 @@
+"""Benchmark of block-sparse retrieval decode on GB300.
+
+One step = one decode step of one Llama-3-8B-shaped layer (batch 1, 32 q / 8 kv heads,
+d 128, bf16, 65536 cached tokens, init 1024, window 7192, top-k 20 %, 5 % planted
+blocks, shuffled 128-token pages): score + top-k of the offload blocks, then split-K
+sparse paged attention and its combine.  The representation vectors are built once per
+page at prefill (as on the method's page: the store is written at prefill and read at
+decode) and reported separately under "prefill_reps".
+
+L2: the step rotates over --layers independent caches (default 8 x 268 MB); between two
+uses of one layer the other layers stream > 500 MB, more than the 129 MB L2, so every
+step reads its pages from HBM.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+--impl reference times the oracle (plain fp64 C on the host cores) on the same workload.
+Under torchrun each rank runs an independent replica (the method shards by request with
+no exchange); rank 0 prints one JSON line.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+PEAKS = os.path.join(ROOT, "MEASURED_PEAKS.json")
+TRAFFIC = os.path.join(ROOT, "profiles", "traffic.json")
+METRIC = "decode steps/s and achieved HBM GB/s (% of GB300 peak) for sparse paged attention"
+WORKLOAD = "llama8b-layer-65536-bf16 (batch 1, 32/8 heads, d 128, init 1024, window 7192, top-k 0.2, 5% planted, shuffled pages)"
+FALLBACK_HBM = 6800.0
+DECODE_SOURCES = ("decode_split_mma.cu", "decode_combine.cu", "decode_plan.cuh",
+                  "srkv_internal.cuh")
+
+
+# ---- distributed plumbing -----------------------------------------------------------------
+
+def dist_init():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        if not dist.is_initialized():
+            backend = "nccl" if torch.cuda.is_available() else "gloo"
+            if torch.cuda.is_available():
+                torch.cuda.set_device(local)
+            dist.init_process_group(backend=backend)
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x: float, world: int, device) -> float:
+    if world == 1:
+        return x
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ---- measurement helpers ------------------------------------------------------------------
+
+def peaks() -> tuple[float, str]:
+    try:
+        with open(PEAKS) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return FALLBACK_HBM, "fallback"
+
+
+def decode_source_hash() -> str:
+    h = hashlib.sha256()
+    for name in DECODE_SOURCES:
+        with open(os.path.join(ROOT, "block_sparse_retrieval_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def committed_traffic():
+    """DRAM bytes per decode launch from the committed ncu summary, if it was taken on the
+    current decode sources; else None."""
+    try:
+        with open(TRAFFIC) as f:
+            t = json.load(f)
+    except (OSError, ValueError):
+        return None
+    if t.get("source_hash") != decode_source_hash():
+        return None
+    return t.get("bytes_per_launch")
+
+
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "50"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        time.sleep(0.15)
+        return self
+
+    def __exit__(self, *exc):
+        time.sleep(0.1)
+        self.lines = []
+        if self.proc:
+            self.proc.terminate()
+            out, _ = self.proc.communicate(timeout=10)
+            self.lines = [l for l in out.splitlines() if l.strip()]
+
+    def summary(self) -> dict:
+        sm, mx, reasons = [], 0.0, set()
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        for line in self.lines:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx = max(mx, float(parts[1]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[4:8]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        busy = [s for s in sm if s > 0.5 * mx] or sm
+        return {"sm_mhz": statistics.median(busy) if busy else None,
+                "sm_max_mhz": mx or None, "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def attended_tokens(L: int, sel, INIT: int, LOCAL: int, S: int = 128) -> tuple[int, int]:
+    """|initial u selected-offload u window| and the number of pages it touches."""
+    W = L - LOCAL
+    ie, ws = min(INIT, L), max(W, 0)
+    base = ie + (L - ws if ws < L else 0) - max(0, ie - ws)
+    blocks = set(range((ie + S - 1) // S)) | set(range(ws // S, (L + S - 1) // S) if ws < L else [])
+    extra = 0
+    for b in sel:
+        lo, hi = max(b * S, INIT), min(b * S + S, W)
+        if lo < hi:
+            extra += hi - lo
+            blocks.add(int(b))
+    return base + extra, len(blocks)
+
+
+# ---- our arm --------------------------------------------------------------------------------
+
+class Layer:
+    def __init__(self, seed: int, device):
+        from block_sparse_retrieval_gb300 import srkv, synth
+        self.case = synth.llama8b_layer(seed=seed, device=device)
+        c = self.case
+        self.buf = srkv.DecodeBuffers(c.cfg, c.batch, c.max_blocks, c.num_pages, device=device)
+        self.srkv = srkv
+
+    def prefill(self):
+        c, b = self.case, self.buf
+        self.srkv.build_block_reps(c.cfg, c.k_cache, c.page_ids, c.page_valid, b.reps,
+                                   b.error_flags)
+
+    def score(self):
+        c, b = self.case, self.buf
+        self.srkv.score_topk(c.cfg, c.q, b.reps, c.block_table, c.seq_lens, c.prompt_lens,
+                             b.sel, b.nsel, b.error_flags)
+
+    def decode(self):
+        c, b = self.case, self.buf
+        self.srkv.sparse_paged_decode(c.cfg, c.q, c.k_cache, c.v_cache, c.block_table,
+                                      c.seq_lens, b.sel, b.nsel, b.out, b.workspace,
+                                      b.error_flags)
+
+    def step_bytes(self) -> dict:
+        """Algorithmic bytes of one step: what the method must read and write."""
+        c, b = self.case, self.buf
+        cfg = c.cfg
+        d, Hkv, Hq = cfg["head_dim"], cfg["num_kv_heads"], cfg["num_q_heads"]
+        sel, nsel = b.sel.cpu().numpy(), b.nsel.cpu().numpy()
+        L = c.seq_lens.cpu().numpy()
+        from block_sparse_retrieval_gb300 import srkv
+        kv = pages = n_cand = 0
+        for r in range(c.batch):
+            n_cand += srkv.num_candidates(cfg, int(L[r])) * Hkv
+            for h in range(Hkv):
+                toks, pg = attended_tokens(int(L[r]), sel[r, h, :nsel[r, h]],
+                                           cfg["init_tokens"], cfg["local_tokens"])
+                kv += toks * 2 * d * 2
+                pages += pg
+        qo = c.batch * Hq * d * 2
+        score = n_cand * (d * 4 + 4) + qo + int(nsel.sum()) * 4 + nsel.size * 4
+        decode = kv + pages * 4 + qo * 2 + int(nsel.sum()) * 4 + nsel.size * 4
+        return {"score": score, "decode": decode, "kv": kv, "total": score + decode}
+
+
+def capture(fn, stream):
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        fn()
+    return g
+
+
+def run_ours(args, world, rank, local):
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    peak, peak_kind = peaks()
+    layers = [Layer(1000 + 17 * i + 1000003 * rank, dev) for i in range(args.layers)]
+
+    # prefill: representation vectors of every page of every layer (timed separately)
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(2 * len(layers))]
+    for ly in layers:                        # warm the kernel once
+        ly.prefill()
+    torch.cuda.synchronize()
+    rep_bytes = 0
+    for i, ly in enumerate(layers):
+        ev[2 * i].record()
+        ly.prefill()
+        ev[2 * i + 1].record()
+        c = ly.case
+        rep_bytes += int(c.page_valid.sum()) * c.cfg["num_kv_heads"] * c.cfg["head_dim"] * 2 \
+            + c.page_ids.numel() * c.cfg["num_kv_heads"] * c.cfg["head_dim"] * 4
+    torch.cuda.synchronize()
+    rep_ms = sum(ev[2 * i].elapsed_time(ev[2 * i + 1]) for i in range(len(layers)))
+
+    for ly in layers:                        # correctness of the step before timing it
+        ly.score()
+        ly.decode()
+    torch.cuda.synchronize()
+    flags = [int(ly.buf.error_flags.item()) for ly in layers]
+    if any(flags):
+        raise RuntimeError(f"device error flags {flags}")
+    step_bytes = [ly.step_bytes() for ly in layers]
+
+    stream = torch.cuda.Stream(device=dev)
+    stream.wait_stream(torch.cuda.current_stream())
+    graphs = []
+    with torch.cuda.stream(stream):
+        for ly in layers:
+            graphs.append((capture(ly.score, stream), capture(ly.decode, stream)))
+    torch.cuda.synchronize()
+
+    R = len(layers)
+    with torch.cuda.stream(stream):
+        for i in range(args.warmup):
+            gs, gd = graphs[i % R]
+            gs.replay()
+            gd.replay()
+    torch.cuda.synchronize()
+
+    K = args.steps
+    e_a = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    e_b = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    e_c = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    barrier(world)
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clocks:
+        with torch.cuda.stream(stream):
+            torch.cuda._sleep(int(2e7))      # let the host queue ahead of the device
+            for i in range(K):
+                gs, gd = graphs[i % R]
+                e_a[i].record(stream)
+                gs.replay()
+                e_b[i].record(stream)
+                gd.replay()
+                e_c[i].record(stream)
+        torch.cuda.synchronize()
+    barrier(world)
+    total_ms = e_a[0].elapsed_time(e_c[-1])
+    score_ms = [e_a[i].elapsed_time(e_b[i]) for i in range(K)]
+    decode_ms = [e_b[i].elapsed_time(e_c[i]) for i in range(K)]
+    total_ms = max_over_ranks(total_ms, world, dev)
+    ms_per_step = total_ms / K
+    value = world * K / (total_ms / 1e3)
+
+    avg_decode_bytes = statistics.mean(sb["decode"] for sb in step_bytes)
+    avg_step_bytes = statistics.mean(sb["total"] for sb in step_bytes)
+    dec_ms = statistics.mean(decode_ms)
+    achieved = avg_decode_bytes / (dec_ms / 1e3) / 1e9
+    traffic = committed_traffic()
+
+    e2e = run_e2e(layers, min(K, args.e2e_steps), world, dev)
+    line = {
+        "metric": METRIC, "value": round(value, 2), "unit": "steps/s", "n_gpus": world,
+        "steps": K, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded N(0,1) q/K/V, 5% planted blocks, shuffled pages)",
+        "config": {"workload": WORKLOAD, "global_batch": world, "seq_len": 65536,
+                   "parallelism": f"replicas x{world}", "layers_rotated": R,
+                   "l2": f"inputs larger than L2: {R} layer caches rotated per step"},
+        "step_GB_s": round(avg_step_bytes / (ms_per_step / 1e3) / 1e9, 1),
+        "step_frac_of_hbm": round(avg_step_bytes / (ms_per_step / 1e3) / 1e9 / peak, 4),
+        "roofline": {"kernel": "srkv_sparse_paged_decode (split + combine)", "bound": "hbm",
+                     "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+                     "frac": round(achieved / peak, 4), "peak_kind": peak_kind,
+                     "bytes_per_launch": int(avg_decode_bytes),
+                     "us_per_launch": round(dec_ms * 1e3, 3), "traffic": traffic},
+        "score_topk_us": round(statistics.mean(score_ms) * 1e3, 3),
+        "prefill_reps": {"kernel": "srkv_build_block_reps", "pages": sum(
+            ly.case.page_ids.numel() for ly in layers), "us": round(rep_ms * 1e3, 1),
+            "GB_s": round(rep_bytes / (rep_ms / 1e3) / 1e9, 1),
+            "frac": round(rep_bytes / (rep_ms / 1e3) / 1e9 / peak, 4)},
+        "clocks": clocks.summary(),
+        "e2e": e2e,
+        "gpu_launches": K * 3,
+    }
+    if rank == 0 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(layers[0], args.cpu_seconds)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+def run_e2e(layers, K, world, dev) -> dict:
+    """The same steps through the public entry point with host buffers: each step copies
+    its query and lengths from pinned host memory, runs srkv_retrieval_decode and reads the
+    output back."""
+    from block_sparse_retrieval_gb300 import srkv
+    host = []
+    for ly in layers:
+        c = ly.case
+        host.append(dict(q=c.q.cpu().pin_memory(), L=c.seq_lens.cpu().pin_memory(),
+                         P=c.prompt_lens.cpu().pin_memory(),
+                         out=torch.empty_like(ly.buf.out, device="cpu").pin_memory()))
+    h2d = host[0]["q"].nbytes + host[0]["L"].nbytes + host[0]["P"].nbytes
+    d2h = host[0]["out"].nbytes
+
+    def step(i):
+        ly, hb = layers[i % len(layers)], host[i % len(layers)]
+        c, b = ly.case, ly.buf
+        c.q.copy_(hb["q"], non_blocking=True)
+        c.seq_lens.copy_(hb["L"], non_blocking=True)
+        c.prompt_lens.copy_(hb["P"], non_blocking=True)
+        srkv.retrieval_decode(c.cfg, c.q, c.k_cache, c.v_cache, b.reps, c.block_table,
+                              c.seq_lens, c.prompt_lens, b.sel, b.nsel, b.out, b.workspace,
+                              b.error_flags)
+        hb["out"].copy_(b.out, non_blocking=True)
+        torch.cuda.current_stream().synchronize()
+
+    for i in range(3):
+        step(i)
+    barrier(world)
+    t0 = time.perf_counter()
+    for i in range(K):
+        step(i)
+    dt = max_over_ranks(time.perf_counter() - t0, world, dev)
+    return {"value": round(world * K / dt, 2), "unit": "steps/s", "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h, "steps": K}
+
+
+# ---- the oracle on the host --------------------------------------------------------------------
+
+def oracle_step_fn(case, threads):
+    import oracle
+    from block_sparse_retrieval_gb300 import synth
+    arr = synth.to_oracle_arrays(case)
+    args = [arr[k] for k in ("q", "k_cache", "v_cache", "block_table", "seq_lens",
+                             "prompt_lens")]
+    return lambda: oracle.decode(case.cfg, *args, threads=threads)
+
+
+def cpu_baseline(layer, seconds: float) -> dict:
+    units = layer.case.batch * layer.case.cfg["num_kv_heads"]
+    threads = max(1, min(os.cpu_count() or 1, units))
+    fn = oracle_step_fn(layer.case, threads)
+    fn()
+    n, t0 = 0, time.perf_counter()
+    while time.perf_counter() - t0 < seconds:
+        fn()
+        n += 1
+    dt = time.perf_counter() - t0
+    return {"value": round(n / dt, 3), "unit": "steps/s", "cores": threads, "kind": "oracle",
+            "sample": f"{n} full decode steps of one 65536-token layer (all {units} kv-head "
+                      "units; the oracle recomputes block means from K as it scores)"}
+
+
+def run_reference(args, world, rank):
+    if rank != 0:
+        return
+    from block_sparse_retrieval_gb300 import synth
+    case = synth.llama8b_layer(seed=1000, device="cpu")
+    units = case.batch * case.cfg["num_kv_heads"]
+    threads = max(1, min(os.cpu_count() or 1, units))
+    fn = oracle_step_fn(case, threads)
+    for _ in range(args.warmup):
+        fn()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        fn()
+    dt = time.perf_counter() - t0
+    value = args.steps / dt
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(value, 3), "unit": "steps/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(dt / args.steps * 1e3, 3), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic (seeded N(0,1) q/K/V, 5% planted blocks, shuffled pages)",
+        "config": {"workload": WORKLOAD, "global_batch": 1, "seq_len": 65536,
+                   "parallelism": "host cores"},
+        "cpu_baseline": {"value": round(value, 3), "unit": "steps/s", "cores": threads,
+                         "kind": "oracle",
+                         "sample": f"{args.steps} full decode steps of one 65536-token layer"},
+        "e2e": {"value": round(value, 3), "unit": "steps/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=4000)
+    ap.add_argument("--warmup", type=int, default=8)
+    ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    ap.add_argument("--layers", type=int, default=8)
+    ap.add_argument("--e2e-steps", type=int, default=1000)
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+    world, rank, local = dist_init()
+    if args.impl == "reference":
+        run_reference(args, world, rank)
+    else:
+        if not torch.cuda.is_available():
+            raise SystemExit("bench.py needs a CUDA GPU for --impl ours")
+        run_ours(args, world, rank, local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -144,6 +144,7 @@ __global__ void __launch_bounds__(kThreads, 1) split_mma_kernel(const DecodeArgs
   int64_t* scratch = reinterpret_cast<int64_t*>(smem + C::kOffScratch);
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  griddep_launch_dependents();  // the combine may be scheduled now; it waits for this grid
   if (tid == 0) {
     for (int s = 0; s < C::kStages; ++s) {
       mbar_init(&full[s], 1);
@@ -155,6 +156,7 @@ __global__ void __launch_bounds__(kThreads, 1) split_mma_kernel(const DecodeArgs
     fence_mbar_init();
   }
   __syncthreads();
+  griddep_wait();  // the selection comes from the previous kernel in the stream
 
   const CtaRange rg = plan_cta_range<kThreads>(a, scratch);
   const int64_t npos = rg.end - rg.begin;
@@ -450,21 +452,25 @@ bool mma_split_supported(const srkv_config& cfg) {
 
 int32_t mma_split_ctas(int32_t sm_count) { return sm_count; }
 
-cudaError_t launch_split_mma(const DecodeArgs& a, cudaStream_t stream) {
-  if (a.d == 128) {
-    auto kernel = split_mma_kernel<128>;
-    cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)Cfg<128>::kSmem);
+template <int D>
+cudaError_t launch_d(const DecodeArgs& a, cudaStream_t stream) {
+  // The shared-memory opt-in is set once per device (not during graph capture).
+  static bool configured[128] = {false};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 128) return cudaErrorInvalidDevice;
+  if (!configured[dev]) {
+    e = cudaFuncSetAttribute(split_mma_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)Cfg<D>::kSmem);
     if (e != cudaSuccess) return e;
-    kernel<<<a.ctas, kThreads, Cfg<128>::kSmem, stream>>>(a);
-  } else {
-    auto kernel = split_mma_kernel<64>;
-    cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)Cfg<64>::kSmem);
-    if (e != cudaSuccess) return e;
-    kernel<<<a.ctas, kThreads, Cfg<64>::kSmem, stream>>>(a);
+    configured[dev] = true;
   }
-  return cudaGetLastError();
+  return launch_pdl(split_mma_kernel<D>, dim3(a.ctas), dim3(kThreads), Cfg<D>::kSmem, stream, a);
+}
+
+cudaError_t launch_split_mma(const DecodeArgs& a, cudaStream_t stream) {
+  return a.d == 128 ? launch_d<128>(a, stream) : launch_d<64>(a, stream);
 }
 
 }  // namespace srkv

@@ -41,6 +41,8 @@ __global__ void __launch_bounds__(kThreads) split_simt_kernel(const DecodeArgs a
   __shared__ float s_acc[kWarps][kGMax][D];
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  griddep_launch_dependents();
+  griddep_wait();
   const CtaRange rg = plan_cta_range<kThreads>(a, scratch);
   const int64_t npos = rg.end - rg.begin;
   if (npos <= 0) return;
@@ -158,8 +160,7 @@ __global__ void __launch_bounds__(kThreads) split_simt_kernel(const DecodeArgs a
 
 template <typename T, int D>
 cudaError_t launch(const DecodeArgs& a, cudaStream_t s) {
-  split_simt_kernel<T, D><<<a.ctas, kThreads, 0, s>>>(a);
-  return cudaGetLastError();
+  return launch_pdl(split_simt_kernel<T, D>, dim3(a.ctas), dim3(kThreads), 0, s, a);
 }
 
 }  // namespace

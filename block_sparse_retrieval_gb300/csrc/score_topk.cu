@@ -8,12 +8,15 @@
 // share one K/V head: here a block's score for a kv head is the inner product with the sum
 // of the group's queries, and selection is per (request, kv head).
 //
-// One CTA per (request, kv head) unit:
-//   1. block-table entries of the candidates -> shared memory (one round of loads);
+// One thread-block cluster (up to 8 CTAs, ~64 candidates each) per (request, kv head) unit:
+//   1. each CTA loads the block-table entries of its share of the candidates;
 //   2. group query sum q_bar (fp32);
 //   3. one warp per candidate: s_b = q_bar . rep (fp32, fixed lane order), turned into an
-//      order-preserving 32-bit key (NaN and out-of-range pages rank lowest);
-//   4. MSB-first radix select (4 passes of 8 bits) finds the k-th largest key exactly;
+//      order-preserving 32-bit key (NaN and out-of-range pages rank lowest) and stored into
+//      the leader CTA's shared memory through distributed shared memory; one cluster
+//      barrier gathers them;
+//   4. the leader runs an MSB-first radix select (4 passes of 8 bits) for the exact k-th
+//      largest key;
 //   5. ties on that key go to the lower block index (an exclusive count in block order),
 //      and a second count writes the kept blocks ascending.
 // Bytes per unit: n * (4 + 4d) read (block table + reps), k * 4 written.
@@ -24,6 +27,7 @@ namespace {
 
 constexpr int kThreads = 512;
 constexpr int kWarps = kThreads / 32;
+constexpr int kMaxDynamicSmem = 200 * 1024;  // keys + pages of up to 25600 blocks
 
 struct ScoreArgs {
   const void* q;
@@ -87,30 +91,80 @@ __device__ __forceinline__ int32_t block_exclusive_scan(int32_t v, int32_t* scra
   return before + x - v;
 }
 
+__device__ __forceinline__ uint32_t cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+__device__ __forceinline__ uint32_t cluster_size() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_nctarank;" : "=r"(r));
+  return r;
+}
+// Store to the same shared-memory offset in CTA `rank` of this cluster.
+__device__ __forceinline__ void st_cluster_u32(uint32_t* local, uint32_t rank, uint32_t v) {
+  uint32_t remote;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(smem_u32(local)), "r"(rank));
+  asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(remote), "r"(v) : "memory");
+}
+__device__ __forceinline__ void cluster_sync() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+// Every warp finds the digit holding the remaining-th largest key from a 256-bin histogram.
+__device__ __forceinline__ void find_digit(const int32_t* hist, int lane, int32_t remaining,
+                                           int32_t* digit, int32_t* rem_out) {
+  int32_t c[8], local = 0;
+#pragma unroll
+  for (int b = 0; b < 8; ++b) {
+    c[b] = hist[lane * 8 + b];
+    local += c[b];
+  }
+  int32_t suffix = local;  // keys in this lane's bins and above
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int32_t y = __shfl_down_sync(0xffffffffu, suffix, o);
+    if (lane + o < 32) suffix += y;
+  }
+  int32_t above = suffix - local, dg = -1, rm = 0;
+#pragma unroll
+  for (int b = 7; b >= 0; --b) {
+    if (above < remaining && above + c[b] >= remaining) {
+      dg = lane * 8 + b;
+      rm = remaining - above;
+    }
+    above += c[b];
+  }
+  const uint32_t who = __ballot_sync(0xffffffffu, dg >= 0);
+  const int src = __ffs(who) - 1;
+  *digit = __shfl_sync(0xffffffffu, dg, src);
+  *rem_out = __shfl_sync(0xffffffffu, rm, src);
+}
+
+// Grid: one cluster of `cluster_size()` CTAs per (request, kv head) unit.
 template <typename T, int D>
 __global__ void __launch_bounds__(kThreads) score_topk_kernel(ScoreArgs a) {
   extern __shared__ uint32_t smem[];
-  uint32_t* keys = smem;                                        // [max_blocks]
+  uint32_t* keys = smem;                                             // [max_blocks], leader
   int32_t* pages = reinterpret_cast<int32_t*>(smem + a.max_blocks);  // [max_blocks]
   __shared__ float qbar[D];
-  __shared__ int32_t hist[256];
+  __shared__ int32_t hist[3][256];
   __shared__ int32_t scratch[32];
-  __shared__ int32_t digit_out, remaining_out;
-  __shared__ uint32_t flags_out;
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int32_t u = blockIdx.x;
+  griddep_launch_dependents();  // the decode may be scheduled now; it waits for this grid
+  const uint32_t crank = cluster_rank(), csize = cluster_size();
+  const int32_t u = blockIdx.x / csize;
   const int32_t r = u / a.Hkv, h = u % a.Hkv;
-  if (tid == 0) flags_out = 0;
 
   int32_t L = a.seq_lens[r];
+  const int32_t prompt = a.prompt_lens ? a.prompt_lens[r] : L;
   const int32_t Lmax = a.max_blocks * kBlock;
   uint32_t eflags = 0;
   if (L < 0 || L > Lmax) {
     eflags |= SRKV_EFLAG_SEQ_LEN;
     L = L < 0 ? 0 : Lmax;
   }
-  const int32_t prompt = a.prompt_lens ? a.prompt_lens[r] : L;
   const int32_t W = L - a.local_tokens;
   int32_t b_lo = 0, n = 0;
   if (W > a.init_tokens) {
@@ -125,49 +179,61 @@ __global__ void __launch_bounds__(kThreads) score_topk_kernel(ScoreArgs a) {
   }
   int32_t* sel_u = a.sel + (int64_t)u * a.kmax;
 
-  if (k == n && n <= a.kmax) {  // every candidate is kept: no scoring needed
-    for (int32_t i = tid; i < n; i += kThreads) sel_u[i] = b_lo + i;
-    if (tid == 0) {
-      a.nsel[u] = n;
-      raise_flags(a.error_flags, eflags);
-    }
-    return;
-  }
-  if (k == 0) {
-    if (tid == 0) {
-      a.nsel[u] = 0;
-      raise_flags(a.error_flags, eflags);
+  // Uniform over the cluster: every CTA takes the same branch.
+  if ((k == n && n <= a.kmax) || k == 0) {  // all candidates, or none: no scoring
+    if (crank == 0) {
+      for (int32_t i = tid; i < k; i += kThreads) sel_u[i] = b_lo + i;
+      if (tid == 0) {
+        a.nsel[u] = k;
+        raise_flags(a.error_flags, eflags);
+      }
     }
     return;
   }
 
-  // 1. physical pages of the candidates.
+  // 1. this CTA's share of the candidates, and their physical pages
+  const int32_t i_lo = (int32_t)((int64_t)n * crank / csize);
+  const int32_t i_hi = (int32_t)((int64_t)n * (crank + 1) / csize);
   const int32_t* bt_r = a.block_table + (int64_t)r * a.max_blocks;
-  for (int32_t i = tid; i < n; i += kThreads) pages[i] = bt_r[b_lo + i];
-  // 2. group query sum.
+  for (int32_t i = i_lo + tid; i < i_hi; i += kThreads) pages[i - i_lo] = bt_r[b_lo + i];
+  // 2. group query sum
   const T* q = static_cast<const T*>(a.q) + ((int64_t)r * a.Hq + (int64_t)h * a.G) * D;
   for (int e = tid; e < D; e += kThreads) {
     float s = 0.f;
-    for (int j = 0; j < a.G; ++j) s += static_cast<float>(q[(int64_t)j * D + e]);
+    int j = 0;
+    for (; j + 4 <= a.G; j += 4) {  // four independent loads in flight
+      const float x0 = static_cast<float>(q[(int64_t)(j + 0) * D + e]);
+      const float x1 = static_cast<float>(q[(int64_t)(j + 1) * D + e]);
+      const float x2 = static_cast<float>(q[(int64_t)(j + 2) * D + e]);
+      const float x3 = static_cast<float>(q[(int64_t)(j + 3) * D + e]);
+      s += x0;
+      s += x1;
+      s += x2;
+      s += x3;
+    }
+    for (; j < a.G; ++j) s += static_cast<float>(q[(int64_t)j * D + e]);
     qbar[e] = s;
   }
   __syncthreads();
 
-  // 3. scores, one warp per candidate, lanes over d.
+  // 3. scores of the share, one warp per candidate; keys go to the leader's shared memory
   constexpr int EPL = D / 32;  // elements per lane: 4 (d 128) or 2 (d 64)
   float qv[EPL];
 #pragma unroll
   for (int e = 0; e < EPL; ++e) qv[e] = qbar[lane * EPL + e];
-  constexpr int UNROLL = 8;
-  for (int32_t i0 = warp; i0 < n; i0 += kWarps * UNROLL) {
+  constexpr int UNROLL = 4;
+  for (int32_t i0 = i_lo + warp; i0 < i_hi; i0 += kWarps * UNROLL) {
     float part[UNROLL];
+    bool ok[UNROLL];
 #pragma unroll
     for (int x = 0; x < UNROLL; ++x) {
       const int32_t i = i0 + x * kWarps;
       part[x] = 0.f;
-      if (i < n) {
-        const int32_t page = pages[i];
-        if (page >= 0 && (int64_t)page < a.num_pages) {
+      ok[x] = false;
+      if (i < i_hi) {
+        const int32_t page = pages[i - i_lo];
+        ok[x] = page >= 0 && (int64_t)page < a.num_pages;
+        if (ok[x]) {
           const float* rep = a.reps + ((int64_t)page * a.Hkv + h) * D + lane * EPL;
           if constexpr (EPL == 4) {
             const float4 v = __ldg(reinterpret_cast<const float4*>(rep));
@@ -180,65 +246,47 @@ __global__ void __launch_bounds__(kThreads) score_topk_kernel(ScoreArgs a) {
       }
     }
 #pragma unroll
-    for (int x = 0; x < UNROLL; ++x) {
-      float s = part[x];
+    for (int o = 16; o > 0; o >>= 1)
 #pragma unroll
-      for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+      for (int x = 0; x < UNROLL; ++x) part[x] += __shfl_xor_sync(0xffffffffu, part[x], o);
+#pragma unroll
+    for (int x = 0; x < UNROLL; ++x) {
       const int32_t i = i0 + x * kWarps;
-      if (lane == 0 && i < n) {
-        const int32_t page = pages[i];
-        if (page >= 0 && (int64_t)page < a.num_pages) {
-          keys[i] = score_key(s);
-        } else {
-          keys[i] = 0u;
-          atomicOr(&flags_out, SRKV_EFLAG_PAGE_RANGE);
-        }
+      if (lane == 0 && i < i_hi) {
+        if (!ok[x]) eflags |= SRKV_EFLAG_PAGE_RANGE;
+        st_cluster_u32(&keys[i], 0, ok[x] ? score_key(part[x]) : 0u);
       }
     }
   }
-  __syncthreads();
+  if (lane == 0 && eflags) raise_flags(a.error_flags, eflags);
+  cluster_sync();  // every key is in the leader's shared memory
+  if (crank != 0) return;
 
-  // 4. radix select of the k-th largest key.
+  // 4. radix select of the k-th largest key (one barrier per pass, triple-buffered bins)
+  for (int i = tid; i < 2 * 256; i += kThreads) hist[i >> 8][i & 255] = 0;
+  __syncthreads();
   uint32_t prefix = 0, pmask = 0;
   int32_t remaining = k;
 #pragma unroll 1
-  for (int shift = 24; shift >= 0; shift -= 8) {
-    for (int i = tid; i < 256; i += kThreads) hist[i] = 0;
-    __syncthreads();
-    for (int32_t i = tid; i < n; i += kThreads) {
-      const uint32_t key = keys[i];
-      if ((key & pmask) == prefix) atomicAdd(&hist[(key >> shift) & 255u], 1);
+  for (int pass = 0; pass < 4; ++pass) {
+    const int shift = 24 - 8 * pass;
+    int32_t* hcur = hist[pass % 3];
+    for (int i = tid; i < 256; i += kThreads) hist[(pass + 1) % 3][i] = 0;
+    for (int32_t i0 = warp * 32; i0 < n; i0 += kThreads) {
+      // Scores cluster in a few digits; lanes with equal digits add once (one leader).
+      const int32_t i = i0 + lane;
+      const uint32_t key = i < n ? keys[i] : 0u;
+      const bool in = i < n && (key & pmask) == prefix;
+      const uint32_t digit = in ? (key >> shift) & 255u : 256u;
+      const uint32_t peers = __match_any_sync(0xffffffffu, digit);
+      if (in && lane == __ffs(peers) - 1) atomicAdd(&hcur[digit], __popc(peers));
     }
     __syncthreads();
-    if (warp == 0) {
-      int32_t c[8], local = 0;
-#pragma unroll
-      for (int b = 0; b < 8; ++b) {
-        c[b] = hist[lane * 8 + b];
-        local += c[b];
-      }
-      // suffix sums over lanes (higher digits first)
-      int32_t suffix = local;
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const int32_t y = __shfl_down_sync(0xffffffffu, suffix, o);
-        if (lane + o < 32) suffix += y;
-      }
-      int32_t above = suffix - local;  // keys whose digit lies in higher lanes
-#pragma unroll
-      for (int b = 7; b >= 0; --b) {
-        if (above < remaining && above + c[b] >= remaining) {
-          digit_out = lane * 8 + b;
-          remaining_out = remaining - above;
-        }
-        above += c[b];
-      }
-    }
-    __syncthreads();
-    prefix |= (uint32_t)digit_out << shift;
+    int32_t dg, rm;
+    find_digit(hcur, lane, remaining, &dg, &rm);
+    prefix |= (uint32_t)dg << shift;
     pmask |= 0xffu << shift;
-    remaining = remaining_out;
-    __syncthreads();
+    remaining = rm;
   }
   const uint32_t kth = prefix;
   const int32_t need_equal = remaining;  // keys equal to kth that are kept (lowest blocks)
@@ -265,23 +313,40 @@ __global__ void __launch_bounds__(kThreads) score_topk_kernel(ScoreArgs a) {
     if (key == kth) take = eq_rank++ < need_equal;
     if (take) sel_u[pos++] = b_lo + i;
   }
-  if (tid == 0) {
-    a.nsel[u] = total;
-    raise_flags(a.error_flags, eflags | flags_out);
-  }
+  if (tid == 0) a.nsel[u] = total;
 }
 
 template <typename T, int D>
-cudaError_t launch(const ScoreArgs& a, int32_t units, cudaStream_t s) {
+cudaError_t launch(const ScoreArgs& a, int32_t units, int32_t cluster, cudaStream_t s) {
   const size_t smem = sizeof(uint32_t) * 2 * (size_t)a.max_blocks;
   auto kernel = score_topk_kernel<T, D>;
   if (smem > 48 * 1024) {
-    cudaError_t e =
-        cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    // Raised once per device to the largest size the host checks allow.
+    static bool configured[128] = {false};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= 128) return cudaErrorInvalidDevice;
+    if (!configured[dev]) {
+      e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               kMaxDynamicSmem);
+      if (e != cudaSuccess) return e;
+      configured[dev] = true;
+    }
   }
-  kernel<<<units, kThreads, smem, s>>>(a);
-  return cudaGetLastError();
+  cudaLaunchConfig_t lc = {};
+  lc.gridDim = dim3((unsigned)(units * cluster));
+  lc.blockDim = dim3(kThreads);
+  lc.dynamicSmemBytes = smem;
+  lc.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = (unsigned)cluster;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  lc.attrs = attr;
+  lc.numAttrs = 1;
+  return cudaLaunchKernelEx(&lc, kernel, a);
 }
 
 }  // namespace
@@ -313,11 +378,18 @@ cudaError_t launch_score_topk(const srkv_config& cfg, const void* q, const float
   a.topk_percent = cfg.topk_percent;
   const int32_t units = batch * cfg.num_kv_heads;
   if (units == 0) return cudaSuccess;
+  // Candidates of the longest request the block table allows -> CTAs per unit (<= 8,
+  // about 64 candidates each).
+  int64_t W = (int64_t)max_blocks * kBlock - cfg.local_tokens;
+  int64_t nmax = W > cfg.init_tokens ? (W + kBlock - 1) / kBlock - cfg.init_tokens / kBlock : 0;
+  int32_t cluster = (int32_t)((nmax + 63) / 64);
+  cluster = cluster < 1 ? 1 : (cluster > 8 ? 8 : cluster);
+  if ((int64_t)units * cluster > INT32_MAX) return cudaErrorInvalidValue;
   if (cfg.dtype == SRKV_BF16)
-    return cfg.head_dim == 128 ? launch<__nv_bfloat16, 128>(a, units, stream)
-                               : launch<__nv_bfloat16, 64>(a, units, stream);
-  return cfg.head_dim == 128 ? launch<float, 128>(a, units, stream)
-                             : launch<float, 64>(a, units, stream);
+    return cfg.head_dim == 128 ? launch<__nv_bfloat16, 128>(a, units, cluster, stream)
+                               : launch<__nv_bfloat16, 64>(a, units, cluster, stream);
+  return cfg.head_dim == 128 ? launch<float, 128>(a, units, cluster, stream)
+                             : launch<float, 64>(a, units, cluster, stream);
 }
 
 }  // namespace srkv
