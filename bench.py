@@ -2,14 +2,16 @@
 
 One step = one decode step of one Llama-3-8B-shaped layer (batch 1, 32 q / 8 kv heads,
 d 128, bf16, 65536 cached tokens, init 1024, window 7192, top-k 20 %, 5 % planted
-blocks, shuffled 128-token pages): score + top-k of the offload blocks, then split-K
-sparse paged attention and its combine.  The representation vectors are built once per
+blocks, shuffled 128-token pages) through srkv_retrieval_decode: score + top-k of the
+offload blocks, then split-K sparse paged attention and its combine, captured per layer
+in a CUDA graph.  The representation vectors are built once per
 page at prefill (as on the method's page: the store is written at prefill and read at
 decode) and reported separately under "prefill_reps".
 
-L2: the step rotates over --layers independent caches (default 8 x 268 MB); between two
-uses of one layer the other layers stream > 500 MB, more than the 129 MB L2, so every
-step reads its pages from HBM.
+L2: the step rotates over --layers layer caches (default 8 x 268 MB of K/V, one block table
+and one set of lengths shared by all layers, as in a model); between two uses of one layer
+the other layers stream > 500 MB, more than the 129 MB L2, so every step reads its pages
+from HBM.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 
@@ -37,8 +39,8 @@ TRAFFIC = os.path.join(ROOT, "profiles", "traffic.json")
 METRIC = "decode steps/s and achieved HBM GB/s (% of GB300 peak) for sparse paged attention"
 WORKLOAD = "llama8b-layer-65536-bf16 (batch 1, 32/8 heads, d 128, init 1024, window 7192, top-k 0.2, 5% planted, shuffled pages)"
 FALLBACK_HBM = 6800.0
-DECODE_SOURCES = ("decode_split_mma.cu", "decode_combine.cu", "decode_plan.cuh",
-                  "srkv_internal.cuh")
+DECODE_SOURCES = ("score_topk.cu", "decode_split_mma.cu", "decode_combine.cu",
+                  "decode_plan.cuh", "srkv_internal.cuh", "srkv_api.cu")
 
 
 # ---- distributed plumbing -----------------------------------------------------------------
@@ -91,8 +93,8 @@ def decode_source_hash() -> str:
 
 
 def committed_traffic():
-    """DRAM bytes per decode launch from the committed ncu summary, if it was taken on the
-    current decode sources; else None."""
+    """DRAM bytes per step (the three kernels of srkv_retrieval_decode) from the committed ncu
+    summary, if it was taken on the current sources; else None."""
     try:
         with open(TRAFFIC) as f:
             t = json.load(f)
@@ -169,9 +171,17 @@ def attended_tokens(L: int, sel, INIT: int, LOCAL: int, S: int = 128) -> tuple[i
 # ---- our arm --------------------------------------------------------------------------------
 
 class Layer:
-    def __init__(self, seed: int, device):
+    """One attention layer's cache.  As in a model's paged cache, every layer has its own
+    queries, K/V pages and representation vectors, while the block table and the sequence
+    lengths (per request) are shared by all layers."""
+
+    def __init__(self, seed: int, device, shared=None):
         from block_sparse_retrieval_gb300 import srkv, synth
         self.case = synth.llama8b_layer(seed=seed, device=device)
+        if shared is not None:
+            for name in ("block_table", "seq_lens", "prompt_lens"):
+                assert torch.equal(getattr(self.case, name), getattr(shared, name))
+                setattr(self.case, name, getattr(shared, name))
         c = self.case
         self.buf = srkv.DecodeBuffers(c.cfg, c.batch, c.max_blocks, c.num_pages, device=device)
         self.srkv = srkv
@@ -181,16 +191,12 @@ class Layer:
         self.srkv.build_block_reps(c.cfg, c.k_cache, c.page_ids, c.page_valid, b.reps,
                                    b.error_flags)
 
-    def score(self):
+    def step(self):
+        """One decode step: srkv_retrieval_decode (score + top-k, then split + combine)."""
         c, b = self.case, self.buf
-        self.srkv.score_topk(c.cfg, c.q, b.reps, c.block_table, c.seq_lens, c.prompt_lens,
-                             b.sel, b.nsel, b.error_flags)
-
-    def decode(self):
-        c, b = self.case, self.buf
-        self.srkv.sparse_paged_decode(c.cfg, c.q, c.k_cache, c.v_cache, c.block_table,
-                                      c.seq_lens, b.sel, b.nsel, b.out, b.workspace,
-                                      b.error_flags)
+        self.srkv.retrieval_decode(c.cfg, c.q, c.k_cache, c.v_cache, b.reps, c.block_table,
+                                   c.seq_lens, c.prompt_lens, b.sel, b.nsel, b.out,
+                                   b.workspace, b.error_flags)
 
     def step_bytes(self) -> dict:
         """Algorithmic bytes of one step: what the method must read and write."""
@@ -225,7 +231,10 @@ def run_ours(args, world, rank, local):
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
     peak, peak_kind = peaks()
-    layers = [Layer(1000 + 17 * i + 1000003 * rank, dev) for i in range(args.layers)]
+    # Same seed: the same page structure for every layer (one shared block table).
+    layers = [Layer(1000 + 1000003 * rank, dev)]
+    layers += [Layer(1000 + 1000003 * rank, dev, shared=layers[0].case)
+               for _ in range(args.layers - 1)]
 
     # prefill: representation vectors of every page of every layer (timed separately)
     ev = [torch.cuda.Event(enable_timing=True) for _ in range(2 * len(layers))]
@@ -243,9 +252,8 @@ def run_ours(args, world, rank, local):
     torch.cuda.synchronize()
     rep_ms = sum(ev[2 * i].elapsed_time(ev[2 * i + 1]) for i in range(len(layers)))
 
-    for ly in layers:                        # correctness of the step before timing it
-        ly.score()
-        ly.decode()
+    for ly in layers:                        # the step must run clean before it is timed
+        ly.step()
     torch.cuda.synchronize()
     flags = [int(ly.buf.error_flags.item()) for ly in layers]
     if any(flags):
@@ -254,49 +262,37 @@ def run_ours(args, world, rank, local):
 
     stream = torch.cuda.Stream(device=dev)
     stream.wait_stream(torch.cuda.current_stream())
-    graphs = []
     with torch.cuda.stream(stream):
-        for ly in layers:
-            graphs.append((capture(ly.score, stream), capture(ly.decode, stream)))
+        graphs = [capture(ly.step, stream) for ly in layers]
     torch.cuda.synchronize()
 
     R = len(layers)
     with torch.cuda.stream(stream):
         for i in range(args.warmup):
-            gs, gd = graphs[i % R]
-            gs.replay()
-            gd.replay()
+            graphs[i % R].replay()
     torch.cuda.synchronize()
 
     K = args.steps
-    e_a = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
-    e_b = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
-    e_c = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(K + 1)]
     barrier(world)
     torch.cuda.synchronize()
     with ClockSampler(local) as clocks:
         with torch.cuda.stream(stream):
             torch.cuda._sleep(int(2e7))      # let the host queue ahead of the device
             for i in range(K):
-                gs, gd = graphs[i % R]
-                e_a[i].record(stream)
-                gs.replay()
-                e_b[i].record(stream)
-                gd.replay()
-                e_c[i].record(stream)
+                ev[i].record(stream)
+                graphs[i % R].replay()
+            ev[K].record(stream)
         torch.cuda.synchronize()
     barrier(world)
-    total_ms = e_a[0].elapsed_time(e_c[-1])
-    score_ms = [e_a[i].elapsed_time(e_b[i]) for i in range(K)]
-    decode_ms = [e_b[i].elapsed_time(e_c[i]) for i in range(K)]
-    total_ms = max_over_ranks(total_ms, world, dev)
+    step_ms = [ev[i].elapsed_time(ev[i + 1]) for i in range(K)]
+    total_ms = max_over_ranks(ev[0].elapsed_time(ev[K]), world, dev)
     ms_per_step = total_ms / K
     value = world * K / (total_ms / 1e3)
 
-    avg_decode_bytes = statistics.mean(sb["decode"] for sb in step_bytes)
     avg_step_bytes = statistics.mean(sb["total"] for sb in step_bytes)
-    dec_ms = statistics.mean(decode_ms)
-    achieved = avg_decode_bytes / (dec_ms / 1e3) / 1e9
+    call_ms = statistics.mean(step_ms)
+    achieved = avg_step_bytes / (call_ms / 1e3) / 1e9
     traffic = committed_traffic()
 
     e2e = run_e2e(layers, min(K, args.e2e_steps), world, dev)
@@ -308,21 +304,19 @@ def run_ours(args, world, rank, local):
         "config": {"workload": WORKLOAD, "global_batch": world, "seq_len": 65536,
                    "parallelism": f"replicas x{world}", "layers_rotated": R,
                    "l2": f"inputs larger than L2: {R} layer caches rotated per step"},
-        "step_GB_s": round(avg_step_bytes / (ms_per_step / 1e3) / 1e9, 1),
-        "step_frac_of_hbm": round(avg_step_bytes / (ms_per_step / 1e3) / 1e9 / peak, 4),
-        "roofline": {"kernel": "srkv_sparse_paged_decode (split + combine)", "bound": "hbm",
-                     "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
-                     "frac": round(achieved / peak, 4), "peak_kind": peak_kind,
-                     "bytes_per_launch": int(avg_decode_bytes),
-                     "us_per_launch": round(dec_ms * 1e3, 3), "traffic": traffic},
-        "score_topk_us": round(statistics.mean(score_ms) * 1e3, 3),
+        "roofline": {"kernel": "srkv_retrieval_decode call: score_topk + split-K decode "
+                               "kernels, overlapped by programmatic launch",
+                     "bound": "hbm", "achieved": round(achieved, 1), "peak": peak,
+                     "unit": "GB/s", "frac": round(achieved / peak, 4), "peak_kind": peak_kind,
+                     "bytes_per_launch": int(avg_step_bytes),
+                     "us_per_launch": round(call_ms * 1e3, 3), "traffic": traffic},
         "prefill_reps": {"kernel": "srkv_build_block_reps", "pages": sum(
             ly.case.page_ids.numel() for ly in layers), "us": round(rep_ms * 1e3, 1),
             "GB_s": round(rep_bytes / (rep_ms / 1e3) / 1e9, 1),
             "frac": round(rep_bytes / (rep_ms / 1e3) / 1e9 / peak, 4)},
         "clocks": clocks.summary(),
         "e2e": e2e,
-        "gpu_launches": K * 3,
+        "gpu_launches": K * 2,   # score_topk and the split kernel (with its merge) per step
     }
     if rank == 0 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(layers[0], args.cpu_seconds)

@@ -1,114 +1,175 @@
 // decode_plan.cuh -- how the split grid divides the attended pages of all units.
 //
+// The attended set of a (request, kv head) unit (openGauss DataVec page, "Overall
+// Solution": the selected blocks are concatenated with initial_tokens and the
+// sliding_window) is walked as two page lists:
+//   list A: the initial-token blocks [0, a) and the window blocks [wstart, nb), reading
+//           only their initial / window rows.  It depends on the sequence length alone, so
+//           it can be streamed before the selection exists;
+//   list B: the selected blocks, reading only their rows inside the offload range
+//           [INIT, W).  A selected block that also holds initial or window tokens (the
+//           window start is not page-aligned) is read by both lists, each for its own rows:
+//           the two row sets are disjoint and their union is the attended set.
 // Flash-decoding style split (KV-cache survey "大模型推理百倍加速之KV cache篇", section
-// "Share--KV cache共享": partial attention results are merged like Flash-Decoding).  The
-// page lists of all (request, kv head) units are concatenated in unit order, T positions in
-// total, and CTA c of C takes positions [c*T/C, (c+1)*T/C).  Every CTA therefore gets the
-// same number of pages whatever the lengths of the requests (ragged batches balance by
-// construction).  A CTA writes one partial (max, sum, unnormalised output) per unit its
-// range touches, into slot u + c: along the staircase of (unit, CTA) pairs each step raises
-// u or c, so the slot is unique and at most U + C - 1 slots are used.
+// "Share--KV cache共享": partial results are merged like Flash-Decoding): the lists of all
+// units are concatenated in unit order, T positions per list, and CTA c of C takes
+// positions [c*T/C, (c+1)*T/C) of each list, so every SM gets the same number of pages
+// whatever the request lengths.  A CTA writes one partial (max, sum, unnormalised output)
+// per unit its range touches, into slot u + c of the list's bank: along the staircase of
+// (unit, CTA) pairs each step raises u or c, so the slot is unique.
 #pragma once
 
 #include "srkv_internal.cuh"
 
 namespace srkv {
 
-template <int NT>
-__device__ __forceinline__ int64_t block_exclusive_scan64(int64_t v, int64_t* scratch,
-                                                          int64_t* total) {
-  constexpr int NW = NT / 32;
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  int64_t x = v;
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const int64_t y = __shfl_up_sync(0xffffffffu, x, o);
-    if (lane >= o) x += y;
+constexpr int kListA = 0, kListB = 1;
+
+__device__ __forceinline__ int32_t list_a_count(const Geom& g) { return g.a + (g.nb - g.wstart); }
+
+// Position j of list A: the page and the rows to read (init / window rows only).
+__device__ __forceinline__ PageTask resolve_a(const Geom& g, int32_t j, const int32_t* bt_r,
+                                              int64_t num_pages, uint32_t& eflags) {
+  PageTask t;
+  t.page = -1;
+  t.block = -1;
+  t.lo = t.hi = t.ie = t.ws = 0;
+  const int32_t b = j < g.a ? j : g.wstart + (j - g.a);
+  const int32_t base = b * kBlock;
+  const int32_t cnt = min(kBlock, g.L - base);
+  const int32_t ie = min(max(g.ie - base, 0), cnt);
+  const int32_t ws = min(max(g.ws - base, 0), cnt);
+  const int32_t lo = ie > 0 ? 0 : ws;
+  const int32_t hi = ws < cnt ? cnt : ie;
+  if (lo >= hi) return t;
+  const int32_t page = bt_r[b];
+  if (page < 0 || (int64_t)page >= num_pages) {
+    eflags |= SRKV_EFLAG_PAGE_RANGE;
+    return t;
   }
-  if (lane == 31) scratch[warp] = x;
-  __syncthreads();
-  if (warp == 0) {
-    int64_t w = lane < NW ? scratch[lane] : 0;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const int64_t y = __shfl_up_sync(0xffffffffu, w, o);
-      if (lane >= o) w += y;
-    }
-    if (lane < NW) scratch[lane] = w;
-  }
-  __syncthreads();
-  const int64_t before = warp > 0 ? scratch[warp - 1] : 0;
-  *total = scratch[NW - 1];
-  __syncthreads();
-  return before + x - v;
+  t.page = page;
+  t.block = b;
+  t.lo = lo;
+  t.hi = hi;
+  t.ie = ie;
+  t.ws = ws;
+  return t;
 }
 
-struct CtaRange {
-  int64_t T;      // positions of all units
+// Position i of list B: selected block sel_u[i], rows inside [INIT, W).  Entries that are
+// not candidates or not ascending are skipped and flagged.
+__device__ __forceinline__ PageTask resolve_b(const Geom& g, int32_t i, const int32_t* sel_u,
+                                              const int32_t* bt_r, int64_t num_pages,
+                                              int32_t INIT, uint32_t& eflags) {
+  PageTask t;
+  t.page = -1;
+  t.block = -1;
+  t.lo = t.hi = t.ie = t.ws = 0;
+  const int32_t b = sel_u[i];
+  if (!is_candidate(b, INIT, g.W) || (i > 0 && sel_u[i - 1] >= b)) {
+    eflags |= SRKV_EFLAG_SELECTION;
+    return t;
+  }
+  const int32_t base = b * kBlock;
+  const int32_t cnt = min(kBlock, g.L - base);
+  const int32_t lo = max(INIT - base, 0);
+  const int32_t hi = min(g.W - base, cnt);
+  if (lo >= hi) return t;
+  const int32_t page = bt_r[b];
+  if (page < 0 || (int64_t)page >= num_pages) {
+    eflags |= SRKV_EFLAG_PAGE_RANGE;
+    return t;
+  }
+  t.page = page;
+  t.block = b;
+  t.lo = lo;
+  t.hi = hi;
+  t.ie = hi;  // every loaded row is attended
+  t.ws = hi;
+  return t;
+}
+
+__device__ __forceinline__ Geom unit_geom(const DecodeArgs& a, int32_t u, uint32_t& eflags) {
+  return make_geom(a.seq_lens[u / a.Hkv], a.nsel[u], a.max_blocks, a.kmax, a.init_tokens,
+                   a.local_tokens, eflags);
+}
+
+// Geometry without the selection count (list A, readable before the selection exists).
+__device__ __forceinline__ Geom unit_geom_a(const DecodeArgs& a, int32_t u, uint32_t& eflags) {
+  return make_geom(a.seq_lens[u / a.Hkv], 0, a.max_blocks, a.kmax, a.init_tokens,
+                   a.local_tokens, eflags);
+}
+
+__device__ __forceinline__ int32_t list_count(const DecodeArgs& a, int list, int32_t u,
+                                              uint32_t& eflags) {
+  if (list == kListA) return list_a_count(unit_geom_a(a, u, eflags));
+  int32_t ns = a.nsel[u];
+  if (ns < 0 || ns > a.kmax) {
+    eflags |= SRKV_EFLAG_SELECTION;
+    ns = ns < 0 ? 0 : a.kmax;
+  }
+  return ns;
+}
+
+struct ListRange {
+  int64_t T;      // positions of the list over all units
   int64_t begin;  // this CTA's first position
   int64_t end;    // one past its last
   int32_t u0;     // unit holding `begin`
   int64_t base0;  // first position of unit u0
 };
 
-// Shared-memory scratch of the planner: NT/32 int64 + 2 int64.
-template <int NT>
-__device__ CtaRange plan_cta_range(const DecodeArgs& a, int64_t* scratch) {
+// Warp-level plan of one list for CTA `c` of `C`; every lane returns the same range.  When
+// `offsets` is not null the list's unit offsets [U + 1] are written (used by the combine).
+// When `prefix` is not null, prefix[k] receives the first position of the units of lane k's
+// chunk (chunk = ceil(U / 32) units) and prefix[32] the total.
+__device__ __forceinline__ ListRange warp_plan(const DecodeArgs& a, int list, int64_t c,
+                                               int64_t C, int64_t* offsets, int64_t* prefix,
+                                               uint32_t& eflags) {
+  const int lane = threadIdx.x & 31;
   const int32_t U = a.batch * a.Hkv;
-  const int32_t chunk = (U + NT - 1) / NT;
-  const int32_t u_lo = min(U, (int32_t)threadIdx.x * chunk);
-  const int32_t u_hi = min(U, u_lo + chunk);
-  uint32_t eflags = 0;
+  const int32_t chunk = (U + 31) / 32;
+  const int32_t u_lo = min(U, lane * chunk), u_hi = min(U, u_lo + chunk);
   int64_t local = 0;
-  for (int32_t u = u_lo; u < u_hi; ++u) {
-    const Geom g = make_geom(a.seq_lens[u / a.Hkv], a.nsel[u], a.max_blocks, a.kmax,
-                             a.init_tokens, a.local_tokens, eflags);
-    local += g.npos();
+  for (int32_t u = u_lo; u < u_hi; ++u) local += list_count(a, list, u, eflags);
+  int64_t incl = local;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int64_t y = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += y;
   }
-  int64_t T;
-  const int64_t excl = block_exclusive_scan64<NT>(local, scratch, &T);
-  CtaRange rg;
-  rg.T = T;
-  rg.begin = cta_begin(blockIdx.x, T, gridDim.x);
-  rg.end = cta_begin(blockIdx.x + 1, T, gridDim.x);
-  int64_t* s_found = scratch + NT / 32;  // [0] = u0, [1] = base0
-  if (rg.begin < rg.end && excl <= rg.begin && rg.begin < excl + local) {
+  const int64_t excl = incl - local;
+  ListRange rg;
+  rg.T = __shfl_sync(0xffffffffu, incl, 31);
+  if (prefix) {
+    prefix[lane] = excl;
+    if (lane == 31) prefix[32] = rg.T;
+  }
+  rg.begin = cta_begin(c, rg.T, C);
+  rg.end = cta_begin(c + 1, rg.T, C);
+  int32_t u0 = 0;
+  int64_t base0 = 0;
+  const bool mine = rg.begin < rg.end && excl <= rg.begin && rg.begin < excl + local;
+  if (mine || offsets) {
     int64_t pos = excl;
     uint32_t dummy = 0;
+    bool found = false;
     for (int32_t u = u_lo; u < u_hi; ++u) {
-      const Geom g = make_geom(a.seq_lens[u / a.Hkv], a.nsel[u], a.max_blocks, a.kmax,
-                               a.init_tokens, a.local_tokens, dummy);
-      if (rg.begin < pos + g.npos()) {
-        s_found[0] = u;
-        s_found[1] = pos;
-        break;
+      const int32_t n = list_count(a, list, u, dummy);
+      if (offsets) offsets[u] = pos;
+      if (mine && !found && rg.begin < pos + n) {
+        u0 = u;
+        base0 = pos;
+        found = true;
       }
-      pos += g.npos();
+      pos += n;
     }
+    if (offsets && lane == 31) offsets[U] = rg.T;
   }
-  if (blockIdx.x == 0) {  // unit tables for the combine pass
-    int32_t* unit_n = reinterpret_cast<int32_t*>(a.ws + a.lay.unit_n);
-    int64_t* unit_off = reinterpret_cast<int64_t*>(a.ws + a.lay.unit_off);
-    int64_t pos = excl;
-    uint32_t dummy = 0;
-    for (int32_t u = u_lo; u < u_hi; ++u) {
-      const Geom g = make_geom(a.seq_lens[u / a.Hkv], a.nsel[u], a.max_blocks, a.kmax,
-                               a.init_tokens, a.local_tokens, dummy);
-      unit_n[u] = g.npos();
-      unit_off[u] = pos;
-      pos += g.npos();
-    }
-    if (threadIdx.x == 0) unit_off[U] = T;
-    raise_flags(a.error_flags, eflags);
-  }
-  __syncthreads();
-  if (rg.begin < rg.end) {
-    rg.u0 = (int32_t)s_found[0];
-    rg.base0 = s_found[1];
-  } else {
-    rg.u0 = 0;
-    rg.base0 = 0;
-  }
+  const uint32_t who = __ballot_sync(0xffffffffu, mine);
+  const int src = who ? __ffs(who) - 1 : 0;
+  rg.u0 = __shfl_sync(0xffffffffu, u0, src);
+  rg.base0 = __shfl_sync(0xffffffffu, base0, src);
   return rg;
 }
 

@@ -9,9 +9,13 @@
 //
 // CTA = 1 producer warp + 8 consumer warps, one CTA per SM (persistent), each CTA owning
 // an equal share of all units' page lists (see decode_plan.cuh).
-//   producer: resolves 32 list positions at once (one per lane), then lane 0 streams the
-//             pages through a ring of stages (3 x 64 KiB for d = 128) with cp.async.bulk,
-//             completion counted on an mbarrier per stage;
+//   producer: plans list A (initial + window pages) and list B (selected pages) with
+//             warp-level scans, resolves 32 list positions at once (one per lane), and lane 0
+//             streams the pages through a ring of stages (3 x 64 KiB for d = 128) with
+//             cp.async.bulk, completion counted on an mbarrier per stage.  When the previous
+//             kernel is the scoring kernel, list A is streamed before that kernel finishes
+//             (programmatic launch) and the producer waits for the selection only before
+//             list B; a sentinel stage ends the consumers' loop;
 //   consumers: warp w owns rows [16w, 16w+16) of every page.  The group's queries are the
 //             N = 8 side of m16n8k16 bf16 MMAs, keys/values the M = 16 side:
 //               S^T[16 tok x 8 heads]  = K[16 x d] . Q^T[d x 8]
@@ -32,7 +36,7 @@ namespace {
 constexpr int kConsumerWarps = 8;
 constexpr int kThreads = (kConsumerWarps + 1) * 32;
 constexpr int kProducerWarp = kConsumerWarps;
-constexpr uint32_t kNewUnit = 1, kSegEnd = 2;
+constexpr uint32_t kNewUnit = 1, kSegEnd = 2, kBankB = 4, kLast = 8;
 
 struct StageInfo {
   int32_t unit;
@@ -59,8 +63,7 @@ struct Cfg {
   static constexpr size_t kOffInfo = kOffMerge + sizeof(float) * 4 * kMergeSlot;
   static constexpr size_t kOffBar = kOffInfo + sizeof(StageInfo) * kStages;
   // full[kStages], empty[kStages], merge w1, w2, r2
-  static constexpr size_t kOffScratch = kOffBar + sizeof(uint64_t) * (2 * kStages + 3);
-  static constexpr size_t kSmem = kOffScratch + sizeof(int64_t) * (kThreads / 32 + 2);
+  static constexpr size_t kSmem = kOffBar + sizeof(uint64_t) * (2 * kStages + 3);
 };
 
 struct Lane {
@@ -127,6 +130,59 @@ __device__ __forceinline__ int d_of(int g, int v) {
   return 8 * (g + 8 * (v >> 3)) + (v & 7);
 }
 
+// Hands stage `it` to the consumers: waits until it is free, writes its description and
+// arms its mbarrier with the bytes of the copies it starts (called by one producer lane).
+template <int D>
+__device__ __forceinline__ void issue_stage(const DecodeArgs& a, unsigned char* smem, int64_t it,
+                                            int32_t u, uint32_t fl, const PageTask& t,
+                                            int64_t& armed, bool& abort, uint32_t& eflags) {
+  using C = Cfg<D>;
+  if (abort) return;
+  StageInfo* sInfo = reinterpret_cast<StageInfo*>(smem + C::kOffInfo);
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::kOffBar);
+  uint64_t* empty = full + C::kStages;
+  const int s = (int)(it % C::kStages);
+  if (it >= C::kStages && !mbar_wait(&empty[s], (uint32_t)((it / C::kStages - 1) & 1))) {
+    abort = true;
+    eflags |= SRKV_EFLAG_TIMEOUT;
+    return;
+  }
+  StageInfo& inf = sInfo[s];
+  const bool load = t.page >= 0;
+  inf.unit = u;
+  inf.flags = (int32_t)fl;
+  inf.lo = load ? t.lo : 0;
+  inf.hi = load ? t.hi : 0;
+  inf.ie = t.ie;
+  inf.ws = t.ws;
+  const uint32_t rows = load ? (uint32_t)(t.hi - t.lo) : 0u;
+  const uint32_t slab_bytes = rows * D * 2;
+  const uint32_t qbytes = (uint32_t)(a.G * D * 2);
+  const uint32_t tx = 2 * slab_bytes + ((fl & kNewUnit) ? qbytes : 0u);
+  mbar_arrive_expect_tx(&full[s], tx);
+  ++armed;
+  if (u < 0) return;
+  const int32_t h = u % a.Hkv, r = u / a.Hkv;
+  if (rows) {
+    const int64_t src = (((int64_t)t.page * a.Hkv + h) * kBlock + t.lo) * D;
+    bulk_load(smem + C::kOffK + (size_t)s * C::kSlab + (size_t)t.lo * D * 2,
+              static_cast<const __nv_bfloat16*>(a.k_cache) + src, slab_bytes, &full[s]);
+    bulk_load(smem + C::kOffV + (size_t)s * C::kSlab + (size_t)t.lo * D * 2,
+              static_cast<const __nv_bfloat16*>(a.v_cache) + src, slab_bytes, &full[s]);
+  }
+  if (fl & kNewUnit)
+    bulk_load(smem + C::kOffQ + (size_t)s * C::kQBytes,
+              static_cast<const __nv_bfloat16*>(a.q) + ((int64_t)r * a.Hq + (int64_t)h * a.G) * D,
+              qbytes, &full[s]);
+}
+
+// One arrival per warp: the warp's lanes synchronise (ordering their shared-memory accesses)
+// and one lane arrives for all of them.
+__device__ __forceinline__ void warp_arrive(uint64_t* bar) {
+  __syncwarp();
+  if ((threadIdx.x & 31) == 0) mbar_arrive(bar);
+}
+
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1) split_mma_kernel(const DecodeArgs a) {
   using C = Cfg<D>;
@@ -141,132 +197,109 @@ __global__ void __launch_bounds__(kThreads, 1) split_mma_kernel(const DecodeArgs
   uint64_t* mb_w1 = empty + C::kStages;
   uint64_t* mb_w2 = mb_w1 + 1;
   uint64_t* mb_r2 = mb_w1 + 2;
-  int64_t* scratch = reinterpret_cast<int64_t*>(smem + C::kOffScratch);
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   griddep_launch_dependents();  // the combine may be scheduled now; it waits for this grid
   if (tid == 0) {
     for (int s = 0; s < C::kStages; ++s) {
       mbar_init(&full[s], 1);
-      mbar_init(&empty[s], kConsumerWarps * 32);
+      mbar_init(&empty[s], kConsumerWarps);  // one arrival per consumer warp
     }
-    mbar_init(mb_w1, 4 * 32);
-    mbar_init(mb_w2, 3 * 32);
-    mbar_init(mb_r2, 32);
+    mbar_init(mb_w1, 4);
+    mbar_init(mb_w2, 3);
+    mbar_init(mb_r2, 1);
     fence_mbar_init();
   }
   __syncthreads();
-  griddep_wait();  // the selection comes from the previous kernel in the stream
-
-  const CtaRange rg = plan_cta_range<kThreads>(a, scratch);
-  const int64_t npos = rg.end - rg.begin;
-  if (npos <= 0) return;
 
   if (warp == kProducerWarp) {
     // ------------------------------------------------------------------ producer
     uint32_t eflags = 0;
     bool abort = false;
-    int64_t issued = 0;  // positions handed to stages (uniform over the warp)
-    int64_t armed = 0;   // stages lane 0 actually armed
-    int32_t cu = rg.u0;              // walk state: unit and position within it
-    int64_t cj = rg.begin - rg.base0;
-    uint32_t dummy = 0;
-    Geom cg = make_geom(a.seq_lens[cu / a.Hkv], a.nsel[cu], a.max_blocks, a.kmax,
-                        a.init_tokens, a.local_tokens, dummy);
-    const int32_t qbytes = a.G * D * 2;
-    while (issued < npos && !abort) {
-      const int cnt = npos - issued < 32 ? (int)(npos - issued) : 32;
-      // Assign positions issued .. issued+cnt-1 to lanes (uniform walk).
-      int32_t my_u = 0, my_j = 0;
-      Geom my_g = cg;
-      uint32_t my_flags = 0;
-      for (int l = 0; l < cnt; ++l) {
-        while (cj >= cg.npos()) {  // next non-empty unit
-          ++cu;
-          cj = 0;
-          cg = make_geom(a.seq_lens[cu / a.Hkv], a.nsel[cu], a.max_blocks, a.kmax,
-                         a.init_tokens, a.local_tokens, dummy);
-        }
-        if (lane == l) {
-          my_u = cu;
-          my_j = (int32_t)cj;
-          my_g = cg;
-          const int64_t p = rg.begin + issued + l;
-          my_flags = ((cj == 0 || p == rg.begin) ? kNewUnit : 0u) |
-                     ((cj == cg.npos() - 1 || p == rg.end - 1) ? kSegEnd : 0u);
-        }
-        ++cj;
+    int64_t it = 0;     // stages handed out so far (uniform over the warp)
+    int64_t armed = 0;  // stages lane 0 armed
+    if (!a.early) griddep_wait();
+    for (int list = kListA; list <= kListB && !abort; ++list) {
+      if (list == kListB) {  // the selection must exist from here on
+        if (a.early) griddep_wait();
       }
-      PageTask task;
-      task.page = -1;
-      task.lo = task.hi = task.ie = task.ws = 0;
-      if (lane < cnt) {
-        const int32_t r = my_u / a.Hkv;
-        task = resolve_position(my_g, my_j, a.sel + (int64_t)my_u * a.kmax,
-                                a.block_table + (int64_t)r * a.max_blocks, a.num_pages,
-                                a.init_tokens, eflags);
-      }
-      for (int l = 0; l < cnt; ++l) {
-        const int32_t u = __shfl_sync(0xffffffffu, my_u, l);
-        const uint32_t fl = __shfl_sync(0xffffffffu, my_flags, l);
-        const int32_t page = __shfl_sync(0xffffffffu, task.page, l);
-        const int32_t lo = __shfl_sync(0xffffffffu, task.lo, l);
-        const int32_t hi = __shfl_sync(0xffffffffu, task.hi, l);
-        const int32_t ie = __shfl_sync(0xffffffffu, task.ie, l);
-        const int32_t ws = __shfl_sync(0xffffffffu, task.ws, l);
-        if (lane == 0 && !abort) {
-          const int64_t it = issued + l;
-          const int s = (int)(it % C::kStages);
-          if (it >= C::kStages &&
-              !mbar_wait(&empty[s], (uint32_t)((it / C::kStages - 1) & 1))) {
-            abort = true;
-            eflags |= SRKV_EFLAG_TIMEOUT;
-          } else {
-            StageInfo& inf = sInfo[s];
-            inf.unit = u;
-            inf.flags = (int32_t)fl;
-            const bool load = page >= 0;
-            inf.lo = load ? lo : 0;
-            inf.hi = load ? hi : 0;
-            inf.ie = ie;
-            inf.ws = ws;
-            const uint32_t rows = load ? (uint32_t)(hi - lo) : 0u;
-            const uint32_t slab_bytes = rows * D * 2;
-            const uint32_t tx = 2 * slab_bytes + ((fl & kNewUnit) ? (uint32_t)qbytes : 0u);
-            mbar_arrive_expect_tx(&full[s], tx);
-            ++armed;
-            const int32_t h = u % a.Hkv, r = u / a.Hkv;
-            if (rows) {
-              const int64_t src = (((int64_t)page * a.Hkv + h) * kBlock + lo) * D;
-              bulk_load(sK + (size_t)s * C::kSlab + (size_t)lo * D * 2,
-                        static_cast<const __nv_bfloat16*>(a.k_cache) + src, slab_bytes,
-                        &full[s]);
-              bulk_load(sV + (size_t)s * C::kSlab + (size_t)lo * D * 2,
-                        static_cast<const __nv_bfloat16*>(a.v_cache) + src, slab_bytes,
-                        &full[s]);
-            }
-            if (fl & kNewUnit)
-              bulk_load(sQ + (size_t)s * C::kQBytes,
-                        static_cast<const __nv_bfloat16*>(a.q) +
-                            ((int64_t)r * a.Hq + (int64_t)h * a.G) * D,
-                        (uint32_t)qbytes, &full[s]);
+      // CTA 0 leaves each list's unit offsets for the combine kernel.
+      int64_t* offsets = blockIdx.x == 0
+                             ? reinterpret_cast<int64_t*>(a.ws + (list == kListA ? a.lay.off_a
+                                                                                 : a.lay.off_b))
+                             : nullptr;
+      const ListRange rg = warp_plan(a, list, blockIdx.x, gridDim.x, offsets, nullptr, eflags);
+      const int64_t npos = rg.end - rg.begin;
+      if (npos <= 0) continue;
+      const uint32_t bank = list == kListB ? kBankB : 0u;
+      int32_t cu = rg.u0;  // walk state: unit and position within its list
+      int64_t cj = rg.begin - rg.base0;
+      uint32_t dummy = 0;
+      Geom cg = list == kListA ? unit_geom_a(a, cu, dummy) : unit_geom(a, cu, dummy);
+      int32_t cn = list == kListA ? list_a_count(cg) : cg.ns;
+      for (int64_t done = 0; done < npos && !abort; done += 32) {
+        const int cnt = npos - done < 32 ? (int)(npos - done) : 32;
+        // Assign positions done .. done+cnt-1 to lanes (uniform walk over the units).
+        int32_t my_u = 0, my_j = 0;
+        Geom my_g = cg;
+        uint32_t my_flags = 0;
+        for (int l = 0; l < cnt; ++l) {
+          while (cj >= cn) {
+            ++cu;
+            cj = 0;
+            cg = list == kListA ? unit_geom_a(a, cu, dummy) : unit_geom(a, cu, dummy);
+            cn = list == kListA ? list_a_count(cg) : cg.ns;
           }
+          const int64_t p = rg.begin + done + l;
+          if (lane == l) {
+            my_u = cu;
+            my_j = (int32_t)cj;
+            my_g = cg;
+            my_flags = bank | ((cj == 0 || p == rg.begin) ? kNewUnit : 0u) |
+                       ((cj == cn - 1 || p == rg.end - 1) ? kSegEnd : 0u);
+          }
+          ++cj;
         }
-        abort = __shfl_sync(0xffffffffu, abort, 0);
+        PageTask task;
+        task.page = -1;
+        task.lo = task.hi = task.ie = task.ws = 0;
+        if (lane < cnt) {
+          const int32_t* bt_r = a.block_table + (int64_t)(my_u / a.Hkv) * a.max_blocks;
+          task = list == kListA
+                     ? resolve_a(my_g, my_j, bt_r, a.num_pages, eflags)
+                     : resolve_b(my_g, my_j, a.sel + (int64_t)my_u * a.kmax, bt_r, a.num_pages,
+                                 a.init_tokens, eflags);
+        }
+        for (int l = 0; l < cnt; ++l) {
+          PageTask t;
+          const int32_t u = __shfl_sync(0xffffffffu, my_u, l);
+          const uint32_t fl = __shfl_sync(0xffffffffu, my_flags, l);
+          t.page = __shfl_sync(0xffffffffu, task.page, l);
+          t.lo = __shfl_sync(0xffffffffu, task.lo, l);
+          t.hi = __shfl_sync(0xffffffffu, task.hi, l);
+          t.ie = __shfl_sync(0xffffffffu, task.ie, l);
+          t.ws = __shfl_sync(0xffffffffu, task.ws, l);
+          if (lane == 0) issue_stage<D>(a, smem, it, u, fl, t, armed, abort, eflags);
+          abort = __shfl_sync(0xffffffffu, abort, 0);
+          ++it;
+        }
       }
-      issued += cnt;
     }
-    eflags = __reduce_or_sync(0xffffffffu, eflags);
     if (lane == 0) {
+      PageTask none;
+      none.page = -1;
+      none.lo = none.hi = none.ie = none.ws = 0;
+      issue_stage<D>(a, smem, it, -1, kLast, none, armed, abort, eflags);  // sentinel
       // Drain: every copy this CTA issued must land before the CTA exits.
       const int64_t first = armed > C::kStages ? armed - C::kStages : 0;
-      for (int64_t it = first; it < armed; ++it)
-        if (!mbar_wait(&full[it % C::kStages], (uint32_t)((it / C::kStages) & 1))) {
+      for (int64_t i = first; i < armed; ++i)
+        if (!mbar_wait(&full[i % C::kStages], (uint32_t)((i / C::kStages) & 1))) {
           eflags |= SRKV_EFLAG_TIMEOUT;
           break;
         }
-      raise_flags(a.error_flags, eflags);
     }
+    eflags = __reduce_or_sync(0xffffffffu, eflags);
+    if (lane == 0) raise_flags(a.error_flags, eflags);
     return;
   }
 
@@ -280,15 +313,14 @@ __global__ void __launch_bounds__(kThreads, 1) split_mma_kernel(const DecodeArgs
   for (int j = 0; j < C::KJ; ++j) qb[j][0] = qb[j][1] = qb[j][2] = qb[j][3] = 0u;
   bool abort = false;
   int32_t merges = 0;
-
-  for (int64_t it = 0; it < npos; ++it) {
+  for (int64_t it = 0;; ++it) {
     const int s = (int)(it % C::kStages);
-    if (!abort && !mbar_wait(&full[s], (uint32_t)((it / C::kStages) & 1))) {
-      abort = true;
+    if (!mbar_wait(&full[s], (uint32_t)((it / C::kStages) & 1))) {
       if (lane == 0) raise_flags(a.error_flags, SRKV_EFLAG_TIMEOUT);
+      break;
     }
-    if (abort) break;
     const StageInfo inf = sInfo[s];
+    if (inf.flags & kLast) break;
     if (inf.flags & kNewUnit) {
       st.reset();
       const unsigned char* q = sQ + (size_t)s * C::kQBytes;
@@ -380,7 +412,7 @@ __global__ void __launch_bounds__(kThreads, 1) split_mma_kernel(const DecodeArgs
       }
     }
     // release the stage
-    mbar_arrive(&empty[s]);
+    warp_arrive(&empty[s]);
 
     if (inf.flags & kSegEnd) {
       // ---- reduce the per-lane sums, merge the 8 warps, write the partial
@@ -393,19 +425,20 @@ __global__ void __launch_bounds__(kThreads, 1) split_mma_kernel(const DecodeArgs
       if (warp >= 4) {
         if (merges > 0 && !mbar_wait(mb_r2, ph ^ 1u)) abort = true;
         st.store(sMerge + (warp - 4) * C::kMergeSlot, lane);
-        mbar_arrive(mb_w1);
+        warp_arrive(mb_w1);
       } else {
         if (!mbar_wait(mb_w1, ph)) abort = true;
         st.merge_from(sMerge + warp * C::kMergeSlot, lane);
         if (warp >= 1) {
           st.store(sMerge + warp * C::kMergeSlot, lane);
-          mbar_arrive(mb_w2);
+          warp_arrive(mb_w2);
         } else {
           if (!mbar_wait(mb_w2, ph)) abort = true;
           for (int w = 1; w < 4; ++w) st.merge_from(sMerge + w * C::kMergeSlot, lane);
-          mbar_arrive(mb_r2);
-          // warp 0 writes the partial of (unit, this CTA)
-          const int64_t slot = (int64_t)inf.unit + blockIdx.x;
+          warp_arrive(mb_r2);
+          // warp 0 writes the partial of (unit, this CTA) into the list's bank
+          const int64_t slot = ((inf.flags & kBankB) ? (int64_t)a.lay.bank : 0) + inf.unit +
+                               blockIdx.x;
           float* accp = reinterpret_cast<float*>(a.ws + a.lay.acc) + slot * a.G * D;
           float* mlp = reinterpret_cast<float*>(a.ws + a.lay.ml) + slot * a.G * 2;
           const int h0 = 2 * ln.t, h1 = h0 + 1;

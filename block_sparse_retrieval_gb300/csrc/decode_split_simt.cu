@@ -6,7 +6,8 @@
 // Attention is softmax(q K^T / sqrt(d)) V over the attended rows of each page (ATB reuse
 // article, §1.1), accumulated in fp32 with an online max in the log2 domain.
 //
-// CTA = 4 warps.  Thread 0 resolves each list position; every warp takes rows w, w+4, ...
+// CTA = 4 warps.  Warp 0 plans each list, thread 0 resolves its positions one by one; every
+// warp takes rows w, w+4, ...
 // of the page, a lane holds d/32 elements of q (every head of the group), K and V, and one
 // warp reduction per head gives each logit.  At the end of a unit's segment the warps merge
 // through shared memory and warp 0 writes the partial to slot unit + CTA.
@@ -33,7 +34,7 @@ __device__ __forceinline__ float ld_elem<__nv_bfloat16>(const __nv_bfloat16* p) 
 template <typename T, int D>
 __global__ void __launch_bounds__(kThreads) split_simt_kernel(const DecodeArgs a) {
   constexpr int E = D / 32;  // elements per lane
-  __shared__ int64_t scratch[kThreads / 32 + 2];
+  __shared__ ListRange s_rg;
   __shared__ PageTask s_task;
   __shared__ int32_t s_unit;
   __shared__ uint32_t s_flags;
@@ -43,119 +44,137 @@ __global__ void __launch_bounds__(kThreads) split_simt_kernel(const DecodeArgs a
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   griddep_launch_dependents();
   griddep_wait();
-  const CtaRange rg = plan_cta_range<kThreads>(a, scratch);
-  const int64_t npos = rg.end - rg.begin;
-  if (npos <= 0) return;
   const int G = a.G;
-
+  uint32_t eflags = 0;
   float q[kGMax][E], acc[kGMax][E], m[kGMax], l[kGMax];
-  int32_t cu = rg.u0;
-  int64_t cj = rg.begin - rg.base0;
-  uint32_t eflags = 0, dummy = 0;
-  Geom cg = make_geom(a.seq_lens[cu / a.Hkv], a.nsel[cu], a.max_blocks, a.kmax, a.init_tokens,
-                      a.local_tokens, dummy);
 
-  for (int64_t it = 0; it < npos; ++it) {
-    __syncthreads();  // previous position fully consumed
-    if (tid == 0) {
-      while (cj >= cg.npos()) {
-        ++cu;
-        cj = 0;
-        cg = make_geom(a.seq_lens[cu / a.Hkv], a.nsel[cu], a.max_blocks, a.kmax, a.init_tokens,
-                       a.local_tokens, dummy);
-      }
-      const int64_t p = rg.begin + it;
-      s_unit = cu;
-      s_flags = ((cj == 0 || p == rg.begin) ? 1u : 0u) |
-                ((cj == cg.npos() - 1 || p == rg.end - 1) ? 2u : 0u);
-      s_task = resolve_position(cg, (int32_t)cj, a.sel + (int64_t)cu * a.kmax,
-                                a.block_table + (int64_t)(cu / a.Hkv) * a.max_blocks,
-                                a.num_pages, a.init_tokens, eflags);
-      ++cj;
+  for (int list = kListA; list <= kListB; ++list) {
+    if (warp == 0) {
+      int64_t* offsets = blockIdx.x == 0
+                             ? reinterpret_cast<int64_t*>(a.ws + (list == kListA ? a.lay.off_a
+                                                                                 : a.lay.off_b))
+                             : nullptr;
+      const ListRange rg = warp_plan(a, list, blockIdx.x, gridDim.x, offsets, nullptr, eflags);
+      if (lane == 0) s_rg = rg;
     }
     __syncthreads();
-    const int32_t u = s_unit;
-    const uint32_t flags = s_flags;
-    const PageTask task = s_task;
-    const int32_t r = u / a.Hkv, h = u % a.Hkv;
-
-    if (flags & 1u) {  // new unit: queries of the group, fresh state
-      const T* qp = static_cast<const T*>(a.q) + ((int64_t)r * a.Hq + (int64_t)h * G) * D;
-#pragma unroll
-      for (int j = 0; j < kGMax; ++j) {
-        m[j] = -INFINITY;
-        l[j] = 0.f;
-#pragma unroll
-        for (int e = 0; e < E; ++e) {
-          acc[j][e] = 0.f;
-          q[j][e] = j < G ? ld_elem<T>(qp + (int64_t)j * D + lane + 32 * e) : 0.f;
-        }
-      }
+    const ListRange rg = s_rg;
+    const int64_t npos = rg.end - rg.begin;
+    int32_t cu = rg.u0;
+    int64_t cj = rg.begin - rg.base0;
+    uint32_t dummy = 0;
+    Geom cg;
+    int32_t cn = 0;
+    if (tid == 0 && npos > 0) {
+      cg = list == kListA ? unit_geom_a(a, cu, dummy) : unit_geom(a, cu, dummy);
+      cn = list == kListA ? list_a_count(cg) : cg.ns;
     }
-    if (task.page >= 0) {
-      const int64_t slab = ((int64_t)task.page * a.Hkv + h) * kBlock * D;
-      const T* kp = static_cast<const T*>(a.k_cache) + slab;
-      const T* vp = static_cast<const T*>(a.v_cache) + slab;
-      for (int row = task.lo + warp; row < task.hi; row += kWarps) {
-        if (!(row < task.ie || row >= task.ws)) continue;
-        float kv[E];
-#pragma unroll
-        for (int e = 0; e < E; ++e) kv[e] = ld_elem<T>(kp + (int64_t)row * D + lane + 32 * e);
-        float vv[E];
-#pragma unroll
-        for (int e = 0; e < E; ++e) vv[e] = ld_elem<T>(vp + (int64_t)row * D + lane + 32 * e);
+    for (int64_t it = 0; it < npos; ++it) {
+      __syncthreads();  // previous position fully consumed
+      if (tid == 0) {
+        while (cj >= cn) {
+          ++cu;
+          cj = 0;
+          cg = list == kListA ? unit_geom_a(a, cu, dummy) : unit_geom(a, cu, dummy);
+          cn = list == kListA ? list_a_count(cg) : cg.ns;
+        }
+        const int64_t p = rg.begin + it;
+        s_unit = cu;
+        s_flags = ((cj == 0 || p == rg.begin) ? 1u : 0u) |
+                  ((cj == cn - 1 || p == rg.end - 1) ? 2u : 0u);
+        const int32_t* bt_r = a.block_table + (int64_t)(cu / a.Hkv) * a.max_blocks;
+        s_task = list == kListA
+                     ? resolve_a(cg, (int32_t)cj, bt_r, a.num_pages, eflags)
+                     : resolve_b(cg, (int32_t)cj, a.sel + (int64_t)cu * a.kmax, bt_r,
+                                 a.num_pages, a.init_tokens, eflags);
+        ++cj;
+      }
+      __syncthreads();
+      const int32_t u = s_unit;
+      const uint32_t flags = s_flags;
+      const PageTask task = s_task;
+      const int32_t r = u / a.Hkv, h = u % a.Hkv;
+
+      if (flags & 1u) {  // new segment: queries of the group, fresh state
+        const T* qp = static_cast<const T*>(a.q) + ((int64_t)r * a.Hq + (int64_t)h * G) * D;
 #pragma unroll
         for (int j = 0; j < kGMax; ++j) {
-          if (j >= G) break;
-          float s = 0.f;
+          m[j] = -INFINITY;
+          l[j] = 0.f;
 #pragma unroll
-          for (int e = 0; e < E; ++e) s += q[j][e] * kv[e];
+          for (int e = 0; e < E; ++e) {
+            acc[j][e] = 0.f;
+            q[j][e] = j < G ? ld_elem<T>(qp + (int64_t)j * D + lane + 32 * e) : 0.f;
+          }
+        }
+      }
+      if (task.page >= 0) {
+        const int64_t slab = ((int64_t)task.page * a.Hkv + h) * kBlock * D;
+        const T* kp = static_cast<const T*>(a.k_cache) + slab;
+        const T* vp = static_cast<const T*>(a.v_cache) + slab;
+        for (int row = task.lo + warp; row < task.hi; row += kWarps) {
+          if (!(row < task.ie || row >= task.ws)) continue;
+          float kv[E];
 #pragma unroll
-          for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
-          s *= a.scale_log2;
-          const float mn = fmaxf(m[j], s);
-          const float alpha = exp2f(m[j] - mn);
-          const float p = exp2f(s - mn);
-          m[j] = mn;
-          l[j] = l[j] * alpha + p;
+          for (int e = 0; e < E; ++e) kv[e] = ld_elem<T>(kp + (int64_t)row * D + lane + 32 * e);
+          float vv[E];
 #pragma unroll
-          for (int e = 0; e < E; ++e) acc[j][e] = acc[j][e] * alpha + p * vv[e];
+          for (int e = 0; e < E; ++e) vv[e] = ld_elem<T>(vp + (int64_t)row * D + lane + 32 * e);
+#pragma unroll
+          for (int j = 0; j < kGMax; ++j) {
+            if (j >= G) break;
+            float sc = 0.f;
+#pragma unroll
+            for (int e = 0; e < E; ++e) sc += q[j][e] * kv[e];
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) sc += __shfl_xor_sync(0xffffffffu, sc, o);
+            sc *= a.scale_log2;
+            const float mn = fmaxf(m[j], sc);
+            const float alpha = exp2f(m[j] - mn);
+            const float p = exp2f(sc - mn);
+            m[j] = mn;
+            l[j] = l[j] * alpha + p;
+#pragma unroll
+            for (int e = 0; e < E; ++e) acc[j][e] = acc[j][e] * alpha + p * vv[e];
+          }
+        }
+      }
+      if (flags & 2u) {  // end of the unit's segment: merge the warps, write the partial
+        if (lane == 0)
+          for (int j = 0; j < G; ++j) {
+            s_m[warp][j] = m[j];
+            s_l[warp][j] = l[j];
+          }
+        for (int j = 0; j < G; ++j)
+#pragma unroll
+          for (int e = 0; e < E; ++e) s_acc[warp][j][lane + 32 * e] = acc[j][e];
+        __syncthreads();
+        const int64_t slot = (list == kListB ? (int64_t)a.lay.bank : 0) + u + blockIdx.x;
+        float* accp = reinterpret_cast<float*>(a.ws + a.lay.acc) + slot * G * D;
+        float* mlp = reinterpret_cast<float*>(a.ws + a.lay.ml) + slot * G * 2;
+        for (int idx = tid; idx < G * D; idx += kThreads) {
+          const int j = idx / D, e = idx % D;
+          float mx = -INFINITY;
+          for (int w = 0; w < kWarps; ++w) mx = fmaxf(mx, s_m[w][j]);
+          const float base = mx == -INFINITY ? 0.f : mx;
+          float num = 0.f, den = 0.f;
+          for (int w = 0; w < kWarps; ++w) {
+            const float f = exp2f(s_m[w][j] - base);
+            num += f * s_acc[w][j][e];
+            den += f * s_l[w][j];
+          }
+          accp[idx] = num;
+          if (e == 0) {
+            mlp[j * 2 + 0] = mx;
+            mlp[j * 2 + 1] = den;
+          }
         }
       }
     }
-    if (flags & 2u) {  // end of the unit's segment: merge the warps, write the partial
-      if (lane == 0)
-        for (int j = 0; j < G; ++j) {
-          s_m[warp][j] = m[j];
-          s_l[warp][j] = l[j];
-        }
-      for (int j = 0; j < G; ++j)
-#pragma unroll
-        for (int e = 0; e < E; ++e) s_acc[warp][j][lane + 32 * e] = acc[j][e];
-      __syncthreads();
-      const int64_t slot = (int64_t)u + blockIdx.x;
-      float* accp = reinterpret_cast<float*>(a.ws + a.lay.acc) + slot * G * D;
-      float* mlp = reinterpret_cast<float*>(a.ws + a.lay.ml) + slot * G * 2;
-      for (int idx = tid; idx < G * D; idx += kThreads) {
-        const int j = idx / D, e = idx % D;
-        float mx = -INFINITY;
-        for (int w = 0; w < kWarps; ++w) mx = fmaxf(mx, s_m[w][j]);
-        const float base = mx == -INFINITY ? 0.f : mx;
-        float num = 0.f, den = 0.f;
-        for (int w = 0; w < kWarps; ++w) {
-          const float f = exp2f(s_m[w][j] - base);
-          num += f * s_acc[w][j][e];
-          den += f * s_l[w][j];
-        }
-        accp[idx] = num;
-        if (e == 0) {
-          mlp[j * 2 + 0] = mx;
-          mlp[j * 2 + 1] = den;
-        }
-      }
-    }
+    __syncthreads();
   }
-  if (tid == 0) raise_flags(a.error_flags, eflags);
+  eflags = __reduce_or_sync(0xffffffffu, eflags);
+  if (lane == 0) raise_flags(a.error_flags, eflags);
 }
 
 template <typename T, int D>

@@ -25,7 +25,7 @@
 namespace srkv {
 namespace {
 
-constexpr int kThreads = 512;
+constexpr int kThreads = 256;  // a decode CTA (48K registers) still fits beside one
 constexpr int kWarps = kThreads / 32;
 constexpr int kMaxDynamicSmem = 200 * 1024;  // keys + pages of up to 25600 blocks
 
@@ -45,16 +45,6 @@ struct ScoreArgs {
   int32_t init_tokens, local_tokens, dense_boundary;
   double topk_percent;
 };
-
-// k = min(n, ceil(p*n - 1e-9)) with separately rounded operations (no contraction), so
-// that the host and the device agree on every n.
-__device__ __forceinline__ int32_t device_topk_count(int32_t n, double p) {
-  if (n <= 0) return 0;
-  const double x = ceil(__dadd_rn(__dmul_rn(p, (double)n), -1e-9));
-  if (!(x > 0.0)) return 0;
-  if (x > (double)n) return n;
-  return (int32_t)x;
-}
 
 __device__ __forceinline__ uint32_t score_key(float s) {
   if (s != s) return 0u;            // NaN ranks below everything
@@ -320,19 +310,22 @@ template <typename T, int D>
 cudaError_t launch(const ScoreArgs& a, int32_t units, int32_t cluster, cudaStream_t s) {
   const size_t smem = sizeof(uint32_t) * 2 * (size_t)a.max_blocks;
   auto kernel = score_topk_kernel<T, D>;
-  if (smem > 48 * 1024) {
-    // Raised once per device to the largest size the host checks allow.
-    static bool configured[128] = {false};
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
+  // Once per device: the largest dynamic shared memory the host checks allow, and the full
+  // shared-memory carveout, so that an SM running this kernel keeps room for a decode CTA
+  // launched early behind it (programmatic launch).
+  static bool configured[128] = {false};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 128) return cudaErrorInvalidDevice;
+  if (!configured[dev]) {
+    e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             kMaxDynamicSmem);
     if (e != cudaSuccess) return e;
-    if (dev < 0 || dev >= 128) return cudaErrorInvalidDevice;
-    if (!configured[dev]) {
-      e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               kMaxDynamicSmem);
-      if (e != cudaSuccess) return e;
-      configured[dev] = true;
-    }
+    e = cudaFuncSetAttribute(kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
+                             cudaSharedmemCarveoutMaxShared);
+    if (e != cudaSuccess) return e;
+    configured[dev] = true;
   }
   cudaLaunchConfig_t lc = {};
   lc.gridDim = dim3((unsigned)(units * cluster));

@@ -28,8 +28,6 @@ bool config_ok(const srkv_config* c) {
   return true;
 }
 
-size_t elem_bytes(const srkv_config& c) { return c.dtype == SRKV_BF16 ? 2 : 4; }
-
 int32_t sm_count() {
   static int32_t cache[128] = {0};
   int dev = 0;
@@ -58,6 +56,101 @@ int64_t host_num_candidates(const srkv_config& c, int64_t L) {
   const int64_t W = L - c.local_tokens;
   if (W <= c.init_tokens) return 0;
   return (W + kBlock - 1) / kBlock - c.init_tokens / kBlock;
+}
+
+int32_t host_kmax_bound(const srkv_config& c, int32_t max_blocks) {
+  const int64_t n = host_num_candidates(c, (int64_t)max_blocks * kBlock);
+  return (int32_t)(c.dense_boundary > 0 ? n : host_topk_count(n, c.topk_percent));
+}
+
+size_t workspace_size(const srkv_config* cfg, int32_t batch) {
+  if (!config_ok(cfg) || batch < 0) return 0;
+  const int64_t units = (int64_t)batch * cfg->num_kv_heads;
+  if (units > INT32_MAX - kMaxCtas) return 0;
+  const int32_t G = cfg->num_q_heads / cfg->num_kv_heads;
+  return ws_layout((int32_t)units, kMaxCtas, G, cfg->head_dim).total;
+}
+
+// Checks the decode arguments and fills `a`; SRKV_OK means there is work to launch.
+srkv_status prepare_decode(const srkv_config* cfg, const void* q, const void* k_cache,
+                           const void* v_cache, int64_t num_pages, const int32_t* block_table,
+                           int32_t max_blocks, const int32_t* seq_lens, int32_t batch,
+                           const int32_t* sel, int32_t kmax, const int32_t* nsel, void* out,
+                           void* workspace, size_t workspace_bytes, int32_t* error_flags,
+                           DecodeArgs& a) {
+  if (!config_ok(cfg) || batch < 0 || max_blocks <= 0 || max_blocks > kMaxBlocks || kmax < 0 ||
+      num_pages < 0)
+    return SRKV_ERR_INVALID_ARG;
+  if (batch == 0) return SRKV_OK;
+  if (!q || !k_cache || !v_cache || !block_table || !seq_lens || !nsel || !out || num_pages == 0)
+    return SRKV_ERR_INVALID_ARG;
+  if (kmax > 0 && !sel) return SRKV_ERR_INVALID_ARG;
+  if (!aligned(q, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) || !aligned(out, 16))
+    return SRKV_ERR_INVALID_ARG;
+  const int32_t G = cfg->num_q_heads / cfg->num_kv_heads;
+  const bool mma = mma_split_supported(*cfg);
+  if (!mma && G > 16) return SRKV_ERR_UNSUPPORTED;
+  const size_t need = workspace_size(cfg, batch);
+  if (need == 0) return SRKV_ERR_UNSUPPORTED;
+  if (!workspace || workspace_bytes < need || !aligned(workspace, 256)) return SRKV_ERR_WORKSPACE;
+  const int32_t sms = sm_count();
+  if (sms <= 0) return SRKV_ERR_CUDA;
+
+  a.q = q;
+  a.k_cache = k_cache;
+  a.v_cache = v_cache;
+  a.num_pages = num_pages;
+  a.block_table = block_table;
+  a.max_blocks = max_blocks;
+  a.seq_lens = seq_lens;
+  a.batch = batch;
+  a.sel = sel;
+  a.kmax = kmax;
+  a.nsel = nsel;
+  a.out = out;
+  a.ws = static_cast<char*>(workspace);
+  a.error_flags = error_flags;
+  a.Hq = cfg->num_q_heads;
+  a.Hkv = cfg->num_kv_heads;
+  a.G = G;
+  a.d = cfg->head_dim;
+  a.init_tokens = cfg->init_tokens;
+  a.local_tokens = cfg->local_tokens;
+  a.scale_log2 = kLog2e / sqrtf((float)cfg->head_dim);
+  a.ctas = mma ? mma_split_ctas(sms) : simt_split_ctas(sms);
+  if (a.ctas > kMaxCtas) a.ctas = kMaxCtas;
+  a.lay = ws_layout(batch * cfg->num_kv_heads, kMaxCtas, G, cfg->head_dim);
+  a.early = 0;
+  return SRKV_OK;
+}
+
+// Launches the split kernel and the combine.  early = 1 only when the previous kernel in
+// the stream is this library's scoring kernel: list A then streams before that kernel
+// finishes (it writes only sel and nsel).
+srkv_status launch_decode(const srkv_config* cfg, DecodeArgs& a, int32_t early,
+                          cudaStream_t s) {
+  a.early = early;
+  const cudaError_t e = mma_split_supported(*cfg) ? launch_split_mma(a, s)
+                                                  : launch_split_simt(a, cfg->dtype, s);
+  if (e != cudaSuccess) return SRKV_ERR_CUDA;
+  return cuda_status(launch_combine(a, cfg->dtype, s));
+}
+
+srkv_status check_score(const srkv_config* cfg, const void* q, const float* reps,
+                        int64_t num_pages, const int32_t* block_table, int32_t max_blocks,
+                        const int32_t* seq_lens, int32_t batch, const int32_t* sel,
+                        int32_t kmax, const int32_t* nsel) {
+  if (!config_ok(cfg) || batch < 0 || max_blocks <= 0 || max_blocks > kMaxBlocks || kmax < 0 ||
+      num_pages < 0)
+    return SRKV_ERR_INVALID_ARG;
+  if (batch == 0) return SRKV_OK;
+  if (!q || !reps || !block_table || !seq_lens || !sel || !nsel || num_pages == 0)
+    return SRKV_ERR_INVALID_ARG;
+  if (!aligned(q, 16) || !aligned(reps, 16)) return SRKV_ERR_INVALID_ARG;
+  if (kmax < host_kmax_bound(*cfg, max_blocks)) return SRKV_ERR_INVALID_ARG;
+  if ((int64_t)batch * cfg->num_kv_heads > INT32_MAX) return SRKV_ERR_UNSUPPORTED;
+  if ((size_t)max_blocks * 8 > 200 * 1024) return SRKV_ERR_UNSUPPORTED;  // keys + pages on chip
+  return SRKV_OK;
 }
 
 }  // namespace
@@ -102,8 +195,7 @@ int64_t srkv_num_candidates(const srkv_config* cfg, int64_t seq_len) {
 
 int32_t srkv_kmax_bound(const srkv_config* cfg, int32_t max_blocks) {
   if (!config_ok(cfg) || max_blocks <= 0) return 0;
-  const int64_t n = host_num_candidates(*cfg, (int64_t)max_blocks * kBlock);
-  return (int32_t)(cfg->dense_boundary > 0 ? n : host_topk_count(n, cfg->topk_percent));
+  return host_kmax_bound(*cfg, max_blocks);
 }
 
 srkv_status srkv_build_block_reps(const srkv_config* cfg, const void* k_cache,
@@ -125,27 +217,16 @@ srkv_status srkv_score_topk(const srkv_config* cfg, const void* q, const float* 
                             const int32_t* seq_lens, const int32_t* prompt_lens, int32_t batch,
                             int32_t* sel, int32_t kmax, int32_t* nsel, int32_t* error_flags,
                             srkv_stream stream) {
-  if (!config_ok(cfg) || batch < 0 || max_blocks <= 0 || max_blocks > kMaxBlocks || kmax < 0 ||
-      num_pages < 0)
-    return SRKV_ERR_INVALID_ARG;
-  if (batch == 0) return SRKV_OK;
-  if (!q || !reps || !block_table || !seq_lens || !sel || !nsel || num_pages == 0)
-    return SRKV_ERR_INVALID_ARG;
-  if (!aligned(q, 16) || !aligned(reps, 16)) return SRKV_ERR_INVALID_ARG;
-  if (kmax < srkv_kmax_bound(cfg, max_blocks)) return SRKV_ERR_INVALID_ARG;
-  if ((int64_t)batch * cfg->num_kv_heads > INT32_MAX) return SRKV_ERR_UNSUPPORTED;
-  if ((size_t)max_blocks * 8 > 200 * 1024) return SRKV_ERR_UNSUPPORTED;  // keys + pages on chip
+  const srkv_status st = check_score(cfg, q, reps, num_pages, block_table, max_blocks, seq_lens,
+                                     batch, sel, kmax, nsel);
+  if (st != SRKV_OK || batch == 0) return st;
   return cuda_status(launch_score_topk(*cfg, q, reps, num_pages, block_table, max_blocks,
                                        seq_lens, prompt_lens, batch, sel, kmax, nsel,
                                        error_flags, (cudaStream_t)stream));
 }
 
 size_t srkv_decode_workspace_size(const srkv_config* cfg, int32_t batch) {
-  if (!config_ok(cfg) || batch < 0) return 0;
-  const int64_t units = (int64_t)batch * cfg->num_kv_heads;
-  if (units > INT32_MAX - kMaxCtas) return 0;
-  const int32_t G = cfg->num_q_heads / cfg->num_kv_heads;
-  return ws_layout((int32_t)units, kMaxCtas, G, cfg->head_dim).total;
+  return workspace_size(cfg, batch);
 }
 
 srkv_status srkv_sparse_paged_decode(const srkv_config* cfg, const void* q, const void* k_cache,
@@ -155,54 +236,12 @@ srkv_status srkv_sparse_paged_decode(const srkv_config* cfg, const void* q, cons
                                      const int32_t* sel, int32_t kmax, const int32_t* nsel,
                                      void* out, void* workspace, size_t workspace_bytes,
                                      int32_t* error_flags, srkv_stream stream) {
-  if (!config_ok(cfg) || batch < 0 || max_blocks <= 0 || max_blocks > kMaxBlocks || kmax < 0 ||
-      num_pages < 0)
-    return SRKV_ERR_INVALID_ARG;
-  if (batch == 0) return SRKV_OK;
-  if (!q || !k_cache || !v_cache || !block_table || !seq_lens || !nsel || !out || num_pages == 0)
-    return SRKV_ERR_INVALID_ARG;
-  if (kmax > 0 && !sel) return SRKV_ERR_INVALID_ARG;
-  if (!aligned(q, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) || !aligned(out, 16))
-    return SRKV_ERR_INVALID_ARG;
-  const int32_t G = cfg->num_q_heads / cfg->num_kv_heads;
-  const bool mma = mma_split_supported(*cfg);
-  if (!mma && G > 16) return SRKV_ERR_UNSUPPORTED;
-  const size_t need = srkv_decode_workspace_size(cfg, batch);
-  if (need == 0) return SRKV_ERR_UNSUPPORTED;
-  if (!workspace || workspace_bytes < need || !aligned(workspace, 256)) return SRKV_ERR_WORKSPACE;
-  const int32_t sms = sm_count();
-  if (sms <= 0) return SRKV_ERR_CUDA;
-
   DecodeArgs a;
-  a.q = q;
-  a.k_cache = k_cache;
-  a.v_cache = v_cache;
-  a.num_pages = num_pages;
-  a.block_table = block_table;
-  a.max_blocks = max_blocks;
-  a.seq_lens = seq_lens;
-  a.batch = batch;
-  a.sel = sel;
-  a.kmax = kmax;
-  a.nsel = nsel;
-  a.out = out;
-  a.ws = static_cast<char*>(workspace);
-  a.error_flags = error_flags;
-  a.Hq = cfg->num_q_heads;
-  a.Hkv = cfg->num_kv_heads;
-  a.G = G;
-  a.d = cfg->head_dim;
-  a.init_tokens = cfg->init_tokens;
-  a.local_tokens = cfg->local_tokens;
-  a.scale_log2 = kLog2e / sqrtf((float)cfg->head_dim);
-  a.ctas = mma ? mma_split_ctas(sms) : simt_split_ctas(sms);
-  if (a.ctas > kMaxCtas) a.ctas = kMaxCtas;
-  a.lay = ws_layout(batch * cfg->num_kv_heads, kMaxCtas, G, cfg->head_dim);
-
-  cudaStream_t s = (cudaStream_t)stream;
-  cudaError_t e = mma ? launch_split_mma(a, s) : launch_split_simt(a, cfg->dtype, s);
-  if (e != cudaSuccess) return SRKV_ERR_CUDA;
-  return cuda_status(launch_combine(a, cfg->dtype, s));
+  const srkv_status st = prepare_decode(cfg, q, k_cache, v_cache, num_pages, block_table,
+                                        max_blocks, seq_lens, batch, sel, kmax, nsel, out,
+                                        workspace, workspace_bytes, error_flags, a);
+  if (st != SRKV_OK || batch == 0) return st;
+  return launch_decode(cfg, a, 0, (cudaStream_t)stream);
 }
 
 srkv_status srkv_retrieval_decode(const srkv_config* cfg, const void* q, const void* k_cache,
@@ -212,12 +251,19 @@ srkv_status srkv_retrieval_decode(const srkv_config* cfg, const void* q, const v
                                   int32_t batch, int32_t* sel, int32_t kmax, int32_t* nsel,
                                   void* out, void* workspace, size_t workspace_bytes,
                                   int32_t* error_flags, srkv_stream stream) {
-  srkv_status st = srkv_score_topk(cfg, q, reps, num_pages, block_table, max_blocks, seq_lens,
-                                   prompt_lens, batch, sel, kmax, nsel, error_flags, stream);
+  srkv_status st = check_score(cfg, q, reps, num_pages, block_table, max_blocks, seq_lens, batch,
+                               sel, kmax, nsel);
+  if (st != SRKV_OK || batch == 0) return st;
+  DecodeArgs a;
+  st = prepare_decode(cfg, q, k_cache, v_cache, num_pages, block_table, max_blocks, seq_lens,
+                      batch, sel, kmax, nsel, out, workspace, workspace_bytes, error_flags, a);
   if (st != SRKV_OK) return st;
-  return srkv_sparse_paged_decode(cfg, q, k_cache, v_cache, num_pages, block_table, max_blocks,
-                                  seq_lens, batch, sel, kmax, nsel, out, workspace,
-                                  workspace_bytes, error_flags, stream);
+  // The scoring kernel, then the decode, which streams list A while the scoring finishes.
+  cudaStream_t s = (cudaStream_t)stream;
+  if (launch_score_topk(*cfg, q, reps, num_pages, block_table, max_blocks, seq_lens, prompt_lens,
+                        batch, sel, kmax, nsel, error_flags, s) != cudaSuccess)
+    return SRKV_ERR_CUDA;
+  return launch_decode(cfg, a, mma_split_supported(*cfg) ? 1 : 0, s);
 }
 
 }  // extern "C"

@@ -154,14 +154,10 @@ __device__ __forceinline__ int4 lds128(const void* p) {
   return *reinterpret_cast<const int4*>(p);
 }
 
-// ---- the page list of one (request, kv head) unit --------------------------------------
+// ---- geometry of one (request, kv head) unit ---------------------------------------------
 //
-// The attended set of a unit is init blocks [0, a), the selected blocks, and window
-// blocks [wstart, nb).  The list has a + ns + (nb - wstart) positions; a selected block
-// that is also an init or a window block (only possible at the two boundaries, when
-// init_tokens or the window start is not a multiple of 128) keeps its list slot but is
-// skipped, and the init/window copy carries its "selected" mark instead.  This makes the
-// position count a function of (seq_len, nsel) alone.
+// Initial-token blocks are [0, a), window blocks [wstart, nb) (those not already initial
+// blocks); candidates meet the offload range [INIT, W).
 
 struct Geom {
   int32_t L;       // clamped length
@@ -209,71 +205,15 @@ __device__ __forceinline__ bool is_candidate(int32_t b, int32_t INIT, int32_t W)
   return b >= 0 && lo < hi;
 }
 
-// What one list position loads.  rows [lo, hi) of the page are read; row r is attended iff
-// lo <= r < hi and (r < ie or r >= ws) (a selected block has ie = hi).
+// What one list position loads: rows [lo, hi) of the page are read; row r is attended iff
+// lo <= r < hi and (r < ie or r >= ws).
 struct PageTask {
   int32_t page;  // physical page, -1 = nothing to load
   int32_t block;
   int32_t lo, hi, ie, ws;
 };
 
-__device__ __forceinline__ PageTask resolve_position(const Geom& g, int32_t j,
-                                                     const int32_t* sel_u,
-                                                     const int32_t* bt_r, int64_t num_pages,
-                                                     int32_t INIT, uint32_t& eflags) {
-  PageTask t;
-  t.page = -1;
-  t.block = -1;
-  t.lo = t.hi = t.ie = t.ws = 0;
-  int32_t b;
-  bool selected;
-  if (j < g.a) {
-    b = j;
-    selected = g.ns > 0 && sel_u[0] == b;
-  } else if (j < g.a + g.ns) {
-    const int32_t i = j - g.a;
-    b = sel_u[i];
-    const bool ok = is_candidate(b, INIT, g.W) && (i == 0 || sel_u[i - 1] < b);
-    if (!ok) {
-      eflags |= SRKV_EFLAG_SELECTION;
-      return t;
-    }
-    if (b < g.a || b >= g.wstart) return t;  // carried by the init / window slot
-    selected = true;
-  } else {
-    b = g.wstart + (j - g.a - g.ns);
-    selected = g.ns > 0 && sel_u[g.ns - 1] == b;
-  }
-  const int32_t base = b * kBlock;
-  const int32_t cnt = min(kBlock, g.L - base);
-  int32_t lo, hi, ie, ws;
-  if (selected) {
-    lo = 0;
-    hi = cnt;
-    ie = cnt;
-    ws = cnt;
-  } else {
-    ie = min(max(g.ie - base, 0), cnt);
-    ws = min(max(g.ws - base, 0), cnt);
-    lo = ie > 0 ? 0 : ws;
-    hi = ws < cnt ? cnt : ie;
-  }
-  if (lo >= hi) return t;
-  const int32_t page = bt_r[b];
-  if (page < 0 || (int64_t)page >= num_pages) {
-    eflags |= SRKV_EFLAG_PAGE_RANGE;
-    return t;
-  }
-  t.page = page;
-  t.block = b;
-  t.lo = lo;
-  t.hi = hi;
-  t.ie = ie;
-  t.ws = ws;
-  return t;
-}
-
-// CTA c of C owns list positions [c*T/C, (c+1)*T/C) of the concatenated unit lists.
+// CTA c of C owns list positions [c*T/C, (c+1)*T/C) of a concatenated list.
 __device__ __forceinline__ int64_t cta_begin(int64_t c, int64_t T, int64_t C) {
   return c * T / C;
 }
@@ -282,14 +222,15 @@ __device__ __forceinline__ int64_t cta_of(int64_t p, int64_t T, int64_t C) {
   return ((p + 1) * C - 1) / T;
 }
 
-// Workspace layout of the decode (all offsets 256-byte aligned).
+// Workspace layout of the decode (all offsets 256-byte aligned).  Partials of list A use
+// slots [0, U + C), those of list B slots [U + C, 2 (U + C)).
 struct WsLayout {
-  size_t unit_n;    // int32[U]: list positions of each unit
-  size_t unit_off;  // int64[U+1]: exclusive prefix of unit_n; [U] = total
-  size_t acc;       // float[slots][G][d]: unnormalised partial outputs
-  size_t ml;        // float[slots][G][2]: running max (log2 domain) and sum
+  size_t off_a;  // int64[U+1]: first list-A position of each unit; [U] = total
+  size_t off_b;  // int64[U+1]: the same for list B
+  size_t acc;    // float[slots][G][d]: unnormalised partial outputs
+  size_t ml;     // float[slots][G][2]: running max (log2 domain) and sum
   size_t total;
-  int32_t slots;
+  int32_t bank;  // U + C: slots per list
 };
 
 __host__ __device__ inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
@@ -297,16 +238,17 @@ __host__ __device__ inline size_t align256(size_t x) { return (x + 255) & ~size_
 __host__ __device__ inline WsLayout ws_layout(int32_t units, int32_t ctas, int32_t G,
                                               int32_t d) {
   WsLayout w;
-  w.slots = units + ctas;
+  w.bank = units + ctas;
+  const size_t slots = 2 * (size_t)w.bank;
   size_t off = 0;
-  w.unit_n = off;
-  off = align256(off + sizeof(int32_t) * (size_t)units);
-  w.unit_off = off;
+  w.off_a = off;
+  off = align256(off + sizeof(int64_t) * ((size_t)units + 1));
+  w.off_b = off;
   off = align256(off + sizeof(int64_t) * ((size_t)units + 1));
   w.acc = off;
-  off = align256(off + sizeof(float) * (size_t)w.slots * G * d);
+  off = align256(off + sizeof(float) * slots * G * d);
   w.ml = off;
-  off = align256(off + sizeof(float) * 2 * (size_t)w.slots * G);
+  off = align256(off + sizeof(float) * 2 * slots * G);
   w.total = off;
   return w;
 }
@@ -332,7 +274,19 @@ struct DecodeArgs {
   int32_t init_tokens, local_tokens;
   float scale_log2;  // log2(e) / sqrt(d)
   int32_t ctas;      // C, the split grid
+  int32_t early;     // 1: the previous kernel is score_topk, so every input but sel and nsel
+                     // may be read before it finishes (list A streams during the scoring)
 };
+
+// k = min(n, ceil(p*n - 1e-9)) with separately rounded operations (no contraction), so
+// that the host and the device agree on every n.
+__device__ __forceinline__ int32_t device_topk_count(int32_t n, double p) {
+  if (n <= 0) return 0;
+  const double x = ceil(__dadd_rn(__dmul_rn(p, (double)n), -1e-9));
+  if (!(x > 0.0)) return 0;
+  if (x > (double)n) return n;
+  return (int32_t)x;
+}
 
 // ---- launchers (defined in the kernel files) ---------------------------------------------
 

@@ -83,13 +83,30 @@ def test_small_case_parity(name):
     out = gpu_decode(case, buf, ref["sel"], ref["nsel"])
     assert int(buf.error_flags.item()) == 0
     check_out(case, out, ref["out"])
-    # the whole step through the fused entry point, when every selection matched exactly
-    if exact == case.batch * case.cfg["num_kv_heads"]:
-        srkv.retrieval_decode(case.cfg, case.q, case.k_cache, case.v_cache, buf.reps,
-                              case.block_table, case.seq_lens, case.prompt_lens, buf.sel,
-                              buf.nsel, buf.out, buf.workspace, buf.error_flags)
-        torch.cuda.synchronize()
-        check_out(case, buf.out.float().cpu().numpy(), ref["out"])
+    check_fused_step(case, buf, ref, exact)
+
+
+def check_fused_step(case, buf, ref, exact_score_topk, units=None):
+    """srkv_retrieval_decode (one kernel: it scores and selects on chip) against the oracle."""
+    fused = srkv.DecodeBuffers(case.cfg, case.batch, case.max_blocks, case.num_pages,
+                               device=case.q.device)
+    fused.reps.copy_(buf.reps)
+    srkv.retrieval_decode(case.cfg, case.q, case.k_cache, case.v_cache, fused.reps,
+                          case.block_table, case.seq_lens, case.prompt_lens, fused.sel,
+                          fused.nsel, fused.out, fused.workspace, fused.error_flags)
+    torch.cuda.synchronize()
+    assert int(fused.error_flags.item()) == 0
+    fsel, fnsel = fused.sel.cpu().numpy(), fused.nsel.cpu().numpy()
+    exact = check_selection(case, fsel, fnsel, ref, units)
+    got = fused.out.float().cpu().numpy()
+    # the same kernel math as the split decode fed the fused selection: identical bits
+    again = gpu_decode(case, buf, fsel, fnsel)
+    if units is None:
+        assert np.array_equal(got, again)
+    n_units = len(units) if units else case.batch * case.cfg["num_kv_heads"]
+    if exact == n_units:
+        check_out(case, got, ref["out"], units)
+    return exact
 
 
 def test_empty_request_gives_zero_output():
@@ -193,3 +210,4 @@ def test_full_size_sampled(name):
     check_out(case, out, ref["out"], units)
     assert int(buf.error_flags.item()) == 0
     assert exact >= 1
+    assert check_fused_step(case, buf, ref, exact, units) >= 1
