@@ -5,6 +5,8 @@
 #include <math.h>
 #include <stdint.h>
 
+#include <atomic>
+
 #include "srkv_internal.cuh"
 
 namespace srkv {
@@ -264,6 +266,33 @@ srkv_status srkv_retrieval_decode(const srkv_config* cfg, const void* q, const v
                         batch, sel, kmax, nsel, error_flags, s) != cudaSuccess)
     return SRKV_ERR_CUDA;
   return launch_decode(cfg, a, mma_split_supported(*cfg) ? 1 : 0, s);
+}
+
+// Scratch of srkv_sparse_paged_decode_noalloc: one array per device that loads the library.
+static __device__ __align__(256) unsigned char g_noalloc_workspace[SRKV_NOALLOC_WORKSPACE_BYTES];
+static std::atomic<void*> g_noalloc_address[128];
+
+srkv_status srkv_sparse_paged_decode_noalloc(const srkv_config* cfg, const void* q,
+                                             const void* k_cache, const void* v_cache,
+                                             int64_t num_pages, const int32_t* block_table,
+                                             int32_t max_blocks, const int32_t* seq_lens,
+                                             int32_t batch, const int32_t* sel, int32_t kmax,
+                                             const int32_t* nsel, void* out,
+                                             int32_t* error_flags, srkv_stream stream) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 128) return SRKV_ERR_CUDA;
+  void* ws = g_noalloc_address[dev].load();
+  if (!ws) {  // once per device, with that device current: the array's device address
+    if (cudaGetSymbolAddress(&ws, g_noalloc_workspace) != cudaSuccess || !ws)
+      return SRKV_ERR_CUDA;
+    g_noalloc_address[dev].store(ws);
+  }
+  DecodeArgs a;
+  const srkv_status st = prepare_decode(cfg, q, k_cache, v_cache, num_pages, block_table,
+                                        max_blocks, seq_lens, batch, sel, kmax, nsel, out, ws,
+                                        SRKV_NOALLOC_WORKSPACE_BYTES, error_flags, a);
+  if (st != SRKV_OK || batch == 0) return st;
+  return launch_decode(cfg, a, 0, (cudaStream_t)stream);
 }
 
 }  // extern "C"

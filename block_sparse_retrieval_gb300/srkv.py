@@ -27,7 +27,8 @@ STATUS = {0: "ok", 1: "invalid argument", 2: "unsupported configuration",
 EXPORTS = ("srkv_default_config", "srkv_status_string", "srkv_topk_count",
            "srkv_num_candidates", "srkv_kmax_bound", "srkv_build_block_reps",
            "srkv_score_topk", "srkv_decode_workspace_size", "srkv_sparse_paged_decode",
-           "srkv_retrieval_decode")
+           "srkv_retrieval_decode", "srkv_sparse_paged_decode_noalloc")
+NOALLOC_WORKSPACE_BYTES = 16 << 20
 
 
 class SrkvError(RuntimeError):
@@ -77,8 +78,11 @@ def load() -> ctypes.CDLL:
                                              _P, _I32, _P, _I32, _P, _P, _P, _SZ, _P, _P]
     lib.srkv_retrieval_decode.argtypes = [ctypes.POINTER(Config), _P, _P, _P, _P, _I64, _P,
                                           _I32, _P, _P, _I32, _P, _I32, _P, _P, _P, _SZ, _P, _P]
+    lib.srkv_sparse_paged_decode_noalloc.argtypes = [ctypes.POINTER(Config), _P, _P, _P, _I64,
+                                                     _P, _I32, _P, _I32, _P, _I32, _P, _P, _P,
+                                                     _P]
     for name in ("srkv_build_block_reps", "srkv_score_topk", "srkv_sparse_paged_decode",
-                 "srkv_retrieval_decode"):
+                 "srkv_retrieval_decode", "srkv_sparse_paged_decode_noalloc"):
         getattr(lib, name).restype = ctypes.c_int
     _lib = lib
     return lib
@@ -210,6 +214,25 @@ def retrieval_decode(cfg: Mapping, q: torch.Tensor, k_cache: torch.Tensor,
         _dev(out, "out", dt), _dev(workspace, "workspace"),
         workspace.numel() * workspace.element_size(),
         _dev(error_flags, "error_flags", torch.int32), _stream(stream)), "srkv_retrieval_decode")
+
+
+def sparse_paged_decode_noalloc(cfg: Mapping, q: torch.Tensor, k_cache: torch.Tensor,
+                                v_cache: torch.Tensor, block_table: torch.Tensor,
+                                seq_lens: torch.Tensor, sel: torch.Tensor, nsel: torch.Tensor,
+                                out: torch.Tensor, error_flags: torch.Tensor | None = None,
+                                stream=None) -> None:
+    """srkv_sparse_paged_decode with the library's own static scratch (no workspace)."""
+    c = config(cfg)
+    dt = _store_dtype(cfg)
+    B, max_blocks = block_table.shape
+    _check(load().srkv_sparse_paged_decode_noalloc(
+        ctypes.byref(c), _dev(q, "q", dt), _dev(k_cache, "k_cache", dt),
+        _dev(v_cache, "v_cache", dt), k_cache.shape[0],
+        _dev(block_table, "block_table", torch.int32), max_blocks,
+        _dev(seq_lens, "seq_lens", torch.int32), B, _dev(sel, "sel", torch.int32),
+        sel.shape[-1], _dev(nsel, "nsel", torch.int32), _dev(out, "out", dt),
+        _dev(error_flags, "error_flags", torch.int32), _stream(stream)),
+        "srkv_sparse_paged_decode_noalloc")
 
 
 # ---- buffers for a step --------------------------------------------------------------------

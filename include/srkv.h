@@ -177,6 +177,37 @@ srkv_status srkv_retrieval_decode(const srkv_config* cfg, const void* q, const v
                                   void* out, void* workspace, size_t workspace_bytes,
                                   int32_t* error_flags, srkv_stream stream);
 
+/*
+ * For callers that cannot allocate device memory: srkv_sparse_paged_decode without a
+ * workspace argument.  (The method's pages have no counterpart of this; it is a service of
+ * this library.)  Some callers cannot call cudaMalloc on the decode path: code running under
+ * stream capture for a CUDA graph (plain cudaMalloc is not a capturable operation), serving
+ * loops that forbid allocator calls so that every step costs the same, plugins handed only
+ * their input and output buffers by a host framework that owns all device memory, and
+ * processes whose device memory is fully reserved up front.  They pass only inputs and
+ * outputs; the scratch space is a file-scope device array of SRKV_NOALLOC_WORKSPACE_BYTES
+ * in this library, which every GPU that loads the library holds until the process exits.
+ *   - Arguments, layouts and results are those of srkv_sparse_paged_decode.
+ *   - A batch whose decode needs more scratch than SRKV_NOALLOC_WORKSPACE_BYTES
+ *     (srkv_decode_workspace_size) is rejected with SRKV_ERR_WORKSPACE before any launch.
+ *   - The first call on a device looks up the array's device address (with that device
+ *     current); make that first call before any stream capture.
+ *   - Every call on a device shares the one array, and each call leaves its contents behind
+ *     (nothing in it needs to start at zero: a call writes every value it reads).  Calls
+ *     whose kernels overlap on the GPU (on different streams, without ordering between
+ *     them) race on it: order them.
+ *   - No allocation, free or allocating library routine is called.
+ */
+#define SRKV_NOALLOC_WORKSPACE_BYTES ((size_t)16 << 20)
+
+srkv_status srkv_sparse_paged_decode_noalloc(const srkv_config* cfg, const void* q,
+                                             const void* k_cache, const void* v_cache,
+                                             int64_t num_pages, const int32_t* block_table,
+                                             int32_t max_blocks, const int32_t* seq_lens,
+                                             int32_t batch, const int32_t* sel, int32_t kmax,
+                                             const int32_t* nsel, void* out,
+                                             int32_t* error_flags, srkv_stream stream);
+
 #ifdef __cplusplus
 }
 #endif
