@@ -304,8 +304,8 @@ def run_ours(args, world, rank, local):
         "config": {"workload": WORKLOAD, "global_batch": world, "seq_len": 65536,
                    "parallelism": f"replicas x{world}", "layers_rotated": R,
                    "l2": f"inputs larger than L2: {R} layer caches rotated per step"},
-        "roofline": {"kernel": "srkv_retrieval_decode call: score_topk + split-K decode "
-                               "kernels, overlapped by programmatic launch",
+        "roofline": {"kernel": "srkv_retrieval_decode call: score_topk, split-K decode and "
+                               "combine kernels, overlapped by programmatic launch",
                      "bound": "hbm", "achieved": round(achieved, 1), "peak": peak,
                      "unit": "GB/s", "frac": round(achieved / peak, 4), "peak_kind": peak_kind,
                      "bytes_per_launch": int(avg_step_bytes),
@@ -316,7 +316,7 @@ def run_ours(args, world, rank, local):
             "frac": round(rep_bytes / (rep_ms / 1e3) / 1e9 / peak, 4)},
         "clocks": clocks.summary(),
         "e2e": e2e,
-        "gpu_launches": K * 2,   # score_topk and the split kernel (with its merge) per step
+        "gpu_launches": K * 3,   # score_topk, the split kernel and the combine per step
     }
     if rank == 0 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(layers[0], args.cpu_seconds)

@@ -8,17 +8,19 @@
 // share one K/V head: here a block's score for a kv head is the inner product with the sum
 // of the group's queries, and selection is per (request, kv head).
 //
-// One thread-block cluster (up to 8 CTAs, ~64 candidates each) per (request, kv head) unit:
-//   1. each CTA loads the block-table entries of its share of the candidates;
-//   2. group query sum q_bar (fp32);
-//   3. one warp per candidate: s_b = q_bar . rep (fp32, fixed lane order), turned into an
-//      order-preserving 32-bit key (NaN and out-of-range pages rank lowest) and stored into
-//      the leader CTA's shared memory through distributed shared memory; one cluster
-//      barrier gathers them;
-//   4. the leader runs an MSB-first radix select (4 passes of 8 bits) for the exact k-th
-//      largest key;
-//   5. ties on that key go to the lower block index (an exclusive count in block order),
-//      and a second count writes the kept blocks ascending.
+// One thread-block cluster (up to 8 CTAs) per (request, kv head) unit:
+//   1. one round of independent loads: the sequence and prompt lengths, the block-table
+//      entries of this CTA's fixed share of the longest possible candidate range, and the
+//      group's queries (summed into q_bar, fp32);
+//   2. one warp per candidate below the request's own count n: s_b = q_bar . rep (fp32,
+//      fixed lane order), turned into an order-preserving 32-bit key (NaN and out-of-range
+//      pages rank lowest) and stored into the leader CTA's shared memory through
+//      distributed shared memory; one cluster barrier gathers them;
+//   3. the leader runs an MSB-first radix select, 8 bits a pass, until the bin holding the
+//      k-th largest key has at most 32 keys; one warp then ranks that bin exactly (score,
+//      then lower block index).  If four passes are needed the k-th key is known exactly
+//      and its equal keys go to the lowest block indices;
+//   4. kept blocks are written ascending (one exclusive count in block order).
 // Bytes per unit: n * (4 + 4d) read (block table + reps), k * 4 written.
 #include "srkv_internal.cuh"
 
@@ -43,6 +45,7 @@ struct ScoreArgs {
   int32_t* error_flags;
   int32_t Hq, Hkv, G;
   int32_t init_tokens, local_tokens, dense_boundary;
+  int32_t nmax;  // candidates of a request as long as the block table allows
   double topk_percent;
 };
 
@@ -103,7 +106,7 @@ __device__ __forceinline__ void cluster_sync() {
 
 // Every warp finds the digit holding the remaining-th largest key from a 256-bin histogram.
 __device__ __forceinline__ void find_digit(const int32_t* hist, int lane, int32_t remaining,
-                                           int32_t* digit, int32_t* rem_out) {
+                                           int32_t* digit, int32_t* rem_out, int32_t* cnt_out) {
   int32_t c[8], local = 0;
 #pragma unroll
   for (int b = 0; b < 8; ++b) {
@@ -116,12 +119,13 @@ __device__ __forceinline__ void find_digit(const int32_t* hist, int lane, int32_
     const int32_t y = __shfl_down_sync(0xffffffffu, suffix, o);
     if (lane + o < 32) suffix += y;
   }
-  int32_t above = suffix - local, dg = -1, rm = 0;
+  int32_t above = suffix - local, dg = -1, rm = 0, cn = 0;
 #pragma unroll
   for (int b = 7; b >= 0; --b) {
     if (above < remaining && above + c[b] >= remaining) {
       dg = lane * 8 + b;
       rm = remaining - above;
+      cn = c[b];
     }
     above += c[b];
   }
@@ -129,6 +133,7 @@ __device__ __forceinline__ void find_digit(const int32_t* hist, int lane, int32_
   const int src = __ffs(who) - 1;
   *digit = __shfl_sync(0xffffffffu, dg, src);
   *rem_out = __shfl_sync(0xffffffffu, rm, src);
+  *cnt_out = __shfl_sync(0xffffffffu, cn, src);
 }
 
 // Grid: one cluster of `cluster_size()` CTAs per (request, kv head) unit.
@@ -140,6 +145,8 @@ __global__ void __launch_bounds__(kThreads) score_topk_kernel(ScoreArgs a) {
   __shared__ float qbar[D];
   __shared__ int32_t hist[3][256];
   __shared__ int32_t scratch[32];
+  __shared__ int32_t bnd_idx[32];
+  __shared__ int32_t bnd_cnt;
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   griddep_launch_dependents();  // the decode may be scheduled now; it waits for this grid
@@ -147,8 +154,35 @@ __global__ void __launch_bounds__(kThreads) score_topk_kernel(ScoreArgs a) {
   const int32_t u = blockIdx.x / csize;
   const int32_t r = u / a.Hkv, h = u % a.Hkv;
 
-  int32_t L = a.seq_lens[r];
-  const int32_t prompt = a.prompt_lens ? a.prompt_lens[r] : L;
+  // 1. independent loads.  The share of block-table entries is fixed by the longest
+  // candidate range the table allows (nmax), so it does not wait for the length.
+  const int32_t L_in = a.seq_lens[r];
+  const int32_t prompt_in = a.prompt_lens ? a.prompt_lens[r] : 0;
+  const int32_t b_lo = a.init_tokens / kBlock;
+  const int32_t s_lo = (int32_t)((int64_t)a.nmax * crank / csize);
+  const int32_t s_hi = (int32_t)((int64_t)a.nmax * (crank + 1) / csize);
+  const int32_t* bt_r = a.block_table + (int64_t)r * a.max_blocks + b_lo;
+  for (int32_t i = s_lo + tid; i < s_hi; i += kThreads) pages[i - s_lo] = bt_r[i];
+  const T* q = static_cast<const T*>(a.q) + ((int64_t)r * a.Hq + (int64_t)h * a.G) * D;
+  for (int e = tid; e < D; e += kThreads) {
+    float s = 0.f;
+    int j = 0;
+    for (; j + 4 <= a.G; j += 4) {  // four independent loads in flight
+      const float x0 = static_cast<float>(q[(int64_t)(j + 0) * D + e]);
+      const float x1 = static_cast<float>(q[(int64_t)(j + 1) * D + e]);
+      const float x2 = static_cast<float>(q[(int64_t)(j + 2) * D + e]);
+      const float x3 = static_cast<float>(q[(int64_t)(j + 3) * D + e]);
+      s += x0;
+      s += x1;
+      s += x2;
+      s += x3;
+    }
+    for (; j < a.G; ++j) s += static_cast<float>(q[(int64_t)j * D + e]);
+    qbar[e] = s;
+  }
+
+  int32_t L = L_in;
+  const int32_t prompt = a.prompt_lens ? prompt_in : L_in;
   const int32_t Lmax = a.max_blocks * kBlock;
   uint32_t eflags = 0;
   if (L < 0 || L > Lmax) {
@@ -156,11 +190,7 @@ __global__ void __launch_bounds__(kThreads) score_topk_kernel(ScoreArgs a) {
     L = L < 0 ? 0 : Lmax;
   }
   const int32_t W = L - a.local_tokens;
-  int32_t b_lo = 0, n = 0;
-  if (W > a.init_tokens) {
-    b_lo = a.init_tokens / kBlock;
-    n = (W + kBlock - 1) / kBlock - b_lo;
-  }
+  const int32_t n = W > a.init_tokens ? (W + kBlock - 1) / kBlock - b_lo : 0;  // <= nmax
   const bool dense = prompt < a.dense_boundary;
   int32_t k = dense ? n : device_topk_count(n, a.topk_percent);
   if (k > a.kmax) {
@@ -180,39 +210,16 @@ __global__ void __launch_bounds__(kThreads) score_topk_kernel(ScoreArgs a) {
     }
     return;
   }
+  __syncthreads();  // pages and qbar
 
-  // 1. this CTA's share of the candidates, and their physical pages
-  const int32_t i_lo = (int32_t)((int64_t)n * crank / csize);
-  const int32_t i_hi = (int32_t)((int64_t)n * (crank + 1) / csize);
-  const int32_t* bt_r = a.block_table + (int64_t)r * a.max_blocks;
-  for (int32_t i = i_lo + tid; i < i_hi; i += kThreads) pages[i - i_lo] = bt_r[b_lo + i];
-  // 2. group query sum
-  const T* q = static_cast<const T*>(a.q) + ((int64_t)r * a.Hq + (int64_t)h * a.G) * D;
-  for (int e = tid; e < D; e += kThreads) {
-    float s = 0.f;
-    int j = 0;
-    for (; j + 4 <= a.G; j += 4) {  // four independent loads in flight
-      const float x0 = static_cast<float>(q[(int64_t)(j + 0) * D + e]);
-      const float x1 = static_cast<float>(q[(int64_t)(j + 1) * D + e]);
-      const float x2 = static_cast<float>(q[(int64_t)(j + 2) * D + e]);
-      const float x3 = static_cast<float>(q[(int64_t)(j + 3) * D + e]);
-      s += x0;
-      s += x1;
-      s += x2;
-      s += x3;
-    }
-    for (; j < a.G; ++j) s += static_cast<float>(q[(int64_t)j * D + e]);
-    qbar[e] = s;
-  }
-  __syncthreads();
-
-  // 3. scores of the share, one warp per candidate; keys go to the leader's shared memory
+  // 2. scores of the share, one warp per candidate; keys go to the leader's shared memory
   constexpr int EPL = D / 32;  // elements per lane: 4 (d 128) or 2 (d 64)
   float qv[EPL];
 #pragma unroll
   for (int e = 0; e < EPL; ++e) qv[e] = qbar[lane * EPL + e];
+  const int32_t i_hi = min(s_hi, n);
   constexpr int UNROLL = 4;
-  for (int32_t i0 = i_lo + warp; i0 < i_hi; i0 += kWarps * UNROLL) {
+  for (int32_t i0 = s_lo + warp; i0 < i_hi; i0 += kWarps * UNROLL) {
     float part[UNROLL];
     bool ok[UNROLL];
 #pragma unroll
@@ -221,7 +228,7 @@ __global__ void __launch_bounds__(kThreads) score_topk_kernel(ScoreArgs a) {
       part[x] = 0.f;
       ok[x] = false;
       if (i < i_hi) {
-        const int32_t page = pages[i - i_lo];
+        const int32_t page = pages[i - s_lo];
         ok[x] = page >= 0 && (int64_t)page < a.num_pages;
         if (ok[x]) {
           const float* rep = a.reps + ((int64_t)page * a.Hkv + h) * D + lane * EPL;
@@ -252,11 +259,14 @@ __global__ void __launch_bounds__(kThreads) score_topk_kernel(ScoreArgs a) {
   cluster_sync();  // every key is in the leader's shared memory
   if (crank != 0) return;
 
-  // 4. radix select of the k-th largest key (one barrier per pass, triple-buffered bins)
+  // 3. radix select (one barrier per pass, triple-buffered bins) until the boundary bin is
+  // small enough for one warp to rank
   for (int i = tid; i < 2 * 256; i += kThreads) hist[i >> 8][i & 255] = 0;
+  if (tid == 0) bnd_cnt = 0;
   __syncthreads();
   uint32_t prefix = 0, pmask = 0;
   int32_t remaining = k;
+  bool ranked = false;
 #pragma unroll 1
   for (int pass = 0; pass < 4; ++pass) {
     const int shift = 24 - 8 * pass;
@@ -272,36 +282,58 @@ __global__ void __launch_bounds__(kThreads) score_topk_kernel(ScoreArgs a) {
       if (in && lane == __ffs(peers) - 1) atomicAdd(&hcur[digit], __popc(peers));
     }
     __syncthreads();
-    int32_t dg, rm;
-    find_digit(hcur, lane, remaining, &dg, &rm);
+    int32_t dg, rm, cnt;
+    find_digit(hcur, lane, remaining, &dg, &rm, &cnt);
     prefix |= (uint32_t)dg << shift;
     pmask |= 0xffu << shift;
     remaining = rm;
+    if (pass < 3 && cnt <= 32) {  // uniform: every warp read the same histogram
+      ranked = true;
+      break;
+    }
   }
-  const uint32_t kth = prefix;
-  const int32_t need_equal = remaining;  // keys equal to kth that are kept (lowest blocks)
+  int32_t* mark = pages;  // the leader's page share is no longer needed
+  if (ranked) {
+    // The <= 32 keys of the boundary bin, ranked by (key desc, block asc); the first
+    // `remaining` of them are kept.
+    for (int32_t i = tid; i < n; i += kThreads)
+      if ((keys[i] & pmask) == prefix) bnd_idx[atomicAdd(&bnd_cnt, 1)] = i;
+    __syncthreads();
+    if (warp == 0) {
+      const int32_t m = bnd_cnt;
+      const int32_t idx = lane < m ? bnd_idx[lane] : INT32_MAX;
+      const uint32_t key = lane < m ? keys[idx] : 0u;
+      int32_t rank = 0;
+      for (int32_t j = 0; j < m; ++j) {
+        const uint32_t kj = __shfl_sync(0xffffffffu, key, j);
+        const int32_t ij = __shfl_sync(0xffffffffu, idx, j);
+        rank += kj > key || (kj == key && ij < idx);
+      }
+      if (lane < m) mark[idx] = rank < remaining;
+    }
+    __syncthreads();
+  }
 
-  // 5. keep key > kth, and the first need_equal keys == kth in block order; write ascending.
+  // 4. keep a key above the boundary bin; inside it, the ranked ones (or, after four
+  // passes, the first `remaining` equal keys in block order).  Written ascending.
   const int32_t chunk = (n + kThreads - 1) / kThreads;
   const int32_t c0 = min(n, tid * chunk), c1 = min(n, c0 + chunk);
-  int32_t n_eq = 0;
-  for (int32_t i = c0; i < c1; ++i) n_eq += keys[i] == kth;
-  int32_t total;
-  int32_t eq_rank = block_exclusive_scan(n_eq, scratch, &total);
+  int32_t total, eq_rank = 0, n_eq = 0;
+  if (!ranked) {
+    for (int32_t i = c0; i < c1; ++i) n_eq += keys[i] == prefix;
+    eq_rank = block_exclusive_scan(n_eq, scratch, &total);
+  }
   int32_t n_take = 0;
   for (int32_t i = c0; i < c1; ++i) {
-    const uint32_t key = keys[i];
-    bool take = key > kth;
-    if (key == kth) take = eq_rank++ < need_equal;
-    n_take += take;
+    const uint32_t hi = keys[i] & pmask;
+    n_take += hi > prefix || (hi == prefix && (ranked ? mark[i] != 0 : eq_rank++ < remaining));
   }
   int32_t pos = block_exclusive_scan(n_take, scratch, &total);
   eq_rank -= n_eq;
   for (int32_t i = c0; i < c1; ++i) {
-    const uint32_t key = keys[i];
-    bool take = key > kth;
-    if (key == kth) take = eq_rank++ < need_equal;
-    if (take) sel_u[pos++] = b_lo + i;
+    const uint32_t hi = keys[i] & pmask;
+    if (hi > prefix || (hi == prefix && (ranked ? mark[i] != 0 : eq_rank++ < remaining)))
+      sel_u[pos++] = b_lo + i;
   }
   if (tid == 0) a.nsel[u] = total;
 }
@@ -375,6 +407,8 @@ cudaError_t launch_score_topk(const srkv_config& cfg, const void* q, const float
   // about 64 candidates each).
   int64_t W = (int64_t)max_blocks * kBlock - cfg.local_tokens;
   int64_t nmax = W > cfg.init_tokens ? (W + kBlock - 1) / kBlock - cfg.init_tokens / kBlock : 0;
+  if (nmax > INT32_MAX) return cudaErrorInvalidValue;
+  a.nmax = (int32_t)nmax;
   int32_t cluster = (int32_t)((nmax + 63) / 64);
   cluster = cluster < 1 ? 1 : (cluster > 8 ? 8 : cluster);
   if ((int64_t)units * cluster > INT32_MAX) return cudaErrorInvalidValue;
