@@ -3,8 +3,9 @@
 One step = one decode step of one Llama-3-8B-shaped layer (batch 1, 32 q / 8 kv heads,
 d 128, bf16, 65536 cached tokens, init 1024, window 7192, top-k 20 %, 5 % planted
 blocks, shuffled 128-token pages) through srkv_retrieval_decode: score + top-k of the
-offload blocks, then split-K sparse paged attention and its combine, captured per layer
-in a CUDA graph.  The representation vectors are built once per
+offload blocks, then split-K sparse paged attention and its combine; one step of every
+rotated layer is captured in one CUDA graph, as a model's decode step would be.  The
+representation vectors are built once per
 page at prefill (as on the method's page: the store is written at prefill and read at
 decode) and reported separately under "prefill_reps".
 
@@ -260,38 +261,40 @@ def run_ours(args, world, rank, local):
         raise RuntimeError(f"device error flags {flags}")
     step_bytes = [ly.step_bytes() for ly in layers]
 
+    # One CUDA graph holds one step of every layer, as a model's decode step would.
+    R = len(layers)
     stream = torch.cuda.Stream(device=dev)
     stream.wait_stream(torch.cuda.current_stream())
     with torch.cuda.stream(stream):
-        graphs = [capture(ly.step, stream) for ly in layers]
+        graph = capture(lambda: [ly.step() for ly in layers], stream)
     torch.cuda.synchronize()
 
-    R = len(layers)
     with torch.cuda.stream(stream):
-        for i in range(args.warmup):
-            graphs[i % R].replay()
+        for i in range(max(1, -(-args.warmup // R))):
+            graph.replay()
     torch.cuda.synchronize()
 
-    K = args.steps
-    ev = [torch.cuda.Event(enable_timing=True) for _ in range(K + 1)]
+    K = -(-args.steps // R) * R               # whole replays of the R-layer graph
+    n_rep = K // R
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(n_rep + 1)]
     barrier(world)
     torch.cuda.synchronize()
     with ClockSampler(local) as clocks:
         with torch.cuda.stream(stream):
             torch.cuda._sleep(int(2e7))      # let the host queue ahead of the device
-            for i in range(K):
+            for i in range(n_rep):
                 ev[i].record(stream)
-                graphs[i % R].replay()
-            ev[K].record(stream)
+                graph.replay()
+            ev[n_rep].record(stream)
         torch.cuda.synchronize()
     barrier(world)
-    step_ms = [ev[i].elapsed_time(ev[i + 1]) for i in range(K)]
-    total_ms = max_over_ranks(ev[0].elapsed_time(ev[K]), world, dev)
+    replay_ms = [ev[i].elapsed_time(ev[i + 1]) for i in range(n_rep)]
+    total_ms = max_over_ranks(ev[0].elapsed_time(ev[n_rep]), world, dev)
     ms_per_step = total_ms / K
     value = world * K / (total_ms / 1e3)
 
     avg_step_bytes = statistics.mean(sb["total"] for sb in step_bytes)
-    call_ms = statistics.mean(step_ms)
+    call_ms = statistics.mean(replay_ms) / R
     achieved = avg_step_bytes / (call_ms / 1e3) / 1e9
     traffic = committed_traffic()
 

@@ -89,8 +89,20 @@ __device__ __forceinline__ PageTask resolve_b(const Geom& g, int32_t i, const in
   return t;
 }
 
+// Selection count of unit u: read from nsel, or, when the scoring kernel is still running
+// (early), the count it is bound to write (selection_count), from the lengths alone.
+__device__ __forceinline__ int32_t nsel_of(const DecodeArgs& a, int32_t u) {
+  if (!a.early) return a.nsel[u];
+  const int32_t r = u / a.Hkv;
+  const int32_t L = a.seq_lens[r];
+  const int32_t prompt = a.prompt_lens ? a.prompt_lens[r] : L;
+  return selection_count(L, prompt, a.max_blocks, a.kmax, a.init_tokens, a.local_tokens,
+                         a.dense_boundary, a.topk_percent)
+      .k;
+}
+
 __device__ __forceinline__ Geom unit_geom(const DecodeArgs& a, int32_t u, uint32_t& eflags) {
-  return make_geom(a.seq_lens[u / a.Hkv], a.nsel[u], a.max_blocks, a.kmax, a.init_tokens,
+  return make_geom(a.seq_lens[u / a.Hkv], nsel_of(a, u), a.max_blocks, a.kmax, a.init_tokens,
                    a.local_tokens, eflags);
 }
 
@@ -103,7 +115,7 @@ __device__ __forceinline__ Geom unit_geom_a(const DecodeArgs& a, int32_t u, uint
 __device__ __forceinline__ int32_t list_count(const DecodeArgs& a, int list, int32_t u,
                                               uint32_t& eflags) {
   if (list == kListA) return list_a_count(unit_geom_a(a, u, eflags));
-  int32_t ns = a.nsel[u];
+  int32_t ns = nsel_of(a, u);
   if (ns < 0 || ns > a.kmax) {
     eflags |= SRKV_EFLAG_SELECTION;
     ns = ns < 0 ? 0 : a.kmax;
@@ -145,8 +157,8 @@ __device__ __forceinline__ ListRange warp_plan(const DecodeArgs& a, int list, in
     prefix[lane] = excl;
     if (lane == 31) prefix[32] = rg.T;
   }
-  rg.begin = cta_begin(c, rg.T, C);
-  rg.end = cta_begin(c + 1, rg.T, C);
+  rg.begin = cta_begin(c < C ? c : C, rg.T, C);  // a CTA c >= C has no position
+  rg.end = cta_begin(c < C ? c + 1 : C, rg.T, C);
   int32_t u0 = 0;
   int64_t base0 = 0;
   const bool mine = rg.begin < rg.end && excl <= rg.begin && rg.begin < excl + local;

@@ -163,12 +163,15 @@ __device__ __forceinline__ void issue_stage(const DecodeArgs& a, unsigned char* 
   ++armed;
   if (u < 0) return;
   const int32_t h = u % a.Hkv, r = u / a.Hkv;
-  if (rows) {
+  if (rows) {  // pages are read once per step: first out of L2
+    const uint64_t once = l2_policy_evict_first();
     const int64_t src = (((int64_t)t.page * a.Hkv + h) * kBlock + t.lo) * D;
-    bulk_load(smem + C::kOffK + (size_t)s * C::kSlab + (size_t)t.lo * D * 2,
-              static_cast<const __nv_bfloat16*>(a.k_cache) + src, slab_bytes, &full[s]);
-    bulk_load(smem + C::kOffV + (size_t)s * C::kSlab + (size_t)t.lo * D * 2,
-              static_cast<const __nv_bfloat16*>(a.v_cache) + src, slab_bytes, &full[s]);
+    bulk_load_hint(smem + C::kOffK + (size_t)s * C::kSlab + (size_t)t.lo * D * 2,
+                   static_cast<const __nv_bfloat16*>(a.k_cache) + src, slab_bytes, &full[s],
+                   once);
+    bulk_load_hint(smem + C::kOffV + (size_t)s * C::kSlab + (size_t)t.lo * D * 2,
+                   static_cast<const __nv_bfloat16*>(a.v_cache) + src, slab_bytes, &full[s],
+                   once);
   }
   if (fl & kNewUnit)
     bulk_load(smem + C::kOffQ + (size_t)s * C::kQBytes,
@@ -183,8 +186,11 @@ __device__ __forceinline__ void warp_arrive(uint64_t* bar) {
   if ((threadIdx.x & 31) == 0) mbar_arrive(bar);
 }
 
+// 128 registers: a quarter-SM register file (16K) then holds this CTA's three warps on one
+// sub-partition (12K) beside one warp of a combine CTA, so the combine is resident and
+// waiting when the last partial is written.
 template <int D>
-__global__ void __launch_bounds__(kThreads, 1) split_mma_kernel(const DecodeArgs a) {
+__global__ void __maxnreg__(128) split_mma_kernel(const DecodeArgs a) {
   using C = Cfg<D>;
   extern __shared__ __align__(128) unsigned char smem[];
   unsigned char* sK = smem + C::kOffK;
@@ -199,7 +205,11 @@ __global__ void __launch_bounds__(kThreads, 1) split_mma_kernel(const DecodeArgs
   uint64_t* mb_r2 = mb_w1 + 2;
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  griddep_launch_dependents();  // the combine may be scheduled now; it waits for this grid
+  // The combine may be scheduled once every CTA has passed this point (it waits for this
+  // grid before reading partials).  Without the early mode the inputs are only read after
+  // the previous kernel in the stream has finished, and the combine reads them too.
+  if (!a.early) griddep_wait();
+  griddep_launch_dependents();
   if (tid == 0) {
     for (int s = 0; s < C::kStages; ++s) {
       mbar_init(&full[s], 1);
@@ -218,17 +228,21 @@ __global__ void __launch_bounds__(kThreads, 1) split_mma_kernel(const DecodeArgs
     bool abort = false;
     int64_t it = 0;     // stages handed out so far (uniform over the warp)
     int64_t armed = 0;  // stages lane 0 armed
-    if (!a.early) griddep_wait();
-    for (int list = kListA; list <= kListB && !abort; ++list) {
-      if (list == kListB) {  // the selection must exist from here on
-        if (a.early) griddep_wait();
-      }
-      // CTA 0 leaves each list's unit offsets for the combine kernel.
+    // Both lists are planned first: list B's counts are the selection counts, known from
+    // the lengths alone in the early mode.  CTA 0 leaves each list's unit offsets for the
+    // combine kernel.
+    ListRange rgs[2];
+#pragma unroll
+    for (int list = kListA; list <= kListB; ++list) {
       int64_t* offsets = blockIdx.x == 0
                              ? reinterpret_cast<int64_t*>(a.ws + (list == kListA ? a.lay.off_a
                                                                                  : a.lay.off_b))
                              : nullptr;
-      const ListRange rg = warp_plan(a, list, blockIdx.x, gridDim.x, offsets, nullptr, eflags);
+      rgs[list] = warp_plan(a, list, blockIdx.x, list_ctas(a, list), offsets, nullptr, eflags);
+    }
+    for (int list = kListA; list <= kListB && !abort; ++list) {
+      if (list == kListB && a.early) griddep_wait();  // the selection must exist from here on
+      const ListRange rg = rgs[list];
       const int64_t npos = rg.end - rg.begin;
       if (npos <= 0) continue;
       const uint32_t bank = list == kListB ? kBankB : 0u;
@@ -265,10 +279,16 @@ __global__ void __launch_bounds__(kThreads, 1) split_mma_kernel(const DecodeArgs
         task.lo = task.hi = task.ie = task.ws = 0;
         if (lane < cnt) {
           const int32_t* bt_r = a.block_table + (int64_t)(my_u / a.Hkv) * a.max_blocks;
+          // Early mode: the count the plan assumed must be the one the scoring wrote.
+          const int32_t written = list == kListB && a.early ? a.nsel[my_u] : my_g.ns;
           task = list == kListA
                      ? resolve_a(my_g, my_j, bt_r, a.num_pages, eflags)
                      : resolve_b(my_g, my_j, a.sel + (int64_t)my_u * a.kmax, bt_r, a.num_pages,
                                  a.init_tokens, eflags);
+          if (list == kListB && (my_j >= written || (my_j == 0 && written != my_g.ns))) {
+            eflags |= SRKV_EFLAG_SELECTION;
+            if (my_j >= written) task.page = -1;
+          }
         }
         for (int l = 0; l < cnt; ++l) {
           PageTask t;

@@ -42,8 +42,8 @@ __global__ void __launch_bounds__(kThreads) split_simt_kernel(const DecodeArgs a
   __shared__ float s_acc[kWarps][kGMax][D];
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  griddep_wait();  // then the combine may be scheduled: it reads the inputs before its wait
   griddep_launch_dependents();
-  griddep_wait();
   const int G = a.G;
   uint32_t eflags = 0;
   float q[kGMax][E], acc[kGMax][E], m[kGMax], l[kGMax];
@@ -54,7 +54,8 @@ __global__ void __launch_bounds__(kThreads) split_simt_kernel(const DecodeArgs a
                              ? reinterpret_cast<int64_t*>(a.ws + (list == kListA ? a.lay.off_a
                                                                                  : a.lay.off_b))
                              : nullptr;
-      const ListRange rg = warp_plan(a, list, blockIdx.x, gridDim.x, offsets, nullptr, eflags);
+      const ListRange rg = warp_plan(a, list, blockIdx.x, list_ctas(a, list), offsets, nullptr,
+                                     eflags);
       if (lane == 0) s_rg = rg;
     }
     __syncthreads();

@@ -14,20 +14,22 @@
 //      group's queries (summed into q_bar, fp32);
 //   2. one warp per candidate below the request's own count n: s_b = q_bar . rep (fp32,
 //      fixed lane order), turned into an order-preserving 32-bit key (NaN and out-of-range
-//      pages rank lowest) and stored into the leader CTA's shared memory through
-//      distributed shared memory; one cluster barrier gathers them;
-//   3. the leader runs an MSB-first radix select, 8 bits a pass, until the bin holding the
-//      k-th largest key has at most 32 keys; one warp then ranks that bin exactly (score,
-//      then lower block index).  If four passes are needed the k-th key is known exactly
-//      and its equal keys go to the lowest block indices;
-//   4. kept blocks are written ascending (one exclusive count in block order).
+//      pages rank lowest), stored into the leader CTA's shared memory and counted into its
+//      histogram of the top 8 key bits through distributed shared memory; one cluster
+//      barrier gathers them;
+//   3. the leader runs an MSB-first radix select, 8 bits a pass (the first from that
+//      histogram), until the bin holding the k-th largest key has at most 32 keys; one warp
+//      then ranks that bin exactly (score, then lower block index).  If four passes are
+//      needed the k-th key is known exactly and its equal keys go to the lowest blocks;
+//   4. the kept blocks are written ascending: a kept key's slot is the number of kept keys
+//      before it in block order, from ballot counts per warp.
 // Bytes per unit: n * (4 + 4d) read (block table + reps), k * 4 written.
 #include "srkv_internal.cuh"
 
 namespace srkv {
 namespace {
 
-constexpr int kThreads = 256;  // a decode CTA (48K registers) still fits beside one
+constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
 constexpr int kMaxDynamicSmem = 200 * 1024;  // keys + pages of up to 25600 blocks
 
@@ -56,32 +58,16 @@ __device__ __forceinline__ uint32_t score_key(float s) {
   return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
 
-// Exclusive scan over the CTA of one int per thread; returns the prefix, *total the sum.
-__device__ __forceinline__ int32_t block_exclusive_scan(int32_t v, int32_t* scratch,
-                                                        int32_t* total) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+// Exclusive scan over the warp of one int per lane; *total gets the sum.
+__device__ __forceinline__ int32_t warp_exclusive_scan(int32_t v, int lane, int32_t* total) {
   int32_t x = v;
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
     const int32_t y = __shfl_up_sync(0xffffffffu, x, o);
     if (lane >= o) x += y;
   }
-  if (lane == 31) scratch[warp] = x;
-  __syncthreads();
-  if (warp == 0) {
-    int32_t w = lane < kWarps ? scratch[lane] : 0;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const int32_t y = __shfl_up_sync(0xffffffffu, w, o);
-      if (lane >= o) w += y;
-    }
-    if (lane < kWarps) scratch[lane] = w;  // inclusive warp totals
-  }
-  __syncthreads();
-  const int32_t before = warp > 0 ? scratch[warp - 1] : 0;
-  *total = scratch[kWarps - 1];
-  __syncthreads();
-  return before + x - v;
+  *total = __shfl_sync(0xffffffffu, x, 31);
+  return x - v;
 }
 
 __device__ __forceinline__ uint32_t cluster_rank() {
@@ -99,6 +85,18 @@ __device__ __forceinline__ void st_cluster_u32(uint32_t* local, uint32_t rank, u
   uint32_t remote;
   asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(smem_u32(local)), "r"(rank));
   asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(remote), "r"(v) : "memory");
+}
+// Atomic add to the same shared-memory offset in CTA `rank` of this cluster.
+__device__ __forceinline__ void red_cluster_add(int32_t* local, uint32_t rank, int32_t v) {
+  uint32_t remote;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(smem_u32(local)), "r"(rank));
+  asm volatile("red.shared::cluster.add.u32 [%0], %1;" ::"r"(remote), "r"(v) : "memory");
+}
+__device__ __forceinline__ void cluster_arrive() {
+  asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_wait() {
+  asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 __device__ __forceinline__ void cluster_sync() {
   asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
@@ -136,23 +134,27 @@ __device__ __forceinline__ void find_digit(const int32_t* hist, int lane, int32_
   *cnt_out = __shfl_sync(0xffffffffu, cn, src);
 }
 
+constexpr int kFastRounds = 4;  // the block-wide finish handles n <= 4 * kThreads
+
 // Grid: one cluster of `cluster_size()` CTAs per (request, kv head) unit.
 template <typename T, int D>
-__global__ void __launch_bounds__(kThreads) score_topk_kernel(ScoreArgs a) {
+__global__ void __launch_bounds__(kThreads, 4) score_topk_kernel(ScoreArgs a) {
   extern __shared__ uint32_t smem[];
   uint32_t* keys = smem;                                             // [max_blocks], leader
   int32_t* pages = reinterpret_cast<int32_t*>(smem + a.max_blocks);  // [max_blocks]
   __shared__ float qbar[D];
-  __shared__ int32_t hist[3][256];
-  __shared__ int32_t scratch[32];
+  __shared__ int32_t hist[3][256];  // leader: radix histograms (pass 0 filled by the cluster)
   __shared__ int32_t bnd_idx[32];
-  __shared__ int32_t bnd_cnt;
+  __shared__ int32_t wcnt[2][kFastRounds * kWarps];  // per (round, warp): above / in the bin
+  __shared__ uint32_t s_take;
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   griddep_launch_dependents();  // the decode may be scheduled now; it waits for this grid
   const uint32_t crank = cluster_rank(), csize = cluster_size();
   const int32_t u = blockIdx.x / csize;
   const int32_t r = u / a.Hkv, h = u % a.Hkv;
+  for (int i = tid; i < 3 * 256; i += kThreads) (&hist[0][0])[i] = 0;
+  cluster_arrive();  // the leader's histograms are zero before any CTA adds to them
 
   // 1. independent loads.  The share of block-table entries is fixed by the longest
   // candidate range the table allows (nmax), so it does not wait for the length.
@@ -181,25 +183,15 @@ __global__ void __launch_bounds__(kThreads) score_topk_kernel(ScoreArgs a) {
     qbar[e] = s;
   }
 
-  int32_t L = L_in;
   const int32_t prompt = a.prompt_lens ? prompt_in : L_in;
-  const int32_t Lmax = a.max_blocks * kBlock;
-  uint32_t eflags = 0;
-  if (L < 0 || L > Lmax) {
-    eflags |= SRKV_EFLAG_SEQ_LEN;
-    L = L < 0 ? 0 : Lmax;
-  }
-  const int32_t W = L - a.local_tokens;
-  const int32_t n = W > a.init_tokens ? (W + kBlock - 1) / kBlock - b_lo : 0;  // <= nmax
-  const bool dense = prompt < a.dense_boundary;
-  int32_t k = dense ? n : device_topk_count(n, a.topk_percent);
-  if (k > a.kmax) {
-    eflags |= SRKV_EFLAG_SELECTION;
-    k = a.kmax;
-  }
+  const SelCount sc = selection_count(L_in, prompt, a.max_blocks, a.kmax, a.init_tokens,
+                                      a.local_tokens, a.dense_boundary, a.topk_percent);
+  const int32_t n = sc.n, k = sc.k;  // n <= nmax
+  uint32_t eflags = sc.flags;
   int32_t* sel_u = a.sel + (int64_t)u * a.kmax;
 
-  // Uniform over the cluster: every CTA takes the same branch.
+  // Uniform over the cluster: every CTA takes the same branch (and none waits at the
+  // cluster barrier it arrived at).
   if ((k == n && n <= a.kmax) || k == 0) {  // all candidates, or none: no scoring
     if (crank == 0) {
       for (int32_t i = tid; i < k; i += kThreads) sel_u[i] = b_lo + i;
@@ -212,13 +204,17 @@ __global__ void __launch_bounds__(kThreads) score_topk_kernel(ScoreArgs a) {
   }
   __syncthreads();  // pages and qbar
 
-  // 2. scores of the share, one warp per candidate; keys go to the leader's shared memory
+  // 2. scores of the share, one warp per candidate.  Lane x of a warp stores the key of
+  // its x-th candidate into the leader's shared memory and adds it to the leader's
+  // pass-0 histogram (top 8 bits; lanes with equal digits add once).
   constexpr int EPL = D / 32;  // elements per lane: 4 (d 128) or 2 (d 64)
   float qv[EPL];
 #pragma unroll
   for (int e = 0; e < EPL; ++e) qv[e] = qbar[lane * EPL + e];
   const int32_t i_hi = min(s_hi, n);
-  constexpr int UNROLL = 4;
+  const uint64_t keep = l2_policy_evict_last();  // the vectors are read again every step
+  constexpr int UNROLL = 8;  // 64 candidates of a CTA in one round of loads
+  cluster_wait();
   for (int32_t i0 = s_lo + warp; i0 < i_hi; i0 += kWarps * UNROLL) {
     float part[UNROLL];
     bool ok[UNROLL];
@@ -233,10 +229,10 @@ __global__ void __launch_bounds__(kThreads) score_topk_kernel(ScoreArgs a) {
         if (ok[x]) {
           const float* rep = a.reps + ((int64_t)page * a.Hkv + h) * D + lane * EPL;
           if constexpr (EPL == 4) {
-            const float4 v = __ldg(reinterpret_cast<const float4*>(rep));
+            const float4 v = ldg_f4_hint(rep, keep);
             part[x] = qv[0] * v.x + qv[1] * v.y + qv[2] * v.z + qv[3] * v.w;
           } else {
-            const float2 v = __ldg(reinterpret_cast<const float2*>(rep));
+            const float2 v = ldg_f2_hint(rep, keep);
             part[x] = qv[0] * v.x + qv[1] * v.y;
           }
         }
@@ -246,24 +242,31 @@ __global__ void __launch_bounds__(kThreads) score_topk_kernel(ScoreArgs a) {
     for (int o = 16; o > 0; o >>= 1)
 #pragma unroll
       for (int x = 0; x < UNROLL; ++x) part[x] += __shfl_xor_sync(0xffffffffu, part[x], o);
+    float mine = part[0];
+    bool mine_ok = ok[0];
 #pragma unroll
-    for (int x = 0; x < UNROLL; ++x) {
-      const int32_t i = i0 + x * kWarps;
-      if (lane == 0 && i < i_hi) {
-        if (!ok[x]) eflags |= SRKV_EFLAG_PAGE_RANGE;
-        st_cluster_u32(&keys[i], 0, ok[x] ? score_key(part[x]) : 0u);
+    for (int x = 1; x < UNROLL; ++x)
+      if (lane == x) {
+        mine = part[x];
+        mine_ok = ok[x];
       }
-    }
+    const int32_t i = i0 + lane * kWarps;
+    const bool valid = lane < UNROLL && i < i_hi;
+    if (valid && !mine_ok) eflags |= SRKV_EFLAG_PAGE_RANGE;
+    const uint32_t key = mine_ok ? score_key(mine) : 0u;
+    if (valid) st_cluster_u32(&keys[i], 0, key);
+    const uint32_t digit = valid ? key >> 24 : 0xffffffffu;
+    const uint32_t peers = __match_any_sync(0xffffffffu, digit);
+    if (valid && lane == __ffs(peers) - 1) red_cluster_add(&hist[0][digit], 0, __popc(peers));
   }
+  eflags = __reduce_or_sync(0xffffffffu, eflags);
   if (lane == 0 && eflags) raise_flags(a.error_flags, eflags);
-  cluster_sync();  // every key is in the leader's shared memory
+  cluster_sync();  // every key and the pass-0 histogram are in the leader
   if (crank != 0) return;
 
-  // 3. radix select (one barrier per pass, triple-buffered bins) until the boundary bin is
-  // small enough for one warp to rank
-  for (int i = tid; i < 2 * 256; i += kThreads) hist[i >> 8][i & 255] = 0;
-  if (tid == 0) bnd_cnt = 0;
-  __syncthreads();
+  // 3. radix select: pass 0 reads the histogram the cluster built; passes 1-3 build theirs
+  // (one barrier a pass, triple-buffered bins) until the boundary bin is small enough for
+  // one warp to rank
   uint32_t prefix = 0, pmask = 0;
   int32_t remaining = k;
   bool ranked = false;
@@ -271,17 +274,18 @@ __global__ void __launch_bounds__(kThreads) score_topk_kernel(ScoreArgs a) {
   for (int pass = 0; pass < 4; ++pass) {
     const int shift = 24 - 8 * pass;
     int32_t* hcur = hist[pass % 3];
-    for (int i = tid; i < 256; i += kThreads) hist[(pass + 1) % 3][i] = 0;
-    for (int32_t i0 = warp * 32; i0 < n; i0 += kThreads) {
-      // Scores cluster in a few digits; lanes with equal digits add once (one leader).
-      const int32_t i = i0 + lane;
-      const uint32_t key = i < n ? keys[i] : 0u;
-      const bool in = i < n && (key & pmask) == prefix;
-      const uint32_t digit = in ? (key >> shift) & 255u : 256u;
-      const uint32_t peers = __match_any_sync(0xffffffffu, digit);
-      if (in && lane == __ffs(peers) - 1) atomicAdd(&hcur[digit], __popc(peers));
+    if (pass > 0) {
+      for (int i = tid; i < 256; i += kThreads) hist[(pass + 1) % 3][i] = 0;
+      for (int32_t i0 = warp * 32; i0 < n; i0 += kThreads) {
+        const int32_t i = i0 + lane;
+        const uint32_t kk = i < n ? keys[i] : 0u;
+        const bool in = i < n && (kk & pmask) == prefix;
+        const uint32_t digit = in ? (kk >> shift) & 255u : 256u;
+        const uint32_t peers = __match_any_sync(0xffffffffu, digit);
+        if (in && lane == __ffs(peers) - 1) atomicAdd(&hcur[digit], __popc(peers));
+      }
+      __syncthreads();
     }
-    __syncthreads();
     int32_t dg, rm, cnt;
     find_digit(hcur, lane, remaining, &dg, &rm, &cnt);
     prefix |= (uint32_t)dg << shift;
@@ -292,55 +296,127 @@ __global__ void __launch_bounds__(kThreads) score_topk_kernel(ScoreArgs a) {
       break;
     }
   }
-  int32_t* mark = pages;  // the leader's page share is no longer needed
-  if (ranked) {
-    // The <= 32 keys of the boundary bin, ranked by (key desc, block asc); the first
-    // `remaining` of them are kept.
-    for (int32_t i = tid; i < n; i += kThreads)
-      if ((keys[i] & pmask) == prefix) bnd_idx[atomicAdd(&bnd_cnt, 1)] = i;
-    __syncthreads();
-    if (warp == 0) {
-      const int32_t m = bnd_cnt;
-      const int32_t idx = lane < m ? bnd_idx[lane] : INT32_MAX;
-      const uint32_t key = lane < m ? keys[idx] : 0u;
-      int32_t rank = 0;
-      for (int32_t j = 0; j < m; ++j) {
-        const uint32_t kj = __shfl_sync(0xffffffffu, key, j);
-        const int32_t ij = __shfl_sync(0xffffffffu, idx, j);
-        rank += kj > key || (kj == key && ij < idx);
+
+  // 4. A key above the boundary bin is kept; inside the bin, taken in block order, the
+  // ranked ones are kept, or after four passes (bin = keys equal to the k-th) the first
+  // `remaining`.  A kept key's output slot = kept keys before it in block order = keys
+  // above the bin before it + kept bin keys before it, so one count of each suffices.
+  if (n <= kFastRounds * kThreads) {
+    uint32_t b_above[kFastRounds], b_in[kFastRounds];
+#pragma unroll
+    for (int rr = 0; rr < kFastRounds; ++rr) {
+      const int32_t i = rr * kThreads + tid;
+      const uint32_t hi = i < n ? keys[i] & pmask : 0u;
+      b_above[rr] = __ballot_sync(0xffffffffu, i < n && hi > prefix);
+      b_in[rr] = __ballot_sync(0xffffffffu, i < n && hi == prefix);
+      if (lane == 0) {
+        wcnt[0][rr * kWarps + warp] = __popc(b_above[rr]);
+        wcnt[1][rr * kWarps + warp] = __popc(b_in[rr]);
       }
-      if (lane < m) mark[idx] = rank < remaining;
     }
     __syncthreads();
+    // exclusive prefixes over (round, warp) in block order: lane j holds entry j
+    int32_t tot_above, tot_in;
+    const int32_t pa = warp_exclusive_scan(wcnt[0][lane], lane, &tot_above);
+    const int32_t pi = warp_exclusive_scan(wcnt[1][lane], lane, &tot_in);
+    const uint32_t lt = (1u << lane) - 1u;
+    int32_t t_in[kFastRounds], a_before[kFastRounds];
+#pragma unroll
+    for (int rr = 0; rr < kFastRounds; ++rr) {
+      t_in[rr] = __shfl_sync(0xffffffffu, pi, rr * kWarps + warp) + __popc(b_in[rr] & lt);
+      a_before[rr] = __shfl_sync(0xffffffffu, pa, rr * kWarps + warp) + __popc(b_above[rr] & lt);
+    }
+    uint32_t take_mask = 0;
+    if (ranked) {  // tot_in <= 32
+#pragma unroll
+      for (int rr = 0; rr < kFastRounds; ++rr)
+        if ((b_in[rr] >> lane) & 1u) bnd_idx[t_in[rr]] = rr * kThreads + tid;
+      __syncthreads();
+      if (warp == 0) {
+        const uint32_t key = lane < tot_in ? keys[bnd_idx[lane]] : 0u;
+        int32_t rank = 0;  // higher score, or equal score and lower block (lane)
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+          const uint32_t kj = __shfl_sync(0xffffffffu, key, j);
+          rank += j < tot_in && (kj > key || (kj == key && j < lane));
+        }
+        const uint32_t m = __ballot_sync(0xffffffffu, lane < tot_in && rank < remaining);
+        if (lane == 0) s_take = m;
+      }
+      __syncthreads();
+      take_mask = s_take;
+    }
+#pragma unroll
+    for (int rr = 0; rr < kFastRounds; ++rr) {
+      const int32_t t = t_in[rr];
+      const int32_t bin_before =
+          ranked ? __popc(t < 32 ? take_mask & ((1u << t) - 1u) : take_mask) : min(t, remaining);
+      const bool take = ((b_above[rr] >> lane) & 1u) ||
+                        (((b_in[rr] >> lane) & 1u) &&
+                         (ranked ? ((take_mask >> t) & 1u) != 0 : t < remaining));
+      if (take) sel_u[a_before[rr] + bin_before] = b_lo + rr * kThreads + tid;
+    }
+    if (tid == 0) a.nsel[u] = tot_above + (ranked ? __popc(take_mask) : min(tot_in, remaining));
+    return;
   }
 
-  // 4. keep a key above the boundary bin; inside it, the ranked ones (or, after four
-  // passes, the first `remaining` equal keys in block order).  Written ascending.
-  const int32_t chunk = (n + kThreads - 1) / kThreads;
-  const int32_t c0 = min(n, tid * chunk), c1 = min(n, c0 + chunk);
-  int32_t total, eq_rank = 0, n_eq = 0;
-  if (!ranked) {
-    for (int32_t i = c0; i < c1; ++i) n_eq += keys[i] == prefix;
-    eq_rank = block_exclusive_scan(n_eq, scratch, &total);
+  // Longer candidate lists: one warp walks the keys, lane l taking [l c, l c + c).
+  if (warp != 0) return;
+  const int32_t chunk = (n + 31) / 32;
+  const int32_t c0 = min(n, lane * chunk), c1 = min(n, c0 + chunk);
+  int32_t in_bin = 0;
+  for (int32_t i = c0; i < c1; ++i) in_bin += (keys[i] & pmask) == prefix;
+  int32_t bin_total;
+  const int32_t bin0 = warp_exclusive_scan(in_bin, lane, &bin_total);
+  uint32_t take_mask = 0;  // ranked: bit t set = the bin's t-th key in block order is kept
+  if (ranked) {            // bin_total <= 32
+    int32_t t = bin0;
+    for (int32_t i = c0; i < c1; ++i)
+      if ((keys[i] & pmask) == prefix) bnd_idx[t++] = i;
+    __syncwarp();
+    const uint32_t key = lane < bin_total ? keys[bnd_idx[lane]] : 0u;
+    int32_t rank = 0;
+#pragma unroll
+    for (int j = 0; j < 32; ++j) {
+      const uint32_t kj = __shfl_sync(0xffffffffu, key, j);
+      rank += j < bin_total && (kj > key || (kj == key && j < lane));
+    }
+    take_mask = __ballot_sync(0xffffffffu, lane < bin_total && rank < remaining);
   }
   int32_t n_take = 0;
-  for (int32_t i = c0; i < c1; ++i) {
-    const uint32_t hi = keys[i] & pmask;
-    n_take += hi > prefix || (hi == prefix && (ranked ? mark[i] != 0 : eq_rank++ < remaining));
+  {
+    int32_t t = bin0;
+    for (int32_t i = c0; i < c1; ++i) {
+      const uint32_t hi = keys[i] & pmask;
+      if (hi > prefix) {
+        ++n_take;
+      } else if (hi == prefix) {
+        n_take += ranked ? (int32_t)((take_mask >> t) & 1u) : (t < remaining);
+        ++t;
+      }
+    }
   }
-  int32_t pos = block_exclusive_scan(n_take, scratch, &total);
-  eq_rank -= n_eq;
-  for (int32_t i = c0; i < c1; ++i) {
-    const uint32_t hi = keys[i] & pmask;
-    if (hi > prefix || (hi == prefix && (ranked ? mark[i] != 0 : eq_rank++ < remaining)))
-      sel_u[pos++] = b_lo + i;
+  int32_t total;
+  int32_t pos = warp_exclusive_scan(n_take, lane, &total);
+  {
+    int32_t t = bin0;
+    for (int32_t i = c0; i < c1; ++i) {
+      const uint32_t hi = keys[i] & pmask;
+      bool take = hi > prefix;
+      if (hi == prefix) {
+        take = ranked ? ((take_mask >> t) & 1u) != 0 : t < remaining;
+        ++t;
+      }
+      if (take) sel_u[pos++] = b_lo + i;
+    }
   }
-  if (tid == 0) a.nsel[u] = total;
+  if (lane == 0) a.nsel[u] = total;
 }
 
 template <typename T, int D>
 cudaError_t launch(const ScoreArgs& a, int32_t units, int32_t cluster, cudaStream_t s) {
-  const size_t smem = sizeof(uint32_t) * 2 * (size_t)a.max_blocks;
+  size_t smem = sizeof(uint32_t) * 2 * (size_t)a.max_blocks;
+  if (smem < (size_t)kScoreExclusiveSmem) smem = kScoreExclusiveSmem;
   auto kernel = score_topk_kernel<T, D>;
   // Once per device: the largest dynamic shared memory the host checks allow, and the full
   // shared-memory carveout, so that an SM running this kernel keeps room for a decode CTA
@@ -364,17 +440,36 @@ cudaError_t launch(const ScoreArgs& a, int32_t units, int32_t cluster, cudaStrea
   lc.blockDim = dim3(kThreads);
   lc.dynamicSmemBytes = smem;
   lc.stream = s;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = (unsigned)cluster;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
+  // One CTA of a cluster per SM, so that every SM keeps room for a decode CTA.
+  attr[1].id = cudaLaunchAttributeClusterSchedulingPolicyPreference;
+  attr[1].val.clusterSchedulingPolicyPreference = cudaClusterSchedulingPolicySpread;
   lc.attrs = attr;
-  lc.numAttrs = 1;
+  lc.numAttrs = 2;
   return cudaLaunchKernelEx(&lc, kernel, a);
 }
 
+// Candidates of the longest request the block table allows.
+int64_t max_candidates(const srkv_config& cfg, int32_t max_blocks) {
+  const int64_t W = (int64_t)max_blocks * kBlock - cfg.local_tokens;
+  return W > cfg.init_tokens ? (W + kBlock - 1) / kBlock - cfg.init_tokens / kBlock : 0;
+}
+
+// CTAs per unit: about 64 candidates each, at most 8 (a portable cluster).
+int32_t cluster_for(int64_t nmax) {
+  const int64_t c = (nmax + 63) / 64;
+  return (int32_t)(c < 1 ? 1 : (c > 8 ? 8 : c));
+}
+
 }  // namespace
+
+int64_t score_topk_ctas(const srkv_config& cfg, int32_t max_blocks, int32_t batch) {
+  return (int64_t)batch * cfg.num_kv_heads * cluster_for(max_candidates(cfg, max_blocks));
+}
 
 cudaError_t launch_score_topk(const srkv_config& cfg, const void* q, const float* reps,
                               int64_t num_pages, const int32_t* block_table,
@@ -403,14 +498,10 @@ cudaError_t launch_score_topk(const srkv_config& cfg, const void* q, const float
   a.topk_percent = cfg.topk_percent;
   const int32_t units = batch * cfg.num_kv_heads;
   if (units == 0) return cudaSuccess;
-  // Candidates of the longest request the block table allows -> CTAs per unit (<= 8,
-  // about 64 candidates each).
-  int64_t W = (int64_t)max_blocks * kBlock - cfg.local_tokens;
-  int64_t nmax = W > cfg.init_tokens ? (W + kBlock - 1) / kBlock - cfg.init_tokens / kBlock : 0;
+  const int64_t nmax = max_candidates(cfg, max_blocks);
   if (nmax > INT32_MAX) return cudaErrorInvalidValue;
   a.nmax = (int32_t)nmax;
-  int32_t cluster = (int32_t)((nmax + 63) / 64);
-  cluster = cluster < 1 ? 1 : (cluster > 8 ? 8 : cluster);
+  const int32_t cluster = cluster_for(nmax);
   if ((int64_t)units * cluster > INT32_MAX) return cudaErrorInvalidValue;
   if (cfg.dtype == SRKV_BF16)
     return cfg.head_dim == 128 ? launch<__nv_bfloat16, 128>(a, units, cluster, stream)

@@ -121,8 +121,12 @@ srkv_status prepare_decode(const srkv_config* cfg, const void* q, const void* k_
   a.scale_log2 = kLog2e / sqrtf((float)cfg->head_dim);
   a.ctas = mma ? mma_split_ctas(sms) : simt_split_ctas(sms);
   if (a.ctas > kMaxCtas) a.ctas = kMaxCtas;
+  a.ctas_a = a.ctas;
   a.lay = ws_layout(batch * cfg->num_kv_heads, kMaxCtas, G, cfg->head_dim);
   a.early = 0;
+  a.prompt_lens = nullptr;
+  a.dense_boundary = cfg->dense_boundary;
+  a.topk_percent = cfg->topk_percent;
   return SRKV_OK;
 }
 
@@ -260,12 +264,19 @@ srkv_status srkv_retrieval_decode(const srkv_config* cfg, const void* q, const v
   st = prepare_decode(cfg, q, k_cache, v_cache, num_pages, block_table, max_blocks, seq_lens,
                       batch, sel, kmax, nsel, out, workspace, workspace_bytes, error_flags, a);
   if (st != SRKV_OK) return st;
-  // The scoring kernel, then the decode, which streams list A while the scoring finishes.
+  // The scoring kernel, then the decode, which streams list A while the scoring finishes
+  // and knows the selection counts it will write from the lengths.  A scoring CTA keeps its
+  // SM to itself, so list A goes to the decode CTAs that find an SM free at once (the grid
+  // is scheduled in block order); the others start when the scoring ends and take list B.
+  a.prompt_lens = prompt_lens;
+  const bool early = mma_split_supported(*cfg);
+  const int64_t scoring = score_topk_ctas(*cfg, max_blocks, batch);
+  if (early && 2 * scoring <= a.ctas) a.ctas_a = a.ctas - (int32_t)scoring;
   cudaStream_t s = (cudaStream_t)stream;
   if (launch_score_topk(*cfg, q, reps, num_pages, block_table, max_blocks, seq_lens, prompt_lens,
                         batch, sel, kmax, nsel, error_flags, s) != cudaSuccess)
     return SRKV_ERR_CUDA;
-  return launch_decode(cfg, a, mma_split_supported(*cfg) ? 1 : 0, s);
+  return launch_decode(cfg, a, early ? 1 : 0, s);
 }
 
 // Scratch of srkv_sparse_paged_decode_noalloc: one array per device that loads the library.

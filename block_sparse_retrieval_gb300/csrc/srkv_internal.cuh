@@ -65,13 +65,27 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   return done != 0;
 }
 
+// try_wait that may suspend the thread for up to `hint_ns` until the phase completes: a
+// waiting warp then sleeps instead of taking issue slots from the warps sharing its SM.
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t* bar, uint32_t parity,
+                                                    uint32_t hint_ns) {
+  uint32_t done;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(done)
+      : "r"(smem_u32(bar)), "r"(parity), "r"(hint_ns)
+      : "memory");
+  return done != 0;
+}
+
 // Waits for the phase with the given parity to complete; gives up after kWaitLimitNs.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = global_ns();
   for (;;) {
-    for (int i = 0; i < 32; ++i)
-      if (mbar_try_wait(bar, parity)) return true;
+    if (mbar_try_wait_sleep(bar, parity, 1000000u)) return true;
     if (global_ns() - t0 > kWaitLimitNs) return false;
   }
 }
@@ -84,6 +98,45 @@ __device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t b
       "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
       ::"r"(smem_u32(dst)), "l"(src), "r"(bytes), "r"(smem_u32(bar))
       : "memory");
+}
+
+// L2 eviction policies: data read once per step (the K/V pages) goes first, data every step
+// reads again (the representation vectors) last.
+__device__ __forceinline__ uint64_t l2_policy_evict_first() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+__device__ __forceinline__ uint64_t l2_policy_evict_last() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+
+// bulk_load with an L2 eviction policy.
+__device__ __forceinline__ void bulk_load_hint(void* dst, const void* src, uint32_t bytes,
+                                               uint64_t* bar, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+      " [%0], [%1], %2, [%3], %4;"
+      ::"r"(smem_u32(dst)), "l"(src), "r"(bytes), "r"(smem_u32(bar)), "l"(policy)
+      : "memory");
+}
+
+// 16-byte read-only global load with an L2 eviction policy.
+__device__ __forceinline__ float4 ldg_f4_hint(const float* p, uint64_t policy) {
+  float4 v;
+  asm volatile("ld.global.nc.L2::cache_hint.v4.f32 {%0, %1, %2, %3}, [%4], %5;"
+               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+               : "l"(p), "l"(policy));
+  return v;
+}
+__device__ __forceinline__ float2 ldg_f2_hint(const float* p, uint64_t policy) {
+  float2 v;
+  asm volatile("ld.global.nc.L2::cache_hint.v2.f32 {%0, %1}, [%2], %3;"
+               : "=f"(v.x), "=f"(v.y)
+               : "l"(p), "l"(policy));
+  return v;
 }
 
 // Programmatic dependent launch: let the next kernel in the stream be scheduled early, and
@@ -274,9 +327,24 @@ struct DecodeArgs {
   int32_t init_tokens, local_tokens;
   float scale_log2;  // log2(e) / sqrt(d)
   int32_t ctas;      // C, the split grid
+  int32_t ctas_a;    // CTAs [0, ctas_a) share list A; the others take list B only
   int32_t early;     // 1: the previous kernel is score_topk, so every input but sel and nsel
                      // may be read before it finishes (list A streams during the scoring)
+  // early = 1 only: what score_topk derives its selection counts from, so that the
+  // decode knows every nsel (selection_count) before the selection exists
+  const int32_t* prompt_lens;
+  int32_t dense_boundary;
+  double topk_percent;
 };
+
+// CTAs that share the positions of a list.
+__host__ __device__ __forceinline__ int32_t list_ctas(const DecodeArgs& a, int list) {
+  return list == 0 ? a.ctas_a : a.ctas;
+}
+
+// Shared memory a scoring CTA takes at least: with it no decode CTA (about 217 KB) fits on
+// the same SM (228 KB), so the scoring never shares an SM with pages streaming in.
+constexpr int kScoreExclusiveSmem = 16 * 1024;
 
 // k = min(n, ceil(p*n - 1e-9)) with separately rounded operations (no contraction), so
 // that the host and the device agree on every n.
@@ -288,11 +356,44 @@ __device__ __forceinline__ int32_t device_topk_count(int32_t n, double p) {
   return (int32_t)x;
 }
 
+// Candidates of one request and how many of them score_topk keeps (it writes exactly k
+// into nsel).  Candidates are the blocks meeting the offload range [INIT, L - LOCAL), from
+// block b_lo = INIT / 128 on; a prompt shorter than the dense boundary keeps all of them,
+// otherwise k = min(n, ceil(p n - 1e-9)); k is capped at kmax (flagged).  `prompt` is the
+// prompt length, or L itself when the caller gives none.
+struct SelCount {
+  int32_t n, k;
+  uint32_t flags;
+};
+
+__device__ __forceinline__ SelCount selection_count(int32_t L, int32_t prompt, int32_t max_blocks,
+                                                    int32_t kmax, int32_t INIT, int32_t LOCAL,
+                                                    int32_t dense_boundary, double p) {
+  SelCount c;
+  c.flags = 0;
+  const int32_t Lmax = max_blocks * kBlock;
+  if (L < 0 || L > Lmax) {
+    c.flags |= SRKV_EFLAG_SEQ_LEN;
+    L = L < 0 ? 0 : Lmax;
+  }
+  const int32_t W = L - LOCAL;
+  c.n = W > INIT ? (W + kBlock - 1) / kBlock - INIT / kBlock : 0;
+  c.k = prompt < dense_boundary ? c.n : device_topk_count(c.n, p);
+  if (c.k > kmax) {
+    c.flags |= SRKV_EFLAG_SELECTION;
+    c.k = kmax;
+  }
+  return c;
+}
+
 // ---- launchers (defined in the kernel files) ---------------------------------------------
 
 cudaError_t launch_block_reps(const srkv_config& cfg, const void* k_cache, int64_t num_pages,
                               const int32_t* page_ids, const int32_t* valid, int32_t n,
                               float* reps, int32_t* error_flags, cudaStream_t stream);
+
+// CTAs of the scoring grid (clusters of up to 8 per (request, kv head) unit).
+int64_t score_topk_ctas(const srkv_config& cfg, int32_t max_blocks, int32_t batch);
 
 cudaError_t launch_score_topk(const srkv_config& cfg, const void* q, const float* reps,
                               int64_t num_pages, const int32_t* block_table,

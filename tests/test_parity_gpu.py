@@ -87,7 +87,7 @@ def test_small_case_parity(name):
 
 
 def check_fused_step(case, buf, ref, exact_score_topk, units=None):
-    """srkv_retrieval_decode (one kernel: it scores and selects on chip) against the oracle."""
+    """srkv_retrieval_decode (scoring, then the decode behind it) against the oracle."""
     fused = srkv.DecodeBuffers(case.cfg, case.batch, case.max_blocks, case.num_pages,
                                device=case.q.device)
     fused.reps.copy_(buf.reps)
@@ -99,10 +99,12 @@ def check_fused_step(case, buf, ref, exact_score_topk, units=None):
     fsel, fnsel = fused.sel.cpu().numpy(), fused.nsel.cpu().numpy()
     exact = check_selection(case, fsel, fnsel, ref, units)
     got = fused.out.float().cpu().numpy()
-    # the same kernel math as the split decode fed the fused selection: identical bits
+    # The split decode fed the fused selection computes the same sums, but the fused call
+    # spreads the initial and window pages over fewer CTAs (the scoring CTAs hold the other
+    # SMs), so the partials split at other pages: equal up to rounding, not to the bit.
     again = gpu_decode(case, buf, fsel, fnsel)
     if units is None:
-        assert np.array_equal(got, again)
+        check_out(case, got, again)
     n_units = len(units) if units else case.batch * case.cfg["num_kv_heads"]
     if exact == n_units:
         check_out(case, got, ref["out"], units)
