@@ -11,12 +11,15 @@
 // an equal share of all units' page lists (see decode_plan.cuh).
 //   producer: plans list A (initial + window pages) and list B (selected pages) with
 //             warp-level scans, resolves 32 list positions at once (one per lane), and lane 0
-//             streams the pages through a ring of stages (3 x 64 KiB for d = 128) with
-//             cp.async.bulk, completion counted on an mbarrier per stage.  When the previous
+//             streams the pages through a ring of stages (3 x 64 KiB for d = 128) with tiled
+//             TMA copies (128-byte swizzle, 64-column boxes of a whole 128-row slab),
+//             completion counted on an mbarrier per stage.  When the previous
 //             kernel is the scoring kernel, list A is streamed before that kernel finishes
 //             (programmatic launch) and the producer waits for the selection only before
 //             list B; a sentinel stage ends the consumers' loop;
-//   consumers: warp w owns rows [16w, 16w+16) of every page.  The group's queries are the
+//   consumers: warp w owns rows [16w, 16w+16) of every page; MMA row m of the tile is token
+//             m ^ 4 (m odd) or m (m even), which with the swizzle lets every 8-lane phase
+//             of a 16-byte fragment load hit 8 distinct bank groups.  The group's queries are the
 //             N = 8 side of m16n8k16 bf16 MMAs, keys/values the M = 16 side:
 //               S^T[16 tok x 8 heads]  = K[16 x d] . Q^T[d x 8]
 //               O^T[d x 8 heads]      += V^T[d x 16 tok] . P[16 tok x 8]
@@ -64,7 +67,23 @@ struct Cfg {
   static constexpr size_t kOffBar = kOffInfo + sizeof(StageInfo) * kStages;
   // full[kStages], empty[kStages], merge w1, w2, r2
   static constexpr size_t kSmem = kOffBar + sizeof(uint64_t) * (2 * kStages + 3);
+  static constexpr size_t kSmemAlloc = kSmem + 1024;  // the swizzled stages need 1 KiB alignment
+  static constexpr int kBoxes = D / 64;                // 64-column TMA boxes per slab
+  static constexpr int kBoxBytes = kBlock * 128;       // 128 rows of 128 bytes
 };
+
+// Tensor maps of the K and V caches, [page][kv head * 128 + row][d] (bf16).
+struct TmaMaps {
+  CUtensorMap k, v;
+};
+
+// MMA tile row m -> token row within the 16-row tile (an involution).
+__device__ __forceinline__ int tile_token(int m) { return m ^ ((m & 1) << 2); }
+
+// Byte offset of (row, 16-byte chunk c) in a slab loaded with the 128-byte swizzle.
+__device__ __forceinline__ uint32_t swz(int row, int c) {
+  return (uint32_t)((c >> 3) * (kBlock * 128) + row * 128 + (((c & 7) ^ (row & 7)) << 4));
+}
 
 struct Lane {
   int g, t;
@@ -133,9 +152,10 @@ __device__ __forceinline__ int d_of(int g, int v) {
 // Hands stage `it` to the consumers: waits until it is free, writes its description and
 // arms its mbarrier with the bytes of the copies it starts (called by one producer lane).
 template <int D>
-__device__ __forceinline__ void issue_stage(const DecodeArgs& a, unsigned char* smem, int64_t it,
-                                            int32_t u, uint32_t fl, const PageTask& t,
-                                            int64_t& armed, bool& abort, uint32_t& eflags) {
+__device__ __forceinline__ void issue_stage(const DecodeArgs& a, const TmaMaps& maps,
+                                            unsigned char* smem, int64_t it, int32_t u,
+                                            uint32_t fl, const PageTask& t, int64_t& armed,
+                                            bool& abort, uint32_t& eflags) {
   using C = Cfg<D>;
   if (abort) return;
   StageInfo* sInfo = reinterpret_cast<StageInfo*>(smem + C::kOffInfo);
@@ -155,23 +175,24 @@ __device__ __forceinline__ void issue_stage(const DecodeArgs& a, unsigned char* 
   inf.hi = load ? t.hi : 0;
   inf.ie = t.ie;
   inf.ws = t.ws;
-  const uint32_t rows = load ? (uint32_t)(t.hi - t.lo) : 0u;
-  const uint32_t slab_bytes = rows * D * 2;
+  // The whole 128-row slab is copied (the swizzle needs whole 1 KiB atoms); rows outside
+  // [lo, hi) are masked by the consumers.
+  const bool rows = load && t.hi > t.lo;
   const uint32_t qbytes = (uint32_t)(a.G * D * 2);
-  const uint32_t tx = 2 * slab_bytes + ((fl & kNewUnit) ? qbytes : 0u);
+  const uint32_t tx = (rows ? 2u * C::kSlab : 0u) + ((fl & kNewUnit) ? qbytes : 0u);
   mbar_arrive_expect_tx(&full[s], tx);
   ++armed;
   if (u < 0) return;
   const int32_t h = u % a.Hkv, r = u / a.Hkv;
   if (rows) {  // pages are read once per step: first out of L2
     const uint64_t once = l2_policy_evict_first();
-    const int64_t src = (((int64_t)t.page * a.Hkv + h) * kBlock + t.lo) * D;
-    bulk_load_hint(smem + C::kOffK + (size_t)s * C::kSlab + (size_t)t.lo * D * 2,
-                   static_cast<const __nv_bfloat16*>(a.k_cache) + src, slab_bytes, &full[s],
-                   once);
-    bulk_load_hint(smem + C::kOffV + (size_t)s * C::kSlab + (size_t)t.lo * D * 2,
-                   static_cast<const __nv_bfloat16*>(a.v_cache) + src, slab_bytes, &full[s],
-                   once);
+#pragma unroll
+    for (int b = 0; b < C::kBoxes; ++b) {
+      tma_load_3d(smem + C::kOffK + (size_t)s * C::kSlab + (size_t)b * C::kBoxBytes, &maps.k,
+                  64 * b, h * kBlock, t.page, &full[s], once);
+      tma_load_3d(smem + C::kOffV + (size_t)s * C::kSlab + (size_t)b * C::kBoxBytes, &maps.v,
+                  64 * b, h * kBlock, t.page, &full[s], once);
+    }
   }
   if (fl & kNewUnit)
     bulk_load(smem + C::kOffQ + (size_t)s * C::kQBytes,
@@ -190,9 +211,11 @@ __device__ __forceinline__ void warp_arrive(uint64_t* bar) {
 // sub-partition (12K) beside one warp of a combine CTA, so the combine is resident and
 // waiting when the last partial is written.
 template <int D>
-__global__ void __maxnreg__(128) split_mma_kernel(const DecodeArgs a) {
+__global__ void __maxnreg__(128) split_mma_kernel(const DecodeArgs a,
+                                                  const __grid_constant__ TmaMaps maps) {
   using C = Cfg<D>;
-  extern __shared__ __align__(128) unsigned char smem[];
+  extern __shared__ __align__(128) unsigned char smem_raw[];
+  unsigned char* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   unsigned char* sK = smem + C::kOffK;
   unsigned char* sV = smem + C::kOffV;
   unsigned char* sQ = smem + C::kOffQ;
@@ -299,7 +322,7 @@ __global__ void __maxnreg__(128) split_mma_kernel(const DecodeArgs a) {
           t.hi = __shfl_sync(0xffffffffu, task.hi, l);
           t.ie = __shfl_sync(0xffffffffu, task.ie, l);
           t.ws = __shfl_sync(0xffffffffu, task.ws, l);
-          if (lane == 0) issue_stage<D>(a, smem, it, u, fl, t, armed, abort, eflags);
+          if (lane == 0) issue_stage<D>(a, maps, smem, it, u, fl, t, armed, abort, eflags);
           abort = __shfl_sync(0xffffffffu, abort, 0);
           ++it;
         }
@@ -309,7 +332,7 @@ __global__ void __maxnreg__(128) split_mma_kernel(const DecodeArgs a) {
       PageTask none;
       none.page = -1;
       none.lo = none.hi = none.ie = none.ws = 0;
-      issue_stage<D>(a, smem, it, -1, kLast, none, armed, abort, eflags);  // sentinel
+      issue_stage<D>(a, maps, smem, it, -1, kLast, none, armed, abort, eflags);  // sentinel
       // Drain: every copy this CTA issued must land before the CTA exits.
       const int64_t first = armed > C::kStages ? armed - C::kStages : 0;
       for (int64_t i = first; i < armed; ++i)
@@ -362,11 +385,11 @@ __global__ void __maxnreg__(128) split_mma_kernel(const DecodeArgs a) {
       const unsigned char* v = sV + (size_t)s * C::kSlab;
       // ---- S^T = K . Q^T
       float sacc[4] = {0.f, 0.f, 0.f, 0.f};
-      const int ra = row0 + ln.g, rb = ra + 8;
+      const int ra = row0 + tile_token(ln.g), rb = ra + 8;
 #pragma unroll
       for (int j = 0; j < C::KJ; ++j) {
-        const int4 k0 = lds128(k + ((size_t)ra * D + 32 * j + 8 * ln.t) * 2);
-        const int4 k1 = lds128(k + ((size_t)rb * D + 32 * j + 8 * ln.t) * 2);
+        const int4 k0 = lds128(k + swz(ra, 4 * j + ln.t));
+        const int4 k1 = lds128(k + swz(rb, 4 * j + ln.t));
         mma_16816(sacc, k0.x, k1.x, k0.y, k1.y, qb[j][0], qb[j][1]);
         mma_16816(sacc, k0.z, k1.z, k0.w, k1.w, qb[j][2], qb[j][3]);
       }
@@ -405,14 +428,14 @@ __global__ void __maxnreg__(128) split_mma_kernel(const DecodeArgs a) {
       const uint32_t b1 = movmatrix_trans(p23);  // (head g, tokens 2t+8, 2t+9)
       // ---- O^T += V^T . P
       int4 vt[4][C::NCH];
-      const int trow[4] = {row0 + 2 * ln.t, row0 + 2 * ln.t + 1, row0 + 2 * ln.t + 8,
-                           row0 + 2 * ln.t + 9};
+      const int trow[4] = {row0 + tile_token(2 * ln.t), row0 + tile_token(2 * ln.t + 1),
+                           row0 + tile_token(2 * ln.t + 8), row0 + tile_token(2 * ln.t + 9)};
 #pragma unroll
       for (int x = 0; x < 4; ++x) {
         const bool in = trow[x] >= inf.lo && trow[x] < inf.hi;
 #pragma unroll
         for (int c = 0; c < C::NCH; ++c)
-          vt[x][c] = in ? lds128(v + ((size_t)trow[x] * D + 8 * (ln.g + 8 * c)) * 2)
+          vt[x][c] = in ? lds128(v + swz(trow[x], ln.g + 8 * c))
                         : make_int4(0, 0, 0, 0);
       }
 #pragma unroll
@@ -462,16 +485,21 @@ __global__ void __maxnreg__(128) split_mma_kernel(const DecodeArgs a) {
           float* accp = reinterpret_cast<float*>(a.ws + a.lay.acc) + slot * a.G * D;
           float* mlp = reinterpret_cast<float*>(a.ws + a.lay.ml) + slot * a.G * 2;
           const int h0 = 2 * ln.t, h1 = h0 + 1;
+          // values 4k..4k+3 of a lane sit at 4 consecutive d (d_of): 16-byte stores
 #pragma unroll
-          for (int i = 0; i < C::MT; ++i) {
-            const int da = d_of<D>(ln.g, i), db = d_of<D>(ln.g, C::MT + i);
+          for (int k4 = 0; k4 < C::MT; k4 += 4) {
+            const int da = d_of<D>(ln.g, k4), db = d_of<D>(ln.g, C::MT + k4);
             if (h0 < a.G) {
-              accp[h0 * D + da] = st.acc[i][0];
-              accp[h0 * D + db] = st.acc[i][2];
+              *reinterpret_cast<float4*>(accp + h0 * D + da) = make_float4(
+                  st.acc[k4][0], st.acc[k4 + 1][0], st.acc[k4 + 2][0], st.acc[k4 + 3][0]);
+              *reinterpret_cast<float4*>(accp + h0 * D + db) = make_float4(
+                  st.acc[k4][2], st.acc[k4 + 1][2], st.acc[k4 + 2][2], st.acc[k4 + 3][2]);
             }
             if (h1 < a.G) {
-              accp[h1 * D + da] = st.acc[i][1];
-              accp[h1 * D + db] = st.acc[i][3];
+              *reinterpret_cast<float4*>(accp + h1 * D + da) = make_float4(
+                  st.acc[k4][1], st.acc[k4 + 1][1], st.acc[k4 + 2][1], st.acc[k4 + 3][1]);
+              *reinterpret_cast<float4*>(accp + h1 * D + db) = make_float4(
+                  st.acc[k4][3], st.acc[k4 + 1][3], st.acc[k4 + 2][3], st.acc[k4 + 3][3]);
             }
           }
           if (ln.g == 0) {
@@ -505,6 +533,39 @@ bool mma_split_supported(const srkv_config& cfg) {
 
 int32_t mma_split_ctas(int32_t sm_count) { return sm_count; }
 
+using EncodeTiled = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                 const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                 const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                 CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+// The driver's tensor-map encoder, looked up once through the runtime.
+EncodeTiled encode_tiled() {
+  static EncodeTiled fn = [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      p = nullptr;
+    return reinterpret_cast<EncodeTiled>(p);
+  }();
+  return fn;
+}
+
+// [num_pages][Hkv * 128][d] bf16, boxes of 64 columns x 128 rows, 128-byte swizzle.
+bool encode_cache_map(CUtensorMap* map, const void* base, int64_t num_pages, int32_t Hkv,
+                      int32_t d) {
+  const EncodeTiled fn = encode_tiled();
+  if (!fn || num_pages > INT32_MAX || (int64_t)Hkv * kBlock > INT32_MAX) return false;
+  const cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)Hkv * kBlock, (cuuint64_t)num_pages};
+  const cuuint64_t strides[2] = {(cuuint64_t)d * 2, (cuuint64_t)Hkv * kBlock * d * 2};
+  const cuuint32_t box[3] = {64, (cuuint32_t)kBlock, 1};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides,
+            box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 template <int D>
 cudaError_t launch_d(const DecodeArgs& a, cudaStream_t stream) {
   // The shared-memory opt-in is set once per device (not during graph capture).
@@ -515,11 +576,16 @@ cudaError_t launch_d(const DecodeArgs& a, cudaStream_t stream) {
   if (dev < 0 || dev >= 128) return cudaErrorInvalidDevice;
   if (!configured[dev]) {
     e = cudaFuncSetAttribute(split_mma_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)Cfg<D>::kSmem);
+                             (int)Cfg<D>::kSmemAlloc);
     if (e != cudaSuccess) return e;
     configured[dev] = true;
   }
-  return launch_pdl(split_mma_kernel<D>, dim3(a.ctas), dim3(kThreads), Cfg<D>::kSmem, stream, a);
+  TmaMaps maps;
+  if (!encode_cache_map(&maps.k, a.k_cache, a.num_pages, a.Hkv, D) ||
+      !encode_cache_map(&maps.v, a.v_cache, a.num_pages, a.Hkv, D))
+    return cudaErrorInvalidValue;
+  return launch_pdl(split_mma_kernel<D>, dim3(a.ctas), dim3(kThreads), Cfg<D>::kSmemAlloc, stream,
+                    a, maps);
 }
 
 cudaError_t launch_split_mma(const DecodeArgs& a, cudaStream_t stream) {
