@@ -65,8 +65,8 @@ struct Cfg {
   static constexpr size_t kOffMerge = kOffQ + (size_t)kStages * kQBytes;
   static constexpr size_t kOffInfo = kOffMerge + sizeof(float) * 4 * kMergeSlot;
   static constexpr size_t kOffBar = kOffInfo + sizeof(StageInfo) * kStages;
-  // full[kStages], empty[kStages], merge w1, w2, r2
-  static constexpr size_t kSmem = kOffBar + sizeof(uint64_t) * (2 * kStages + 3);
+  // full (K, query, stage info)[kStages], full_v[kStages], empty[kStages], merge w1, w2, r2
+  static constexpr size_t kSmem = kOffBar + sizeof(uint64_t) * (3 * kStages + 3);
   static constexpr size_t kSmemAlloc = kSmem + 1024;  // the swizzled stages need 1 KiB alignment
   static constexpr int kBoxes = D / 64;                // 64-column TMA boxes per slab
   static constexpr int kBoxBytes = kBlock * 128;       // 128 rows of 128 bytes
@@ -160,7 +160,8 @@ __device__ __forceinline__ void issue_stage(const DecodeArgs& a, const TmaMaps& 
   if (abort) return;
   StageInfo* sInfo = reinterpret_cast<StageInfo*>(smem + C::kOffInfo);
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::kOffBar);
-  uint64_t* empty = full + C::kStages;
+  uint64_t* full_v = full + C::kStages;
+  uint64_t* empty = full_v + C::kStages;
   const int s = (int)(it % C::kStages);
   if (it >= C::kStages && !mbar_wait(&empty[s], (uint32_t)((it / C::kStages - 1) & 1))) {
     abort = true;
@@ -177,27 +178,33 @@ __device__ __forceinline__ void issue_stage(const DecodeArgs& a, const TmaMaps& 
   inf.ws = t.ws;
   // The whole 128-row slab is copied (the swizzle needs whole 1 KiB atoms); rows outside
   // [lo, hi) are masked by the consumers.
+  // K and the query complete `full`, V completes `full_v`, so the logits can start while V
+  // is still arriving.
   const bool rows = load && t.hi > t.lo;
   const uint32_t qbytes = (uint32_t)(a.G * D * 2);
-  const uint32_t tx = (rows ? 2u * C::kSlab : 0u) + ((fl & kNewUnit) ? qbytes : 0u);
-  mbar_arrive_expect_tx(&full[s], tx);
+  mbar_arrive_expect_tx(&full[s], (rows ? (uint32_t)C::kSlab : 0u) +
+                                      ((fl & kNewUnit) ? qbytes : 0u));
+  mbar_arrive_expect_tx(&full_v[s], rows ? (uint32_t)C::kSlab : 0u);
   ++armed;
   if (u < 0) return;
   const int32_t h = u % a.Hkv, r = u / a.Hkv;
-  if (rows) {  // pages are read once per step: first out of L2
-    const uint64_t once = l2_policy_evict_first();
+  const uint64_t once = l2_policy_evict_first();  // pages are read once per step
+  if (rows) {
 #pragma unroll
-    for (int b = 0; b < C::kBoxes; ++b) {
+    for (int b = 0; b < C::kBoxes; ++b)
       tma_load_3d(smem + C::kOffK + (size_t)s * C::kSlab + (size_t)b * C::kBoxBytes, &maps.k,
                   64 * b, h * kBlock, t.page, &full[s], once);
-      tma_load_3d(smem + C::kOffV + (size_t)s * C::kSlab + (size_t)b * C::kBoxBytes, &maps.v,
-                  64 * b, h * kBlock, t.page, &full[s], once);
-    }
   }
   if (fl & kNewUnit)
     bulk_load(smem + C::kOffQ + (size_t)s * C::kQBytes,
               static_cast<const __nv_bfloat16*>(a.q) + ((int64_t)r * a.Hq + (int64_t)h * a.G) * D,
               qbytes, &full[s]);
+  if (rows) {
+#pragma unroll
+    for (int b = 0; b < C::kBoxes; ++b)
+      tma_load_3d(smem + C::kOffV + (size_t)s * C::kSlab + (size_t)b * C::kBoxBytes, &maps.v,
+                  64 * b, h * kBlock, t.page, &full_v[s], once);
+  }
 }
 
 // One arrival per warp: the warp's lanes synchronise (ordering their shared-memory accesses)
@@ -222,7 +229,8 @@ __global__ void __maxnreg__(128) split_mma_kernel(const DecodeArgs a,
   float* sMerge = reinterpret_cast<float*>(smem + C::kOffMerge);
   StageInfo* sInfo = reinterpret_cast<StageInfo*>(smem + C::kOffInfo);
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::kOffBar);
-  uint64_t* empty = full + C::kStages;
+  uint64_t* full_v = full + C::kStages;
+  uint64_t* empty = full_v + C::kStages;
   uint64_t* mb_w1 = empty + C::kStages;
   uint64_t* mb_w2 = mb_w1 + 1;
   uint64_t* mb_r2 = mb_w1 + 2;
@@ -236,6 +244,7 @@ __global__ void __maxnreg__(128) split_mma_kernel(const DecodeArgs a,
   if (tid == 0) {
     for (int s = 0; s < C::kStages; ++s) {
       mbar_init(&full[s], 1);
+      mbar_init(&full_v[s], 1);
       mbar_init(&empty[s], kConsumerWarps);  // one arrival per consumer warp
     }
     mbar_init(mb_w1, 4);
@@ -336,7 +345,8 @@ __global__ void __maxnreg__(128) split_mma_kernel(const DecodeArgs a,
       // Drain: every copy this CTA issued must land before the CTA exits.
       const int64_t first = armed > C::kStages ? armed - C::kStages : 0;
       for (int64_t i = first; i < armed; ++i)
-        if (!mbar_wait(&full[i % C::kStages], (uint32_t)((i / C::kStages) & 1))) {
+        if (!mbar_wait(&full[i % C::kStages], (uint32_t)((i / C::kStages) & 1)) ||
+            !mbar_wait(&full_v[i % C::kStages], (uint32_t)((i / C::kStages) & 1))) {
           eflags |= SRKV_EFLAG_TIMEOUT;
           break;
         }
@@ -426,7 +436,11 @@ __global__ void __maxnreg__(128) split_mma_kernel(const DecodeArgs a,
       }
       const uint32_t b0 = movmatrix_trans(p01);  // (head g, tokens 2t, 2t+1)
       const uint32_t b1 = movmatrix_trans(p23);  // (head g, tokens 2t+8, 2t+9)
-      // ---- O^T += V^T . P
+      // ---- O^T += V^T . P, once V has landed
+      if (!mbar_wait(&full_v[s], (uint32_t)((it / C::kStages) & 1))) {
+        if (lane == 0) raise_flags(a.error_flags, SRKV_EFLAG_TIMEOUT);
+        break;
+      }
       int4 vt[4][C::NCH];
       const int trow[4] = {row0 + tile_token(2 * ln.t), row0 + tile_token(2 * ln.t + 1),
                            row0 + tile_token(2 * ln.t + 8), row0 + tile_token(2 * ln.t + 9)};

@@ -122,6 +122,7 @@ srkv_status prepare_decode(const srkv_config* cfg, const void* q, const void* k_
   a.ctas = mma ? mma_split_ctas(sms) : simt_split_ctas(sms);
   if (a.ctas > kMaxCtas) a.ctas = kMaxCtas;
   a.ctas_a = a.ctas;
+  a.ctas_b = a.ctas;
   a.lay = ws_layout(batch * cfg->num_kv_heads, kMaxCtas, G, cfg->head_dim);
   a.early = 0;
   a.prompt_lens = nullptr;
@@ -267,11 +268,16 @@ srkv_status srkv_retrieval_decode(const srkv_config* cfg, const void* q, const v
   // The scoring kernel, then the decode, which streams list A while the scoring finishes
   // and knows the selection counts it will write from the lengths.  A scoring CTA keeps its
   // SM to itself, so list A goes to the decode CTAs that find an SM free at once (the grid
-  // is scheduled in block order); the others start when the scoring ends and take list B.
+  // is scheduled in block order), list B to those that start before the scoring ends (all
+  // but one SM per (request, kv head) cluster, whose leader selects last).
   a.prompt_lens = prompt_lens;
   const bool early = mma_split_supported(*cfg);
   const int64_t scoring = score_topk_ctas(*cfg, max_blocks, batch);
-  if (early && 2 * scoring <= a.ctas) a.ctas_a = a.ctas - (int32_t)scoring;
+  const int64_t leaders = (int64_t)batch * cfg->num_kv_heads;
+  if (early && 2 * scoring <= a.ctas) {
+    a.ctas_a = a.ctas - (int32_t)scoring;
+    a.ctas_b = a.ctas - (int32_t)leaders;
+  }
   cudaStream_t s = (cudaStream_t)stream;
   if (launch_score_topk(*cfg, q, reps, num_pages, block_table, max_blocks, seq_lens, prompt_lens,
                         batch, sel, kmax, nsel, error_flags, s) != cudaSuccess)

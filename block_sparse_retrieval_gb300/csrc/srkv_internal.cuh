@@ -341,7 +341,8 @@ struct DecodeArgs {
   int32_t init_tokens, local_tokens;
   float scale_log2;  // log2(e) / sqrt(d)
   int32_t ctas;      // C, the split grid
-  int32_t ctas_a;    // CTAs [0, ctas_a) share list A; the others take list B only
+  int32_t ctas_a;    // CTAs [0, ctas_a) share list A
+  int32_t ctas_b;    // CTAs [0, ctas_b) share list B
   int32_t early;     // 1: the previous kernel is score_topk, so every input but sel and nsel
                      // may be read before it finishes (list A streams during the scoring)
   // early = 1 only: what score_topk derives its selection counts from, so that the
@@ -353,7 +354,7 @@ struct DecodeArgs {
 
 // CTAs that share the positions of a list.
 __host__ __device__ __forceinline__ int32_t list_ctas(const DecodeArgs& a, int list) {
-  return list == 0 ? a.ctas_a : a.ctas;
+  return list == 0 ? a.ctas_a : a.ctas_b;
 }
 
 // Shared memory a scoring CTA takes at least: with it no decode CTA (about 217 KB) fits on
