@@ -1,22 +1,26 @@
 """Benchmark of block-sparse retrieval decode on GB300.
 
-One step = one decode step of one Llama-3-8B-shaped layer (batch 1, 32 q / 8 kv heads,
-d 128, bf16, 65536 cached tokens, init 1024, window 7192, top-k 20 %, 5 % planted
-blocks, shuffled 128-token pages) through srkv_retrieval_decode: score + top-k of the
-offload blocks, then split-K sparse paged attention and its combine; one step of every
+One step = one decode step of one layer through srkv_retrieval_decode: score + top-k of
+the offload blocks, then split-K sparse paged attention and its combine; one step of every
 rotated layer is captured in one CUDA graph, as a model's decode step would be.  The
-representation vectors are built once per
-page at prefill (as on the method's page: the store is written at prefill and read at
-decode) and reported separately under "prefill_reps".
+representation vectors are built once per page at prefill (as on the method's page: the
+store is written at prefill and read at decode) and reported separately under
+"prefill_reps".
 
-L2: the step rotates over --layers layer caches (default 8 x 268 MB of K/V, one block table
-and one set of lengths shared by all layers, as in a model); between two uses of one layer
-the other layers stream > 500 MB, more than the 129 MB L2, so every step reads its pages
-from HBM.
+Workloads (--workload): the default, and the metric's, is one Llama-3-8B-shaped layer
+(batch 1, 32 q / 8 kv heads, d 128, bf16, 65536 cached tokens, init 1024, window 7192,
+top-k 20 %, 5 % planted blocks, shuffled 128-token pages); the others are a ragged batch of
+16 requests, batch 4 x 131072 at top-k 1.0 / 0.1 / 0.2 / 0.4, and 64 requests sharing a
+16384-token prefix.
 
-  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+L2: the step rotates over --layers layer caches (default: about 2 GB of K/V, 8 x 268 MB for
+the default workload; one block table and one set of lengths shared by all layers, as in a
+model); between two uses of one layer the others stream far more than the 129 MB L2, so
+every step reads its pages from HBM.
 
---impl reference times the oracle (plain fp64 C on the host cores) on the same workload.
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--workload W]
+
+--impl reference times the oracle (plain fp64 C on the host cores) on the default workload.
 Under torchrun each rank runs an independent replica (the method shards by request with
 no exchange); rank 0 prints one JSON line.
 """
@@ -38,7 +42,29 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 PEAKS = os.path.join(ROOT, "MEASURED_PEAKS.json")
 TRAFFIC = os.path.join(ROOT, "profiles", "traffic.json")
 METRIC = "decode steps/s and achieved HBM GB/s (% of GB300 peak) for sparse paged attention"
-WORKLOAD = "llama8b-layer-65536-bf16 (batch 1, 32/8 heads, d 128, init 1024, window 7192, top-k 0.2, 5% planted, shuffled pages)"
+# name -> (case factory, description, longest sequence).  The first is the metric's workload;
+# the others are the remaining configurations, measured with --workload.
+WORKLOADS = {
+    "llama8b-65536": (
+        lambda seed, dev: __import__("block_sparse_retrieval_gb300.synth", fromlist=["x"]).llama8b_layer(seed=seed, device=dev),
+        "llama8b-layer-65536-bf16 (batch 1, 32/8 heads, d 128, init 1024, window 7192, top-k 0.2, 5% planted, shuffled pages)",
+        65536),
+    "ragged-16": (
+        lambda seed, dev: __import__("block_sparse_retrieval_gb300.synth", fromlist=["x"]).ragged_batch(seed=seed, device=dev),
+        "ragged-16x[32768,131072]-bf16 (16 requests, lengths U[32768, 131072], 32/8 heads, d 128, top-k 0.2, shuffled pages)",
+        131072),
+    "prefix-shared-64": (
+        lambda seed, dev: __import__("block_sparse_retrieval_gb300.synth", fromlist=["x"]).prefix_shared(seed=seed, device=dev),
+        "prefix-shared-64 (64 requests, 64/8 heads, d 128, 16384-token shared prefix + U[2048, 8192], top-k 0.2, DENSE_BOUNDARY 0)",
+        24576),
+}
+for _p in (1.0, 0.1, 0.2, 0.4):
+    WORKLOADS[f"dense-vs-sparse-p{_p}"] = (
+        (lambda p: lambda seed, dev: __import__("block_sparse_retrieval_gb300.synth", fromlist=["x"]).dense_vs_sparse(p, seed=seed, device=dev))(_p),
+        f"dense-vs-sparse-4x131072-bf16 (batch 4, 32/8 heads, d 128, top-k {_p}, 3% planted, shuffled pages)",
+        131072)
+DEFAULT_WORKLOAD = "llama8b-65536"
+WORKLOAD = WORKLOADS[DEFAULT_WORKLOAD][1]
 FALLBACK_HBM = 6800.0
 DECODE_SOURCES = ("score_topk.cu", "decode_split_mma.cu", "decode_combine.cu",
                   "decode_plan.cuh", "srkv_internal.cuh", "srkv_api.cu")
@@ -162,11 +188,42 @@ def attended_tokens(L: int, sel, INIT: int, LOCAL: int, S: int = 128) -> tuple[i
     blocks = set(range((ie + S - 1) // S)) | set(range(ws // S, (L + S - 1) // S) if ws < L else [])
     extra = 0
     for b in sel:
+        b = int(b)
         lo, hi = max(b * S, INIT), min(b * S + S, W)
         if lo < hi:
             extra += hi - lo
             blocks.add(int(b))
     return base + extra, len(blocks)
+
+
+def unique_kv_bytes(case, sel, nsel, S: int = 128) -> int:
+    """K/V bytes of the distinct (physical page, kv head, row) triples the step attends: a
+    page shared by several requests counts once."""
+    cfg = case.cfg
+    d, Hkv = cfg["head_dim"], cfg["num_kv_heads"]
+    INIT, LOCAL = cfg["init_tokens"], cfg["local_tokens"]
+    bt = case.block_table.cpu().numpy()
+    L = case.seq_lens.cpu().numpy()
+    masks = {}
+    for r in range(case.batch):
+        Lr = int(L[r])
+        W = Lr - LOCAL
+        ranges = [(0, min(INIT, Lr))]
+        if W < Lr:
+            ranges.append((max(W, 0), Lr))
+        for h in range(Hkv):
+            rr = list(ranges) + [(max(int(b) * S, INIT), min(int(b) * S + S, W))
+                                 for b in sel[r, h, :nsel[r, h]]]
+            for lo, hi in rr:
+                t = lo
+                while t < hi:
+                    b = t // S
+                    e = min(hi, (b + 1) * S)
+                    key = (int(bt[r, b]), h)
+                    masks[key] = masks.get(key, 0) | (((1 << (e - b * S)) - 1) ^ ((1 << (t - b * S)) - 1))
+                    t = e
+    rows = sum(bin(m).count("1") for m in masks.values())
+    return rows * 2 * d * case.k_cache.element_size()
 
 
 # ---- our arm --------------------------------------------------------------------------------
@@ -176,9 +233,9 @@ class Layer:
     queries, K/V pages and representation vectors, while the block table and the sequence
     lengths (per request) are shared by all layers."""
 
-    def __init__(self, seed: int, device, shared=None):
-        from block_sparse_retrieval_gb300 import srkv, synth
-        self.case = synth.llama8b_layer(seed=seed, device=device)
+    def __init__(self, seed: int, device, shared=None, workload: str = DEFAULT_WORKLOAD):
+        from block_sparse_retrieval_gb300 import srkv
+        self.case = WORKLOADS[workload][0](seed, device)
         if shared is not None:
             for name in ("block_table", "seq_lens", "prompt_lens"):
                 assert torch.equal(getattr(self.case, name), getattr(shared, name))
@@ -218,7 +275,8 @@ class Layer:
         qo = c.batch * Hq * d * 2
         score = n_cand * (d * 4 + 4) + qo + int(nsel.sum()) * 4 + nsel.size * 4
         decode = kv + pages * 4 + qo * 2 + int(nsel.sum()) * 4 + nsel.size * 4
-        return {"score": score, "decode": decode, "kv": kv, "total": score + decode}
+        return {"score": score, "decode": decode, "kv": kv, "total": score + decode,
+                "kv_unique": unique_kv_bytes(c, sel, nsel)}
 
 
 def capture(fn, stream):
@@ -232,10 +290,16 @@ def run_ours(args, world, rank, local):
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
     peak, peak_kind = peaks()
-    # Same seed: the same page structure for every layer (one shared block table).
-    layers = [Layer(1000 + 1000003 * rank, dev)]
-    layers += [Layer(1000 + 1000003 * rank, dev, shared=layers[0].case)
-               for _ in range(args.layers - 1)]
+    # Same seed: the same page structure for every layer (one shared block table).  Enough
+    # layers for about 2 GB of K/V in the rotation (8 for the 65536-token layer).
+    wl = args.workload
+    first = Layer(1000 + 1000003 * rank, dev, workload=wl)
+    n_layers = args.layers
+    if n_layers is None:
+        layer_bytes = 2 * first.case.k_cache.numel() * first.case.k_cache.element_size()
+        n_layers = max(2, min(8, -(-2_000_000_000 // layer_bytes)))
+    layers = [first] + [Layer(1000 + 1000003 * rank, dev, shared=first.case, workload=wl)
+                        for _ in range(n_layers - 1)]
 
     # prefill: representation vectors of every page of every layer (timed separately)
     ev = [torch.cuda.Event(enable_timing=True) for _ in range(2 * len(layers))]
@@ -294,9 +358,10 @@ def run_ours(args, world, rank, local):
     value = world * K / (total_ms / 1e3)
 
     avg_step_bytes = statistics.mean(sb["total"] for sb in step_bytes)
+    avg_unique = statistics.mean(sb["total"] - sb["kv"] + sb["kv_unique"] for sb in step_bytes)
     call_ms = statistics.mean(replay_ms) / R
     achieved = avg_step_bytes / (call_ms / 1e3) / 1e9
-    traffic = committed_traffic()
+    traffic = committed_traffic() if wl == DEFAULT_WORKLOAD else None
 
     e2e = run_e2e(layers, min(K, args.e2e_steps), world, dev)
     line = {
@@ -304,14 +369,16 @@ def run_ours(args, world, rank, local):
         "steps": K, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic (seeded N(0,1) q/K/V, 5% planted blocks, shuffled pages)",
-        "config": {"workload": WORKLOAD, "global_batch": world, "seq_len": 65536,
-                   "parallelism": f"replicas x{world}", "layers_rotated": R,
+        "config": {"workload": WORKLOADS[wl][1], "global_batch": world * layers[0].case.batch,
+                   "seq_len": WORKLOADS[wl][2], "parallelism": f"replicas x{world}",
+                   "layers_rotated": R,
                    "l2": f"inputs larger than L2: {R} layer caches rotated per step"},
         "roofline": {"kernel": "srkv_retrieval_decode call: score_topk, split-K decode and "
                                "combine kernels, overlapped by programmatic launch",
                      "bound": "hbm", "achieved": round(achieved, 1), "peak": peak,
                      "unit": "GB/s", "frac": round(achieved / peak, 4), "peak_kind": peak_kind,
                      "bytes_per_launch": int(avg_step_bytes),
+                     "unique_bytes_per_launch": int(avg_unique),
                      "us_per_launch": round(call_ms * 1e3, 3), "traffic": traffic},
         "prefill_reps": {"kernel": "srkv_build_block_reps", "pages": sum(
             ly.case.page_ids.numel() for ly in layers), "us": round(rep_ms * 1e3, 1),
@@ -321,7 +388,7 @@ def run_ours(args, world, rank, local):
         "e2e": e2e,
         "gpu_launches": K * 3,   # score_topk, the split kernel and the combine per step
     }
-    if rank == 0 and not args.no_cpu_baseline:
+    if rank == 0 and not args.no_cpu_baseline and wl == DEFAULT_WORKLOAD:
         line["cpu_baseline"] = cpu_baseline(layers[0], args.cpu_seconds)
     if rank == 0:
         print(json.dumps(line), flush=True)
@@ -428,7 +495,9 @@ def main(argv=None):
     ap.add_argument("--steps", type=int, default=4000)
     ap.add_argument("--warmup", type=int, default=8)
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
-    ap.add_argument("--layers", type=int, default=8)
+    ap.add_argument("--layers", type=int, default=None,
+                    help="rotated layer caches (default: enough to stream > 500 MB between uses)")
+    ap.add_argument("--workload", choices=list(WORKLOADS), default=DEFAULT_WORKLOAD)
     ap.add_argument("--e2e-steps", type=int, default=1000)
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
