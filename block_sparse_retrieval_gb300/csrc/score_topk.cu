@@ -24,7 +24,7 @@
 //   4. the kept blocks are written ascending: a kept key's slot is the number of kept keys
 //      before it in block order, from ballot counts per warp.
 // Bytes per unit: n * (4 + 4d) read (block table + reps), k * 4 written.
-#include "srkv_internal.cuh"
+#include "select.cuh"
 
 namespace srkv {
 namespace {
@@ -51,91 +51,6 @@ struct ScoreArgs {
   double topk_percent;
 };
 
-__device__ __forceinline__ uint32_t score_key(float s) {
-  if (s != s) return 0u;            // NaN ranks below everything
-  if (s == 0.0f) s = 0.0f;          // -0 and +0 tie
-  const uint32_t u = __float_as_uint(s);
-  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
-}
-
-// Exclusive scan over the warp of one int per lane; *total gets the sum.
-__device__ __forceinline__ int32_t warp_exclusive_scan(int32_t v, int lane, int32_t* total) {
-  int32_t x = v;
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const int32_t y = __shfl_up_sync(0xffffffffu, x, o);
-    if (lane >= o) x += y;
-  }
-  *total = __shfl_sync(0xffffffffu, x, 31);
-  return x - v;
-}
-
-__device__ __forceinline__ uint32_t cluster_rank() {
-  uint32_t r;
-  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-  return r;
-}
-__device__ __forceinline__ uint32_t cluster_size() {
-  uint32_t r;
-  asm volatile("mov.u32 %0, %%cluster_nctarank;" : "=r"(r));
-  return r;
-}
-// Store to the same shared-memory offset in CTA `rank` of this cluster.
-__device__ __forceinline__ void st_cluster_u32(uint32_t* local, uint32_t rank, uint32_t v) {
-  uint32_t remote;
-  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(smem_u32(local)), "r"(rank));
-  asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(remote), "r"(v) : "memory");
-}
-// Atomic add to the same shared-memory offset in CTA `rank` of this cluster.
-__device__ __forceinline__ void red_cluster_add(int32_t* local, uint32_t rank, int32_t v) {
-  uint32_t remote;
-  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(smem_u32(local)), "r"(rank));
-  asm volatile("red.shared::cluster.add.u32 [%0], %1;" ::"r"(remote), "r"(v) : "memory");
-}
-__device__ __forceinline__ void cluster_arrive() {
-  asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
-}
-__device__ __forceinline__ void cluster_wait() {
-  asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
-}
-__device__ __forceinline__ void cluster_sync() {
-  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
-}
-
-// Every warp finds the digit holding the remaining-th largest key from a 256-bin histogram.
-__device__ __forceinline__ void find_digit(const int32_t* hist, int lane, int32_t remaining,
-                                           int32_t* digit, int32_t* rem_out, int32_t* cnt_out) {
-  int32_t c[8], local = 0;
-#pragma unroll
-  for (int b = 0; b < 8; ++b) {
-    c[b] = hist[lane * 8 + b];
-    local += c[b];
-  }
-  int32_t suffix = local;  // keys in this lane's bins and above
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const int32_t y = __shfl_down_sync(0xffffffffu, suffix, o);
-    if (lane + o < 32) suffix += y;
-  }
-  int32_t above = suffix - local, dg = -1, rm = 0, cn = 0;
-#pragma unroll
-  for (int b = 7; b >= 0; --b) {
-    if (above < remaining && above + c[b] >= remaining) {
-      dg = lane * 8 + b;
-      rm = remaining - above;
-      cn = c[b];
-    }
-    above += c[b];
-  }
-  const uint32_t who = __ballot_sync(0xffffffffu, dg >= 0);
-  const int src = __ffs(who) - 1;
-  *digit = __shfl_sync(0xffffffffu, dg, src);
-  *rem_out = __shfl_sync(0xffffffffu, rm, src);
-  *cnt_out = __shfl_sync(0xffffffffu, cn, src);
-}
-
-constexpr int kFastRounds = 4;  // the block-wide finish handles n <= 4 * kThreads
-
 // Grid: one cluster of `cluster_size()` CTAs per (request, kv head) unit.
 template <typename T, int D>
 __global__ void __launch_bounds__(kThreads, 4) score_topk_kernel(ScoreArgs a) {
@@ -144,9 +59,7 @@ __global__ void __launch_bounds__(kThreads, 4) score_topk_kernel(ScoreArgs a) {
   int32_t* pages = reinterpret_cast<int32_t*>(smem + a.max_blocks);  // [max_blocks]
   __shared__ float qbar[D];
   __shared__ int32_t hist[3][256];  // leader: radix histograms (pass 0 filled by the cluster)
-  __shared__ int32_t bnd_idx[32];
-  __shared__ int32_t wcnt[2][kFastRounds * kWarps];  // per (round, warp): above / in the bin
-  __shared__ uint32_t s_take;
+  __shared__ FinishShared<kThreads> fin;
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   griddep_launch_dependents();  // the decode may be scheduled now; it waits for this grid
@@ -204,161 +117,29 @@ __global__ void __launch_bounds__(kThreads, 4) score_topk_kernel(ScoreArgs a) {
   }
   __syncthreads();  // pages and qbar
 
-  // 2. scores of the share, one warp per candidate.  Lane x of a warp stores the key of
-  // its x-th candidate into the leader's shared memory and adds it to the leader's
-  // pass-0 histogram (top 8 bits; lanes with equal digits add once).
-  constexpr int EPL = D / 32;  // elements per lane: 4 (d 128) or 2 (d 64)
-  float qv[EPL];
-#pragma unroll
-  for (int e = 0; e < EPL; ++e) qv[e] = qbar[lane * EPL + e];
-  const int32_t i_hi = min(s_hi, n);
-  const uint64_t keep = l2_policy_evict_last();  // the vectors are read again every step
-  constexpr int UNROLL = 8;  // 64 candidates of a CTA in one round of loads
+  // 2. scores of the share, one warp per candidate, into the leader's keys and histogram
   cluster_wait();
-  for (int32_t i0 = s_lo + warp; i0 < i_hi; i0 += kWarps * UNROLL) {
-    float part[UNROLL];
-    bool ok[UNROLL];
-#pragma unroll
-    for (int x = 0; x < UNROLL; ++x) {
-      const int32_t i = i0 + x * kWarps;
-      part[x] = 0.f;
-      ok[x] = false;
-      if (i < i_hi) {
-        const int32_t page = pages[i - s_lo];
-        ok[x] = page >= 0 && (int64_t)page < a.num_pages;
-        if (ok[x]) {
-          const float* rep = a.reps + ((int64_t)page * a.Hkv + h) * D + lane * EPL;
-          if constexpr (EPL == 4) {
-            const float4 v = ldg_f4_hint(rep, keep);
-            part[x] = qv[0] * v.x + qv[1] * v.y + qv[2] * v.z + qv[3] * v.w;
-          } else {
-            const float2 v = ldg_f2_hint(rep, keep);
-            part[x] = qv[0] * v.x + qv[1] * v.y;
-          }
-        }
-      }
-    }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1)
-#pragma unroll
-      for (int x = 0; x < UNROLL; ++x) part[x] += __shfl_xor_sync(0xffffffffu, part[x], o);
-    float mine = part[0];
-    bool mine_ok = ok[0];
-#pragma unroll
-    for (int x = 1; x < UNROLL; ++x)
-      if (lane == x) {
-        mine = part[x];
-        mine_ok = ok[x];
-      }
-    const int32_t i = i0 + lane * kWarps;
-    const bool valid = lane < UNROLL && i < i_hi;
-    if (valid && !mine_ok) eflags |= SRKV_EFLAG_PAGE_RANGE;
-    const uint32_t key = mine_ok ? score_key(mine) : 0u;
-    if (valid) st_cluster_u32(&keys[i], 0, key);
-    const uint32_t digit = valid ? key >> 24 : 0xffffffffu;
-    const uint32_t peers = __match_any_sync(0xffffffffu, digit);
-    if (valid && lane == __ffs(peers) - 1) red_cluster_add(&hist[0][digit], 0, __popc(peers));
-  }
-  eflags = __reduce_or_sync(0xffffffffu, eflags);
+  eflags |= score_share<D, kWarps>(qbar, pages, s_lo, min(s_hi, n), a.reps, a.num_pages, a.Hkv,
+                                   h, keys, &hist[0][0], nullptr, warp, lane);
   if (lane == 0 && eflags) raise_flags(a.error_flags, eflags);
   cluster_sync();  // every key and the pass-0 histogram are in the leader
   if (crank != 0) return;
 
-  // 3. radix select: pass 0 reads the histogram the cluster built; passes 1-3 build theirs
-  // (one barrier a pass, triple-buffered bins) until the boundary bin is small enough for
-  // one warp to rank
-  uint32_t prefix = 0, pmask = 0;
-  int32_t remaining = k;
-  bool ranked = false;
-#pragma unroll 1
-  for (int pass = 0; pass < 4; ++pass) {
-    const int shift = 24 - 8 * pass;
-    int32_t* hcur = hist[pass % 3];
-    if (pass > 0) {
-      for (int i = tid; i < 256; i += kThreads) hist[(pass + 1) % 3][i] = 0;
-      for (int32_t i0 = warp * 32; i0 < n; i0 += kThreads) {
-        const int32_t i = i0 + lane;
-        const uint32_t kk = i < n ? keys[i] : 0u;
-        const bool in = i < n && (kk & pmask) == prefix;
-        const uint32_t digit = in ? (kk >> shift) & 255u : 256u;
-        const uint32_t peers = __match_any_sync(0xffffffffu, digit);
-        if (in && lane == __ffs(peers) - 1) atomicAdd(&hcur[digit], __popc(peers));
-      }
-      __syncthreads();
-    }
-    int32_t dg, rm, cnt;
-    find_digit(hcur, lane, remaining, &dg, &rm, &cnt);
-    prefix |= (uint32_t)dg << shift;
-    pmask |= 0xffu << shift;
-    remaining = rm;
-    if (pass < 3 && cnt <= 32) {  // uniform: every warp read the same histogram
-      ranked = true;
-      break;
-    }
-  }
+  // 3. radix select until the boundary bin is small enough for one warp to rank
+  auto bar = [] { __syncthreads(); };
+  const RadixState rs = radix_narrow<kThreads>(keys, n, k, hist, tid, bar);
 
-  // 4. A key above the boundary bin is kept; inside the bin, taken in block order, the
-  // ranked ones are kept, or after four passes (bin = keys equal to the k-th) the first
-  // `remaining`.  A kept key's output slot = kept keys before it in block order = keys
-  // above the bin before it + kept bin keys before it, so one count of each suffices.
+  // 4. kept blocks written ascending
   if (n <= kFastRounds * kThreads) {
-    uint32_t b_above[kFastRounds], b_in[kFastRounds];
-#pragma unroll
-    for (int rr = 0; rr < kFastRounds; ++rr) {
-      const int32_t i = rr * kThreads + tid;
-      const uint32_t hi = i < n ? keys[i] & pmask : 0u;
-      b_above[rr] = __ballot_sync(0xffffffffu, i < n && hi > prefix);
-      b_in[rr] = __ballot_sync(0xffffffffu, i < n && hi == prefix);
-      if (lane == 0) {
-        wcnt[0][rr * kWarps + warp] = __popc(b_above[rr]);
-        wcnt[1][rr * kWarps + warp] = __popc(b_in[rr]);
-      }
-    }
-    __syncthreads();
-    // exclusive prefixes over (round, warp) in block order: lane j holds entry j
-    int32_t tot_above, tot_in;
-    const int32_t pa = warp_exclusive_scan(wcnt[0][lane], lane, &tot_above);
-    const int32_t pi = warp_exclusive_scan(wcnt[1][lane], lane, &tot_in);
-    const uint32_t lt = (1u << lane) - 1u;
-    int32_t t_in[kFastRounds], a_before[kFastRounds];
-#pragma unroll
-    for (int rr = 0; rr < kFastRounds; ++rr) {
-      t_in[rr] = __shfl_sync(0xffffffffu, pi, rr * kWarps + warp) + __popc(b_in[rr] & lt);
-      a_before[rr] = __shfl_sync(0xffffffffu, pa, rr * kWarps + warp) + __popc(b_above[rr] & lt);
-    }
-    uint32_t take_mask = 0;
-    if (ranked) {  // tot_in <= 32
-#pragma unroll
-      for (int rr = 0; rr < kFastRounds; ++rr)
-        if ((b_in[rr] >> lane) & 1u) bnd_idx[t_in[rr]] = rr * kThreads + tid;
-      __syncthreads();
-      if (warp == 0) {
-        const uint32_t key = lane < tot_in ? keys[bnd_idx[lane]] : 0u;
-        int32_t rank = 0;  // higher score, or equal score and lower block (lane)
-#pragma unroll
-        for (int j = 0; j < 32; ++j) {
-          const uint32_t kj = __shfl_sync(0xffffffffu, key, j);
-          rank += j < tot_in && (kj > key || (kj == key && j < lane));
-        }
-        const uint32_t m = __ballot_sync(0xffffffffu, lane < tot_in && rank < remaining);
-        if (lane == 0) s_take = m;
-      }
-      __syncthreads();
-      take_mask = s_take;
-    }
-#pragma unroll
-    for (int rr = 0; rr < kFastRounds; ++rr) {
-      const int32_t t = t_in[rr];
-      const int32_t bin_before =
-          ranked ? __popc(t < 32 ? take_mask & ((1u << t) - 1u) : take_mask) : min(t, remaining);
-      const bool take = ((b_above[rr] >> lane) & 1u) ||
-                        (((b_in[rr] >> lane) & 1u) &&
-                         (ranked ? ((take_mask >> t) & 1u) != 0 : t < remaining));
-      if (take) sel_u[a_before[rr] + bin_before] = b_lo + rr * kThreads + tid;
-    }
-    if (tid == 0) a.nsel[u] = tot_above + (ranked ? __popc(take_mask) : min(tot_in, remaining));
+    const int32_t kept = finish_fast<kThreads>(keys, n, rs, fin, tid, bar,
+                                               [&](int32_t pos, int32_t i) { sel_u[pos] = b_lo + i; });
+    if (tid == 0) a.nsel[u] = kept;
     return;
   }
+  const uint32_t prefix = rs.prefix, pmask = rs.pmask;
+  const int32_t remaining = rs.remaining;
+  const bool ranked = rs.ranked;
+  int32_t* bnd_idx = fin.bnd_idx;
 
   // Longer candidate lists: one warp walks the keys, lane l taking [l c, l c + c).
   if (warp != 0) return;
