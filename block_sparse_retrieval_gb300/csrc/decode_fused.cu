@@ -1,0 +1,448 @@
+// decode_fused.cu -- block-sparse retrieval decode of a small batch in one kernel.
+//
+// openGauss DataVec "KV Cache Query-Based Computation Inference Acceleration", section
+// "Overall Solution": the query is scored against every offload block's representation
+// vector, the topK closest blocks are kept and attended together with the initial tokens and
+// the sliding window; the KV-cache survey ("Share--KV cache共享") merges partial attention
+// results the Flash-Decoding way.  Here one thread-block cluster does all of it for one
+// (request, kv head) unit, so nothing crosses a kernel boundary or global memory between
+// the steps:
+//   * every CTA scores its share of the candidates (select.cuh: keys, page ids and the top-8-
+//     bit histogram go to the leader, CTA 0, through distributed shared memory);
+//   * meanwhile the other CTAs' producer warps stream their share of the initial and window
+//     pages (list A) into the stage ring (decode_mma.cuh);
+//   * the leader selects (radix narrowing, ranked finish), writes sel / nsel, and hands each
+//     streaming CTA its share of the kept blocks (page and block ids) in that CTA's shared
+//     memory, releasing an mbarrier there;
+//   * the streaming CTAs attend list A then their kept blocks as one segment and store the
+//     merged partial (max, sum, unnormalised output) into the leader's shared memory;
+//   * the leader merges the partials and writes the output.
+// The selection count of a unit (selection_count) follows from the lengths, so list B's
+// shares are known before the selection: a CTA plans its whole segment up front.  Every wait
+// is bounded (SRKV_EFLAG_TIMEOUT); every thread ends at one cluster barrier, so no CTA leaves
+// while another may still reach its shared memory.
+#include "decode_mma.cuh"
+#include "select.cuh"
+
+namespace srkv {
+namespace {
+
+constexpr int kSelThreads = kConsumerWarps * 32;  // the consumer warps score and select
+constexpr int32_t kMaxCand = kFastRounds * kSelThreads;  // candidates per unit (1024)
+constexpr int kMaxShare = 128;                             // candidates scored per CTA
+constexpr int kMaxList = 160;                              // kept blocks per streaming CTA
+
+template <int D>
+struct FusedCfg {
+  using C = Cfg<D>;
+  // after the ring (every CTA)
+  // keys_ready, list_ready, parts_ready, scored
+  static constexpr size_t kOffBars = (C::kSmem + 15) & ~size_t(15);
+  static constexpr size_t kOffQbar = kOffBars + 4 * sizeof(uint64_t);
+  static constexpr size_t kOffShare = kOffQbar + sizeof(float) * D;
+  static constexpr size_t kOffList = kOffShare + sizeof(int32_t) * kMaxShare;  // int2 (page, block)
+  static constexpr size_t kSmem = kOffList + sizeof(int2) * kMaxList;
+  static constexpr size_t kSmemAlloc = kSmem + 1024;
+  // the leader streams no pages: its K ring holds the selection state ...
+  static constexpr size_t kOffKeys = C::kOffK;
+  static constexpr size_t kOffPages = kOffKeys + sizeof(uint32_t) * kMaxCand;
+  static constexpr size_t kOffHist = kOffPages + sizeof(int32_t) * kMaxCand;
+  static constexpr size_t kOffFin = kOffHist + sizeof(int32_t) * 3 * 256;
+  static constexpr size_t kOffKept = (kOffFin + sizeof(FinishShared<kSelThreads>) + 15) & ~size_t(15);
+  static constexpr size_t kSelEnd = kOffKept + sizeof(int32_t) * kMaxCand;
+  // ... and its V ring the streaming CTAs' partials: acc [15][8][D], then (m, l) [15][8][2]
+  static constexpr size_t kOffPartAcc = C::kOffV;
+  static constexpr size_t kOffPartMl = kOffPartAcc + sizeof(float) * 15 * 8 * D;
+  static constexpr size_t kPartEnd = kOffPartMl + sizeof(float) * 15 * 8 * 2;
+  static_assert(kSelEnd <= C::kOffV, "selection state fits in the K ring");
+  static_assert(kPartEnd <= C::kOffQ, "partials fit in the V ring");
+  static_assert(kSmemAlloc <= 232448, "shared memory opt-in limit");
+};
+
+// Share [q*n/S, (q+1)*n/S) of n items for part q of S (n * S < 2^31: n <= 1024 kept or
+// candidate blocks, or list-A pages of one request, S < 16).
+__device__ __forceinline__ int32_t share_begin(int32_t q, int32_t n, int32_t S) {
+  return n * q / S;
+}
+
+// Grid: one cluster of CS CTAs per unit; 8 consumer warps + 1 producer warp per CTA.
+template <int D>
+__global__ void __maxnreg__(128) fused_decode_kernel(const DecodeArgs a,
+                                                     const __grid_constant__ TmaMaps maps) {
+  using C = Cfg<D>;
+  using F = FusedCfg<D>;
+  extern __shared__ __align__(128) unsigned char smem_raw[];
+  unsigned char* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+  uint64_t* keys_ready = reinterpret_cast<uint64_t*>(smem + F::kOffBars);
+  uint64_t* list_ready = keys_ready + 1;
+  uint64_t* parts_ready = keys_ready + 2;
+  uint64_t* scored = keys_ready + 3;  // this CTA's scoring loads have landed
+  float* qbar = reinterpret_cast<float*>(smem + F::kOffQbar);
+  int32_t* share = reinterpret_cast<int32_t*>(smem + F::kOffShare);
+  int2* blist = reinterpret_cast<int2*>(smem + F::kOffList);
+  uint32_t* keys = reinterpret_cast<uint32_t*>(smem + F::kOffKeys);    // leader
+  int32_t* pages = reinterpret_cast<int32_t*>(smem + F::kOffPages);    // leader
+  int32_t(*hist)[256] = reinterpret_cast<int32_t(*)[256]>(smem + F::kOffHist);  // leader
+  FinishShared<kSelThreads>& fin = *reinterpret_cast<FinishShared<kSelThreads>*>(smem + F::kOffFin);
+  int32_t* kept_list = reinterpret_cast<int32_t*>(smem + F::kOffKept);  // leader
+  float* part_acc = reinterpret_cast<float*>(smem + F::kOffPartAcc);  // leader
+  float* part_ml = reinterpret_cast<float*>(smem + F::kOffPartMl);    // leader
+
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const uint32_t crank = cluster_rank(), CS = cluster_size();
+  const int32_t S = (int32_t)CS - 1;  // streaming CTAs
+  const int32_t u = blockIdx.x / CS;
+  const int32_t r = u / a.Hkv, h = u % a.Hkv;
+  const bool leader = crank == 0;
+
+  if (tid == 0) {
+    init_ring<D>(smem);
+    mbar_init(keys_ready, kMaxCand);            // one per candidate, the rest at once
+    mbar_init(list_ready, kMaxList);            // one per kept block handed over, the rest at once
+    mbar_init(parts_ready, 32u * (uint32_t)S);  // one per lane of a streaming CTA's warp 0
+    mbar_init(scored, kConsumerWarps);
+    fence_mbar_init();
+  }
+  if (leader)
+    for (int i = tid; i < 3 * 256; i += blockDim.x) (&hist[0][0])[i] = 0;
+  __syncthreads();
+  cluster_arrive();  // this CTA's barriers and the leader's histogram are ready (waited for
+                     // before the first access to another CTA)
+
+  // The unit's sizes: candidates n, kept k (what the selection will write), list A length.
+  const int32_t L_in = a.seq_lens[r];
+  const int32_t prompt = a.prompt_lens ? a.prompt_lens[r] : L_in;
+  const SelCount sc = selection_count(L_in, prompt, a.max_blocks, a.kmax, a.init_tokens,
+                                      a.local_tokens, a.dense_boundary, a.topk_percent);
+  const int32_t n = sc.n, k = sc.k;
+  uint32_t geflags = 0;
+  const Geom g = make_geom(L_in, k, a.max_blocks, a.kmax, a.init_tokens, a.local_tokens, geflags);
+  const int32_t nA = list_a_count(g);
+  const int32_t b_lo = a.init_tokens / kBlock;
+  const int32_t* bt_r = a.block_table + (int64_t)r * a.max_blocks;
+  const int32_t q = (int32_t)crank - 1;  // streaming rank
+  const int32_t a0 = leader ? 0 : share_begin(q, nA, S), a1 = leader ? 0 : share_begin(q + 1, nA, S);
+  const int32_t l0 = leader ? 0 : share_begin(q, k, S), l1 = leader ? 0 : share_begin(q + 1, k, S);
+  const int32_t npos = (a1 - a0) + (l1 - l0);
+
+
+  if (warp == kProducerWarp) {
+    // ------------------------------------------------------------------ producer
+    cluster_wait();
+    if (!leader && npos > 0) {
+      uint32_t eflags = 0;
+      bool abort = false;
+      int64_t it = 0, armed = 0;
+      // position p of this CTA's segment (t uniform over the warp)
+      auto hand_out = [&](int32_t p, const PageTask& t) {
+        const uint32_t fl = (p == 0 ? kNewUnit : 0u) | (p == npos - 1 ? kSegEnd : 0u);
+        if (lane == 0) issue_stage<D>(a, maps, smem, it, u, fl, t, armed, abort, eflags);
+        abort = __shfl_sync(0xffffffffu, abort, 0);
+        ++it;
+      };
+      // list A: 32 positions resolved at once, handed out in order; the first copy waits
+      // until this CTA's scoring loads are on their way (pages requested before them would
+      // delay them)
+      for (int32_t j0 = a0; j0 < a1 && !abort; j0 += 32) {
+        const int32_t cnt = min(32, a1 - j0);
+        PageTask task;
+        task.page = -1;
+        task.lo = task.hi = task.ie = task.ws = 0;
+        if (lane < cnt) task = resolve_a(g, j0 + lane, bt_r, a.num_pages, eflags);
+        if (j0 == a0 && !mbar_wait(scored, 0)) {
+          eflags |= SRKV_EFLAG_TIMEOUT;
+          abort = true;
+        }
+        for (int l = 0; l < cnt && !abort; ++l) {
+          PageTask tl;
+          tl.page = __shfl_sync(0xffffffffu, task.page, l);
+          tl.lo = __shfl_sync(0xffffffffu, task.lo, l);
+          tl.hi = __shfl_sync(0xffffffffu, task.hi, l);
+          tl.ie = __shfl_sync(0xffffffffu, task.ie, l);
+          tl.ws = __shfl_sync(0xffffffffu, task.ws, l);
+          hand_out(j0 + l - a0, tl);
+        }
+      }
+      // list B: the kept blocks the leader hands over
+      if (l1 > l0 && !abort) {
+        if (!mbar_wait_cluster(list_ready, 0)) {
+          eflags |= SRKV_EFLAG_TIMEOUT;
+          abort = true;
+        }
+        for (int32_t i0 = 0; i0 < l1 - l0 && !abort; i0 += 32) {
+          const int32_t cnt = min(32, l1 - l0 - i0);
+          PageTask task;
+          task.page = -1;
+          task.lo = task.hi = task.ie = task.ws = 0;
+          if (lane < cnt) {
+            const int2 e = blist[i0 + lane];  // (page, block)
+            const int32_t base = e.y * kBlock, rows = min(kBlock, g.L - base);
+            const int32_t lo = max(a.init_tokens - base, 0), hi = min(g.W - base, rows);
+            if (lo < hi && e.x >= 0 && (int64_t)e.x < a.num_pages) {
+              task.page = e.x;
+              task.block = e.y;
+              task.lo = lo;
+              task.hi = hi;
+              task.ie = hi;  // every loaded row is attended
+              task.ws = hi;
+            } else if (lo < hi) {
+              eflags |= SRKV_EFLAG_PAGE_RANGE;
+            }
+          }
+          for (int l = 0; l < cnt && !abort; ++l) {
+            PageTask tl;
+            tl.page = __shfl_sync(0xffffffffu, task.page, l);
+            tl.lo = __shfl_sync(0xffffffffu, task.lo, l);
+            tl.hi = __shfl_sync(0xffffffffu, task.hi, l);
+            tl.ie = __shfl_sync(0xffffffffu, task.ie, l);
+            tl.ws = __shfl_sync(0xffffffffu, task.ws, l);
+            hand_out((a1 - a0) + i0 + l, tl);
+          }
+        }
+      }
+      if (lane == 0) {
+        PageTask none;
+        none.page = -1;
+        none.lo = none.hi = none.ie = none.ws = 0;
+        issue_stage<D>(a, maps, smem, it, -1, kLast, none, armed, abort, eflags);  // sentinel
+        uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::kOffBar);
+        uint64_t* full_v = full + C::kStages;
+        const int64_t first = armed > C::kStages ? armed - C::kStages : 0;
+        for (int64_t i = first; i < armed; ++i)  // every copy lands before the CTA ends
+          if (!mbar_wait(&full[i % C::kStages], (uint32_t)((i / C::kStages) & 1)) ||
+              !mbar_wait(&full_v[i % C::kStages], (uint32_t)((i / C::kStages) & 1))) {
+            eflags |= SRKV_EFLAG_TIMEOUT;
+            break;
+          }
+      }
+      eflags = __reduce_or_sync(0xffffffffu, eflags | geflags);
+      if (lane == 0) raise_flags(a.error_flags, eflags);
+    } else if (!leader && lane == 0) {
+      // no positions: the consumers still need their sentinel
+      int64_t it = 0, armed = 0;
+      bool abort = false;
+      uint32_t eflags = 0;
+      PageTask none;
+      none.page = -1;
+      none.lo = none.hi = none.ie = none.ws = 0;
+      issue_stage<D>(a, maps, smem, it, -1, kLast, none, armed, abort, eflags);
+      if (eflags) raise_flags(a.error_flags, eflags);
+    }
+  } else {
+    // ------------------------------------------------------------------ consumers
+    auto bar = [] { named_bar_sync(1, kSelThreads); };
+    // 1. this CTA's share of the candidates: table entries and the group query sum
+    const int32_t s_lo = share_begin((int32_t)crank, n, (int32_t)CS);
+    const int32_t s_hi = share_begin((int32_t)crank + 1, n, (int32_t)CS);
+    for (int32_t i = s_lo + tid; i < s_hi; i += kSelThreads) share[i - s_lo] = bt_r[b_lo + i];
+    const __nv_bfloat16* qp =
+        static_cast<const __nv_bfloat16*>(a.q) + ((int64_t)r * a.Hq + (int64_t)h * a.G) * D;
+    for (int e = tid; e < D; e += kSelThreads) {
+      float s = 0.f;
+      for (int j = 0; j < a.G; ++j) s += __bfloat162float(qp[(int64_t)j * D + e]);
+      qbar[e] = s;
+    }
+    bar();
+    // 2. scores into the leader (keys, pages, top-8-bit histogram)
+    // the pages of list A start streaming once every warp's vector loads are on their way;
+    // keys go to the leader once every CTA has passed its setup (cluster barrier)
+    bool waited = false;
+    uint32_t eflags = score_share<D, kConsumerWarps>(
+        qbar, share, s_lo, s_hi, a.reps, a.num_pages, a.Hkv, h, keys, &hist[0][0], pages, warp,
+        lane,
+        [&] {
+          if (lane == 0) mbar_arrive(scored);
+          cluster_wait();
+          waited = true;
+        },
+        [&] { mbar_arrive_cluster(keys_ready, 0); });  // releases this lane's key, page, count
+    if (!waited) {  // a warp without candidates
+      if (lane == 0) mbar_arrive(scored);
+      cluster_wait();
+    }
+    if (lane == 0 && eflags) raise_flags(a.error_flags, eflags);
+    // the arrivals the leader's barrier expects beyond the n candidates, at once
+    if (leader && tid == 0 && n < kMaxCand)
+      mbar_arrive_cluster_n(keys_ready, 0, (uint32_t)(kMaxCand - n));
+
+    if (leader) {
+      // 3. select the k kept blocks, write sel / nsel, hand each streaming CTA its share
+      if (!mbar_wait_cluster(keys_ready, 0)) {
+        if (tid == 0) raise_flags(a.error_flags, SRKV_EFLAG_TIMEOUT);
+      }
+      int32_t kept = 0;
+      if (k == n) {
+        for (int32_t i = tid; i < n; i += kSelThreads) kept_list[i] = i;
+        kept = n;
+      } else if (k > 0) {
+        const RadixState rs = radix_narrow<kSelThreads>(keys, n, k, hist, tid, bar);
+        kept = finish_fast<kSelThreads>(keys, n, rs, fin, tid, bar,
+                                        [&](int32_t pos, int32_t i) { kept_list[pos] = i; });
+      }
+      bar();
+      // each entry is released to its CTA by the thread that wrote it
+      for (int32_t p = tid; p < kept; p += kSelThreads) {
+        const int32_t i = kept_list[p];
+        const int32_t qq = ((p + 1) * S - 1) / k;  // streaming CTA of position p
+        int2* dst = static_cast<int2*>(map_cluster_ptr(blist + (p - share_begin(qq, k, S)),
+                                                        (uint32_t)qq + 1));
+        *dst = make_int2(pages[i], b_lo + i);
+        mbar_arrive_cluster(list_ready, (uint32_t)qq + 1);
+      }
+      // the arrivals a CTA's barrier expects beyond its entries, at once
+      for (int32_t qq = tid; qq < S; qq += kSelThreads) {
+        const int32_t rest = kMaxList - (share_begin(qq + 1, k, S) - share_begin(qq, k, S));
+        if (rest > 0) mbar_arrive_cluster_n(list_ready, (uint32_t)qq + 1, (uint32_t)rest);
+      }
+      // the selection, for the caller (nobody in the cluster reads it)
+      int32_t* sel_u = a.sel_out + (int64_t)u * a.kmax;
+      for (int32_t p = tid; p < kept; p += kSelThreads) sel_u[p] = b_lo + kept_list[p];
+      if (tid == 0) {
+        a.nsel_out[u] = kept;
+        if (kept != k) raise_flags(a.error_flags, SRKV_EFLAG_SELECTION);
+      }
+      // 4. merge the streaming CTAs' partials (warp w: query head w of the group)
+      if (!mbar_wait_cluster(parts_ready, 0)) {
+        if (tid == 0) raise_flags(a.error_flags, SRKV_EFLAG_TIMEOUT);
+      }
+      if (warp < a.G) {
+        // lane qq holds the (max, sum) of streaming CTA qq; weights by shuffles, then every
+        // lane adds its d-slice of the weighted partials
+        constexpr int V = D / 32;
+        float m = -INFINITY, l = 0.f;
+        if (lane < S) {
+          const int32_t np = (share_begin(lane + 1, nA, S) - share_begin(lane, nA, S)) +
+                             (share_begin(lane + 1, k, S) - share_begin(lane, k, S));
+          if (np > 0) {
+            m = part_ml[(lane * a.G + warp) * 2];
+            l = part_ml[(lane * a.G + warp) * 2 + 1];
+          }
+        }
+        float mx = m;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+        const float w = mx == -INFINITY ? 0.f : fast_exp2(m - mx);  // 0 for an absent part
+        float l_run = w * l;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) l_run += __shfl_xor_sync(0xffffffffu, l_run, o);
+        float acc[V];
+#pragma unroll
+        for (int e = 0; e < V; ++e) acc[e] = 0.f;
+        for (int32_t qq = 0; qq < S; ++qq) {
+          const float wq = __shfl_sync(0xffffffffu, w, qq);
+          if (wq == 0.f) continue;
+          const float* src = part_acc + (qq * a.G + warp) * D + lane * V;
+#pragma unroll
+          for (int e = 0; e < V; ++e) acc[e] += wq * src[e];
+        }
+        __nv_bfloat16* o = static_cast<__nv_bfloat16*>(a.out) +
+                           ((int64_t)r * a.Hq + (int64_t)h * a.G + warp) * D + lane * V;
+#pragma unroll
+        for (int e = 0; e < V; e += 2) {
+          const float x0 = l_run > 0.f ? acc[e] / l_run : 0.f;
+          const float x1 = l_run > 0.f ? acc[e + 1] / l_run : 0.f;
+          *reinterpret_cast<__nv_bfloat162*>(o + e) = __floats2bfloat162_rn(x0, x1);
+        }
+      }
+    } else {
+      // 3'. attend list A, then the kept blocks, as one segment; the merged partial goes to
+      // the leader's shared memory
+      consumer_loop<D>(a, smem, lane, warp,
+                       [&](const SoftmaxState<D>& st, const StageInfo&, Lane ln) {
+                         float* acc_l = part_acc + (int64_t)q * a.G * D;
+                         float* ml_l = part_ml + (int64_t)q * a.G * 2;
+                         store_partial<D>(static_cast<float*>(map_cluster_ptr(acc_l, 0)),
+                                          static_cast<float*>(map_cluster_ptr(ml_l, 0)), st, ln,
+                                          a.G);
+                       });
+      // each lane of warp 0 releases the part of the partial it wrote
+      if (warp == 0) mbar_arrive_cluster(parts_ready, 0);
+    }
+  }
+  __syncwarp();
+  cluster_sync();  // nobody leaves while another CTA may still reach its shared memory
+}
+
+}  // namespace
+
+// Cluster size for `units` units (0 = the fused path does not apply): the largest of 16,
+// 12, 8 CTAs per unit such that every cluster is resident at once.
+int32_t fused_cluster_size(const srkv_config& cfg, int32_t units, int32_t max_blocks) {
+  if (!mma_split_supported(cfg) || units <= 0) return 0;
+  const int64_t W = (int64_t)max_blocks * kBlock - cfg.local_tokens;
+  const int64_t nmax = W > cfg.init_tokens ? (W + kBlock - 1) / kBlock - cfg.init_tokens / kBlock : 0;
+  if (nmax > kMaxCand) return 0;
+  static int32_t cached[128][2][3];  // [device][d 64 / 128][cluster 16, 12, 8]: max active + 1
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 128) return 0;
+  const int di = cfg.head_dim == 128 ? 1 : 0;
+  const int32_t sizes[3] = {16, 12, 8};
+  for (int c = 0; c < 3; ++c) {
+    const int32_t cs = sizes[c];
+    if (nmax > (int64_t)kMaxShare * cs) continue;                    // per-CTA scoring share
+    if ((int64_t)kMaxList * (cs - 1) < nmax) continue;              // per-CTA kept share
+    if (cached[dev][di][c] == 0) {
+      cudaLaunchConfig_t lc = {};
+      lc.gridDim = dim3((unsigned)cs);
+      lc.blockDim = dim3((kConsumerWarps + 1) * 32);
+      cudaLaunchAttribute attr[1];
+      attr[0].id = cudaLaunchAttributeClusterDimension;
+      attr[0].val.clusterDim.x = (unsigned)cs;
+      attr[0].val.clusterDim.y = 1;
+      attr[0].val.clusterDim.z = 1;
+      lc.attrs = attr;
+      lc.numAttrs = 1;
+      int n = 0;
+      cudaError_t e;
+      if (di) {
+        lc.dynamicSmemBytes = FusedCfg<128>::kSmemAlloc;
+        cudaFuncSetAttribute(fused_decode_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)FusedCfg<128>::kSmemAlloc);
+        cudaFuncSetAttribute(fused_decode_kernel<128>,
+                             cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+        e = cudaOccupancyMaxActiveClusters(&n, fused_decode_kernel<128>, &lc);
+      } else {
+        lc.dynamicSmemBytes = FusedCfg<64>::kSmemAlloc;
+        cudaFuncSetAttribute(fused_decode_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)FusedCfg<64>::kSmemAlloc);
+        cudaFuncSetAttribute(fused_decode_kernel<64>,
+                             cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+        e = cudaOccupancyMaxActiveClusters(&n, fused_decode_kernel<64>, &lc);
+      }
+      if (e != cudaSuccess) {
+        (void)cudaGetLastError();
+        n = 0;
+      }
+      cached[dev][di][c] = n + 1;
+    }
+    if (units <= cached[dev][di][c] - 1) return cs;
+  }
+  return 0;
+}
+
+cudaError_t launch_fused(const DecodeArgs& a, int32_t cluster, cudaStream_t stream) {
+  TmaMaps maps;
+  if (!encode_cache_map(&maps.k, a.k_cache, a.num_pages, a.Hkv, a.d) ||
+      !encode_cache_map(&maps.v, a.v_cache, a.num_pages, a.Hkv, a.d))
+    return cudaErrorInvalidValue;
+  const int64_t grid = (int64_t)a.batch * a.Hkv * cluster;
+  cudaLaunchConfig_t lc = {};
+  lc.gridDim = dim3((unsigned)grid);
+  lc.blockDim = dim3((kConsumerWarps + 1) * 32);
+  lc.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = (unsigned)cluster;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  lc.attrs = attr;
+  lc.numAttrs = 1;
+  if (a.d == 128) {
+    lc.dynamicSmemBytes = FusedCfg<128>::kSmemAlloc;
+    return cudaLaunchKernelEx(&lc, fused_decode_kernel<128>, a, maps);
+  }
+  lc.dynamicSmemBytes = FusedCfg<64>::kSmemAlloc;
+  return cudaLaunchKernelEx(&lc, fused_decode_kernel<64>, a, maps);
+}
+
+}  // namespace srkv

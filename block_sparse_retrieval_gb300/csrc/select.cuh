@@ -120,6 +120,14 @@ __device__ __forceinline__ void mbar_arrive_cluster(uint64_t* local, uint32_t ra
   asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(remote)
                : "memory");
 }
+// The same, counting `n` arrivals.
+__device__ __forceinline__ void mbar_arrive_cluster_n(uint64_t* local, uint32_t rank, uint32_t n) {
+  uint32_t remote;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(smem_u32(local)), "r"(rank));
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0], %1;" ::"r"(remote),
+               "r"(n)
+               : "memory");
+}
 // Waits (bounded, acquire at cluster scope) for the phase with the given parity.
 __device__ __forceinline__ bool mbar_wait_cluster(uint64_t* bar, uint32_t parity) {
   const uint64_t t0 = global_ns();
@@ -141,13 +149,19 @@ __device__ __forceinline__ bool mbar_wait_cluster(uint64_t* bar, uint32_t parity
 // warp in one round of loads; lane x of the warp stores its x-th key into the leader's
 // keys[i] and counts it into the leader's hist0 (and, with pages_to_leader, the
 // candidate's page into the leader's pages[i]).  `pages` holds the share's pages at
-// [i - s_lo].  Returns the error flags seen (pages out of range).
-template <int D, int kWarps>
+// [i - s_lo].  issued() runs once, right after the warp's first round of vector loads has
+// been issued (before any of them is used; it may wait, e.g. for the cluster barrier that
+// makes the leader's shared memory safe to write).  Returns the error flags seen (pages out
+// of range).
+//
+// stored() runs on every lane that wrote a key, after its writes (e.g. to release them).
+template <int D, int kWarps, typename Issued, typename Stored>
 __device__ __forceinline__ uint32_t score_share(const float* qbar, const int32_t* pages,
                                                 int32_t s_lo, int32_t i_hi, const float* reps,
                                                 int64_t num_pages, int32_t Hkv, int32_t h,
                                                 uint32_t* leader_keys, int32_t* leader_hist0,
-                                                int32_t* leader_pages, int warp, int lane) {
+                                                int32_t* leader_pages, int warp, int lane,
+                                                Issued issued, Stored stored) {
   constexpr int EPL = D / 32;  // elements per lane: 4 (d 128) or 2 (d 64)
   uint32_t eflags = 0;
   float qv[EPL];
@@ -155,28 +169,39 @@ __device__ __forceinline__ uint32_t score_share(const float* qbar, const int32_t
   for (int e = 0; e < EPL; ++e) qv[e] = qbar[lane * EPL + e];
   const uint64_t keep = l2_policy_evict_last();  // the vectors are read again every step
   constexpr int UNROLL = 8;
+  bool first = true;
   for (int32_t i0 = s_lo + warp; i0 < i_hi; i0 += kWarps * UNROLL) {
     float part[UNROLL];
     bool ok[UNROLL];
+    float4 v[UNROLL];
 #pragma unroll
-    for (int x = 0; x < UNROLL; ++x) {
+    for (int x = 0; x < UNROLL; ++x) {  // every load of the round first
       const int32_t i = i0 + x * kWarps;
-      part[x] = 0.f;
       ok[x] = false;
+      v[x] = make_float4(0.f, 0.f, 0.f, 0.f);
       if (i < i_hi) {
         const int32_t page = pages[i - s_lo];
         ok[x] = page >= 0 && (int64_t)page < num_pages;
         if (ok[x]) {
           const float* rep = reps + ((int64_t)page * Hkv + h) * D + lane * EPL;
           if constexpr (EPL == 4) {
-            const float4 v = ldg_f4_hint(rep, keep);
-            part[x] = qv[0] * v.x + qv[1] * v.y + qv[2] * v.z + qv[3] * v.w;
+            v[x] = ldg_f4_hint(rep, keep);
           } else {
-            const float2 v = ldg_f2_hint(rep, keep);
-            part[x] = qv[0] * v.x + qv[1] * v.y;
+            const float2 w = ldg_f2_hint(rep, keep);
+            v[x].x = w.x;
+            v[x].y = w.y;
           }
         }
       }
+    }
+    if (first) issued();
+    first = false;
+#pragma unroll
+    for (int x = 0; x < UNROLL; ++x) {
+      if constexpr (EPL == 4)
+        part[x] = qv[0] * v[x].x + qv[1] * v[x].y + qv[2] * v[x].z + qv[3] * v[x].w;
+      else
+        part[x] = qv[0] * v[x].x + qv[1] * v[x].y;
     }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1)
@@ -203,6 +228,7 @@ __device__ __forceinline__ uint32_t score_share(const float* qbar, const int32_t
     const uint32_t digit = valid ? key >> 24 : 0xffffffffu;
     const uint32_t peers = __match_any_sync(0xffffffffu, digit);
     if (valid && lane == __ffs(peers) - 1) red_cluster_add(&leader_hist0[digit], 0, __popc(peers));
+    if (valid) stored();
   }
   return __reduce_or_sync(0xffffffffu, eflags);
 }

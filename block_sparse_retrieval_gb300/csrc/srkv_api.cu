@@ -126,6 +126,9 @@ srkv_status prepare_decode(const srkv_config* cfg, const void* q, const void* k_
   a.lay = ws_layout(batch * cfg->num_kv_heads, kMaxCtas, G, cfg->head_dim);
   a.early = 0;
   a.prompt_lens = nullptr;
+  a.reps = nullptr;
+  a.sel_out = nullptr;
+  a.nsel_out = nullptr;
   a.dense_boundary = cfg->dense_boundary;
   a.topk_percent = cfg->topk_percent;
   return SRKV_OK;
@@ -271,6 +274,13 @@ srkv_status srkv_retrieval_decode(const srkv_config* cfg, const void* q, const v
   // is scheduled in block order), list B to those that start before the scoring ends (all
   // but one SM per (request, kv head) cluster, whose leader selects last).
   a.prompt_lens = prompt_lens;
+  a.reps = reps;
+  a.sel_out = sel;
+  a.nsel_out = nsel;
+  cudaStream_t s = (cudaStream_t)stream;
+  // A batch small enough for one cluster per unit to be resident: one kernel does it all.
+  const int32_t cluster = fused_cluster_size(*cfg, batch * cfg->num_kv_heads, max_blocks);
+  if (cluster > 0) return cuda_status(launch_fused(a, cluster, s));
   const bool early = mma_split_supported(*cfg);
   const int64_t scoring = score_topk_ctas(*cfg, max_blocks, batch);
   const int64_t leaders = (int64_t)batch * cfg->num_kv_heads;
@@ -278,7 +288,6 @@ srkv_status srkv_retrieval_decode(const srkv_config* cfg, const void* q, const v
     a.ctas_a = a.ctas - (int32_t)scoring;
     a.ctas_b = a.ctas - (int32_t)leaders;
   }
-  cudaStream_t s = (cudaStream_t)stream;
   if (launch_score_topk(*cfg, q, reps, num_pages, block_table, max_blocks, seq_lens, prompt_lens,
                         batch, sel, kmax, nsel, error_flags, s) != cudaSuccess)
     return SRKV_ERR_CUDA;

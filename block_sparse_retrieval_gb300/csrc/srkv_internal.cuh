@@ -350,6 +350,9 @@ struct DecodeArgs {
   const int32_t* prompt_lens;
   int32_t dense_boundary;
   double topk_percent;
+  const float* reps;  // the fused small-batch decode scores too, and writes the selection:
+  int32_t* sel_out;
+  int32_t* nsel_out;
 };
 
 // CTAs that share the positions of a list.
@@ -427,5 +430,11 @@ int32_t simt_split_ctas(int32_t sm_count);
 cudaError_t launch_split_simt(const DecodeArgs& a, int32_t dtype, cudaStream_t stream);
 
 cudaError_t launch_combine(const DecodeArgs& a, int32_t dtype, cudaStream_t stream);
+
+// Scoring, selection and attention of a small batch in one kernel, one thread-block cluster
+// per (request, kv head) unit: the cluster size to use for `units` units (0 = not
+// applicable: dtype, head size, group, candidates per unit or residency), and its launch.
+int32_t fused_cluster_size(const srkv_config& cfg, int32_t units, int32_t max_blocks);
+cudaError_t launch_fused(const DecodeArgs& a, int32_t cluster, cudaStream_t stream);
 
 }  // namespace srkv
