@@ -67,7 +67,8 @@ DEFAULT_WORKLOAD = "llama8b-65536"
 WORKLOAD = WORKLOADS[DEFAULT_WORKLOAD][1]
 FALLBACK_HBM = 6800.0
 DECODE_SOURCES = ("score_topk.cu", "decode_split_mma.cu", "decode_combine.cu",
-                  "decode_plan.cuh", "srkv_internal.cuh", "srkv_api.cu")
+                  "decode_fused.cu", "decode_mma.cuh", "select.cuh", "decode_plan.cuh",
+                  "srkv_internal.cuh", "srkv_api.cu")
 
 
 # ---- distributed plumbing -----------------------------------------------------------------
@@ -120,8 +121,8 @@ def decode_source_hash() -> str:
 
 
 def committed_traffic():
-    """DRAM bytes per step (the three kernels of srkv_retrieval_decode) from the committed ncu
-    summary, if it was taken on the current sources; else None."""
+    """DRAM bytes per step (the kernels of one srkv_retrieval_decode call) from the committed
+    ncu summary, if it was taken on the current sources; else None."""
     try:
         with open(TRAFFIC) as f:
             t = json.load(f)
@@ -362,6 +363,12 @@ def run_ours(args, world, rank, local):
     call_ms = statistics.mean(replay_ms) / R
     achieved = avg_step_bytes / (call_ms / 1e3) / 1e9
     traffic = committed_traffic() if wl == DEFAULT_WORKLOAD else None
+    c0 = layers[0].case
+    launches = layers[0].srkv.retrieval_decode_launches(c0.cfg, c0.batch, c0.max_blocks)
+    kernel_desc = ("srkv_retrieval_decode call: one kernel (a thread-block cluster per "
+                   "(request, kv head) scores, selects and attends)" if launches == 1 else
+                   "srkv_retrieval_decode call: score_topk, split-K decode and combine kernels, "
+                   "overlapped by programmatic launch")
 
     e2e = run_e2e(layers, min(K, args.e2e_steps), world, dev)
     line = {
@@ -373,9 +380,8 @@ def run_ours(args, world, rank, local):
                    "seq_len": WORKLOADS[wl][2], "parallelism": f"replicas x{world}",
                    "layers_rotated": R,
                    "l2": f"inputs larger than L2: {R} layer caches rotated per step"},
-        "roofline": {"kernel": "srkv_retrieval_decode call: score_topk, split-K decode and "
-                               "combine kernels, overlapped by programmatic launch",
-                     "bound": "hbm", "achieved": round(achieved, 1), "peak": peak,
+        "roofline": {"kernel": kernel_desc, "bound": "hbm", "achieved": round(achieved, 1),
+                     "peak": peak,
                      "unit": "GB/s", "frac": round(achieved / peak, 4), "peak_kind": peak_kind,
                      "bytes_per_launch": int(avg_step_bytes),
                      "unique_bytes_per_launch": int(avg_unique),
@@ -386,7 +392,7 @@ def run_ours(args, world, rank, local):
             "frac": round(rep_bytes / (rep_ms / 1e3) / 1e9 / peak, 4)},
         "clocks": clocks.summary(),
         "e2e": e2e,
-        "gpu_launches": K * 3,   # score_topk, the split kernel and the combine per step
+        "gpu_launches": K * launches,  # kernels per srkv_retrieval_decode call x steps
     }
     if rank == 0 and not args.no_cpu_baseline and wl == DEFAULT_WORKLOAD:
         line["cpu_baseline"] = cpu_baseline(layers[0], args.cpu_seconds)

@@ -239,6 +239,13 @@ size_t srkv_decode_workspace_size(const srkv_config* cfg, int32_t batch) {
   return workspace_size(cfg, batch);
 }
 
+int32_t srkv_retrieval_decode_launches(const srkv_config* cfg, int32_t batch,
+                                       int32_t max_blocks) {
+  if (!config_ok(cfg) || batch < 0 || max_blocks <= 0) return 0;
+  if (batch == 0) return 0;
+  return fused_cluster_size(*cfg, batch * cfg->num_kv_heads, max_blocks) > 0 ? 1 : 3;
+}
+
 srkv_status srkv_sparse_paged_decode(const srkv_config* cfg, const void* q, const void* k_cache,
                                      const void* v_cache, int64_t num_pages,
                                      const int32_t* block_table, int32_t max_blocks,

@@ -27,7 +27,8 @@ STATUS = {0: "ok", 1: "invalid argument", 2: "unsupported configuration",
 EXPORTS = ("srkv_default_config", "srkv_status_string", "srkv_topk_count",
            "srkv_num_candidates", "srkv_kmax_bound", "srkv_build_block_reps",
            "srkv_score_topk", "srkv_decode_workspace_size", "srkv_sparse_paged_decode",
-           "srkv_retrieval_decode", "srkv_sparse_paged_decode_noalloc")
+           "srkv_retrieval_decode", "srkv_sparse_paged_decode_noalloc",
+           "srkv_retrieval_decode_launches")
 NOALLOC_WORKSPACE_BYTES = 16 << 20
 
 
@@ -74,6 +75,8 @@ def load() -> ctypes.CDLL:
                                     _I32, _P, _I32, _P, _P, _P]
     lib.srkv_decode_workspace_size.argtypes = [ctypes.POINTER(Config), _I32]
     lib.srkv_decode_workspace_size.restype = _SZ
+    lib.srkv_retrieval_decode_launches.argtypes = [ctypes.POINTER(Config), _I32, _I32]
+    lib.srkv_retrieval_decode_launches.restype = _I32
     lib.srkv_sparse_paged_decode.argtypes = [ctypes.POINTER(Config), _P, _P, _P, _I64, _P, _I32,
                                              _P, _I32, _P, _I32, _P, _P, _P, _SZ, _P, _P]
     lib.srkv_retrieval_decode.argtypes = [ctypes.POINTER(Config), _P, _P, _P, _P, _I64, _P,
@@ -119,6 +122,12 @@ def kmax_bound(cfg: Mapping, max_blocks: int) -> int:
 def decode_workspace_size(cfg: Mapping, batch: int) -> int:
     c = config(cfg)
     return int(load().srkv_decode_workspace_size(ctypes.byref(c), batch))
+
+
+def retrieval_decode_launches(cfg: Mapping, batch: int, max_blocks: int) -> int:
+    """Kernels one retrieval_decode call launches on the current device (1 or 3)."""
+    c = config(cfg)
+    return int(load().srkv_retrieval_decode_launches(ctypes.byref(c), batch, max_blocks))
 
 
 # ---- marshalling helpers ----------------------------------------------------------------

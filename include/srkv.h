@@ -166,8 +166,17 @@ srkv_status srkv_sparse_paged_decode(const srkv_config* cfg, const void* q, cons
                                      int32_t* error_flags, srkv_stream stream);
 
 /*
- * One whole decode step: srkv_score_topk followed by srkv_sparse_paged_decode on the same
- * stream, with the selection written to the caller's sel/nsel buffers.
+ * One whole decode step: the result of srkv_score_topk followed by srkv_sparse_paged_decode
+ * on the same stream, with the selection written to the caller's sel/nsel buffers (openGauss
+ * page, "Overall Solution": score, keep the topK blocks, attend them with the initial tokens
+ * and the window).  Arguments as for those two calls; prompt_lens may be NULL (the prompt
+ * is then the sequence length).
+ *   How: a batch small enough for one thread-block cluster per (request, kv head) unit to be
+ *   resident (at most 15 units, <= 1024 candidate blocks per request, bf16, d 64 or 128,
+ *   group <= 8) runs as one kernel; otherwise the scoring kernel, the split decode (which
+ *   streams the initial and window pages while the scoring runs) and the combine.  The first
+ *   call for a configuration on a device queries the device (cluster residency); make it
+ *   before any stream capture.
  */
 srkv_status srkv_retrieval_decode(const srkv_config* cfg, const void* q, const void* k_cache,
                                   const void* v_cache, const float* reps, int64_t num_pages,
@@ -176,6 +185,13 @@ srkv_status srkv_retrieval_decode(const srkv_config* cfg, const void* q, const v
                                   int32_t batch, int32_t* sel, int32_t kmax, int32_t* nsel,
                                   void* out, void* workspace, size_t workspace_bytes,
                                   int32_t* error_flags, srkv_stream stream);
+
+/*
+ * Number of kernels one srkv_retrieval_decode call with these arguments launches on the
+ * current device (1 for the one-kernel small-batch path, else 3); 0 if cfg is invalid.
+ * Host only; queries the device like the first call does.
+ */
+int32_t srkv_retrieval_decode_launches(const srkv_config* cfg, int32_t batch, int32_t max_blocks);
 
 /*
  * For callers that cannot allocate device memory: srkv_sparse_paged_decode without a

@@ -213,3 +213,13 @@ def test_full_size_sampled(name):
     assert int(buf.error_flags.item()) == 0
     assert exact >= 1
     assert check_fused_step(case, buf, ref, exact, units) >= 1
+
+
+def test_retrieval_decode_paths():
+    """One kernel for a batch whose clusters are all resident, three otherwise."""
+    small = synth.llama8b_layer(seq_len=16384, device=DEV)
+    big = synth.ragged_batch(n_requests=4, lo=9000, hi=20000, device=DEV)
+    assert srkv.retrieval_decode_launches(small.cfg, small.batch, small.max_blocks) == 1
+    assert srkv.retrieval_decode_launches(big.cfg, big.batch, big.max_blocks) == 3
+    f32 = CASES["f32-d128"]()
+    assert srkv.retrieval_decode_launches(f32.cfg, f32.batch, f32.max_blocks) == 3
