@@ -9,8 +9,8 @@
 // the steps:
 //   * every CTA scores its share of the candidates (select.cuh: keys, page ids and the top-8-
 //     bit histogram go to the leader, CTA 0, through distributed shared memory);
-//   * meanwhile the other CTAs' producer warps stream their share of the initial and window
-//     pages (list A) into the stage ring (decode_mma.cuh);
+//   * then the other CTAs' producer warps stream their share of the initial and window pages
+//     (list A) into the stage ring (decode_mma.cuh) while the leader selects;
 //   * the leader selects (radix narrowing, ranked finish), writes sel / nsel, and hands each
 //     streaming CTA its share of the kept blocks (page and block ids) in that CTA's shared
 //     memory, releasing an mbarrier there;
@@ -76,7 +76,7 @@ __global__ void __maxnreg__(128) fused_decode_kernel(const DecodeArgs a,
   uint64_t* keys_ready = reinterpret_cast<uint64_t*>(smem + F::kOffBars);
   uint64_t* list_ready = keys_ready + 1;
   uint64_t* parts_ready = keys_ready + 2;
-  uint64_t* scored = keys_ready + 3;  // this CTA's scoring loads have landed
+  uint64_t* scored = keys_ready + 3;  // this CTA's keys are out
   float* qbar = reinterpret_cast<float*>(smem + F::kOffQbar);
   int32_t* share = reinterpret_cast<int32_t*>(smem + F::kOffShare);
   int2* blist = reinterpret_cast<int2*>(smem + F::kOffList);
@@ -141,8 +141,7 @@ __global__ void __maxnreg__(128) fused_decode_kernel(const DecodeArgs a,
         ++it;
       };
       // list A: 32 positions resolved at once, handed out in order; the first copy waits
-      // until this CTA's scoring loads are on their way (pages requested before them would
-      // delay them)
+      // until this CTA's keys are out
       for (int32_t j0 = a0; j0 < a1 && !abort; j0 += 32) {
         const int32_t cnt = min(32, a1 - j0);
         PageTask task;
@@ -244,22 +243,20 @@ __global__ void __maxnreg__(128) fused_decode_kernel(const DecodeArgs a,
     }
     bar();
     // 2. scores into the leader (keys, pages, top-8-bit histogram)
-    // the pages of list A start streaming once every warp's vector loads are on their way;
-    // keys go to the leader once every CTA has passed its setup (cluster barrier)
+    // keys go to the leader once every CTA has passed its setup (cluster barrier); the pages
+    // of list A start streaming once this CTA's keys are out (pages requested earlier would
+    // delay the vector loads, and with them the selection everything waits for)
     bool waited = false;
     uint32_t eflags = score_share<D, kConsumerWarps>(
         qbar, share, s_lo, s_hi, a.reps, a.num_pages, a.Hkv, h, keys, &hist[0][0], pages, warp,
         lane,
         [&] {
-          if (lane == 0) mbar_arrive(scored);
           cluster_wait();
           waited = true;
         },
         [&] { mbar_arrive_cluster(keys_ready, 0); });  // releases this lane's key, page, count
-    if (!waited) {  // a warp without candidates
-      if (lane == 0) mbar_arrive(scored);
-      cluster_wait();
-    }
+    if (!waited) cluster_wait();  // a warp without candidates
+    if (lane == 0) mbar_arrive(scored);
     if (lane == 0 && eflags) raise_flags(a.error_flags, eflags);
     // the arrivals the leader's barrier expects beyond the n candidates, at once
     if (leader && tid == 0 && n < kMaxCand)
