@@ -371,6 +371,7 @@ def run_ours(args, world, rank, local):
                    "overlapped by programmatic launch")
 
     e2e = run_e2e(layers, min(K, args.e2e_steps), world, dev)
+    append = time_append(dev, layers[0].case.cfg)
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": "steps/s", "n_gpus": world,
         "steps": K, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5),
@@ -392,12 +393,37 @@ def run_ours(args, world, rank, local):
             "frac": round(rep_bytes / (rep_ms / 1e3) / 1e9 / peak, 4)},
         "clocks": clocks.summary(),
         "e2e": e2e,
+        "append_kv": append,
         "gpu_launches": K * launches,  # kernels per srkv_retrieval_decode call x steps
     }
     if rank == 0 and not args.no_cpu_baseline and wl == DEFAULT_WORKLOAD:
         line["cpu_baseline"] = cpu_baseline(layers[0], args.cpu_seconds)
     if rank == 0:
         print(json.dumps(line), flush=True)
+
+
+def time_append(dev, cfg, n: int = 200) -> dict:
+    """Decode-time maintenance of the same layer shape: srkv_append_kv of one new token
+    (every kv head) and the refresh of its page's representation vector, per call."""
+    from block_sparse_retrieval_gb300 import srkv, synth
+    case = synth.llama8b_layer(seq_len=65536 - 128 + n, device=dev, seed=7)
+    lens = case.seq_lens - n
+    buf = srkv.DecodeBuffers(case.cfg, case.batch, case.max_blocks, case.num_pages, device=dev)
+    Hkv, d = case.cfg["num_kv_heads"], case.cfg["head_dim"]
+    kn = torch.randn(n, case.batch, Hkv, d, device=dev).to(case.k_cache.dtype)
+    lens_all = torch.stack([lens + i for i in range(n)])  # position of every call
+    srkv.append_kv(case.cfg, kn[0], kn[0], case.k_cache, case.v_cache, case.block_table,
+                   lens_all[0], buf.reps, buf.error_flags)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for i in range(n):
+        srkv.append_kv(case.cfg, kn[i], kn[i], case.k_cache, case.v_cache, case.block_table,
+                       lens_all[i], buf.reps, buf.error_flags)
+    e1.record()
+    torch.cuda.synchronize()
+    return {"kernel": "srkv_append_kv", "us_per_call": round(e0.elapsed_time(e1) * 1e3 / n, 2),
+            "calls": n, "note": "back-to-back launches of one token each, same layer shape"}
 
 
 def run_e2e(layers, K, world, dev) -> dict:

@@ -222,6 +222,27 @@ srkv_status srkv_build_block_reps(const srkv_config* cfg, const void* k_cache,
                                        n_pages, reps, error_flags, (cudaStream_t)stream));
 }
 
+srkv_status srkv_append_kv(const srkv_config* cfg, const void* k_new, const void* v_new,
+                           void* k_cache, void* v_cache, int64_t num_pages,
+                           const int32_t* block_table, int32_t max_blocks,
+                           const int32_t* seq_lens, int32_t batch, float* reps,
+                           int32_t* error_flags, srkv_stream stream) {
+  if (!config_ok(cfg) || batch < 0 || max_blocks <= 0 || max_blocks > kMaxBlocks ||
+      num_pages < 0)
+    return SRKV_ERR_INVALID_ARG;
+  if (batch == 0) return SRKV_OK;
+  if (!k_new || !v_new || !k_cache || !v_cache || !block_table || !seq_lens || !reps ||
+      num_pages == 0)
+    return SRKV_ERR_INVALID_ARG;
+  if (!aligned(k_new, 16) || !aligned(v_new, 16) || !aligned(k_cache, 16) ||
+      !aligned(v_cache, 16) || !aligned(reps, 16))
+    return SRKV_ERR_INVALID_ARG;
+  if ((int64_t)batch * cfg->num_kv_heads > INT32_MAX) return SRKV_ERR_UNSUPPORTED;
+  return cuda_status(launch_append_kv(*cfg, k_new, v_new, k_cache, v_cache, num_pages,
+                                      block_table, max_blocks, seq_lens, batch, reps,
+                                      error_flags, (cudaStream_t)stream));
+}
+
 srkv_status srkv_score_topk(const srkv_config* cfg, const void* q, const float* reps,
                             int64_t num_pages, const int32_t* block_table, int32_t max_blocks,
                             const int32_t* seq_lens, const int32_t* prompt_lens, int32_t batch,

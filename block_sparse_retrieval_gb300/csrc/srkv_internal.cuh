@@ -413,6 +413,12 @@ cudaError_t launch_block_reps(const srkv_config& cfg, const void* k_cache, int64
 // CTAs of the scoring grid (clusters of up to 8 per (request, kv head) unit).
 int64_t score_topk_ctas(const srkv_config& cfg, int32_t max_blocks, int32_t batch);
 
+cudaError_t launch_append_kv(const srkv_config& cfg, const void* k_new, const void* v_new,
+                             void* k_cache, void* v_cache, int64_t num_pages,
+                             const int32_t* block_table, int32_t max_blocks,
+                             const int32_t* seq_lens, int32_t batch, float* reps,
+                             int32_t* error_flags, cudaStream_t stream);
+
 cudaError_t launch_score_topk(const srkv_config& cfg, const void* q, const float* reps,
                               int64_t num_pages, const int32_t* block_table,
                               int32_t max_blocks, const int32_t* seq_lens,

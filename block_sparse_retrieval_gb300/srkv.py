@@ -28,7 +28,7 @@ EXPORTS = ("srkv_default_config", "srkv_status_string", "srkv_topk_count",
            "srkv_num_candidates", "srkv_kmax_bound", "srkv_build_block_reps",
            "srkv_score_topk", "srkv_decode_workspace_size", "srkv_sparse_paged_decode",
            "srkv_retrieval_decode", "srkv_sparse_paged_decode_noalloc",
-           "srkv_retrieval_decode_launches")
+           "srkv_retrieval_decode_launches", "srkv_append_kv")
 NOALLOC_WORKSPACE_BYTES = 16 << 20
 
 
@@ -71,6 +71,8 @@ def load() -> ctypes.CDLL:
     lib.srkv_kmax_bound.restype = _I32
     lib.srkv_build_block_reps.argtypes = [ctypes.POINTER(Config), _P, _I64, _P, _P, _I32, _P,
                                           _P, _P]
+    lib.srkv_append_kv.argtypes = [ctypes.POINTER(Config), _P, _P, _P, _P, _I64, _P, _I32, _P,
+                                   _I32, _P, _P, _P]
     lib.srkv_score_topk.argtypes = [ctypes.POINTER(Config), _P, _P, _I64, _P, _I32, _P, _P,
                                     _I32, _P, _I32, _P, _P, _P]
     lib.srkv_decode_workspace_size.argtypes = [ctypes.POINTER(Config), _I32]
@@ -170,6 +172,23 @@ def build_block_reps(cfg: Mapping, k_cache: torch.Tensor, page_ids: torch.Tensor
                                                       torch.int32),
         page_ids.numel(), _dev(reps, "reps", torch.float32),
         _dev(error_flags, "error_flags", torch.int32), _stream(stream)), "srkv_build_block_reps")
+
+
+def append_kv(cfg: Mapping, k_new: torch.Tensor, v_new: torch.Tensor, k_cache: torch.Tensor,
+              v_cache: torch.Tensor, block_table: torch.Tensor, seq_lens: torch.Tensor,
+              reps: torch.Tensor, error_flags: torch.Tensor | None = None,
+              stream=None) -> None:
+    """Writes each request's new token (k_new, v_new: [B][Hkv][d]) at position seq_lens[r]
+    and refreshes that page's representation vector; the caller then advances seq_lens."""
+    c = config(cfg)
+    st = _store_dtype(cfg)
+    _check(load().srkv_append_kv(
+        ctypes.byref(c), _dev(k_new, "k_new", st), _dev(v_new, "v_new", st),
+        _dev(k_cache, "k_cache", st), _dev(v_cache, "v_cache", st), k_cache.shape[0],
+        _dev(block_table, "block_table", torch.int32), block_table.shape[1],
+        _dev(seq_lens, "seq_lens", torch.int32), seq_lens.numel(),
+        _dev(reps, "reps", torch.float32), _dev(error_flags, "error_flags", torch.int32),
+        _stream(stream)), "srkv_append_kv")
 
 
 def score_topk(cfg: Mapping, q: torch.Tensor, reps: torch.Tensor, block_table: torch.Tensor,

@@ -125,6 +125,29 @@ srkv_status srkv_build_block_reps(const srkv_config* cfg, const void* k_cache,
                                   float* reps, int32_t* error_flags, srkv_stream stream);
 
 /*
+ * Decode-time maintenance of the cache and of the vector store (openGauss page, "Feature
+ * Description": the representation vectors are extracted block by block, and "Overall
+ * Solution": decode keeps adding tokens to the cache).  For every request r and kv head h,
+ * the new token's key and value k_new[r][h][:], v_new[r][h][:] are written at position
+ * L = seq_lens[r] of the request, i.e. row L % S of page block_table[r][L / S], and that
+ * page's representation vector reps[page][h][:] is recomputed over its rows [0, L % S] -- the
+ * same value srkv_build_block_reps gives for the page with L % S + 1 valid tokens.
+ *   k_new, v_new: [B][Hkv][d] in the cache dtype, 16-byte aligned; k_cache, v_cache,
+ *   num_pages, block_table, max_blocks, reps: as for the other calls (written in place).
+ *   seq_lens: device int32 [B], read only: the caller advances the lengths (seq_lens[r] += 1)
+ *   after the call, and must give request r a page of its own at block L / S (a page shared
+ *   with other requests would change for them too).
+ *   A length outside [0, max_blocks * S) (SRKV_EFLAG_SEQ_LEN) or a page id outside
+ *   [0, num_pages) (SRKV_EFLAG_PAGE_RANGE) skips that request and is flagged.
+ * Asynchronous on `stream`; one kernel.
+ */
+srkv_status srkv_append_kv(const srkv_config* cfg, const void* k_new, const void* v_new,
+                           void* k_cache, void* v_cache, int64_t num_pages,
+                           const int32_t* block_table, int32_t max_blocks,
+                           const int32_t* seq_lens, int32_t batch, float* reps,
+                           int32_t* error_flags, srkv_stream stream);
+
+/*
  * Scoring and top-k ("Overall Solution": inner product of the current query with each
  * representation vector, keep the topK closest).  For every request r and kv head h:
  * sel[r][h][0..nsel[r][h]) = the selected candidate blocks of (r, h), ascending; dense
