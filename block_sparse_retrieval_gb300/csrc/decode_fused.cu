@@ -11,16 +11,17 @@
 //     bit histogram go to the leader, CTA 0, through distributed shared memory);
 //   * then the other CTAs' producer warps stream their share of the initial and window pages
 //     (list A) into the stage ring (decode_mma.cuh) while the leader selects;
-//   * the leader selects (radix narrowing, ranked finish), writes sel / nsel, and hands each
-//     streaming CTA its share of the kept blocks (page and block ids) in that CTA's shared
-//     memory, releasing an mbarrier there;
-//   * the streaming CTAs attend list A then their kept blocks as one segment and store the
-//     merged partial (max, sum, unnormalised output) into the leader's shared memory;
+//   * the leader selects (radix narrowing, ranked finish), writes sel / nsel, lays the kept
+//     blocks (page and block ids) out as a pool in its own shared memory and releases an
+//     mbarrier in every streaming CTA;
+//   * each streaming CTA attends its share of list A, then takes kept blocks from the pool one
+//     at a time (an atomic counter in the leader's shared memory) until it is empty, so the
+//     CTAs whose pages arrive sooner take more and all finish within about one page of each
+//     other; the merged partial (max, sum, unnormalised output) of the whole segment goes into
+//     the leader's shared memory when the pool is empty;
 //   * the leader merges the partials and writes the output.
-// The selection count of a unit (selection_count) follows from the lengths, so list B's
-// shares are known before the selection: a CTA plans its whole segment up front.  Every wait
-// is bounded (SRKV_EFLAG_TIMEOUT); every thread ends at one cluster barrier, so no CTA leaves
-// while another may still reach its shared memory.
+// Every wait is bounded (SRKV_EFLAG_TIMEOUT); every thread ends at one cluster barrier, so no
+// CTA leaves while another may still reach its shared memory.
 #include "decode_mma.cuh"
 #include "select.cuh"
 
@@ -30,7 +31,6 @@ namespace {
 constexpr int kSelThreads = kConsumerWarps * 32;  // the consumer warps score and select
 constexpr int32_t kMaxCand = kFastRounds * kSelThreads;  // candidates per unit (1024)
 constexpr int kMaxShare = 128;                             // candidates scored per CTA
-constexpr int kMaxList = 160;                              // kept blocks per streaming CTA
 
 template <int D>
 struct FusedCfg {
@@ -40,8 +40,7 @@ struct FusedCfg {
   static constexpr size_t kOffBars = (C::kSmem + 15) & ~size_t(15);
   static constexpr size_t kOffQbar = kOffBars + 4 * sizeof(uint64_t);
   static constexpr size_t kOffShare = kOffQbar + sizeof(float) * D;
-  static constexpr size_t kOffList = kOffShare + sizeof(int32_t) * kMaxShare;  // int2 (page, block)
-  static constexpr size_t kSmem = kOffList + sizeof(int2) * kMaxList;
+  static constexpr size_t kSmem = kOffShare + sizeof(int32_t) * kMaxShare;
   static constexpr size_t kSmemAlloc = kSmem + 1024;
   // the leader streams no pages: its K ring holds the selection state ...
   static constexpr size_t kOffKeys = C::kOffK;
@@ -49,7 +48,9 @@ struct FusedCfg {
   static constexpr size_t kOffHist = kOffPages + sizeof(int32_t) * kMaxCand;
   static constexpr size_t kOffFin = kOffHist + sizeof(int32_t) * 3 * 256;
   static constexpr size_t kOffKept = (kOffFin + sizeof(FinishShared<kSelThreads>) + 15) & ~size_t(15);
-  static constexpr size_t kSelEnd = kOffKept + sizeof(int32_t) * kMaxCand;
+  static constexpr size_t kOffPool = kOffKept + sizeof(int32_t) * kMaxCand;  // int2 (page, block)
+  static constexpr size_t kOffTaken = kOffPool + sizeof(int2) * kMaxCand;    // pool counter
+  static constexpr size_t kSelEnd = kOffTaken + 16;
   // ... and its V ring the streaming CTAs' partials: acc [15][8][D], then (m, l) [15][8][2]
   static constexpr size_t kOffPartAcc = C::kOffV;
   static constexpr size_t kOffPartMl = kOffPartAcc + sizeof(float) * 15 * 8 * D;
@@ -79,12 +80,13 @@ __global__ void __maxnreg__(128) fused_decode_kernel(const DecodeArgs a,
   uint64_t* scored = keys_ready + 3;  // this CTA's keys are out
   float* qbar = reinterpret_cast<float*>(smem + F::kOffQbar);
   int32_t* share = reinterpret_cast<int32_t*>(smem + F::kOffShare);
-  int2* blist = reinterpret_cast<int2*>(smem + F::kOffList);
   uint32_t* keys = reinterpret_cast<uint32_t*>(smem + F::kOffKeys);    // leader
   int32_t* pages = reinterpret_cast<int32_t*>(smem + F::kOffPages);    // leader
   int32_t(*hist)[256] = reinterpret_cast<int32_t(*)[256]>(smem + F::kOffHist);  // leader
   FinishShared<kSelThreads>& fin = *reinterpret_cast<FinishShared<kSelThreads>*>(smem + F::kOffFin);
   int32_t* kept_list = reinterpret_cast<int32_t*>(smem + F::kOffKept);  // leader
+  int2* pool = reinterpret_cast<int2*>(smem + F::kOffPool);              // leader
+  uint32_t* taken = reinterpret_cast<uint32_t*>(smem + F::kOffTaken);    // leader
   float* part_acc = reinterpret_cast<float*>(smem + F::kOffPartAcc);  // leader
   float* part_ml = reinterpret_cast<float*>(smem + F::kOffPartMl);    // leader
 
@@ -98,16 +100,22 @@ __global__ void __maxnreg__(128) fused_decode_kernel(const DecodeArgs a,
   if (tid == 0) {
     init_ring<D>(smem);
     mbar_init(keys_ready, kMaxCand);            // one per candidate, the rest at once
-    mbar_init(list_ready, kMaxList);            // one per kept block handed over, the rest at once
+    mbar_init(list_ready, 1);                   // the leader, once the pool is laid out
     mbar_init(parts_ready, 32u * (uint32_t)S);  // one per lane of a streaming CTA's warp 0
     mbar_init(scored, kConsumerWarps);
     fence_mbar_init();
   }
-  if (leader)
+  if (leader) {
     for (int i = tid; i < 3 * 256; i += blockDim.x) (&hist[0][0])[i] = 0;
+    if (tid == 0) *taken = 0u;
+  }
   __syncthreads();
   cluster_arrive();  // this CTA's barriers and the leader's histogram are ready (waited for
                      // before the first access to another CTA)
+  // Launched behind the previous kernel of the stream (programmatic launch): everything above
+  // touches shared memory only; every input may be that kernel's output, so wait for it here.
+  griddep_wait();
+  griddep_launch_dependents();
 
   // The unit's sizes: candidates n, kept k (what the selection will write), list A length.
   const int32_t L_in = a.seq_lens[r];
@@ -122,24 +130,14 @@ __global__ void __maxnreg__(128) fused_decode_kernel(const DecodeArgs a,
   const int32_t* bt_r = a.block_table + (int64_t)r * a.max_blocks;
   const int32_t q = (int32_t)crank - 1;  // streaming rank
   const int32_t a0 = leader ? 0 : share_begin(q, nA, S), a1 = leader ? 0 : share_begin(q + 1, nA, S);
-  const int32_t l0 = leader ? 0 : share_begin(q, k, S), l1 = leader ? 0 : share_begin(q + 1, k, S);
-  const int32_t npos = (a1 - a0) + (l1 - l0);
-
 
   if (warp == kProducerWarp) {
     // ------------------------------------------------------------------ producer
     cluster_wait();
-    if (!leader && npos > 0) {
+    if (!leader) {
       uint32_t eflags = 0;
       bool abort = false;
       int64_t it = 0, armed = 0;
-      // position p of this CTA's segment (t uniform over the warp)
-      auto hand_out = [&](int32_t p, const PageTask& t) {
-        const uint32_t fl = (p == 0 ? kNewUnit : 0u) | (p == npos - 1 ? kSegEnd : 0u);
-        if (lane == 0) issue_stage<D>(a, maps, smem, it, u, fl, t, armed, abort, eflags);
-        abort = __shfl_sync(0xffffffffu, abort, 0);
-        ++it;
-      };
       // list A: 32 positions resolved at once, handed out in order; the first copy waits
       // until this CTA's keys are out
       for (int32_t j0 = a0; j0 < a1 && !abort; j0 += 32) {
@@ -159,51 +157,56 @@ __global__ void __maxnreg__(128) fused_decode_kernel(const DecodeArgs a,
           tl.hi = __shfl_sync(0xffffffffu, task.hi, l);
           tl.ie = __shfl_sync(0xffffffffu, task.ie, l);
           tl.ws = __shfl_sync(0xffffffffu, task.ws, l);
-          hand_out(j0 + l - a0, tl);
-        }
-      }
-      // list B: the kept blocks the leader hands over
-      if (l1 > l0 && !abort) {
-        if (!mbar_wait_cluster(list_ready, 0)) {
-          eflags |= SRKV_EFLAG_TIMEOUT;
-          abort = true;
-        }
-        for (int32_t i0 = 0; i0 < l1 - l0 && !abort; i0 += 32) {
-          const int32_t cnt = min(32, l1 - l0 - i0);
-          PageTask task;
-          task.page = -1;
-          task.lo = task.hi = task.ie = task.ws = 0;
-          if (lane < cnt) {
-            const int2 e = blist[i0 + lane];  // (page, block)
-            const int32_t base = e.y * kBlock, rows = min(kBlock, g.L - base);
-            const int32_t lo = max(a.init_tokens - base, 0), hi = min(g.W - base, rows);
-            if (lo < hi && e.x >= 0 && (int64_t)e.x < a.num_pages) {
-              task.page = e.x;
-              task.block = e.y;
-              task.lo = lo;
-              task.hi = hi;
-              task.ie = hi;  // every loaded row is attended
-              task.ws = hi;
-            } else if (lo < hi) {
-              eflags |= SRKV_EFLAG_PAGE_RANGE;
-            }
-          }
-          for (int l = 0; l < cnt && !abort; ++l) {
-            PageTask tl;
-            tl.page = __shfl_sync(0xffffffffu, task.page, l);
-            tl.lo = __shfl_sync(0xffffffffu, task.lo, l);
-            tl.hi = __shfl_sync(0xffffffffu, task.hi, l);
-            tl.ie = __shfl_sync(0xffffffffu, task.ie, l);
-            tl.ws = __shfl_sync(0xffffffffu, task.ws, l);
-            hand_out((a1 - a0) + i0 + l, tl);
-          }
+          if (lane == 0)
+            issue_stage<D>(a, maps, smem, it, u, it == 0 ? kNewUnit : 0u, tl, armed, abort, eflags);
+          abort = __shfl_sync(0xffffffffu, abort, 0);
+          ++it;
         }
       }
       if (lane == 0) {
+        // list B: kept blocks from the leader's pool until it is empty; the next entry is
+        // taken before waiting for a free stage, so its two cluster round trips overlap that
+        // wait
+        if (k > 0 && !abort && !mbar_wait_cluster(list_ready, 0)) {
+          eflags |= SRKV_EFLAG_TIMEOUT;
+          abort = true;
+        }
+        auto take = [&](int2& e) -> bool {
+          const uint32_t i = atom_cluster_add(taken, 0, 1u);
+          if (i >= (uint32_t)k) return false;
+          e = ld_cluster_int2(pool + i, 0);
+          return true;
+        };
+        int2 e = make_int2(-1, 0);
+        bool have = k > 0 && !abort && take(e);
+        while (have && !abort) {
+          int2 next = make_int2(-1, 0);
+          const bool more = take(next);
+          PageTask t;
+          t.page = -1;
+          t.lo = t.hi = t.ie = t.ws = 0;
+          const int32_t base = e.y * kBlock, rows = min(kBlock, g.L - base);
+          const int32_t lo = max(a.init_tokens - base, 0), hi = min(g.W - base, rows);
+          if (lo < hi && e.x >= 0 && (int64_t)e.x < a.num_pages) {
+            t.page = e.x;
+            t.block = e.y;
+            t.lo = lo;
+            t.hi = hi;
+            t.ie = hi;  // every loaded row is attended
+            t.ws = hi;
+          } else if (lo < hi) {
+            eflags |= SRKV_EFLAG_PAGE_RANGE;
+          }
+          issue_stage<D>(a, maps, smem, it, u, it == 0 ? kNewUnit : 0u, t, armed, abort, eflags);
+          ++it;
+          e = next;
+          have = more;
+        }
+        // the sentinel closes the segment (empty if this CTA took no page)
         PageTask none;
         none.page = -1;
         none.lo = none.hi = none.ie = none.ws = 0;
-        issue_stage<D>(a, maps, smem, it, -1, kLast, none, armed, abort, eflags);  // sentinel
+        issue_stage<D>(a, maps, smem, it, -1, kLast | kSegEnd, none, armed, abort, eflags);
         uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::kOffBar);
         uint64_t* full_v = full + C::kStages;
         const int64_t first = armed > C::kStages ? armed - C::kStages : 0;
@@ -216,16 +219,6 @@ __global__ void __maxnreg__(128) fused_decode_kernel(const DecodeArgs a,
       }
       eflags = __reduce_or_sync(0xffffffffu, eflags | geflags);
       if (lane == 0) raise_flags(a.error_flags, eflags);
-    } else if (!leader && lane == 0) {
-      // no positions: the consumers still need their sentinel
-      int64_t it = 0, armed = 0;
-      bool abort = false;
-      uint32_t eflags = 0;
-      PageTask none;
-      none.page = -1;
-      none.lo = none.hi = none.ie = none.ws = 0;
-      issue_stage<D>(a, maps, smem, it, -1, kLast, none, armed, abort, eflags);
-      if (eflags) raise_flags(a.error_flags, eflags);
     }
   } else {
     // ------------------------------------------------------------------ consumers
@@ -263,7 +256,7 @@ __global__ void __maxnreg__(128) fused_decode_kernel(const DecodeArgs a,
       mbar_arrive_cluster_n(keys_ready, 0, (uint32_t)(kMaxCand - n));
 
     if (leader) {
-      // 3. select the k kept blocks, write sel / nsel, hand each streaming CTA its share
+      // 3. select the k kept blocks, write sel / nsel, lay out the pool of kept blocks
       if (!mbar_wait_cluster(keys_ready, 0)) {
         if (tid == 0) raise_flags(a.error_flags, SRKV_EFLAG_TIMEOUT);
       }
@@ -277,20 +270,12 @@ __global__ void __maxnreg__(128) fused_decode_kernel(const DecodeArgs a,
                                         [&](int32_t pos, int32_t i) { kept_list[pos] = i; });
       }
       bar();
-      // each entry is released to its CTA by the thread that wrote it
-      for (int32_t p = tid; p < kept; p += kSelThreads) {
-        const int32_t i = kept_list[p];
-        const int32_t qq = ((p + 1) * S - 1) / k;  // streaming CTA of position p
-        int2* dst = static_cast<int2*>(map_cluster_ptr(blist + (p - share_begin(qq, k, S)),
-                                                        (uint32_t)qq + 1));
-        *dst = make_int2(pages[i], b_lo + i);
-        mbar_arrive_cluster(list_ready, (uint32_t)qq + 1);
-      }
-      // the arrivals a CTA's barrier expects beyond its entries, at once
-      for (int32_t qq = tid; qq < S; qq += kSelThreads) {
-        const int32_t rest = kMaxList - (share_begin(qq + 1, k, S) - share_begin(qq, k, S));
-        if (rest > 0) mbar_arrive_cluster_n(list_ready, (uint32_t)qq + 1, (uint32_t)rest);
-      }
+      // the pool: k entries (an entry the selection did not fill has no page); the barrier
+      // orders every thread's entries before the releases below
+      for (int32_t p = tid; p < k; p += kSelThreads)
+        pool[p] = p < kept ? make_int2(pages[kept_list[p]], b_lo + kept_list[p]) : make_int2(-1, 0);
+      bar();
+      for (int32_t qq = tid; qq < S; qq += kSelThreads) mbar_arrive_cluster(list_ready, (uint32_t)qq + 1);
       // the selection, for the caller (nobody in the cluster reads it)
       int32_t* sel_u = a.sel_out + (int64_t)u * a.kmax;
       for (int32_t p = tid; p < kept; p += kSelThreads) sel_u[p] = b_lo + kept_list[p];
@@ -306,14 +291,10 @@ __global__ void __maxnreg__(128) fused_decode_kernel(const DecodeArgs a,
         // lane qq holds the (max, sum) of streaming CTA qq; weights by shuffles, then every
         // lane adds its d-slice of the weighted partials
         constexpr int V = D / 32;
-        float m = -INFINITY, l = 0.f;
+        float m = -INFINITY, l = 0.f;  // a CTA that attended nothing wrote (-inf, 0)
         if (lane < S) {
-          const int32_t np = (share_begin(lane + 1, nA, S) - share_begin(lane, nA, S)) +
-                             (share_begin(lane + 1, k, S) - share_begin(lane, k, S));
-          if (np > 0) {
-            m = part_ml[(lane * a.G + warp) * 2];
-            l = part_ml[(lane * a.G + warp) * 2 + 1];
-          }
+          m = part_ml[(lane * a.G + warp) * 2];
+          l = part_ml[(lane * a.G + warp) * 2 + 1];
         }
         float mx = m;
 #pragma unroll
@@ -342,8 +323,8 @@ __global__ void __maxnreg__(128) fused_decode_kernel(const DecodeArgs a,
         }
       }
     } else {
-      // 3'. attend list A, then the kept blocks, as one segment; the merged partial goes to
-      // the leader's shared memory
+      // 3'. attend list A, then the kept blocks taken from the pool, as one segment; the
+      // merged partial goes to the leader's shared memory
       consumer_loop<D>(a, smem, lane, warp,
                        [&](const SoftmaxState<D>& st, const StageInfo&, Lane ln) {
                          float* acc_l = part_acc + (int64_t)q * a.G * D;
@@ -377,7 +358,6 @@ int32_t fused_cluster_size(const srkv_config& cfg, int32_t units, int32_t max_bl
   for (int c = 0; c < 3; ++c) {
     const int32_t cs = sizes[c];
     if (nmax > (int64_t)kMaxShare * cs) continue;                    // per-CTA scoring share
-    if ((int64_t)kMaxList * (cs - 1) < nmax) continue;              // per-CTA kept share
     if (cached[dev][di][c] == 0) {
       cudaLaunchConfig_t lc = {};
       lc.gridDim = dim3((unsigned)cs);
@@ -427,13 +407,15 @@ cudaError_t launch_fused(const DecodeArgs& a, int32_t cluster, cudaStream_t stre
   lc.gridDim = dim3((unsigned)grid);
   lc.blockDim = dim3((kConsumerWarps + 1) * 32);
   lc.stream = stream;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = (unsigned)cluster;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
   lc.attrs = attr;
-  lc.numAttrs = 1;
+  lc.numAttrs = 2;
   if (a.d == 128) {
     lc.dynamicSmemBytes = FusedCfg<128>::kSmemAlloc;
     return cudaLaunchKernelEx(&lc, fused_decode_kernel<128>, a, maps);

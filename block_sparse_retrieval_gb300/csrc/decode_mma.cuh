@@ -233,8 +233,9 @@ __device__ __forceinline__ void store_partial(float* accp, float* mlp, const Sof
 }
 
 // The 8 consumer warps' loop over the stages the producer hands out, until the sentinel.
-// At the end of each segment the warps merge their states and warp 0 calls
-// write_partial(state, stage info, lane) with the merged state.
+// At the end of each segment (a stage flagged kSegEnd; the sentinel may carry the flag too,
+// closing a segment whose length the producer did not know in advance) the warps merge their
+// states and warp 0 calls write_partial(state, stage info, lane) with the merged state.
 template <int D, typename WritePartial>
 __device__ __forceinline__ void consumer_loop(const DecodeArgs& a, unsigned char* smem, int lane,
                                               int warp, WritePartial&& write_partial) {
@@ -259,6 +260,33 @@ __device__ __forceinline__ void consumer_loop(const DecodeArgs& a, unsigned char
   for (int j = 0; j < C::KJ; ++j) qb[j][0] = qb[j][1] = qb[j][2] = qb[j][3] = 0u;
   bool abort = false;
   int32_t merges = 0;
+  // End of a segment: reduce the per-lane sums, merge the 8 warps, write the partial.
+  auto close_segment = [&](const StageInfo& inf) {
+#pragma unroll
+    for (int o = 4; o < 32; o <<= 1) {
+      st.l[0] += __shfl_xor_sync(0xffffffffu, st.l[0], o);
+      st.l[1] += __shfl_xor_sync(0xffffffffu, st.l[1], o);
+    }
+    const uint32_t ph = (uint32_t)(merges & 1);
+    if (warp >= 4) {
+      if (merges > 0 && !mbar_wait(mb_r2, ph ^ 1u)) abort = true;
+      st.store(sMerge + (warp - 4) * C::kMergeSlot, lane);
+      warp_arrive(mb_w1);
+    } else {
+      if (!mbar_wait(mb_w1, ph)) abort = true;
+      st.merge_from(sMerge + warp * C::kMergeSlot, lane);
+      if (warp >= 1) {
+        st.store(sMerge + warp * C::kMergeSlot, lane);
+        warp_arrive(mb_w2);
+      } else {
+        if (!mbar_wait(mb_w2, ph)) abort = true;
+        for (int w = 1; w < 4; ++w) st.merge_from(sMerge + w * C::kMergeSlot, lane);
+        warp_arrive(mb_r2);
+        write_partial(st, inf, ln);
+      }
+    }
+    ++merges;
+  };
   for (int64_t it = 0;; ++it) {
     const int s = (int)(it % C::kStages);
     if (!mbar_wait(&full[s], (uint32_t)((it / C::kStages) & 1))) {
@@ -266,7 +294,13 @@ __device__ __forceinline__ void consumer_loop(const DecodeArgs& a, unsigned char
       break;
     }
     const StageInfo inf = sInfo[s];
-    if (inf.flags & kLast) break;
+    if (inf.flags & kLast) {  // the sentinel; it may close the last segment
+      if (inf.flags & kSegEnd) {
+        close_segment(inf);
+        if (abort && lane == 0) raise_flags(a.error_flags, SRKV_EFLAG_TIMEOUT);
+      }
+      break;
+    }
     if (inf.flags & kNewUnit) {
       st.reset();
       const unsigned char* q = sQ + (size_t)s * C::kQBytes;
@@ -365,31 +399,7 @@ __device__ __forceinline__ void consumer_loop(const DecodeArgs& a, unsigned char
     warp_arrive(&empty[s]);
 
     if (inf.flags & kSegEnd) {
-      // ---- reduce the per-lane sums, merge the 8 warps, write the partial
-#pragma unroll
-      for (int o = 4; o < 32; o <<= 1) {
-        st.l[0] += __shfl_xor_sync(0xffffffffu, st.l[0], o);
-        st.l[1] += __shfl_xor_sync(0xffffffffu, st.l[1], o);
-      }
-      const uint32_t ph = (uint32_t)(merges & 1);
-      if (warp >= 4) {
-        if (merges > 0 && !mbar_wait(mb_r2, ph ^ 1u)) abort = true;
-        st.store(sMerge + (warp - 4) * C::kMergeSlot, lane);
-        warp_arrive(mb_w1);
-      } else {
-        if (!mbar_wait(mb_w1, ph)) abort = true;
-        st.merge_from(sMerge + warp * C::kMergeSlot, lane);
-        if (warp >= 1) {
-          st.store(sMerge + warp * C::kMergeSlot, lane);
-          warp_arrive(mb_w2);
-        } else {
-          if (!mbar_wait(mb_w2, ph)) abort = true;
-          for (int w = 1; w < 4; ++w) st.merge_from(sMerge + w * C::kMergeSlot, lane);
-          warp_arrive(mb_r2);
-          write_partial(st, inf, ln);
-        }
-      }
-      ++merges;
+      close_segment(inf);
       if (abort) {
         if (lane == 0) raise_flags(a.error_flags, SRKV_EFLAG_TIMEOUT);
         break;

@@ -62,6 +62,21 @@ __device__ __forceinline__ void red_cluster_add(int32_t* local, uint32_t rank, i
   asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(smem_u32(local)), "r"(rank));
   asm volatile("red.shared::cluster.add.u32 [%0], %1;" ::"r"(remote), "r"(v) : "memory");
 }
+// Atomic add to the same shared-memory offset in CTA `rank`, returning the old value.
+__device__ __forceinline__ uint32_t atom_cluster_add(uint32_t* local, uint32_t rank, uint32_t v) {
+  uint32_t remote, old;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(smem_u32(local)), "r"(rank));
+  asm volatile("atom.shared::cluster.add.u32 %0, [%1], %2;" : "=r"(old) : "r"(remote), "r"(v) : "memory");
+  return old;
+}
+// Load of the int2 at the same shared-memory offset in CTA `rank`.
+__device__ __forceinline__ int2 ld_cluster_int2(const int2* local, uint32_t rank) {
+  uint32_t remote;
+  int2 v;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(smem_u32(local)), "r"(rank));
+  asm volatile("ld.shared::cluster.v2.s32 {%0, %1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(remote) : "memory");
+  return v;
+}
 __device__ __forceinline__ void cluster_arrive() {
   asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
 }
