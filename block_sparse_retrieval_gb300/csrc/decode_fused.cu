@@ -31,6 +31,7 @@ namespace {
 constexpr int kSelThreads = kConsumerWarps * 32;  // the consumer warps score and select
 constexpr int32_t kMaxCand = kFastRounds * kSelThreads;  // candidates per unit (1024)
 constexpr int kMaxShare = 128;                             // candidates scored per CTA
+constexpr int kMaxCluster = 16;                            // CTAs per unit, at most
 
 template <int D>
 struct FusedCfg {
@@ -53,8 +54,8 @@ struct FusedCfg {
   static constexpr size_t kSelEnd = kOffTaken + 16;
   // ... and its V ring the streaming CTAs' partials: acc [15][8][D], then (m, l) [15][8][2]
   static constexpr size_t kOffPartAcc = C::kOffV;
-  static constexpr size_t kOffPartMl = kOffPartAcc + sizeof(float) * 15 * 8 * D;
-  static constexpr size_t kPartEnd = kOffPartMl + sizeof(float) * 15 * 8 * 2;
+  static constexpr size_t kOffPartMl = kOffPartAcc + sizeof(float) * (kMaxCluster - 1) * 8 * D;
+  static constexpr size_t kPartEnd = kOffPartMl + sizeof(float) * (kMaxCluster - 1) * 8 * 2;
   static_assert(kSelEnd <= C::kOffV, "selection state fits in the K ring");
   static_assert(kPartEnd <= C::kOffQ, "partials fit in the V ring");
   static_assert(kSmemAlloc <= 232448, "shared memory opt-in limit");
@@ -303,15 +304,39 @@ __global__ void __maxnreg__(128) fused_decode_kernel(const DecodeArgs a,
         float l_run = w * l;
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) l_run += __shfl_xor_sync(0xffffffffu, l_run, o);
+        // every streaming CTA wrote a partial (zeros if it attended nothing).  The loads and
+        // weight shuffles of a batch of 8 slots are unconditional, so they issue together
+        // (the partial area holds kMaxCluster - 1 slots, so every address is in it); a select
+        // drops the slots beyond S and those of weight 0
         float acc[V];
 #pragma unroll
         for (int e = 0; e < V; ++e) acc[e] = 0.f;
-        for (int32_t qq = 0; qq < S; ++qq) {
-          const float wq = __shfl_sync(0xffffffffu, w, qq);
-          if (wq == 0.f) continue;
-          const float* src = part_acc + (qq * a.G + warp) * D + lane * V;
 #pragma unroll
-          for (int e = 0; e < V; ++e) acc[e] += wq * src[e];
+        for (int b0 = 0; b0 < kMaxCluster - 1; b0 += 8) {
+          float x[8][V], wv[8];
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            const int qq = b0 + j < kMaxCluster - 1 ? b0 + j : kMaxCluster - 2;
+            wv[j] = __shfl_sync(0xffffffffu, w, qq);
+            const float* src = part_acc + (qq * a.G + warp) * D + lane * V;
+            if constexpr (V == 4) {
+              const float4 v4 = *reinterpret_cast<const float4*>(src);
+              x[j][0] = v4.x;
+              x[j][1] = v4.y;
+              x[j][2] = v4.z;
+              x[j][3] = v4.w;
+            } else {
+              const float2 v2 = *reinterpret_cast<const float2*>(src);
+              x[j][0] = v2.x;
+              x[j][1] = v2.y;
+            }
+          }
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            const bool use = b0 + j < S && wv[j] != 0.f;
+#pragma unroll
+            for (int e = 0; e < V; ++e) acc[e] = use ? fmaf(wv[j], x[j][e], acc[e]) : acc[e];
+          }
         }
         __nv_bfloat16* o = static_cast<__nv_bfloat16*>(a.out) +
                            ((int64_t)r * a.Hq + (int64_t)h * a.G + warp) * D + lane * V;
