@@ -63,6 +63,14 @@ for _p in (1.0, 0.1, 0.2, 0.4):
         (lambda p: lambda seed, dev: __import__("block_sparse_retrieval_gb300.synth", fromlist=["x"]).dense_vs_sparse(p, seed=seed, device=dev))(_p),
         f"dense-vs-sparse-4x131072-bf16 (batch 4, 32/8 heads, d 128, top-k {_p}, 3% planted, shuffled pages)",
         131072)
+# The offload tier: the same layer with every page that holds only offload-range tokens
+# ([INIT, L - LOCAL)) in a pinned host pool, read in place over NVLink-C2C.
+WORKLOADS["offload-65536"] = (
+    WORKLOADS["llama8b-65536"][0],
+    "offload-llama8b-layer-65536-bf16 (batch 1, 32/8 heads, d 128, top-k 0.2; the offload-range "
+    "pages in a pinned host pool, initial and window pages in HBM)",
+    65536)
+OFFLOAD_WORKLOADS = ("offload-65536",)
 DEFAULT_WORKLOAD = "llama8b-65536"
 WORKLOAD = WORKLOADS[DEFAULT_WORKLOAD][1]
 FALLBACK_HBM = 6800.0
@@ -244,6 +252,21 @@ class Layer:
         c = self.case
         self.buf = srkv.DecodeBuffers(c.cfg, c.batch, c.max_blocks, c.num_pages, device=device)
         self.srkv = srkv
+        self.k_host = self.v_host = None  # the host pool of the offload workload
+
+    def to_host(self, dev_ids, host_ids, new_id):
+        """Moves pages host_ids into a pinned host pool: the device pool keeps dev_ids (in that
+        order), the vectors are renumbered; the caller renumbers the shared block table."""
+        c, b = self.case, self.buf
+        d_idx = torch.as_tensor(dev_ids, device=c.k_cache.device)
+        h_idx = torch.as_tensor(host_ids, device=c.k_cache.device)
+        self.k_host = c.k_cache[h_idx].cpu().contiguous().pin_memory()
+        self.v_host = c.v_cache[h_idx].cpu().contiguous().pin_memory()
+        c.k_cache = c.k_cache[d_idx].contiguous()
+        c.v_cache = c.v_cache[d_idx].contiguous()
+        reps = torch.empty_like(b.reps)
+        reps[torch.as_tensor(new_id, device=reps.device)] = b.reps
+        b.reps.copy_(reps)
 
     def prefill(self):
         c, b = self.case, self.buf
@@ -251,8 +274,15 @@ class Layer:
                                    b.error_flags)
 
     def step(self):
-        """One decode step: srkv_retrieval_decode (score + top-k, then split + combine)."""
+        """One decode step: srkv_retrieval_decode (score + top-k, then split + combine), or
+        srkv_retrieval_decode_tiered when pages live in a host pool."""
         c, b = self.case, self.buf
+        if self.k_host is not None:
+            self.srkv.retrieval_decode_tiered(c.cfg, c.q, c.k_cache, c.v_cache, self.k_host,
+                                              self.v_host, b.reps, c.block_table, c.seq_lens,
+                                              c.prompt_lens, b.sel, b.nsel, b.out, b.workspace,
+                                              b.error_flags)
+            return
         self.srkv.retrieval_decode(c.cfg, c.q, c.k_cache, c.v_cache, b.reps, c.block_table,
                                    c.seq_lens, c.prompt_lens, b.sel, b.nsel, b.out,
                                    b.workspace, b.error_flags)
@@ -276,8 +306,16 @@ class Layer:
         qo = c.batch * Hq * d * 2
         score = n_cand * (d * 4 + 4) + qo + int(nsel.sum()) * 4 + nsel.size * 4
         decode = kv + pages * 4 + qo * 2 + int(nsel.sum()) * 4 + nsel.size * 4
+        host_kv = 0  # K/V of kept blocks read from the host pool (whole 128-token pages)
+        if self.k_host is not None:
+            bt = c.block_table.cpu().numpy()
+            P_dev = c.k_cache.shape[0]
+            for r in range(c.batch):
+                for h in range(Hkv):
+                    blocks = sel[r, h, :nsel[r, h]]
+                    host_kv += int((bt[r, blocks] >= P_dev).sum()) * 128 * d * 2 * 2
         return {"score": score, "decode": decode, "kv": kv, "total": score + decode,
-                "kv_unique": unique_kv_bytes(c, sel, nsel)}
+                "kv_unique": unique_kv_bytes(c, sel, nsel), "host_kv": host_kv}
 
 
 def capture(fn, stream):
@@ -317,6 +355,8 @@ def run_ours(args, world, rank, local):
             + c.page_ids.numel() * c.cfg["num_kv_heads"] * c.cfg["head_dim"] * 4
     torch.cuda.synchronize()
     rep_ms = sum(ev[2 * i].elapsed_time(ev[2 * i + 1]) for i in range(len(layers)))
+    if wl in OFFLOAD_WORKLOADS:
+        offload_layers(layers)
 
     for ly in layers:                        # the step must run clean before it is timed
         ly.step()
@@ -363,6 +403,21 @@ def run_ours(args, world, rank, local):
     call_ms = statistics.mean(replay_ms) / R
     achieved = avg_step_bytes / (call_ms / 1e3) / 1e9
     traffic = committed_traffic() if wl == DEFAULT_WORKLOAD else None
+    roofline = {"kernel": None, "bound": "hbm", "achieved": round(achieved, 1), "peak": peak,
+                "unit": "GB/s", "frac": round(achieved / peak, 4), "peak_kind": peak_kind,
+                "bytes_per_launch": int(avg_step_bytes), "unique_bytes_per_launch": int(avg_unique),
+                "us_per_launch": round(call_ms * 1e3, 3), "traffic": traffic}
+    if wl in OFFLOAD_WORKLOADS:
+        # bound by the host pool's reads over the chip-to-chip link
+        host = statistics.mean(sb["host_kv"] for sb in step_bytes)
+        c2c = c2c_copy_peak(dev)
+        roofline.update({"bound": "c2c", "achieved": round(host / (call_ms / 1e3) / 1e9, 1),
+                         "peak": c2c, "frac": round(host / (call_ms / 1e3) / 1e9 / c2c, 4),
+                         "peak_kind": "measured in this run: pinned host to device copy",
+                         "bytes_per_launch": int(host),
+                         "unique_bytes_per_launch": int(host),
+                         "device_bytes_per_launch": int(avg_step_bytes - host),
+                         "device_GB_s": round((avg_step_bytes - host) / (call_ms / 1e3) / 1e9, 1)})
     c0 = layers[0].case
     launches = layers[0].srkv.retrieval_decode_launches(c0.cfg, c0.batch, c0.max_blocks)
     kernel_desc = ("srkv_retrieval_decode call: one kernel (a thread-block cluster per "
@@ -381,12 +436,7 @@ def run_ours(args, world, rank, local):
                    "seq_len": WORKLOADS[wl][2], "parallelism": f"replicas x{world}",
                    "layers_rotated": R,
                    "l2": f"inputs larger than L2: {R} layer caches rotated per step"},
-        "roofline": {"kernel": kernel_desc, "bound": "hbm", "achieved": round(achieved, 1),
-                     "peak": peak,
-                     "unit": "GB/s", "frac": round(achieved / peak, 4), "peak_kind": peak_kind,
-                     "bytes_per_launch": int(avg_step_bytes),
-                     "unique_bytes_per_launch": int(avg_unique),
-                     "us_per_launch": round(call_ms * 1e3, 3), "traffic": traffic},
+        "roofline": dict(roofline, kernel=kernel_desc),
         "prefill_reps": {"kernel": "srkv_build_block_reps", "pages": sum(
             ly.case.page_ids.numel() for ly in layers), "us": round(rep_ms * 1e3, 1),
             "GB_s": round(rep_bytes / (rep_ms / 1e3) / 1e9, 1),
@@ -400,6 +450,45 @@ def run_ours(args, world, rank, local):
         line["cpu_baseline"] = cpu_baseline(layers[0], args.cpu_seconds)
     if rank == 0:
         print(json.dumps(line), flush=True)
+
+
+def offload_layers(layers):
+    """Moves every page holding only offload-range tokens of some request (blocks b with
+    INIT <= b*S and (b+1)*S <= L - LOCAL) of every layer into a pinned host pool; the layers
+    share one block table, renumbered once."""
+    c = layers[0].case
+    cfg = c.cfg
+    bt = c.block_table.cpu().numpy()
+    to_host = np.zeros(c.num_pages, bool)
+    for r, L in enumerate(c.seq_lens.cpu().numpy()):
+        W = int(L) - cfg["local_tokens"]
+        for b in range(-(-cfg["init_tokens"] // 128), max(W, 0) // 128):
+            if bt[r, b] >= 0:
+                to_host[bt[r, b]] = True
+    dev_ids, host_ids = np.nonzero(~to_host)[0], np.nonzero(to_host)[0]
+    new_id = np.empty(c.num_pages, np.int64)
+    new_id[dev_ids] = np.arange(len(dev_ids))
+    new_id[host_ids] = len(dev_ids) + np.arange(len(host_ids))
+    for ly in layers:
+        ly.to_host(dev_ids, host_ids, new_id)
+    ok = bt >= 0
+    bt[ok] = new_id[bt[ok]]
+    c.block_table.copy_(torch.from_numpy(bt))
+
+
+def c2c_copy_peak(dev, nbytes: int = 1 << 30, reps: int = 5) -> float:
+    """GB/s of a pinned host to device copy (the copy engines over NVLink-C2C)."""
+    h = torch.empty(nbytes, dtype=torch.uint8).pin_memory()
+    d = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+    d.copy_(h, non_blocking=True)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(reps):
+        d.copy_(h, non_blocking=True)
+    e1.record()
+    torch.cuda.synchronize()
+    return round(reps * nbytes / (e0.elapsed_time(e1) / 1e3) / 1e9, 1)
 
 
 def time_append(dev, cfg, n: int = 200) -> dict:
@@ -454,9 +543,7 @@ def run_e2e(layers, K, world, dev) -> dict:
         c.q.copy_(hb["q"], non_blocking=True)
         c.seq_lens.copy_(hb["L"], non_blocking=True)
         c.prompt_lens.copy_(hb["P"], non_blocking=True)
-        srkv.retrieval_decode(c.cfg, c.q, c.k_cache, c.v_cache, b.reps, c.block_table,
-                              c.seq_lens, c.prompt_lens, b.sel, b.nsel, b.out, b.workspace,
-                              b.error_flags)
+        ly.step()
         hb["out"].copy_(b.out, non_blocking=True)
         torch.cuda.current_stream().synchronize()
 

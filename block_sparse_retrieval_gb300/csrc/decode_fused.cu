@@ -146,7 +146,7 @@ __global__ void __maxnreg__(128) fused_decode_kernel(const DecodeArgs a,
         PageTask task;
         task.page = -1;
         task.lo = task.hi = task.ie = task.ws = 0;
-        if (lane < cnt) task = resolve_a(g, j0 + lane, bt_r, a.num_pages, eflags);
+        if (lane < cnt) task = resolve_a(g, j0 + lane, bt_r, total_pages(a), eflags);
         if (j0 == a0 && !mbar_wait(scored, 0)) {
           eflags |= SRKV_EFLAG_TIMEOUT;
           abort = true;
@@ -158,51 +158,59 @@ __global__ void __maxnreg__(128) fused_decode_kernel(const DecodeArgs a,
           tl.hi = __shfl_sync(0xffffffffu, task.hi, l);
           tl.ie = __shfl_sync(0xffffffffu, task.ie, l);
           tl.ws = __shfl_sync(0xffffffffu, task.ws, l);
-          if (lane == 0)
-            issue_stage<D>(a, maps, smem, it, u, it == 0 ? kNewUnit : 0u, tl, armed, abort, eflags);
-          abort = __shfl_sync(0xffffffffu, abort, 0);
+          issue_stage_warp<D>(a, maps, smem, it, u, it == 0 ? kNewUnit : 0u, tl, armed, abort,
+                              eflags, lane);
           ++it;
         }
       }
-      if (lane == 0) {
-        // list B: kept blocks from the leader's pool until it is empty; the next entry is
-        // taken before waiting for a free stage, so its two cluster round trips overlap that
-        // wait
-        if (k > 0 && !abort && !mbar_wait_cluster(list_ready, 0)) {
+      // list B: kept blocks from the leader's pool until it is empty.  Lane 0 takes the entries
+      // (a cluster atomic, then a cluster load) one ahead: the next entry is taken before the
+      // current one waits for a free stage, and read by the other lanes only after that wait.
+      if (k > 0 && !abort) {
+        bool ok = true;
+        if (lane == 0) ok = mbar_wait_cluster(list_ready, 0);
+        if (!__shfl_sync(0xffffffffu, ok, 0)) {
           eflags |= SRKV_EFLAG_TIMEOUT;
           abort = true;
         }
-        auto take = [&](int2& e) -> bool {
-          const uint32_t i = atom_cluster_add(taken, 0, 1u);
-          if (i >= (uint32_t)k) return false;
-          e = ld_cluster_int2(pool + i, 0);
-          return true;
-        };
-        int2 e = make_int2(-1, 0);
-        bool have = k > 0 && !abort && take(e);
-        while (have && !abort) {
-          int2 next = make_int2(-1, 0);
-          const bool more = take(next);
-          PageTask t;
-          t.page = -1;
-          t.lo = t.hi = t.ie = t.ws = 0;
-          const int32_t base = e.y * kBlock, rows = min(kBlock, g.L - base);
-          const int32_t lo = max(a.init_tokens - base, 0), hi = min(g.W - base, rows);
-          if (lo < hi && e.x >= 0 && (int64_t)e.x < a.num_pages) {
-            t.page = e.x;
-            t.block = e.y;
-            t.lo = lo;
-            t.hi = hi;
-            t.ie = hi;  // every loaded row is attended
-            t.ws = hi;
-          } else if (lo < hi) {
-            eflags |= SRKV_EFLAG_PAGE_RANGE;
-          }
-          issue_stage<D>(a, maps, smem, it, u, it == 0 ? kNewUnit : 0u, t, armed, abort, eflags);
-          ++it;
-          e = next;
-          have = more;
+      }
+      auto take = [&](int2& e) -> bool {  // lane 0
+        const uint32_t i = atom_cluster_add(taken, 0, 1u);
+        if (i >= (uint32_t)k) return false;
+        e = ld_cluster_int2(pool + i, 0);
+        return true;
+      };
+      int2 e0 = make_int2(-1, 0);  // lane 0's entry
+      bool have = false;
+      if (k > 0 && !abort && lane == 0) have = take(e0);
+      have = __shfl_sync(0xffffffffu, have, 0);
+      while (have && !abort) {
+        const int2 e = make_int2(__shfl_sync(0xffffffffu, e0.x, 0), __shfl_sync(0xffffffffu, e0.y, 0));
+        int2 next0 = make_int2(-1, 0);
+        bool more = false;
+        if (lane == 0) more = take(next0);
+        PageTask t;
+        t.page = -1;
+        t.lo = t.hi = t.ie = t.ws = 0;
+        const int32_t base = e.y * kBlock, rows = min(kBlock, g.L - base);
+        const int32_t lo = max(a.init_tokens - base, 0), hi = min(g.W - base, rows);
+        if (lo < hi && e.x >= 0 && (int64_t)e.x < total_pages(a)) {
+          t.page = e.x;
+          t.block = e.y;
+          t.lo = lo;
+          t.hi = hi;
+          t.ie = hi;  // every loaded row is attended
+          t.ws = hi;
+        } else if (lo < hi) {
+          eflags |= SRKV_EFLAG_PAGE_RANGE;
         }
+        issue_stage_warp<D>(a, maps, smem, it, u, it == 0 ? kNewUnit : 0u, t, armed, abort,
+                            eflags, lane);
+        ++it;
+        e0 = next0;
+        have = __shfl_sync(0xffffffffu, more, 0);
+      }
+      if (lane == 0) {
         // the sentinel closes the segment (empty if this CTA took no page)
         PageTask none;
         none.page = -1;
@@ -242,7 +250,7 @@ __global__ void __maxnreg__(128) fused_decode_kernel(const DecodeArgs a,
     // delay the vector loads, and with them the selection everything waits for)
     bool waited = false;
     uint32_t eflags = score_share<D, kConsumerWarps>(
-        qbar, share, s_lo, s_hi, a.reps, a.num_pages, a.Hkv, h, keys, &hist[0][0], pages, warp,
+        qbar, share, s_lo, s_hi, a.reps, total_pages(a), a.Hkv, h, keys, &hist[0][0], pages, warp,
         lane,
         [&] {
           cluster_wait();

@@ -164,6 +164,18 @@ __device__ __forceinline__ void issue_stage(const DecodeArgs& a, const TmaMaps& 
   // is still arriving.
   const bool rows = load && t.hi > t.lo;
   const uint32_t qbytes = (uint32_t)(a.G * D * 2);
+  if (rows && t.page >= a.num_pages) {
+    // A page of the host pool: the producer warp copies its slabs and then arrives
+    // (issue_stage_warp); here only the query's bytes are announced and requested.
+    if (fl & kNewUnit) {
+      const int32_t h = u % a.Hkv, r = u / a.Hkv;
+      mbar_expect_tx(&full[s], qbytes);
+      bulk_load(smem + C::kOffQ + (size_t)s * C::kQBytes,
+                static_cast<const __nv_bfloat16*>(a.q) + ((int64_t)r * a.Hq + (int64_t)h * a.G) * D,
+                qbytes, &full[s]);
+    }
+    return;
+  }
   mbar_arrive_expect_tx(&full[s], (rows ? (uint32_t)C::kSlab : 0u) +
                                       ((fl & kNewUnit) ? qbytes : 0u));
   mbar_arrive_expect_tx(&full_v[s], rows ? (uint32_t)C::kSlab : 0u);
@@ -186,6 +198,47 @@ __device__ __forceinline__ void issue_stage(const DecodeArgs& a, const TmaMaps& 
     for (int b = 0; b < C::kBoxes; ++b)
       tma_load_3d(smem + C::kOffV + (size_t)s * C::kSlab + (size_t)b * C::kBoxBytes, &maps.v,
                   64 * b, h * kBlock, t.page, &full_v[s], once);
+  }
+}
+
+// issue_stage for the whole producer warp (every lane calls it with the same arguments).  A
+// page of the host pool is copied by all 32 lanes, 16 bytes per cp.async, into the layout the
+// tensor-map copies produce (128-byte swizzle), so the consumers read both kinds of stage
+// alike: over NVLink-C2C the host pool is read in place, with no staging copy in HBM.  Each
+// lane ties its copies to the stage's barriers, then lane 0 arrives.
+template <int D>
+__device__ __forceinline__ void issue_stage_warp(const DecodeArgs& a, const TmaMaps& maps,
+                                                 unsigned char* smem, int64_t it, int32_t u,
+                                                 uint32_t fl, const PageTask& t, int64_t& armed,
+                                                 bool& abort, uint32_t& eflags, int lane) {
+  using C = Cfg<D>;
+  const bool host = t.page >= 0 && t.hi > t.lo && t.page >= a.num_pages;  // uniform
+  if (lane == 0) issue_stage<D>(a, maps, smem, it, u, fl, t, armed, abort, eflags);
+  abort = __shfl_sync(0xffffffffu, abort, 0);
+  if (!host || abort) return;
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::kOffBar);
+  uint64_t* full_v = full + C::kStages;
+  const int s = (int)(it % C::kStages);
+  const int64_t slab = ((int64_t)(t.page - a.num_pages) * a.Hkv + u % a.Hkv) * kBlock * D;
+  const __nv_bfloat16* ks = static_cast<const __nv_bfloat16*>(a.k_host) + slab;
+  const __nv_bfloat16* vs = static_cast<const __nv_bfloat16*>(a.v_host) + slab;
+  const uint32_t k_dst = smem_u32(smem + C::kOffK + (size_t)s * C::kSlab);
+  const uint32_t v_dst = smem_u32(smem + C::kOffV + (size_t)s * C::kSlab);
+  constexpr int kPerRow = D / 8;  // 16-byte chunks per row
+  // lane i copies chunks i, i + 32, ...: consecutive lanes read consecutive 16 bytes
+#pragma unroll 8
+  for (int i = lane; i < kBlock * kPerRow; i += 32)
+    cp_async_16(k_dst + swz(i / kPerRow, i % kPerRow), ks + (int64_t)i * 8);
+  cp_async_mbar_arrive(&full[s]);
+#pragma unroll 8
+  for (int i = lane; i < kBlock * kPerRow; i += 32)
+    cp_async_16(v_dst + swz(i / kPerRow, i % kPerRow), vs + (int64_t)i * 8);
+  cp_async_mbar_arrive(&full_v[s]);
+  __syncwarp();  // every lane's pending-count increments precede the arrivals below
+  if (lane == 0) {
+    mbar_arrive(&full[s]);
+    mbar_arrive(&full_v[s]);
+    ++armed;
   }
 }
 

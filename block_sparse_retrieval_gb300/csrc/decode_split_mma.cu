@@ -106,8 +106,8 @@ __global__ void __maxnreg__(128) split_mma_kernel(const DecodeArgs a,
           // Early mode: the count the plan assumed must be the one the scoring wrote.
           const int32_t written = list == kListB && a.early ? a.nsel[my_u] : my_g.ns;
           task = list == kListA
-                     ? resolve_a(my_g, my_j, bt_r, a.num_pages, eflags)
-                     : resolve_b(my_g, my_j, a.sel + (int64_t)my_u * a.kmax, bt_r, a.num_pages,
+                     ? resolve_a(my_g, my_j, bt_r, total_pages(a), eflags)
+                     : resolve_b(my_g, my_j, a.sel + (int64_t)my_u * a.kmax, bt_r, total_pages(a),
                                  a.init_tokens, eflags);
           if (list == kListB && (my_j >= written || (my_j == 0 && written != my_g.ns))) {
             eflags |= SRKV_EFLAG_SELECTION;
@@ -123,8 +123,7 @@ __global__ void __maxnreg__(128) split_mma_kernel(const DecodeArgs a,
           t.hi = __shfl_sync(0xffffffffu, task.hi, l);
           t.ie = __shfl_sync(0xffffffffu, task.ie, l);
           t.ws = __shfl_sync(0xffffffffu, task.ws, l);
-          if (lane == 0) issue_stage<D>(a, maps, smem, it, u, fl, t, armed, abort, eflags);
-          abort = __shfl_sync(0xffffffffu, abort, 0);
+          issue_stage_warp<D>(a, maps, smem, it, u, fl, t, armed, abort, eflags, lane);
           ++it;
         }
       }

@@ -129,6 +129,9 @@ srkv_status prepare_decode(const srkv_config* cfg, const void* q, const void* k_
   a.reps = nullptr;
   a.sel_out = nullptr;
   a.nsel_out = nullptr;
+  a.k_host = nullptr;
+  a.v_host = nullptr;
+  a.num_host_pages = 0;
   a.dense_boundary = cfg->dense_boundary;
   a.topk_percent = cfg->topk_percent;
   return SRKV_OK;
@@ -161,6 +164,52 @@ srkv_status check_score(const srkv_config* cfg, const void* q, const float* reps
   if ((int64_t)batch * cfg->num_kv_heads > INT32_MAX) return SRKV_ERR_UNSUPPORTED;
   if ((size_t)max_blocks * 8 > 200 * 1024) return SRKV_ERR_UNSUPPORTED;  // keys + pages on chip
   return SRKV_OK;
+}
+
+// srkv_retrieval_decode over a device pool [0, num_pages) and a host pool
+// [num_pages, num_pages + num_host_pages) of page ids (num_host_pages = 0: no host pool).
+srkv_status retrieval_decode(const srkv_config* cfg, const void* q, const void* k_cache,
+                             const void* v_cache, int64_t num_pages, const void* k_host,
+                             const void* v_host, int64_t num_host_pages, const float* reps,
+                             const int32_t* block_table, int32_t max_blocks,
+                             const int32_t* seq_lens, const int32_t* prompt_lens, int32_t batch,
+                             int32_t* sel, int32_t kmax, int32_t* nsel, void* out,
+                             void* workspace, size_t workspace_bytes, int32_t* error_flags,
+                             cudaStream_t s) {
+  srkv_status st = check_score(cfg, q, reps, num_pages + num_host_pages, block_table, max_blocks,
+                               seq_lens, batch, sel, kmax, nsel);
+  if (st != SRKV_OK || batch == 0) return st;
+  DecodeArgs a;
+  st = prepare_decode(cfg, q, k_cache, v_cache, num_pages, block_table, max_blocks, seq_lens,
+                      batch, sel, kmax, nsel, out, workspace, workspace_bytes, error_flags, a);
+  if (st != SRKV_OK) return st;
+  a.k_host = k_host;
+  a.v_host = v_host;
+  a.num_host_pages = num_host_pages;
+  // The scoring kernel, then the decode, which streams list A while the scoring finishes
+  // and knows the selection counts it will write from the lengths.  A scoring CTA keeps its
+  // SM to itself, so list A goes to the decode CTAs that find an SM free at once (the grid
+  // is scheduled in block order), list B to those that start before the scoring ends (all
+  // but one SM per (request, kv head) cluster, whose leader selects last).
+  a.prompt_lens = prompt_lens;
+  a.reps = reps;
+  a.sel_out = sel;
+  a.nsel_out = nsel;
+  // A batch small enough for one cluster per unit to be resident: one kernel does it all.
+  const int32_t cluster = fused_cluster_size(*cfg, batch * cfg->num_kv_heads, max_blocks);
+  if (cluster > 0) return cuda_status(launch_fused(a, cluster, s));
+  const bool early = mma_split_supported(*cfg);
+  const int64_t scoring = score_topk_ctas(*cfg, max_blocks, batch);
+  const int64_t leaders = (int64_t)batch * cfg->num_kv_heads;
+  if (early && 2 * scoring <= a.ctas) {
+    a.ctas_a = a.ctas - (int32_t)scoring;
+    a.ctas_b = a.ctas - (int32_t)leaders;
+  }
+  if (launch_score_topk(*cfg, q, reps, num_pages + num_host_pages, block_table, max_blocks,
+                        seq_lens, prompt_lens, batch, sel, kmax, nsel, error_flags, s) !=
+      cudaSuccess)
+    return SRKV_ERR_CUDA;
+  return launch_decode(cfg, a, early ? 1 : 0, s);
 }
 
 }  // namespace
@@ -289,37 +338,47 @@ srkv_status srkv_retrieval_decode(const srkv_config* cfg, const void* q, const v
                                   int32_t batch, int32_t* sel, int32_t kmax, int32_t* nsel,
                                   void* out, void* workspace, size_t workspace_bytes,
                                   int32_t* error_flags, srkv_stream stream) {
-  srkv_status st = check_score(cfg, q, reps, num_pages, block_table, max_blocks, seq_lens, batch,
-                               sel, kmax, nsel);
-  if (st != SRKV_OK || batch == 0) return st;
-  DecodeArgs a;
-  st = prepare_decode(cfg, q, k_cache, v_cache, num_pages, block_table, max_blocks, seq_lens,
-                      batch, sel, kmax, nsel, out, workspace, workspace_bytes, error_flags, a);
-  if (st != SRKV_OK) return st;
-  // The scoring kernel, then the decode, which streams list A while the scoring finishes
-  // and knows the selection counts it will write from the lengths.  A scoring CTA keeps its
-  // SM to itself, so list A goes to the decode CTAs that find an SM free at once (the grid
-  // is scheduled in block order), list B to those that start before the scoring ends (all
-  // but one SM per (request, kv head) cluster, whose leader selects last).
-  a.prompt_lens = prompt_lens;
-  a.reps = reps;
-  a.sel_out = sel;
-  a.nsel_out = nsel;
-  cudaStream_t s = (cudaStream_t)stream;
-  // A batch small enough for one cluster per unit to be resident: one kernel does it all.
-  const int32_t cluster = fused_cluster_size(*cfg, batch * cfg->num_kv_heads, max_blocks);
-  if (cluster > 0) return cuda_status(launch_fused(a, cluster, s));
-  const bool early = mma_split_supported(*cfg);
-  const int64_t scoring = score_topk_ctas(*cfg, max_blocks, batch);
-  const int64_t leaders = (int64_t)batch * cfg->num_kv_heads;
-  if (early && 2 * scoring <= a.ctas) {
-    a.ctas_a = a.ctas - (int32_t)scoring;
-    a.ctas_b = a.ctas - (int32_t)leaders;
+  return retrieval_decode(cfg, q, k_cache, v_cache, num_pages, nullptr, nullptr, 0, reps,
+                          block_table, max_blocks, seq_lens, prompt_lens, batch, sel, kmax, nsel,
+                          out, workspace, workspace_bytes, error_flags, (cudaStream_t)stream);
+}
+
+srkv_status srkv_retrieval_decode_tiered(const srkv_config* cfg, const void* q,
+                                         const void* k_cache, const void* v_cache,
+                                         int64_t num_pages, const void* k_host,
+                                         const void* v_host, int64_t num_host_pages,
+                                         const float* reps, const int32_t* block_table,
+                                         int32_t max_blocks, const int32_t* seq_lens,
+                                         const int32_t* prompt_lens, int32_t batch, int32_t* sel,
+                                         int32_t kmax, int32_t* nsel, void* out, void* workspace,
+                                         size_t workspace_bytes, int32_t* error_flags,
+                                         srkv_stream stream) {
+  if (!cfg || num_host_pages < 0 || num_pages < 0 || num_pages > INT32_MAX - num_host_pages)
+    return SRKV_ERR_INVALID_ARG;
+  if (num_host_pages > 0) {
+    if (!config_ok(cfg)) return SRKV_ERR_INVALID_ARG;
+    if (!mma_split_supported(*cfg)) return SRKV_ERR_UNSUPPORTED;
+    if (!k_host || !v_host || !aligned(k_host, 16) || !aligned(v_host, 16))
+      return SRKV_ERR_INVALID_ARG;
+    // The pool must be reachable from the device: pinned (page-locked) or managed host
+    // memory, or device memory.  Pageable memory is refused.
+    const void* hp[2] = {k_host, v_host};
+    for (int i = 0; i < 2; ++i) {
+      cudaPointerAttributes at;
+      if (cudaPointerGetAttributes(&at, hp[i]) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return SRKV_ERR_INVALID_ARG;
+      }
+      if (at.type == cudaMemoryTypeUnregistered || !at.devicePointer) return SRKV_ERR_INVALID_ARG;
+      hp[i] = at.devicePointer;
+    }
+    k_host = hp[0];
+    v_host = hp[1];
   }
-  if (launch_score_topk(*cfg, q, reps, num_pages, block_table, max_blocks, seq_lens, prompt_lens,
-                        batch, sel, kmax, nsel, error_flags, s) != cudaSuccess)
-    return SRKV_ERR_CUDA;
-  return launch_decode(cfg, a, early ? 1 : 0, s);
+  return retrieval_decode(cfg, q, k_cache, v_cache, num_pages, k_host, v_host, num_host_pages,
+                          reps, block_table, max_blocks, seq_lens, prompt_lens, batch, sel, kmax,
+                          nsel, out, workspace, workspace_bytes, error_flags,
+                          (cudaStream_t)stream);
 }
 
 // Scratch of srkv_sparse_paged_decode_noalloc: one array per device that loads the library.

@@ -54,6 +54,24 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t by
                : "memory");
 }
 
+// Adds `bytes` to the transaction count the current phase waits for, without arriving.
+__device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.expect_tx.relaxed.cta.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)),
+               "r"(bytes)
+               : "memory");
+}
+
+// 16-byte copy global -> shared through L2 (an ordinary global load: the source may be
+// device memory or host memory mapped into the device's address space).
+__device__ __forceinline__ void cp_async_16(uint32_t dst_smem, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst_smem), "l"(src) : "memory");
+}
+// The mbarrier's current phase also waits for every cp.async this thread issued so far (the
+// pending count rises by one now and falls by one when they have landed).
+__device__ __forceinline__ void cp_async_mbar_arrive(uint64_t* bar) {
+  asm volatile("cp.async.mbarrier.arrive.shared::cta.b64 [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
 __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   uint32_t done;
   asm volatile(
@@ -353,7 +371,17 @@ struct DecodeArgs {
   const float* reps;  // the fused small-batch decode scores too, and writes the selection:
   int32_t* sel_out;
   int32_t* nsel_out;
+  // Offload tier: page ids [num_pages, num_pages + num_host_pages) name pages of a pool in
+  // host memory mapped into the device's address space (same [Hkv][128][d] page layout).
+  const void* k_host;
+  const void* v_host;
+  int64_t num_host_pages;
 };
+
+// Page ids a block table may hold: the device pool, then the host pool.
+__host__ __device__ __forceinline__ int64_t total_pages(const DecodeArgs& a) {
+  return a.num_pages + a.num_host_pages;
+}
 
 // CTAs that share the positions of a list.
 __host__ __device__ __forceinline__ int32_t list_ctas(const DecodeArgs& a, int list) {

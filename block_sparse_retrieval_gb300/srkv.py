@@ -28,7 +28,8 @@ EXPORTS = ("srkv_default_config", "srkv_status_string", "srkv_topk_count",
            "srkv_num_candidates", "srkv_kmax_bound", "srkv_build_block_reps",
            "srkv_score_topk", "srkv_decode_workspace_size", "srkv_sparse_paged_decode",
            "srkv_retrieval_decode", "srkv_sparse_paged_decode_noalloc",
-           "srkv_retrieval_decode_launches", "srkv_append_kv")
+           "srkv_retrieval_decode_launches", "srkv_append_kv",
+           "srkv_retrieval_decode_tiered")
 NOALLOC_WORKSPACE_BYTES = 16 << 20
 
 
@@ -86,8 +87,12 @@ def load() -> ctypes.CDLL:
     lib.srkv_sparse_paged_decode_noalloc.argtypes = [ctypes.POINTER(Config), _P, _P, _P, _I64,
                                                      _P, _I32, _P, _I32, _P, _I32, _P, _P, _P,
                                                      _P]
+    lib.srkv_retrieval_decode_tiered.argtypes = [ctypes.POINTER(Config), _P, _P, _P, _I64, _P,
+                                                 _P, _I64, _P, _P, _I32, _P, _P, _I32, _P, _I32,
+                                                 _P, _P, _P, _SZ, _P, _P]
     for name in ("srkv_build_block_reps", "srkv_score_topk", "srkv_sparse_paged_decode",
-                 "srkv_retrieval_decode", "srkv_sparse_paged_decode_noalloc"):
+                 "srkv_retrieval_decode", "srkv_sparse_paged_decode_noalloc",
+                 "srkv_retrieval_decode_tiered"):
         getattr(lib, name).restype = ctypes.c_int
     _lib = lib
     return lib
@@ -242,6 +247,44 @@ def retrieval_decode(cfg: Mapping, q: torch.Tensor, k_cache: torch.Tensor,
         _dev(out, "out", dt), _dev(workspace, "workspace"),
         workspace.numel() * workspace.element_size(),
         _dev(error_flags, "error_flags", torch.int32), _stream(stream)), "srkv_retrieval_decode")
+
+
+def _host(t: torch.Tensor | None, name: str, dtype: torch.dtype):
+    if t is None:
+        return None
+    if t.is_cuda or not t.is_pinned():
+        raise ValueError(f"{name} must be a pinned host tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def retrieval_decode_tiered(cfg: Mapping, q: torch.Tensor, k_cache: torch.Tensor,
+                            v_cache: torch.Tensor, k_host: torch.Tensor | None,
+                            v_host: torch.Tensor | None, reps: torch.Tensor,
+                            block_table: torch.Tensor, seq_lens: torch.Tensor,
+                            prompt_lens: torch.Tensor | None, sel: torch.Tensor,
+                            nsel: torch.Tensor, out: torch.Tensor, workspace: torch.Tensor,
+                            error_flags: torch.Tensor | None = None, stream=None) -> None:
+    """srkv_retrieval_decode_tiered: page ids >= k_cache.shape[0] name pages of the pinned
+    host pool k_host / v_host (page id - k_cache.shape[0])."""
+    c = config(cfg)
+    dt = _store_dtype(cfg)
+    B, max_blocks = block_table.shape
+    n_host = 0 if k_host is None else k_host.shape[0]
+    _check(load().srkv_retrieval_decode_tiered(
+        ctypes.byref(c), _dev(q, "q", dt), _dev(k_cache, "k_cache", dt),
+        _dev(v_cache, "v_cache", dt), k_cache.shape[0], _host(k_host, "k_host", dt),
+        _host(v_host, "v_host", dt), n_host, _dev(reps, "reps", torch.float32),
+        _dev(block_table, "block_table", torch.int32), max_blocks,
+        _dev(seq_lens, "seq_lens", torch.int32), _dev(prompt_lens, "prompt_lens", torch.int32),
+        B, _dev(sel, "sel", torch.int32), sel.shape[-1], _dev(nsel, "nsel", torch.int32),
+        _dev(out, "out", dt), _dev(workspace, "workspace"),
+        workspace.numel() * workspace.element_size(),
+        _dev(error_flags, "error_flags", torch.int32), _stream(stream)),
+        "srkv_retrieval_decode_tiered")
 
 
 def sparse_paged_decode_noalloc(cfg: Mapping, q: torch.Tensor, k_cache: torch.Tensor,

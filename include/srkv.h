@@ -210,6 +210,38 @@ srkv_status srkv_retrieval_decode(const srkv_config* cfg, const void* q, const v
                                   int32_t* error_flags, srkv_stream stream);
 
 /*
+ * srkv_retrieval_decode with an offload tier (openGauss page, "Overall Solution" and
+ * "Feature Description": KV blocks past the offload boundary live off the accelerator's
+ * memory, their representation vectors stay resident, and only the topK blocks the query
+ * selects are fetched each step).  Page ids in [0, num_pages) name pages of the device pool
+ * k_cache/v_cache; ids in [num_pages, num_pages + num_host_pages) name page
+ * (id - num_pages) of a second pool k_host/v_host with the same [page][Hkv][S][d] layout.
+ * The decode reads host pages in place, over the chip-to-chip link, straight into the shared
+ * memory stages the device pages go through (no staging copy in HBM); which pages live where
+ * is the caller's choice (typically the candidate blocks go to the host pool and the initial
+ * and window pages stay on the device).  Results equal srkv_retrieval_decode's on the same
+ * page contents.
+ *   k_host, v_host: pinned (page-locked, e.g. cudaHostAlloc) or managed host memory, or
+ *     device memory; 16-byte aligned; pageable memory is rejected (SRKV_ERR_INVALID_ARG).
+ *     May be NULL when num_host_pages = 0 (the call is then srkv_retrieval_decode).
+ *   reps: [num_pages + num_host_pages][Hkv][d] fp32 in device memory (computed while the
+ *     pages were on the device, e.g. by srkv_build_block_reps before they are moved).
+ *   A host pool needs the tensor-core decode (bf16, d 64 or 128, group <= 8), else
+ *     SRKV_ERR_UNSUPPORTED.  Other arguments, ownership and errors: srkv_retrieval_decode.
+ *     The host pool must not be written while the call runs.
+ */
+srkv_status srkv_retrieval_decode_tiered(const srkv_config* cfg, const void* q,
+                                         const void* k_cache, const void* v_cache,
+                                         int64_t num_pages, const void* k_host,
+                                         const void* v_host, int64_t num_host_pages,
+                                         const float* reps, const int32_t* block_table,
+                                         int32_t max_blocks, const int32_t* seq_lens,
+                                         const int32_t* prompt_lens, int32_t batch, int32_t* sel,
+                                         int32_t kmax, int32_t* nsel, void* out, void* workspace,
+                                         size_t workspace_bytes, int32_t* error_flags,
+                                         srkv_stream stream);
+
+/*
  * Number of kernels one srkv_retrieval_decode call with these arguments launches on the
  * current device (1 for the one-kernel small-batch path, else 3); 0 if cfg is invalid.
  * Host only; queries the device like the first call does.
