@@ -11,7 +11,8 @@ and the readings taken where they are silent.
 
 Inputs follow the layouts of the method on the pages:
   q            [B][Hq][d]            bf16 (as uint16 bit patterns) or float32
-  k/v caches   [P][Hkv][S][d]        same dtype as q
+  k/v caches   [P][Hkv][S][d]        same dtype as q, or (dtype 2) E4M3 codes (uint8) with
+                                     fp32 scales [P][Hkv][S] per row, q then bf16
   block_table  [B][max_blocks] int32 logical block -> physical page
   seq_lens     [B] int32             tokens in the cache (current token included)
   prompt_lens  [B] int32             prefill length, compared with DENSE_BOUNDARY
@@ -51,7 +52,8 @@ class _Inputs(ctypes.Structure):
                 ("v_cache", ctypes.c_void_p), ("num_pages", ctypes.c_int64),
                 ("block_table", ctypes.c_void_p), ("max_blocks", ctypes.c_int32),
                 ("seq_lens", ctypes.c_void_p), ("prompt_lens", ctypes.c_void_p),
-                ("batch", ctypes.c_int32)]
+                ("batch", ctypes.c_int32), ("k_scale", ctypes.c_void_p),
+                ("v_scale", ctypes.c_void_p)]
 
 
 def build(force: bool = False) -> str:
@@ -82,6 +84,11 @@ def load() -> ctypes.CDLL:
         lib.oracle_num_candidates.argtypes = [ctypes.c_int64, ctypes.c_int32,
                                               ctypes.c_int32, ctypes.c_int32]
         lib.oracle_block_reps.restype = ctypes.c_int
+        lib.oracle_e4m3_value.restype = ctypes.c_double
+        lib.oracle_e4m3_value.argtypes = [ctypes.c_uint32]
+        lib.oracle_e4m3_code.restype = ctypes.c_uint32
+        lib.oracle_e4m3_code.argtypes = [ctypes.c_double]
+        lib.oracle_quantize_e4m3.restype = ctypes.c_int
         lib.oracle_unit.restype = ctypes.c_int
         lib.oracle_decode_units.restype = ctypes.c_int
         _lib = lib
@@ -102,9 +109,10 @@ def _ptr(a: np.ndarray | None) -> ctypes.c_void_p | None:
 
 
 def _values(a, dtype: int) -> np.ndarray:
-    """bf16 inputs travel as uint16 bit patterns, fp32 as float32 (C order)."""
+    """bf16 inputs travel as uint16 bit patterns, fp32 as float32, E4M3 codes as uint8
+    (C order)."""
     a = np.ascontiguousarray(a)
-    want = np.uint16 if dtype == 0 else np.float32
+    want = {0: np.uint16, 1: np.float32, 2: np.uint8}[dtype]
     if a.dtype != want:
         raise TypeError(f"oracle expects {np.dtype(want).name} for dtype {dtype}, got {a.dtype}")
     return a
@@ -145,28 +153,39 @@ def block_reps(cfg: Mapping, k_cache, page_ids, valid) -> np.ndarray:
 
 # ---- decode ----------------------------------------------------------------------------------
 
-def _inputs(cfg, q, k_cache, v_cache, block_table, seq_lens, prompt_lens):
+def _inputs(cfg, q, k_cache, v_cache, block_table, seq_lens, prompt_lens, k_scale=None,
+            v_scale=None):
     dt = cfg["dtype"]
-    arrs = dict(q=_values(q, dt), k=_values(k_cache, dt), v=_values(v_cache, dt),
-                bt=_i32(block_table), L=_i32(seq_lens),
+    arrs = dict(q=_values(q, 0 if dt == 2 else dt), k=_values(k_cache, dt),
+                v=_values(v_cache, dt), bt=_i32(block_table), L=_i32(seq_lens),
                 prompt=_i32(seq_lens if prompt_lens is None else prompt_lens))
+    if dt == 2:
+        shape = arrs["k"].shape[:-1]
+        arrs["ks"] = np.ascontiguousarray(k_scale, dtype=np.float32)
+        arrs["vs"] = np.ascontiguousarray(v_scale, dtype=np.float32)
+        if arrs["ks"].shape != shape or arrs["vs"].shape != shape:
+            raise ValueError(f"scales must be {shape}")
     B, max_blocks = arrs["bt"].shape
     ins = _Inputs(_ptr(arrs["q"]), _ptr(arrs["k"]), _ptr(arrs["v"]), arrs["k"].shape[0],
-                  _ptr(arrs["bt"]), max_blocks, _ptr(arrs["L"]), _ptr(arrs["prompt"]), B)
+                  _ptr(arrs["bt"]), max_blocks, _ptr(arrs["L"]), _ptr(arrs["prompt"]), B,
+                  _ptr(arrs.get("ks")), _ptr(arrs.get("vs")))
     return ins, arrs
 
 
 def decode(cfg: Mapping, q, k_cache, v_cache, block_table, seq_lens, prompt_lens=None, *,
            units: Sequence[tuple[int, int]] | None = None, sel=None, nsel=None,
-           kmax: int | None = None, threads: int = 1) -> dict:
+           kmax: int | None = None, threads: int = 1, k_scale=None, v_scale=None) -> dict:
     """Decode the listed (request, kv head) units (default: all).
 
     Returns ``out`` [B][Hq][d] fp64, ``sel`` [B][Hkv][kmax] int32 (ascending block ids,
     -1 padded), ``nsel`` [B][Hkv], ``scores`` [B][Hkv][max_blocks] fp64 (NaN where the
     block is not a candidate).  Rows of units not listed stay zero / -1 / NaN.
-    ``sel``/``nsel`` given as inputs replace the oracle's own selection.
+    ``sel``/``nsel`` given as inputs replace the oracle's own selection.  With
+    ``cfg["dtype"] == 2`` the caches are E4M3 codes with per-row scales ``k_scale`` /
+    ``v_scale`` [P][Hkv][S] (R10); pass the selection of the full-precision cache (R11).
     """
-    ins, arrs = _inputs(cfg, q, k_cache, v_cache, block_table, seq_lens, prompt_lens)
+    ins, arrs = _inputs(cfg, q, k_cache, v_cache, block_table, seq_lens, prompt_lens,
+                        k_scale, v_scale)
     B, max_blocks = arrs["bt"].shape
     Hq, Hkv, d = cfg["num_q_heads"], cfg["num_kv_heads"], cfg["head_dim"]
     if units is None:
@@ -190,6 +209,39 @@ def decode(cfg: Mapping, q, k_cache, v_cache, block_table, seq_lens, prompt_lens
         _ptr(sel_in), _ptr(nsel_in), _ptr(sel_out), _ptr(nsel_out), ctypes.c_int32(kmax),
         _ptr(scores), _ptr(out), ctypes.c_int32(threads)))
     return dict(out=out, sel=sel_out, nsel=nsel_out, scores=scores)
+
+
+# ---- E4M3 compressed pages ---------------------------------------------------------------------
+
+def e4m3_value(codes) -> np.ndarray:
+    """fp64 value of each E4M3 code (NaN for S.1111.111)."""
+    c = np.ascontiguousarray(np.asarray(codes, dtype=np.uint8))
+    out = np.empty(c.shape, np.float64)
+    load().oracle_e4m3_values(_ptr(c), ctypes.c_int64(c.size), _ptr(out))
+    return out
+
+
+def e4m3_code(x) -> np.ndarray:
+    """R10: nearest E4M3 code of each value (ties to even, saturating at +-448)."""
+    a = np.ascontiguousarray(np.asarray(x, dtype=np.float64))
+    out = np.empty(a.shape, np.uint8)
+    load().oracle_e4m3_codes(_ptr(a), ctypes.c_int64(a.size), _ptr(out))
+    return out
+
+
+def quantize_e4m3(cfg: Mapping, cache, page_ids=None) -> tuple[np.ndarray, np.ndarray]:
+    """R10 on the listed pages (default: all) of a bf16 cache [P][Hkv][S][d] (uint16 bit
+    patterns): (codes [n][Hkv][S][d] uint8, scales [n][Hkv][S] float32)."""
+    x = _values(cache, 0)
+    ids = _i32(np.arange(x.shape[0]) if page_ids is None else page_ids)
+    n = ids.shape[0]
+    codes = np.zeros((n,) + x.shape[1:], np.uint8)
+    scales = np.zeros((n,) + x.shape[1:3], np.float32)
+    c = _cfg(dict(cfg, dtype=0))
+    _check(load().oracle_quantize_e4m3(ctypes.byref(c), _ptr(x), ctypes.c_int64(x.shape[0]),
+                                       _ptr(ids), ctypes.c_int64(n), _ptr(codes),
+                                       _ptr(scales)))
+    return codes, scales
 
 
 def unit_weights(cfg: Mapping, q, k_cache, v_cache, block_table, seq_lens, prompt_lens,

@@ -37,6 +37,17 @@
  *  R9 the cache already holds the current token at position L - 1; softmax scale
  *     is 1/sqrt(d); no causal mask is needed at decode; L = 0 gives a zero output.
  *
+ * Compressed pages ([KVS] lists KV quantisation among the ways to shrink the cache; the
+ * format is the 8-bit floating point "E4M3" of the OCP 8-bit floating point specification,
+ * OFP8): with dtype 2 the K and V caches hold one E4M3 code per value and a fp32 scale per
+ * (page, kv head, token) row; a value is code x scale.  The query stays bf16.
+ *  R10 quantisation of a row x[0..d): scale = max_e |x_e| / 448 in fp32 (1 for an all-zero
+ *      row), code_e = E4M3(x_e / scale) with the quotient rounded to fp32 first, then to
+ *      the nearest E4M3 value, ties to the even code, finite values past 448 to +-448.
+ *  R11 with compressed pages the selection is computed from the representation vectors of
+ *      the full-precision keys (they are extracted at prefill, before the pages are
+ *      compressed); the attended values are the compressed ones.
+ *
  * Arithmetic is fp64 throughout, from the exact input values (bf16 inputs are
  * widened exactly).  The build uses -ffp-contract=off so that the integer
  * decision in R5 is taken with separately rounded multiply and subtract on every
@@ -57,7 +68,7 @@ typedef struct {
   int32_t local_tokens;  /* LOCAL (sliding window) */
   double topk_percent;   /* p in [0, 1] */
   int32_t dense_boundary;
-  int32_t dtype;         /* 0: bf16 bit patterns (uint16), 1: fp32 */
+  int32_t dtype;         /* 0: bf16 bit patterns (uint16), 1: fp32, 2: E4M3 K/V (bf16 q) */
 } oracle_cfg;
 
 typedef struct {
@@ -70,6 +81,8 @@ typedef struct {
   const int32_t* seq_lens;     /* [B] L: tokens in the cache, current token included */
   const int32_t* prompt_lens;  /* [B] prefill length, compared with DENSE_BOUNDARY */
   int32_t batch;
+  const float* k_scale;        /* dtype 2: [P][Hkv][S] scale of each K row */
+  const float* v_scale;        /* dtype 2: [P][Hkv][S] scale of each V row */
 } oracle_inputs;
 
 enum { ORACLE_OK = 0, ORACLE_BAD_ARG = -1, ORACLE_BAD_PAGE = -2, ORACLE_NO_MEM = -3,
@@ -84,6 +97,81 @@ static double value_at(const void* base, int32_t dtype, int64_t i) {
   memcpy(&f, &bits, sizeof f);
   return (double)f;
 }
+
+/* ---- E4M3 (OCP OFP8): 1 sign bit, 4 exponent bits (bias 7), 3 mantissa bits -------------
+ * Exponent field 0 holds subnormals m/8 x 2^-6; fields 1..15 hold (1 + m/8) x 2^(e-7),
+ * except S.1111.111, which is NaN; there are no infinities, the largest finite value is
+ * 1.75 x 2^8 = 448. */
+double oracle_e4m3_value(uint32_t code) {
+  code &= 0xffu;
+  const int s = (int)(code >> 7), e = (int)((code >> 3) & 15u), m = (int)(code & 7u);
+  if (e == 15 && m == 7) return NAN;
+  const double mag = e == 0 ? ldexp((double)m / 8.0, -6) : ldexp(1.0 + (double)m / 8.0, e - 7);
+  return s ? -mag : mag;
+}
+
+/* R10: the code of the nearest E4M3 value to x (searched over every finite magnitude),
+ * ties to the even code; |x| >= 448 gives +-448; NaN gives 0x7f. */
+uint32_t oracle_e4m3_code(double x) {
+  if (isnan(x)) return 0x7fu;
+  const uint32_t sign = signbit(x) ? 0x80u : 0u;
+  const double a = fabs(x);
+  if (a >= 448.0) return sign | 0x7eu;
+  uint32_t best = 0;
+  double bd = INFINITY;
+  for (uint32_t code = 0; code <= 0x7eu; ++code) {
+    const double dist = fabs(oracle_e4m3_value(code) - a);
+    if (dist < bd || (dist == bd && (code & 1u) == 0)) {
+      bd = dist;
+      best = code;
+    }
+  }
+  return sign | best;
+}
+
+void oracle_e4m3_values(const uint8_t* codes, int64_t n, double* out) {
+  for (int64_t i = 0; i < n; ++i) out[i] = oracle_e4m3_value(codes[i]);
+}
+
+void oracle_e4m3_codes(const double* x, int64_t n, uint8_t* out) {
+  for (int64_t i = 0; i < n; ++i) out[i] = (uint8_t)oracle_e4m3_code(x[i]);
+}
+
+/* R10 for the listed pages of a bf16 cache: codes [n][Hkv][S][d], scales [n][Hkv][S]. */
+int oracle_quantize_e4m3(const oracle_cfg* c, const uint16_t* cache, int64_t num_pages,
+                         const int32_t* page_ids, int64_t n, uint8_t* codes, float* scales) {
+  const int64_t Hkv = c->num_kv_heads, S = c->block_size, d = c->head_dim;
+  for (int64_t i = 0; i < n; ++i) {
+    const int64_t page = page_ids[i];
+    if (page < 0 || page >= num_pages) return ORACLE_BAD_PAGE;
+    for (int64_t row = 0; row < Hkv * S; ++row) {
+      const uint16_t* x = cache + (page * Hkv * S + row) * d;
+      float amax = 0.0f;
+      for (int64_t e = 0; e < d; ++e) {
+        const float v = fabsf((float)value_at(x, 0, e));
+        if (v > amax) amax = v;
+      }
+      const float scale = amax > 0.0f ? amax / 448.0f : 1.0f;
+      scales[i * Hkv * S + row] = scale;
+      for (int64_t e = 0; e < d; ++e) {
+        const float y = (float)value_at(x, 0, e) / scale;  /* fp32 quotient */
+        codes[(i * Hkv * S + row) * d + e] = (uint8_t)oracle_e4m3_code((double)y);
+      }
+    }
+  }
+  return ORACLE_OK;
+}
+
+/* K (which = 0) or V (1) value i of the cache, decoded for the configured dtype. */
+static double kv_value(const oracle_cfg* c, const oracle_inputs* in, int which, int64_t i) {
+  const void* base = which ? in->v_cache : in->k_cache;
+  if (c->dtype != 2) return value_at(base, c->dtype, i);
+  const float* sc = which ? in->v_scale : in->k_scale;
+  return oracle_e4m3_value(((const uint8_t*)base)[i]) * (double)sc[i / c->head_dim];
+}
+
+/* The query's dtype: bf16 when the pages are compressed. */
+static int32_t q_dtype(const oracle_cfg* c) { return c->dtype == 2 ? 0 : c->dtype; }
 
 /* ---- closed forms ---------------------------------------------------------------- */
 
@@ -130,6 +218,7 @@ int oracle_block_reps(const oracle_cfg* c, const void* k_cache, int64_t num_page
                       const int32_t* page_ids, const int32_t* valid, int64_t n,
                       double* reps_out) {
   const int64_t Hkv = c->num_kv_heads, S = c->block_size, d = c->head_dim;
+  if (c->dtype == 2) return ORACLE_BAD_ARG;  /* R11: vectors come from the full-precision keys */
   for (int64_t i = 0; i < n; ++i) {
     int64_t page = page_ids[i];
     int64_t v = valid[i];
@@ -195,6 +284,7 @@ int oracle_unit(const oracle_cfg* c, const oracle_inputs* in, int32_t r, int32_t
   if (Hkv <= 0 || Hq % Hkv != 0 || d <= 0 || S <= 0 || r < 0 || r >= in->batch || h < 0 ||
       h >= Hkv)
     return ORACLE_BAD_ARG;
+  if (c->dtype == 2 && (!in->k_scale || !in->v_scale)) return ORACLE_BAD_ARG;
   const int64_t G = Hq / Hkv;
   const int64_t L = in->seq_lens[r];
   const int64_t prompt = in->prompt_lens ? in->prompt_lens[r] : L;
@@ -218,7 +308,7 @@ int oracle_unit(const oracle_cfg* c, const oracle_inputs* in, int32_t r, int32_t
   /* R2: the group's summed query. */
   for (int64_t j = 0; j < G; ++j)
     for (int64_t e = 0; e < d; ++e)
-      qbar[e] += value_at(in->q, c->dtype, ((int64_t)r * Hq + h * G + j) * d + e);
+      qbar[e] += value_at(in->q, q_dtype(c), ((int64_t)r * Hq + h * G + j) * d + e);
 
   if (scores_out)
     for (int64_t b = 0; b < in->max_blocks; ++b) scores_out[b] = NAN;
@@ -237,7 +327,7 @@ int oracle_unit(const oracle_cfg* c, const oracle_inputs* in, int32_t r, int32_t
     for (int64_t e = 0; e < d; ++e) {
       double sum = 0.0;
       for (int64_t t = first; t < last; ++t)
-        sum += value_at(in->k_cache, c->dtype, ((page * Hkv + h) * S + (t - first)) * d + e);
+        sum += kv_value(c, in, 0, ((page * Hkv + h) * S + (t - first)) * d + e);
       rep[e] = sum / (double)(last - first);
     }
     double s = 0.0;
@@ -297,8 +387,8 @@ int oracle_unit(const oracle_cfg* c, const oracle_inputs* in, int32_t r, int32_t
       }
       double dot = 0.0;
       for (int64_t e = 0; e < d; ++e)
-        dot += value_at(in->q, c->dtype, ((int64_t)r * Hq + qh) * d + e) *
-               value_at(in->k_cache, c->dtype, ((page * Hkv + h) * S + t % S) * d + e);
+        dot += value_at(in->q, q_dtype(c), ((int64_t)r * Hq + qh) * d + e) *
+               kv_value(c, in, 0, ((page * Hkv + h) * S + t % S) * d + e);
       logits[t] = dot * scale;
       if (logits[t] > m) m = logits[t];
     }
@@ -309,7 +399,7 @@ int oracle_unit(const oracle_cfg* c, const oracle_inputs* in, int32_t r, int32_t
       double w = exp(logits[t] - m);
       denom += w;
       for (int64_t e = 0; e < d; ++e)
-        o[e] += w * value_at(in->v_cache, c->dtype, ((page * Hkv + h) * S + t % S) * d + e);
+        o[e] += w * kv_value(c, in, 1, ((page * Hkv + h) * S + t % S) * d + e);
     }
     if (denom > 0.0)
       for (int64_t e = 0; e < d; ++e) o[e] /= denom;

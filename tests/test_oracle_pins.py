@@ -400,3 +400,92 @@ def test_candidate_scores_match_enumeration():
                     assert abs(got - want) <= 1e-12 * (1 + abs(want)), (trial, b)
                 else:
                     assert math.isnan(got)
+
+
+# ---- E4M3 compressed pages (OCP 8-bit floating point, "E4M3") -----------------------------
+
+def test_e4m3_values_match_the_library_format():
+    """Every code's value against PyTorch's float8_e4m3fn, the same OCP format, and the
+    specification's landmarks."""
+    codes = np.arange(256, dtype=np.uint8)
+    got = oracle.e4m3_value(codes)
+    lib = torch.from_numpy(codes).view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    nan = (codes & 0x7F) == 0x7F
+    assert np.isnan(got[nan]).all() and np.isnan(lib[nan]).all()
+    np.testing.assert_array_equal(got[~nan], lib[~nan])
+    assert got[0x7E] == 448.0 and got[0xFE] == -448.0          # largest finite
+    assert got[0x08] == 2.0 ** -6 and got[0x07] == 7 / 8 * 2.0 ** -6  # normal / subnormal edge
+    assert got[0x01] == 2.0 ** -9 and got[0x38] == 1.0
+    assert math.copysign(1.0, got[0x80]) == -1.0 and got[0x80] == 0.0
+
+
+def test_e4m3_rounding_matches_the_library_and_ties_go_even():
+    rng = np.random.default_rng(3)
+    x = np.concatenate([rng.uniform(-448, 448, 4000), rng.normal(0, 1, 4000),
+                        rng.normal(0, 2.0 ** -7, 2000)]).astype(np.float32)
+    lib = torch.from_numpy(x).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    np.testing.assert_array_equal(oracle.e4m3_code(x.astype(np.float64)), lib)
+    # exact midpoints between neighbouring codes go to the even code
+    vals = oracle.e4m3_value(np.arange(0x7F, dtype=np.uint8))
+    mids = (vals[:-1] + vals[1:]) / 2
+    want = np.where(np.arange(0x7E) % 2 == 0, np.arange(0x7E), np.arange(1, 0x7F))
+    np.testing.assert_array_equal(oracle.e4m3_code(mids), want)
+    # saturation past the largest finite value, both signs
+    np.testing.assert_array_equal(oracle.e4m3_code([449.0, 1e9, -500.0]), [0x7E, 0x7E, 0xFE])
+
+
+def test_e4m3_quantiser_scale_and_error_bound():
+    """R10: the largest magnitude of a row lands on +-448, and every value comes back within
+    half a unit in the last place of its binade (relative 2^-4 for normals)."""
+    cfg = dict(num_q_heads=4, num_kv_heads=2, head_dim=64, block_size=128, init_tokens=0,
+               local_tokens=0, topk_percent=0.2, dense_boundary=0, dtype=0)
+    rng = np.random.default_rng(5)
+    x = (rng.normal(0, 1, (3, 2, 128, 64)) * rng.uniform(0.01, 50, (3, 2, 128, 1)))
+    x[1, 0, 7] = 0.0  # an all-zero row
+    bits = (torch.from_numpy(x.astype(np.float32)).to(torch.bfloat16).view(torch.int16)
+            .numpy().view(np.uint16))
+    codes, scales = oracle.quantize_e4m3(cfg, bits)
+    xs = widen(bits)
+    amax = np.abs(xs).max(-1)
+    np.testing.assert_array_equal(scales, np.where(amax > 0, (amax.astype(np.float32)
+                                                              / np.float32(448)), 1.0))
+    assert (scales[1, 0, 7] == 1.0) and (codes[1, 0, 7] == 0).all()
+    top = np.abs(xs).argmax(-1)
+    lead = np.take_along_axis(codes, top[..., None], -1)[..., 0]
+    assert np.all((lead & 0x7F)[amax > 0] == 0x7E)
+    deq = oracle.e4m3_value(codes) * scales[..., None]
+    y = np.abs(xs / scales[..., None])
+    ulp_half = np.where(y >= 2.0 ** -6, 2.0 ** (np.floor(np.log2(np.maximum(y, 2.0 ** -6))) - 4),
+                        2.0 ** -10)
+    assert np.all(np.abs(deq - xs) <= (ulp_half * 1.0001 + 1e-12) * scales[..., None])
+
+
+def test_e4m3_pages_decode_as_the_equivalent_bf16_cache():
+    """A compressed cache whose values code x scale are exact in bf16 (power-of-two
+    scales) decodes exactly like that bf16 cache given the same selection: pins the per-row
+    scale indexing and the reading of codes."""
+    case = synth.make_case(seq_lens=[1500, 900], num_q_heads=8, num_kv_heads=2, head_dim=64,
+                           init_tokens=256, local_tokens=384, topk_percent=0.3,
+                           dense_boundary=0, seed=21)
+    arr = synth.to_oracle_arrays(case)
+    cfg = case.cfg
+    rng = np.random.default_rng(9)
+    P, Hkv, S, d = arr["k_cache"].shape
+    kc = rng.integers(0, 256, (P, Hkv, S, d)).astype(np.uint8)
+    vc = rng.integers(0, 256, (P, Hkv, S, d)).astype(np.uint8)
+    kc[(kc & 0x7F) == 0x7F] = 0x38  # no NaN codes
+    vc[(vc & 0x7F) == 0x7F] = 0x38
+    ks = (2.0 ** rng.integers(-8, 3, (P, Hkv, S))).astype(np.float32)
+    vs = (2.0 ** rng.integers(-8, 3, (P, Hkv, S))).astype(np.float32)
+
+    def as_bf16(codes, scales):  # code x scale: 4 significant bits, exact in bf16
+        v = (oracle.e4m3_value(codes) * scales[..., None]).astype(np.float32)
+        return (v.view(np.uint32) >> 16).astype(np.uint16)
+
+    kb, vb = as_bf16(kc, ks), as_bf16(vc, vs)
+    ref = oracle.decode(cfg, arr["q"], kb, vb, arr["block_table"], arr["seq_lens"],
+                        arr["prompt_lens"])
+    got = oracle.decode(dict(cfg, dtype=2), arr["q"], kc, vc, arr["block_table"],
+                        arr["seq_lens"], arr["prompt_lens"], sel=ref["sel"], nsel=ref["nsel"],
+                        k_scale=ks, v_scale=vs)
+    np.testing.assert_array_equal(got["out"], ref["out"])
