@@ -34,9 +34,9 @@ constexpr int32_t kMaxCand = kFastRounds * kSelThreads;  // candidates per unit 
 constexpr int kMaxShare = 128;                             // candidates scored per CTA
 constexpr int kMaxCluster = 16;                            // CTAs per unit, at most
 
-template <int D>
+template <int D, bool F8 = false>
 struct FusedCfg {
-  using C = Cfg<D>;
+  using C = Cfg<D, F8>;
   // after the ring (every CTA)
   // keys_ready, list_ready, parts_ready
   static constexpr size_t kOffBars = (C::kSmem + 15) & ~size_t(15);
@@ -69,11 +69,11 @@ __device__ __forceinline__ int32_t share_begin(int32_t q, int32_t n, int32_t S) 
 }
 
 // Grid: one cluster of CS CTAs per unit; 8 consumer warps + 1 producer warp per CTA.
-template <int D>
+template <int D, bool F8>
 __global__ void __maxnreg__(128) fused_decode_kernel(const DecodeArgs a,
                                                      const __grid_constant__ TmaMaps maps) {
-  using C = Cfg<D>;
-  using F = FusedCfg<D>;
+  using C = Cfg<D, F8>;
+  using F = FusedCfg<D, F8>;
   extern __shared__ __align__(128) unsigned char smem_raw[];
   unsigned char* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   uint64_t* keys_ready = reinterpret_cast<uint64_t*>(smem + F::kOffBars);
@@ -99,7 +99,7 @@ __global__ void __maxnreg__(128) fused_decode_kernel(const DecodeArgs a,
   const bool leader = crank == 0;
 
   if (tid == 0) {
-    init_ring<D>(smem);
+    init_ring<D, F8>(smem);
     mbar_init(keys_ready, kMaxCand);            // one per candidate, the rest at once
     mbar_init(list_ready, 1);                   // the leader, once the pool is laid out
     mbar_init(parts_ready, 32u * (uint32_t)S);  // one per lane of a streaming CTA's warp 0
@@ -156,7 +156,7 @@ __global__ void __maxnreg__(128) fused_decode_kernel(const DecodeArgs a,
           tl.hi = __shfl_sync(0xffffffffu, task.hi, l);
           tl.ie = __shfl_sync(0xffffffffu, task.ie, l);
           tl.ws = __shfl_sync(0xffffffffu, task.ws, l);
-          issue_stage_warp<D>(a, maps, smem, it, u, it == 0 ? kNewUnit : 0u, tl, armed, abort,
+          issue_stage_warp<D, F8>(a, maps, smem, it, u, it == 0 ? kNewUnit : 0u, tl, armed, abort,
                               eflags, lane);
           ++it;
         }
@@ -202,7 +202,7 @@ __global__ void __maxnreg__(128) fused_decode_kernel(const DecodeArgs a,
         } else if (lo < hi) {
           eflags |= SRKV_EFLAG_PAGE_RANGE;
         }
-        issue_stage_warp<D>(a, maps, smem, it, u, it == 0 ? kNewUnit : 0u, t, armed, abort,
+        issue_stage_warp<D, F8>(a, maps, smem, it, u, it == 0 ? kNewUnit : 0u, t, armed, abort,
                             eflags, lane);
         ++it;
         e0 = next0;
@@ -213,7 +213,7 @@ __global__ void __maxnreg__(128) fused_decode_kernel(const DecodeArgs a,
         PageTask none;
         none.page = -1;
         none.lo = none.hi = none.ie = none.ws = 0;
-        issue_stage<D>(a, maps, smem, it, -1, kLast | kSegEnd, none, armed, abort, eflags);
+        issue_stage<D, F8>(a, maps, smem, it, -1, kLast | kSegEnd, none, armed, abort, eflags);
         uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::kOffBar);
         uint64_t* full_v = full + C::kStages;
         const int64_t first = armed > C::kStages ? armed - C::kStages : 0;
@@ -353,11 +353,11 @@ __global__ void __maxnreg__(128) fused_decode_kernel(const DecodeArgs a,
     } else {
       // 3'. attend list A, then the kept blocks taken from the pool, as one segment; the
       // merged partial goes to the leader's shared memory
-      consumer_loop<D>(a, smem, lane, warp,
+      consumer_loop<D, F8>(a, smem, lane, warp,
                        [&](const SoftmaxState<D>& st, const StageInfo&, Lane ln) {
                          float* acc_l = part_acc + (int64_t)q * a.G * D;
                          float* ml_l = part_ml + (int64_t)q * a.G * 2;
-                         store_partial<D>(static_cast<float*>(map_cluster_ptr(acc_l, 0)),
+                         store_partial<D, F8>(static_cast<float*>(map_cluster_ptr(acc_l, 0)),
                                           static_cast<float*>(map_cluster_ptr(ml_l, 0)), st, ln,
                                           a.G);
                        });
@@ -371,53 +371,55 @@ __global__ void __maxnreg__(128) fused_decode_kernel(const DecodeArgs a,
 
 }  // namespace
 
+// Clusters of `cs` CTAs of fused_decode_kernel<D, F8> that can be resident at once (0 on error).
+template <int D, bool F8>
+int32_t max_active_clusters(int32_t cs) {
+  using F = FusedCfg<D, F8>;
+  cudaLaunchConfig_t lc = {};
+  lc.gridDim = dim3((unsigned)cs);
+  lc.blockDim = dim3((kConsumerWarps + 1) * 32);
+  lc.dynamicSmemBytes = F::kSmemAlloc;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = (unsigned)cs;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  lc.attrs = attr;
+  lc.numAttrs = 1;
+  cudaFuncSetAttribute(fused_decode_kernel<D, F8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                       (int)F::kSmemAlloc);
+  cudaFuncSetAttribute(fused_decode_kernel<D, F8>, cudaFuncAttributeNonPortableClusterSizeAllowed,
+                       1);
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, fused_decode_kernel<D, F8>, &lc) != cudaSuccess) {
+    (void)cudaGetLastError();
+    n = 0;
+  }
+  return n;
+}
+
 // Cluster size for `units` units (0 = the fused path does not apply): the largest of 16,
-// 12, 8 CTAs per unit such that every cluster is resident at once.
-int32_t fused_cluster_size(const srkv_config& cfg, int32_t units, int32_t max_blocks) {
+// 12, 8 CTAs per unit such that every cluster is resident at once.  e4m3: compressed pages.
+int32_t fused_cluster_size(const srkv_config& cfg, int32_t units, int32_t max_blocks,
+                           bool e4m3) {
   if (!mma_split_supported(cfg) || units <= 0) return 0;
+  if (e4m3 && cfg.head_dim != 128) return 0;
   const int64_t W = (int64_t)max_blocks * kBlock - cfg.local_tokens;
   const int64_t nmax = W > cfg.init_tokens ? (W + kBlock - 1) / kBlock - cfg.init_tokens / kBlock : 0;
   if (nmax > kMaxCand) return 0;
-  static int32_t cached[128][2][3];  // [device][d 64 / 128][cluster 16, 12, 8]: max active + 1
+  // [device][d 64, d 128, d 128 compressed][cluster 16, 12, 8]: max active + 1
+  static int32_t cached[128][3][3];
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 128) return 0;
-  const int di = cfg.head_dim == 128 ? 1 : 0;
+  const int di = e4m3 ? 2 : cfg.head_dim == 128 ? 1 : 0;
   const int32_t sizes[3] = {16, 12, 8};
   for (int c = 0; c < 3; ++c) {
     const int32_t cs = sizes[c];
-    if (nmax > (int64_t)kMaxShare * cs) continue;                    // per-CTA scoring share
+    if (nmax > (int64_t)kMaxShare * cs) continue;  // per-CTA scoring share
     if (cached[dev][di][c] == 0) {
-      cudaLaunchConfig_t lc = {};
-      lc.gridDim = dim3((unsigned)cs);
-      lc.blockDim = dim3((kConsumerWarps + 1) * 32);
-      cudaLaunchAttribute attr[1];
-      attr[0].id = cudaLaunchAttributeClusterDimension;
-      attr[0].val.clusterDim.x = (unsigned)cs;
-      attr[0].val.clusterDim.y = 1;
-      attr[0].val.clusterDim.z = 1;
-      lc.attrs = attr;
-      lc.numAttrs = 1;
-      int n = 0;
-      cudaError_t e;
-      if (di) {
-        lc.dynamicSmemBytes = FusedCfg<128>::kSmemAlloc;
-        cudaFuncSetAttribute(fused_decode_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)FusedCfg<128>::kSmemAlloc);
-        cudaFuncSetAttribute(fused_decode_kernel<128>,
-                             cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
-        e = cudaOccupancyMaxActiveClusters(&n, fused_decode_kernel<128>, &lc);
-      } else {
-        lc.dynamicSmemBytes = FusedCfg<64>::kSmemAlloc;
-        cudaFuncSetAttribute(fused_decode_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)FusedCfg<64>::kSmemAlloc);
-        cudaFuncSetAttribute(fused_decode_kernel<64>,
-                             cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
-        e = cudaOccupancyMaxActiveClusters(&n, fused_decode_kernel<64>, &lc);
-      }
-      if (e != cudaSuccess) {
-        (void)cudaGetLastError();
-        n = 0;
-      }
+      const int32_t n = di == 2   ? max_active_clusters<128, true>(cs)
+                        : di == 1 ? max_active_clusters<128, false>(cs)
+                                  : max_active_clusters<64, false>(cs);
       cached[dev][di][c] = n + 1;
     }
     if (units <= cached[dev][di][c] - 1) return cs;
@@ -425,15 +427,17 @@ int32_t fused_cluster_size(const srkv_config& cfg, int32_t units, int32_t max_bl
   return 0;
 }
 
-cudaError_t launch_fused(const DecodeArgs& a, int32_t cluster, cudaStream_t stream) {
+template <int D, bool F8>
+cudaError_t launch_fused_t(const DecodeArgs& a, int32_t cluster, cudaStream_t stream) {
   TmaMaps maps;
-  if (!encode_cache_map(&maps.k, a.k_cache, a.num_pages, a.Hkv, a.d) ||
-      !encode_cache_map(&maps.v, a.v_cache, a.num_pages, a.Hkv, a.d))
+  if (!encode_cache_map(&maps.k, a.k_cache, a.num_pages, a.Hkv, D, F8) ||
+      !encode_cache_map(&maps.v, a.v_cache, a.num_pages, a.Hkv, D, F8))
     return cudaErrorInvalidValue;
   const int64_t grid = (int64_t)a.batch * a.Hkv * cluster;
   cudaLaunchConfig_t lc = {};
   lc.gridDim = dim3((unsigned)grid);
   lc.blockDim = dim3((kConsumerWarps + 1) * 32);
+  lc.dynamicSmemBytes = FusedCfg<D, F8>::kSmemAlloc;
   lc.stream = stream;
   cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -444,12 +448,13 @@ cudaError_t launch_fused(const DecodeArgs& a, int32_t cluster, cudaStream_t stre
   attr[1].val.programmaticStreamSerializationAllowed = 1;
   lc.attrs = attr;
   lc.numAttrs = 2;
-  if (a.d == 128) {
-    lc.dynamicSmemBytes = FusedCfg<128>::kSmemAlloc;
-    return cudaLaunchKernelEx(&lc, fused_decode_kernel<128>, a, maps);
-  }
-  lc.dynamicSmemBytes = FusedCfg<64>::kSmemAlloc;
-  return cudaLaunchKernelEx(&lc, fused_decode_kernel<64>, a, maps);
+  return cudaLaunchKernelEx(&lc, fused_decode_kernel<D, F8>, a, maps);
+}
+
+cudaError_t launch_fused(const DecodeArgs& a, int32_t cluster, cudaStream_t stream) {
+  if (a.k_scale) return launch_fused_t<128, true>(a, cluster, stream);  // compressed pages
+  return a.d == 128 ? launch_fused_t<128, false>(a, cluster, stream)
+                    : launch_fused_t<64, false>(a, cluster, stream);
 }
 
 }  // namespace srkv

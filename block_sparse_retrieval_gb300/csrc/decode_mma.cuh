@@ -30,10 +30,14 @@ struct StageInfo {
   int32_t pad[2];
 };
 
-template <int D>
+// F8: the pages hold E4M3 codes (one byte per value) and each stage also carries the 128
+// K and 128 V row scales of its page.
+template <int D, bool F8 = false>
 struct Cfg {
-  static constexpr int kSlab = kBlock * D * 2;          // bytes of one K or V slab
-  static constexpr int kStages = D == 128 ? 3 : 6;
+  static_assert(!F8 || D == 128, "compressed pages: d 128");
+  static constexpr int kElem = F8 ? 1 : 2;              // bytes per cached value
+  static constexpr int kSlab = kBlock * D * kElem;      // bytes of one K or V slab
+  static constexpr int kStages = F8 ? 5 : (D == 128 ? 3 : 6);
   static constexpr int kQBytes = 8 * D * 2;              // up to 8 query heads
   static constexpr int MT = D / 16;                      // PV m-tiles over d
   static constexpr int KJ = D / 32;                      // 16-byte K chunks per thread-row
@@ -44,13 +48,15 @@ struct Cfg {
   static constexpr size_t kOffK = 0;
   static constexpr size_t kOffV = kOffK + (size_t)kStages * kSlab;
   static constexpr size_t kOffQ = kOffV + (size_t)kStages * kSlab;
-  static constexpr size_t kOffMerge = kOffQ + (size_t)kStages * kQBytes;
+  static constexpr int kScaleBytes = F8 ? 2 * kBlock * 4 : 0;  // K, then V row scales
+  static constexpr size_t kOffScale = kOffQ + (size_t)kStages * kQBytes;
+  static constexpr size_t kOffMerge = kOffScale + (size_t)kStages * kScaleBytes;
   static constexpr size_t kOffInfo = kOffMerge + sizeof(float) * 4 * kMergeSlot;
   static constexpr size_t kOffBar = kOffInfo + sizeof(StageInfo) * kStages;
   // full (K, query, stage info)[kStages], full_v[kStages], empty[kStages], merge w1, w2, r2
   static constexpr size_t kSmem = kOffBar + sizeof(uint64_t) * (3 * kStages + 3);
   static constexpr size_t kSmemAlloc = kSmem + 1024;  // the swizzled stages need 1 KiB alignment
-  static constexpr int kBoxes = D / 64;                // 64-column TMA boxes per slab
+  static constexpr int kBoxes = D * kElem / 128;       // 128-byte-wide TMA boxes per slab
   static constexpr int kBoxBytes = kBlock * 128;       // 128 rows of 128 bytes
 };
 
@@ -133,12 +139,12 @@ __device__ __forceinline__ int d_of(int g, int v) {
 
 // Hands stage `it` to the consumers: waits until it is free, writes its description and
 // arms its mbarrier with the bytes of the copies it starts (called by one producer lane).
-template <int D>
+template <int D, bool F8 = false>
 __device__ __forceinline__ void issue_stage(const DecodeArgs& a, const TmaMaps& maps,
                                             unsigned char* smem, int64_t it, int32_t u,
                                             uint32_t fl, const PageTask& t, int64_t& armed,
                                             bool& abort, uint32_t& eflags) {
-  using C = Cfg<D>;
+  using C = Cfg<D, F8>;
   if (abort) return;
   StageInfo* sInfo = reinterpret_cast<StageInfo*>(smem + C::kOffInfo);
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::kOffBar);
@@ -164,7 +170,8 @@ __device__ __forceinline__ void issue_stage(const DecodeArgs& a, const TmaMaps& 
   // is still arriving.
   const bool rows = load && t.hi > t.lo;
   const uint32_t qbytes = (uint32_t)(a.G * D * 2);
-  if (rows && t.page >= a.num_pages) {
+  constexpr uint32_t kRowScales = F8 ? kBlock * 4 : 0;  // one fp32 scale per row
+  if (!F8 && rows && t.page >= a.num_pages) {
     // A page of the host pool: the producer warp copies its slabs and then arrives
     // (issue_stage_warp); here only the query's bytes are announced and requested.
     if (fl & kNewUnit) {
@@ -176,9 +183,9 @@ __device__ __forceinline__ void issue_stage(const DecodeArgs& a, const TmaMaps& 
     }
     return;
   }
-  mbar_arrive_expect_tx(&full[s], (rows ? (uint32_t)C::kSlab : 0u) +
+  mbar_arrive_expect_tx(&full[s], (rows ? (uint32_t)C::kSlab + kRowScales : 0u) +
                                       ((fl & kNewUnit) ? qbytes : 0u));
-  mbar_arrive_expect_tx(&full_v[s], rows ? (uint32_t)C::kSlab : 0u);
+  mbar_arrive_expect_tx(&full_v[s], rows ? (uint32_t)C::kSlab + kRowScales : 0u);
   ++armed;
   if (u < 0) return;
   const int32_t h = u % a.Hkv, r = u / a.Hkv;
@@ -187,7 +194,11 @@ __device__ __forceinline__ void issue_stage(const DecodeArgs& a, const TmaMaps& 
 #pragma unroll
     for (int b = 0; b < C::kBoxes; ++b)
       tma_load_3d(smem + C::kOffK + (size_t)s * C::kSlab + (size_t)b * C::kBoxBytes, &maps.k,
-                  64 * b, h * kBlock, t.page, &full[s], once);
+                  b * 128 / C::kElem, h * kBlock, t.page, &full[s], once);
+    if constexpr (F8)
+      bulk_load_hint(smem + C::kOffScale + (size_t)s * C::kScaleBytes,
+                     a.k_scale + ((int64_t)t.page * a.Hkv + h) * kBlock, kRowScales, &full[s],
+                     once);
   }
   if (fl & kNewUnit)
     bulk_load(smem + C::kOffQ + (size_t)s * C::kQBytes,
@@ -197,7 +208,11 @@ __device__ __forceinline__ void issue_stage(const DecodeArgs& a, const TmaMaps& 
 #pragma unroll
     for (int b = 0; b < C::kBoxes; ++b)
       tma_load_3d(smem + C::kOffV + (size_t)s * C::kSlab + (size_t)b * C::kBoxBytes, &maps.v,
-                  64 * b, h * kBlock, t.page, &full_v[s], once);
+                  b * 128 / C::kElem, h * kBlock, t.page, &full_v[s], once);
+    if constexpr (F8)
+      bulk_load_hint(smem + C::kOffScale + (size_t)s * C::kScaleBytes + kRowScales,
+                     a.v_scale + ((int64_t)t.page * a.Hkv + h) * kBlock, kRowScales,
+                     &full_v[s], once);
   }
 }
 
@@ -206,14 +221,15 @@ __device__ __forceinline__ void issue_stage(const DecodeArgs& a, const TmaMaps& 
 // tensor-map copies produce (128-byte swizzle), so the consumers read both kinds of stage
 // alike: over NVLink-C2C the host pool is read in place, with no staging copy in HBM.  Each
 // lane ties its copies to the stage's barriers, then lane 0 arrives.
-template <int D>
+template <int D, bool F8 = false>
 __device__ __forceinline__ void issue_stage_warp(const DecodeArgs& a, const TmaMaps& maps,
                                                  unsigned char* smem, int64_t it, int32_t u,
                                                  uint32_t fl, const PageTask& t, int64_t& armed,
                                                  bool& abort, uint32_t& eflags, int lane) {
-  using C = Cfg<D>;
-  const bool host = t.page >= 0 && t.hi > t.lo && t.page >= a.num_pages;  // uniform
-  if (lane == 0) issue_stage<D>(a, maps, smem, it, u, fl, t, armed, abort, eflags);
+  using C = Cfg<D, F8>;
+  // (compressed pages have no host pool)
+  const bool host = !F8 && t.page >= 0 && t.hi > t.lo && t.page >= a.num_pages;  // uniform
+  if (lane == 0) issue_stage<D, F8>(a, maps, smem, it, u, fl, t, armed, abort, eflags);
   abort = __shfl_sync(0xffffffffu, abort, 0);
   if (!host || abort) return;
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::kOffBar);
@@ -251,11 +267,26 @@ __device__ __forceinline__ void warp_arrive(uint64_t* bar) {
 
 // Writes a merged state (acc, m, l of the lane's two heads) as a partial: acc[G][D] and
 // ml[G][2] floats (generic pointers: global memory or another CTA's shared memory).
-template <int D>
+template <int D, bool F8 = false>
 __device__ __forceinline__ void store_partial(float* accp, float* mlp, const SoftmaxState<D>& st,
                                               Lane ln, int G) {
   using C = Cfg<D>;
   const int h0 = 2 * ln.t, h1 = h0 + 1;
+  if constexpr (F8) {
+    // compressed pages: m-tile i row g holds d = 16g + 2i, row g + 8 holds d = 16g + 2i + 1,
+    // so the lane's 16 values per head are d = 16g .. 16g + 15 in the order
+    // (i 0 row g, i 0 row g+8, i 1 row g, ...)
+#pragma unroll
+    for (int k4 = 0; k4 < C::MT; k4 += 2) {
+      const int dd = 16 * ln.g + 2 * k4;
+      if (h0 < G)
+        *reinterpret_cast<float4*>(accp + h0 * D + dd) =
+            make_float4(st.acc[k4][0], st.acc[k4][2], st.acc[k4 + 1][0], st.acc[k4 + 1][2]);
+      if (h1 < G)
+        *reinterpret_cast<float4*>(accp + h1 * D + dd) =
+            make_float4(st.acc[k4][1], st.acc[k4][3], st.acc[k4 + 1][1], st.acc[k4 + 1][3]);
+    }
+  } else {
   // values 4k..4k+3 of a lane sit at 4 consecutive d (d_of): 16-byte stores
 #pragma unroll
   for (int k4 = 0; k4 < C::MT; k4 += 4) {
@@ -273,6 +304,7 @@ __device__ __forceinline__ void store_partial(float* accp, float* mlp, const Sof
           st.acc[k4][3], st.acc[k4 + 1][3], st.acc[k4 + 2][3], st.acc[k4 + 3][3]);
     }
   }
+  }
   if (ln.g == 0) {
     if (h0 < G) {
       mlp[h0 * 2 + 0] = st.m[0];
@@ -289,13 +321,14 @@ __device__ __forceinline__ void store_partial(float* accp, float* mlp, const Sof
 // At the end of each segment (a stage flagged kSegEnd; the sentinel may carry the flag too,
 // closing a segment whose length the producer did not know in advance) the warps merge their
 // states and warp 0 calls write_partial(state, stage info, lane) with the merged state.
-template <int D, typename WritePartial>
+template <int D, bool F8 = false, typename WritePartial>
 __device__ __forceinline__ void consumer_loop(const DecodeArgs& a, unsigned char* smem, int lane,
                                               int warp, WritePartial&& write_partial) {
-  using C = Cfg<D>;
+  using C = Cfg<D, F8>;
   unsigned char* sK = smem + C::kOffK;
   unsigned char* sV = smem + C::kOffV;
   unsigned char* sQ = smem + C::kOffQ;
+  const float* sScale = reinterpret_cast<const float*>(smem + C::kOffScale);
   float* sMerge = reinterpret_cast<float*>(smem + C::kOffMerge);
   StageInfo* sInfo = reinterpret_cast<StageInfo*>(smem + C::kOffInfo);
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::kOffBar);
@@ -357,6 +390,22 @@ __device__ __forceinline__ void consumer_loop(const DecodeArgs& a, unsigned char
     if (inf.flags & kNewUnit) {
       st.reset();
       const unsigned char* q = sQ + (size_t)s * C::kQBytes;
+      if constexpr (F8) {
+        // fp16 query in the order the E4M3 K fragments take d (see the S^T product below):
+        // k-step m of lane t covers d = 64 (m >= 4) + 16 t + 4 (m mod 4) + 0..3
+#pragma unroll
+        for (int m = 0; m < 8; ++m) {
+          uint32_t lo = 0u, hi = 0u;
+          if (ln.g < a.G) {
+            const uint2 w = *reinterpret_cast<const uint2*>(
+                q + ((size_t)ln.g * D + 64 * (m >> 2) + 16 * ln.t + 4 * (m & 3)) * 2);
+            lo = pack_f16(bf16_lo(w.x), bf16_hi(w.x));
+            hi = pack_f16(bf16_lo(w.y), bf16_hi(w.y));
+          }
+          qb[m >> 1][2 * (m & 1)] = lo;
+          qb[m >> 1][2 * (m & 1) + 1] = hi;
+        }
+      } else {
 #pragma unroll
       for (int j = 0; j < C::KJ; ++j) {
         if (ln.g < a.G) {
@@ -369,6 +418,7 @@ __device__ __forceinline__ void consumer_loop(const DecodeArgs& a, unsigned char
           qb[j][0] = qb[j][1] = qb[j][2] = qb[j][3] = 0u;
         }
       }
+      }
     }
     if (row0 < inf.hi && row0 + 16 > inf.lo) {
       const unsigned char* k = sK + (size_t)s * C::kSlab;
@@ -376,12 +426,36 @@ __device__ __forceinline__ void consumer_loop(const DecodeArgs& a, unsigned char
       // ---- S^T = K . Q^T
       float sacc[4] = {0.f, 0.f, 0.f, 0.f};
       const int ra = row0 + tile_token(ln.g), rb = ra + 8;
+      if constexpr (F8) {
+        // a row is 128 codes in 8 chunks of 16; lane t reads chunks t and t + 4 of rows ra,
+        // rb, and byte pairs of a chunk widen to fp16 pairs (exact): 8 k-steps of 16
+        const int4 kq[2][2] = {{lds128(k + swz(ra, ln.t)), lds128(k + swz(rb, ln.t))},
+                               {lds128(k + swz(ra, 4 + ln.t)), lds128(k + swz(rb, 4 + ln.t))}};
+        auto word = [](const int4& x, int w) -> uint32_t {
+          return (uint32_t)(w == 0 ? x.x : w == 1 ? x.y : w == 2 ? x.z : x.w);
+        };
+#pragma unroll
+        for (int m = 0; m < 8; ++m) {
+          const uint32_t wa = word(kq[m >> 2][0], m & 3), wb = word(kq[m >> 2][1], m & 3);
+          mma_16816_f16(sacc, e4m3x2_to_f16x2(wa), e4m3x2_to_f16x2(wb),
+                        e4m3x2_to_f16x2(wa >> 16), e4m3x2_to_f16x2(wb >> 16),
+                        qb[m >> 1][2 * (m & 1)], qb[m >> 1][2 * (m & 1) + 1]);
+        }
+        // the rows' K scales (a masked row's scale is never used)
+        const float* ks = sScale + (size_t)s * (C::kScaleBytes / 4);
+        const float ka = ks[ra], kb = ks[rb];
+        sacc[0] *= ka;
+        sacc[1] *= ka;
+        sacc[2] *= kb;
+        sacc[3] *= kb;
+      } else {
 #pragma unroll
       for (int j = 0; j < C::KJ; ++j) {
         const int4 k0 = lds128(k + swz(ra, 4 * j + ln.t));
         const int4 k1 = lds128(k + swz(rb, 4 * j + ln.t));
         mma_16816(sacc, k0.x, k1.x, k0.y, k1.y, qb[j][0], qb[j][1]);
         mma_16816(sacc, k0.z, k1.z, k0.w, k1.w, qb[j][2], qb[j][3]);
+      }
       }
       // ---- mask, online softmax (log2 domain)
       const bool va = ra >= inf.lo && ra < inf.hi && (ra < inf.ie || ra >= inf.ws);
@@ -403,10 +477,18 @@ __device__ __forceinline__ void consumer_loop(const DecodeArgs& a, unsigned char
       const float alpha1 = fast_exp2(st.m[1] - base1);
       st.m[0] = mn0;
       st.m[1] = mn1;
-      const uint32_t p01 = pack_bf16(fast_exp2(s0 - base0), fast_exp2(s1 - base1));
-      const uint32_t p23 = pack_bf16(fast_exp2(s2 - base0), fast_exp2(s3 - base1));
-      st.l[0] = st.l[0] * alpha0 + bf16_lo(p01) + bf16_lo(p23);
-      st.l[1] = st.l[1] * alpha1 + bf16_hi(p01) + bf16_hi(p23);
+      uint32_t p01, p23;  // the weights as the second product's operand rounds them
+      if constexpr (F8) {
+        p01 = pack_f16(fast_exp2(s0 - base0), fast_exp2(s1 - base1));
+        p23 = pack_f16(fast_exp2(s2 - base0), fast_exp2(s3 - base1));
+        st.l[0] = st.l[0] * alpha0 + f16_lo(p01) + f16_lo(p23);
+        st.l[1] = st.l[1] * alpha1 + f16_hi(p01) + f16_hi(p23);
+      } else {
+        p01 = pack_bf16(fast_exp2(s0 - base0), fast_exp2(s1 - base1));
+        p23 = pack_bf16(fast_exp2(s2 - base0), fast_exp2(s3 - base1));
+        st.l[0] = st.l[0] * alpha0 + bf16_lo(p01) + bf16_lo(p23);
+        st.l[1] = st.l[1] * alpha1 + bf16_hi(p01) + bf16_hi(p23);
+      }
 #pragma unroll
       for (int i = 0; i < C::MT; ++i) {
         st.acc[i][0] *= alpha0;
@@ -421,9 +503,42 @@ __device__ __forceinline__ void consumer_loop(const DecodeArgs& a, unsigned char
         if (lane == 0) raise_flags(a.error_flags, SRKV_EFLAG_TIMEOUT);
         break;
       }
-      int4 vt[4][C::NCH];
       const int trow[4] = {row0 + tile_token(2 * ln.t), row0 + tile_token(2 * ln.t + 1),
                            row0 + tile_token(2 * ln.t + 8), row0 + tile_token(2 * ln.t + 9)};
+      if constexpr (F8) {
+        // O^T += V^T . P: m-tile i takes d = 16 g + 2 i (row g) and 16 g + 2 i + 1 (row g + 8)
+        // from the lane's chunk g of the four token rows; a byte permute pairs the two tokens
+        // of each product row, widened to fp16 and multiplied by the tokens' V scales
+        // (masked rows load as zero codes with a zero scale)
+        const float* vsp = sScale + (size_t)s * (C::kScaleBytes / 4) + kBlock;
+        int4 vq[4];
+        float vsc[4];
+#pragma unroll
+        for (int x = 0; x < 4; ++x) {
+          const bool in = trow[x] >= inf.lo && trow[x] < inf.hi;
+          vq[x] = in ? lds128(v + swz(trow[x], ln.g)) : make_int4(0, 0, 0, 0);
+          vsc[x] = in ? vsp[trow[x]] : 0.f;
+        }
+        const uint32_t sc01 = pack_f16(vsc[0], vsc[1]), sc23 = pack_f16(vsc[2], vsc[3]);
+        auto word = [](const int4& x, int w) -> uint32_t {
+          return (uint32_t)(w == 0 ? x.x : w == 1 ? x.y : w == 2 ? x.z : x.w);
+        };
+#pragma unroll
+        for (int i = 0; i < C::MT; ++i) {
+          const int wi = i >> 1, bo = 2 * (i & 1);
+          // bytes (token a, d0), (token b, d0), (token a, d1), (token b, d1)
+          const uint32_t sel = (uint32_t)(bo | ((4 + bo) << 4) | ((bo + 1) << 8) | ((5 + bo) << 12));
+          const uint32_t x01 = __byte_perm(word(vq[0], wi), word(vq[1], wi), sel);
+          const uint32_t x23 = __byte_perm(word(vq[2], wi), word(vq[3], wi), sel);
+          const uint32_t a0 = mul_f16x2(e4m3x2_to_f16x2(x01), sc01);
+          const uint32_t a1 = mul_f16x2(e4m3x2_to_f16x2(x01 >> 16), sc01);
+          const uint32_t a2 = mul_f16x2(e4m3x2_to_f16x2(x23), sc23);
+          const uint32_t a3 = mul_f16x2(e4m3x2_to_f16x2(x23 >> 16), sc23);
+          mma_16816_f16(st.acc[i], a0, a1, a2, a3, b0, b1);
+        }
+      } else {
+      int4 vt[4][C::NCH];
+
 #pragma unroll
       for (int x = 0; x < 4; ++x) {
         const bool in = trow[x] >= inf.lo && trow[x] < inf.hi;
@@ -447,6 +562,7 @@ __device__ __forceinline__ void consumer_loop(const DecodeArgs& a, unsigned char
         const uint32_t a3 = __byte_perm(word(vt[2][c1], e1 >> 1), word(vt[3][c1], e1 >> 1), sel1);
         mma_16816(st.acc[i], a0, a1, a2, a3, b0, b1);
       }
+      }
     }
     // release the stage
     warp_arrive(&empty[s]);
@@ -462,9 +578,9 @@ __device__ __forceinline__ void consumer_loop(const DecodeArgs& a, unsigned char
 }
 
 // Barrier setup of the stage ring (one thread; fenced for the async proxy and the cluster).
-template <int D>
+template <int D, bool F8 = false>
 __device__ __forceinline__ void init_ring(unsigned char* smem) {
-  using C = Cfg<D>;
+  using C = Cfg<D, F8>;
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::kOffBar);
   uint64_t* full_v = full + C::kStages;
   uint64_t* empty = full_v + C::kStages;
@@ -480,9 +596,9 @@ __device__ __forceinline__ void init_ring(unsigned char* smem) {
   fence_mbar_init();
 }
 
-// Host: tensor map of a cache [num_pages][Hkv * 128][d] bf16 (64-column x 128-row boxes,
-// 128-byte swizzle); false if it cannot be encoded.
+// Host: tensor map of a cache [num_pages][Hkv * 128][d] of bf16 (64-column x 128-row boxes)
+// or of E4M3 bytes (128-column boxes), 128-byte swizzle; false if it cannot be encoded.
 bool encode_cache_map(CUtensorMap* map, const void* base, int64_t num_pages, int32_t Hkv,
-                      int32_t d);
+                      int32_t d, bool e4m3);
 
 }  // namespace srkv

@@ -26,10 +26,10 @@ namespace {
 // 128 registers: a quarter-SM register file (16K) then holds this CTA's three warps on one
 // sub-partition (12K) beside one warp of a combine CTA, so the combine is resident and
 // waiting when the last partial is written.
-template <int D>
+template <int D, bool F8>
 __global__ void __maxnreg__(128) split_mma_kernel(const DecodeArgs a,
                                                   const __grid_constant__ TmaMaps maps) {
-  using C = Cfg<D>;
+  using C = Cfg<D, F8>;
   extern __shared__ __align__(128) unsigned char smem_raw[];
   unsigned char* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   StageInfo* sInfo = reinterpret_cast<StageInfo*>(smem + C::kOffInfo);
@@ -43,7 +43,7 @@ __global__ void __maxnreg__(128) split_mma_kernel(const DecodeArgs a,
   // the previous kernel in the stream has finished, and the combine reads them too.
   if (!a.early) griddep_wait();
   griddep_launch_dependents();
-  if (tid == 0) init_ring<D>(smem);
+  if (tid == 0) init_ring<D, F8>(smem);
   __syncthreads();
 
   if (warp == kProducerWarp) {
@@ -123,7 +123,7 @@ __global__ void __maxnreg__(128) split_mma_kernel(const DecodeArgs a,
           t.hi = __shfl_sync(0xffffffffu, task.hi, l);
           t.ie = __shfl_sync(0xffffffffu, task.ie, l);
           t.ws = __shfl_sync(0xffffffffu, task.ws, l);
-          issue_stage_warp<D>(a, maps, smem, it, u, fl, t, armed, abort, eflags, lane);
+          issue_stage_warp<D, F8>(a, maps, smem, it, u, fl, t, armed, abort, eflags, lane);
           ++it;
         }
       }
@@ -132,7 +132,7 @@ __global__ void __maxnreg__(128) split_mma_kernel(const DecodeArgs a,
       PageTask none;
       none.page = -1;
       none.lo = none.hi = none.ie = none.ws = 0;
-      issue_stage<D>(a, maps, smem, it, -1, kLast, none, armed, abort, eflags);  // sentinel
+      issue_stage<D, F8>(a, maps, smem, it, -1, kLast, none, armed, abort, eflags);  // sentinel
       // Drain: every copy this CTA issued must land before the CTA exits.
       const int64_t first = armed > C::kStages ? armed - C::kStages : 0;
       for (int64_t i = first; i < armed; ++i)
@@ -149,11 +149,11 @@ __global__ void __maxnreg__(128) split_mma_kernel(const DecodeArgs a,
 
   // -------------------------------------------------------------------- consumers
   // warp 0 writes the partial of (unit, this CTA) into the list's bank
-  consumer_loop<D>(a, smem, lane, warp, [&](const SoftmaxState<D>& st, const StageInfo& inf,
+  consumer_loop<D, F8>(a, smem, lane, warp, [&](const SoftmaxState<D>& st, const StageInfo& inf,
                                             Lane ln) {
     const int64_t slot =
         ((inf.flags & kBankB) ? (int64_t)a.lay.bank : 0) + inf.unit + blockIdx.x;
-    store_partial<D>(reinterpret_cast<float*>(a.ws + a.lay.acc) + slot * a.G * D,
+    store_partial<D, F8>(reinterpret_cast<float*>(a.ws + a.lay.acc) + slot * a.G * D,
                      reinterpret_cast<float*>(a.ws + a.lay.ml) + slot * a.G * 2, st, ln, a.G);
   });
 }
@@ -187,21 +187,24 @@ EncodeTiled encode_tiled() {
   return fn;
 }
 
-// [num_pages][Hkv * 128][d] bf16, boxes of 64 columns x 128 rows, 128-byte swizzle.
+// [num_pages][Hkv * 128][d] of bf16 (boxes of 64 columns) or E4M3 bytes (boxes of 128
+// columns): 128-byte-wide boxes of 128 rows, 128-byte swizzle.
 bool encode_cache_map(CUtensorMap* map, const void* base, int64_t num_pages, int32_t Hkv,
-                      int32_t d) {
+                      int32_t d, bool e4m3) {
   const EncodeTiled fn = encode_tiled();
   if (!fn || num_pages > INT32_MAX || (int64_t)Hkv * kBlock > INT32_MAX) return false;
+  const cuuint64_t elem = e4m3 ? 1 : 2;
   const cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)Hkv * kBlock, (cuuint64_t)num_pages};
-  const cuuint64_t strides[2] = {(cuuint64_t)d * 2, (cuuint64_t)Hkv * kBlock * d * 2};
-  const cuuint32_t box[3] = {64, (cuuint32_t)kBlock, 1};
+  const cuuint64_t strides[2] = {(cuuint64_t)d * elem, (cuuint64_t)Hkv * kBlock * d * elem};
+  const cuuint32_t box[3] = {(cuuint32_t)(128 / elem), (cuuint32_t)kBlock, 1};
   const cuuint32_t estr[3] = {1, 1, 1};
-  return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides,
+  return fn(map, e4m3 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3,
+            const_cast<void*>(base), dims, strides,
             box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int D>
+template <int D, bool F8>
 cudaError_t launch_d(const DecodeArgs& a, cudaStream_t stream) {
   // The shared-memory opt-in is set once per device (not during graph capture).
   static bool configured[128] = {false};
@@ -210,21 +213,23 @@ cudaError_t launch_d(const DecodeArgs& a, cudaStream_t stream) {
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= 128) return cudaErrorInvalidDevice;
   if (!configured[dev]) {
-    e = cudaFuncSetAttribute(split_mma_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)Cfg<D>::kSmemAlloc);
+    e = cudaFuncSetAttribute(split_mma_kernel<D, F8>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)Cfg<D, F8>::kSmemAlloc);
     if (e != cudaSuccess) return e;
     configured[dev] = true;
   }
   TmaMaps maps;
-  if (!encode_cache_map(&maps.k, a.k_cache, a.num_pages, a.Hkv, D) ||
-      !encode_cache_map(&maps.v, a.v_cache, a.num_pages, a.Hkv, D))
+  if (!encode_cache_map(&maps.k, a.k_cache, a.num_pages, a.Hkv, D, F8) ||
+      !encode_cache_map(&maps.v, a.v_cache, a.num_pages, a.Hkv, D, F8))
     return cudaErrorInvalidValue;
-  return launch_pdl(split_mma_kernel<D>, dim3(a.ctas), dim3(kThreads), Cfg<D>::kSmemAlloc, stream,
-                    a, maps);
+  return launch_pdl(split_mma_kernel<D, F8>, dim3(a.ctas), dim3(kThreads),
+                    Cfg<D, F8>::kSmemAlloc, stream, a, maps);
 }
 
 cudaError_t launch_split_mma(const DecodeArgs& a, cudaStream_t stream) {
-  return a.d == 128 ? launch_d<128>(a, stream) : launch_d<64>(a, stream);
+  if (a.k_scale) return launch_d<128, true>(a, stream);  // compressed pages (d 128)
+  return a.d == 128 ? launch_d<128, false>(a, stream) : launch_d<64, false>(a, stream);
 }
 
 }  // namespace srkv

@@ -132,6 +132,8 @@ srkv_status prepare_decode(const srkv_config* cfg, const void* q, const void* k_
   a.k_host = nullptr;
   a.v_host = nullptr;
   a.num_host_pages = 0;
+  a.k_scale = nullptr;
+  a.v_scale = nullptr;
   a.dense_boundary = cfg->dense_boundary;
   a.topk_percent = cfg->topk_percent;
   return SRKV_OK;
@@ -170,7 +172,8 @@ srkv_status check_score(const srkv_config* cfg, const void* q, const float* reps
 // [num_pages, num_pages + num_host_pages) of page ids (num_host_pages = 0: no host pool).
 srkv_status retrieval_decode(const srkv_config* cfg, const void* q, const void* k_cache,
                              const void* v_cache, int64_t num_pages, const void* k_host,
-                             const void* v_host, int64_t num_host_pages, const float* reps,
+                             const void* v_host, int64_t num_host_pages, const float* k_scale,
+                             const float* v_scale, const float* reps,
                              const int32_t* block_table, int32_t max_blocks,
                              const int32_t* seq_lens, const int32_t* prompt_lens, int32_t batch,
                              int32_t* sel, int32_t kmax, int32_t* nsel, void* out,
@@ -186,6 +189,8 @@ srkv_status retrieval_decode(const srkv_config* cfg, const void* q, const void* 
   a.k_host = k_host;
   a.v_host = v_host;
   a.num_host_pages = num_host_pages;
+  a.k_scale = k_scale;  // compressed pages when set
+  a.v_scale = v_scale;
   // The scoring kernel, then the decode, which streams list A while the scoring finishes
   // and knows the selection counts it will write from the lengths.  A scoring CTA keeps its
   // SM to itself, so list A goes to the decode CTAs that find an SM free at once (the grid
@@ -196,7 +201,8 @@ srkv_status retrieval_decode(const srkv_config* cfg, const void* q, const void* 
   a.sel_out = sel;
   a.nsel_out = nsel;
   // A batch small enough for one cluster per unit to be resident: one kernel does it all.
-  const int32_t cluster = fused_cluster_size(*cfg, batch * cfg->num_kv_heads, max_blocks);
+  const int32_t cluster =
+      fused_cluster_size(*cfg, batch * cfg->num_kv_heads, max_blocks, k_scale != nullptr);
   if (cluster > 0) return cuda_status(launch_fused(a, cluster, s));
   const bool early = mma_split_supported(*cfg);
   const int64_t scoring = score_topk_ctas(*cfg, max_blocks, batch);
@@ -271,6 +277,25 @@ srkv_status srkv_build_block_reps(const srkv_config* cfg, const void* k_cache,
                                        n_pages, reps, error_flags, (cudaStream_t)stream));
 }
 
+srkv_status srkv_quantize_kv_fp8(const srkv_config* cfg, const void* k_cache,
+                                 const void* v_cache, int64_t num_pages,
+                                 const int32_t* page_ids, int32_t n_pages, void* k_fp8,
+                                 void* v_fp8, float* k_scale, float* v_scale,
+                                 int32_t* error_flags, srkv_stream stream) {
+  if (!config_ok(cfg) || n_pages < 0 || num_pages < 0) return SRKV_ERR_INVALID_ARG;
+  if (cfg->dtype != SRKV_BF16) return SRKV_ERR_UNSUPPORTED;
+  if (n_pages == 0) return SRKV_OK;
+  if (!k_cache || !v_cache || !page_ids || !k_fp8 || !v_fp8 || !k_scale || !v_scale ||
+      num_pages == 0)
+    return SRKV_ERR_INVALID_ARG;
+  if (!aligned(k_cache, 16) || !aligned(v_cache, 16) || !aligned(k_fp8, 16) ||
+      !aligned(v_fp8, 16) || !aligned(k_scale, 16) || !aligned(v_scale, 16))
+    return SRKV_ERR_INVALID_ARG;
+  return cuda_status(launch_quantize_fp8(*cfg, k_cache, v_cache, num_pages, page_ids, n_pages,
+                                         k_fp8, v_fp8, k_scale, v_scale, error_flags,
+                                         (cudaStream_t)stream));
+}
+
 srkv_status srkv_append_kv(const srkv_config* cfg, const void* k_new, const void* v_new,
                            void* k_cache, void* v_cache, int64_t num_pages,
                            const int32_t* block_table, int32_t max_blocks,
@@ -338,7 +363,8 @@ srkv_status srkv_retrieval_decode(const srkv_config* cfg, const void* q, const v
                                   int32_t batch, int32_t* sel, int32_t kmax, int32_t* nsel,
                                   void* out, void* workspace, size_t workspace_bytes,
                                   int32_t* error_flags, srkv_stream stream) {
-  return retrieval_decode(cfg, q, k_cache, v_cache, num_pages, nullptr, nullptr, 0, reps,
+  return retrieval_decode(cfg, q, k_cache, v_cache, num_pages, nullptr, nullptr, 0, nullptr,
+                          nullptr, reps,
                           block_table, max_blocks, seq_lens, prompt_lens, batch, sel, kmax, nsel,
                           out, workspace, workspace_bytes, error_flags, (cudaStream_t)stream);
 }
@@ -376,6 +402,25 @@ srkv_status srkv_retrieval_decode_tiered(const srkv_config* cfg, const void* q,
     v_host = hp[1];
   }
   return retrieval_decode(cfg, q, k_cache, v_cache, num_pages, k_host, v_host, num_host_pages,
+                          nullptr, nullptr, reps, block_table, max_blocks, seq_lens, prompt_lens, batch, sel, kmax,
+                          nsel, out, workspace, workspace_bytes, error_flags,
+                          (cudaStream_t)stream);
+}
+
+srkv_status srkv_retrieval_decode_fp8(const srkv_config* cfg, const void* q, const void* k_fp8,
+                                      const void* v_fp8, const float* k_scale,
+                                      const float* v_scale, const float* reps,
+                                      int64_t num_pages, const int32_t* block_table,
+                                      int32_t max_blocks, const int32_t* seq_lens,
+                                      const int32_t* prompt_lens, int32_t batch, int32_t* sel,
+                                      int32_t kmax, int32_t* nsel, void* out, void* workspace,
+                                      size_t workspace_bytes, int32_t* error_flags,
+                                      srkv_stream stream) {
+  if (!config_ok(cfg)) return SRKV_ERR_INVALID_ARG;
+  if (!mma_split_supported(*cfg) || cfg->head_dim != 128) return SRKV_ERR_UNSUPPORTED;
+  if (batch > 0 && (!k_scale || !v_scale || !aligned(k_scale, 16) || !aligned(v_scale, 16)))
+    return SRKV_ERR_INVALID_ARG;
+  return retrieval_decode(cfg, q, k_fp8, v_fp8, num_pages, nullptr, nullptr, 0, k_scale, v_scale,
                           reps, block_table, max_blocks, seq_lens, prompt_lens, batch, sel, kmax,
                           nsel, out, workspace, workspace_bytes, error_flags,
                           (cudaStream_t)stream);

@@ -3,6 +3,8 @@
 #pragma once
 
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_fp8.h>
 #include <cuda.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
@@ -219,6 +221,41 @@ __device__ __forceinline__ void mma_16816(float (&d)[4], uint32_t a0, uint32_t a
 }
 
 // Transpose of an 8x8 matrix of 16-bit values held one row per four lanes.
+// D += A * B, m16n8k16, fp16 inputs, fp32 accumulate (the compressed-page decode: E4M3
+// values widen to fp16 exactly).
+__device__ __forceinline__ void mma_16816_f16(float (&d)[4], uint32_t a0, uint32_t a1,
+                                              uint32_t a2, uint32_t a3, uint32_t b0,
+                                              uint32_t b1) {
+  asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+      "{%8,%9}, {%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// Two E4M3 codes (low byte -> low half) as two fp16 values (exact).
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t two_codes) {
+  const __half2_raw h =
+      __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(two_codes & 0xffffu), __NV_E4M3);
+  return (uint32_t)h.x | ((uint32_t)h.y << 16);
+}
+
+__device__ __forceinline__ uint32_t pack_f16(float lo, float hi) {
+  const __half2 v = __floats2half2_rn(lo, hi);
+  return *reinterpret_cast<const uint32_t*>(&v);
+}
+__device__ __forceinline__ float f16_lo(uint32_t v) {
+  return __half2float(__ushort_as_half((unsigned short)(v & 0xffffu)));
+}
+__device__ __forceinline__ float f16_hi(uint32_t v) {
+  return __half2float(__ushort_as_half((unsigned short)(v >> 16)));
+}
+// Lane-wise fp16 product of two fp16 pairs.
+__device__ __forceinline__ uint32_t mul_f16x2(uint32_t a, uint32_t b) {
+  const __half2 r = __hmul2(*reinterpret_cast<const __half2*>(&a),
+                            *reinterpret_cast<const __half2*>(&b));
+  return *reinterpret_cast<const uint32_t*>(&r);
+}
+
 __device__ __forceinline__ uint32_t movmatrix_trans(uint32_t x) {
   uint32_t y;
   asm("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(y) : "r"(x));
@@ -376,6 +413,9 @@ struct DecodeArgs {
   const void* k_host;
   const void* v_host;
   int64_t num_host_pages;
+  // Compressed pages (the E4M3 decode): fp32 scale of every (page, kv head, token) row.
+  const float* k_scale;
+  const float* v_scale;
 };
 
 // Page ids a block table may hold: the device pool, then the host pool.
@@ -441,6 +481,10 @@ cudaError_t launch_block_reps(const srkv_config& cfg, const void* k_cache, int64
 // CTAs of the scoring grid (clusters of up to 8 per (request, kv head) unit).
 int64_t score_topk_ctas(const srkv_config& cfg, int32_t max_blocks, int32_t batch);
 
+cudaError_t launch_quantize_fp8(const srkv_config& cfg, const void* k_src, const void* v_src,
+                                int64_t num_pages, const int32_t* page_ids, int32_t n_pages,
+                                void* k8, void* v8, float* k_scale, float* v_scale,
+                                int32_t* error_flags, cudaStream_t stream);
 cudaError_t launch_append_kv(const srkv_config& cfg, const void* k_new, const void* v_new,
                              void* k_cache, void* v_cache, int64_t num_pages,
                              const int32_t* block_table, int32_t max_blocks,
@@ -468,7 +512,8 @@ cudaError_t launch_combine(const DecodeArgs& a, int32_t dtype, cudaStream_t stre
 // Scoring, selection and attention of a small batch in one kernel, one thread-block cluster
 // per (request, kv head) unit: the cluster size to use for `units` units (0 = not
 // applicable: dtype, head size, group, candidates per unit or residency), and its launch.
-int32_t fused_cluster_size(const srkv_config& cfg, int32_t units, int32_t max_blocks);
+int32_t fused_cluster_size(const srkv_config& cfg, int32_t units, int32_t max_blocks,
+                           bool e4m3 = false);
 cudaError_t launch_fused(const DecodeArgs& a, int32_t cluster, cudaStream_t stream);
 
 }  // namespace srkv

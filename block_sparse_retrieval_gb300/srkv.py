@@ -29,7 +29,8 @@ EXPORTS = ("srkv_default_config", "srkv_status_string", "srkv_topk_count",
            "srkv_score_topk", "srkv_decode_workspace_size", "srkv_sparse_paged_decode",
            "srkv_retrieval_decode", "srkv_sparse_paged_decode_noalloc",
            "srkv_retrieval_decode_launches", "srkv_append_kv",
-           "srkv_retrieval_decode_tiered")
+           "srkv_retrieval_decode_tiered", "srkv_quantize_kv_fp8",
+           "srkv_retrieval_decode_fp8")
 NOALLOC_WORKSPACE_BYTES = 16 << 20
 
 
@@ -90,9 +91,15 @@ def load() -> ctypes.CDLL:
     lib.srkv_retrieval_decode_tiered.argtypes = [ctypes.POINTER(Config), _P, _P, _P, _I64, _P,
                                                  _P, _I64, _P, _P, _I32, _P, _P, _I32, _P, _I32,
                                                  _P, _P, _P, _SZ, _P, _P]
+    lib.srkv_quantize_kv_fp8.argtypes = [ctypes.POINTER(Config), _P, _P, _I64, _P, _I32, _P, _P,
+                                         _P, _P, _P, _P]
+    lib.srkv_retrieval_decode_fp8.argtypes = [ctypes.POINTER(Config), _P, _P, _P, _P, _P, _P,
+                                              _I64, _P, _I32, _P, _P, _I32, _P, _I32, _P, _P,
+                                              _P, _SZ, _P, _P]
     for name in ("srkv_build_block_reps", "srkv_score_topk", "srkv_sparse_paged_decode",
                  "srkv_retrieval_decode", "srkv_sparse_paged_decode_noalloc",
-                 "srkv_retrieval_decode_tiered"):
+                 "srkv_retrieval_decode_tiered", "srkv_quantize_kv_fp8",
+                 "srkv_retrieval_decode_fp8"):
         getattr(lib, name).restype = ctypes.c_int
     _lib = lib
     return lib
@@ -285,6 +292,44 @@ def retrieval_decode_tiered(cfg: Mapping, q: torch.Tensor, k_cache: torch.Tensor
         workspace.numel() * workspace.element_size(),
         _dev(error_flags, "error_flags", torch.int32), _stream(stream)),
         "srkv_retrieval_decode_tiered")
+
+
+def quantize_kv_fp8(cfg: Mapping, k_cache: torch.Tensor, v_cache: torch.Tensor,
+                    page_ids: torch.Tensor, k_fp8: torch.Tensor, v_fp8: torch.Tensor,
+                    k_scale: torch.Tensor, v_scale: torch.Tensor,
+                    error_flags: torch.Tensor | None = None, stream=None) -> None:
+    """srkv_quantize_kv_fp8: pages page_ids of the bf16 caches as E4M3 codes (uint8 tensors
+    of the caches' shape) with one fp32 scale per (page, kv head, token) row."""
+    c = config(cfg)
+    _check(load().srkv_quantize_kv_fp8(
+        ctypes.byref(c), _dev(k_cache, "k_cache", torch.bfloat16),
+        _dev(v_cache, "v_cache", torch.bfloat16), k_cache.shape[0],
+        _dev(page_ids, "page_ids", torch.int32), page_ids.numel(),
+        _dev(k_fp8, "k_fp8", torch.uint8), _dev(v_fp8, "v_fp8", torch.uint8),
+        _dev(k_scale, "k_scale", torch.float32), _dev(v_scale, "v_scale", torch.float32),
+        _dev(error_flags, "error_flags", torch.int32), _stream(stream)), "srkv_quantize_kv_fp8")
+
+
+def retrieval_decode_fp8(cfg: Mapping, q: torch.Tensor, k_fp8: torch.Tensor,
+                         v_fp8: torch.Tensor, k_scale: torch.Tensor, v_scale: torch.Tensor,
+                         reps: torch.Tensor, block_table: torch.Tensor, seq_lens: torch.Tensor,
+                         prompt_lens: torch.Tensor | None, sel: torch.Tensor, nsel: torch.Tensor,
+                         out: torch.Tensor, workspace: torch.Tensor,
+                         error_flags: torch.Tensor | None = None, stream=None) -> None:
+    """srkv_retrieval_decode_fp8: the decode step over E4M3 pages (bf16 query and output)."""
+    c = config(cfg)
+    B, max_blocks = block_table.shape
+    _check(load().srkv_retrieval_decode_fp8(
+        ctypes.byref(c), _dev(q, "q", torch.bfloat16), _dev(k_fp8, "k_fp8", torch.uint8),
+        _dev(v_fp8, "v_fp8", torch.uint8), _dev(k_scale, "k_scale", torch.float32),
+        _dev(v_scale, "v_scale", torch.float32), _dev(reps, "reps", torch.float32),
+        k_fp8.shape[0], _dev(block_table, "block_table", torch.int32), max_blocks,
+        _dev(seq_lens, "seq_lens", torch.int32), _dev(prompt_lens, "prompt_lens", torch.int32),
+        B, _dev(sel, "sel", torch.int32), sel.shape[-1], _dev(nsel, "nsel", torch.int32),
+        _dev(out, "out", torch.bfloat16), _dev(workspace, "workspace"),
+        workspace.numel() * workspace.element_size(),
+        _dev(error_flags, "error_flags", torch.int32), _stream(stream)),
+        "srkv_retrieval_decode_fp8")
 
 
 def sparse_paged_decode_noalloc(cfg: Mapping, q: torch.Tensor, k_cache: torch.Tensor,

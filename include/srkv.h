@@ -148,6 +148,29 @@ srkv_status srkv_append_kv(const srkv_config* cfg, const void* k_new, const void
                            int32_t* error_flags, srkv_stream stream);
 
 /*
+ * Compressed pages (KV-cache survey "大模型推理百倍加速之KV cache篇": quantising the cache is
+ * one of the ways to shrink it).  Writes the listed pages of a bf16 cache as E4M3 codes (the
+ * 8-bit floating point format "E4M3" of the OCP 8-bit floating point specification: 4
+ * exponent bits, 3 mantissa bits, largest finite value 448) with one fp32 scale per
+ * (page, kv head, token) row:
+ *   scale = max over the row of |x| / 448   (1 for an all-zero row),
+ *   code  = E4M3(x / scale), the quotient in fp32, rounded to nearest, ties to even,
+ *           finite values past 448 saturated,
+ * so a value is code x scale.  Per row rather than per page, so that a later token needs no
+ * re-quantisation of its page.
+ *   cfg->dtype must be SRKV_BF16 (the source); k_cache, v_cache: [num_pages][Hkv][S][d] bf16;
+ *   k_fp8, v_fp8: [num_pages][Hkv][S][d] bytes; k_scale, v_scale: [num_pages][Hkv][S] fp32;
+ *   every pointer 16-byte aligned.  Page page_ids[i] of the source is written to the same
+ *   page of the destination; other pages are untouched.  An id outside [0, num_pages) is
+ *   skipped and flags SRKV_EFLAG_PAGE_RANGE.
+ */
+srkv_status srkv_quantize_kv_fp8(const srkv_config* cfg, const void* k_cache,
+                                 const void* v_cache, int64_t num_pages,
+                                 const int32_t* page_ids, int32_t n_pages, void* k_fp8,
+                                 void* v_fp8, float* k_scale, float* v_scale,
+                                 int32_t* error_flags, srkv_stream stream);
+
+/*
  * Scoring and top-k ("Overall Solution": inner product of the current query with each
  * representation vector, keep the topK closest).  For every request r and kv head h:
  * sel[r][h][0..nsel[r][h]) = the selected candidate blocks of (r, h), ascending; dense
@@ -240,6 +263,27 @@ srkv_status srkv_retrieval_decode_tiered(const srkv_config* cfg, const void* q,
                                          int32_t kmax, int32_t* nsel, void* out, void* workspace,
                                          size_t workspace_bytes, int32_t* error_flags,
                                          srkv_stream stream);
+
+/*
+ * srkv_retrieval_decode over compressed pages (srkv_quantize_kv_fp8): the attended K and V
+ * values are code x scale of the E4M3 caches, widened to fp16 (exactly) for the tensor-core
+ * products, with fp32 accumulation as in the bf16 decode.  The selection comes from `reps`,
+ * the representation vectors of the full-precision keys (built by srkv_build_block_reps
+ * before the pages are compressed), so it is the selection the bf16 call makes.
+ *   cfg->dtype = SRKV_BF16 (the query and the output), head_dim 128, group <= 8, else
+ *   SRKV_ERR_UNSUPPORTED.  k_fp8, v_fp8: [num_pages][Hkv][S][d] bytes; k_scale, v_scale:
+ *   [num_pages][Hkv][S] fp32; all 16-byte aligned.  Other arguments, ownership, paths (one
+ *   kernel for small batches, else three) and errors: srkv_retrieval_decode.
+ */
+srkv_status srkv_retrieval_decode_fp8(const srkv_config* cfg, const void* q, const void* k_fp8,
+                                      const void* v_fp8, const float* k_scale,
+                                      const float* v_scale, const float* reps,
+                                      int64_t num_pages, const int32_t* block_table,
+                                      int32_t max_blocks, const int32_t* seq_lens,
+                                      const int32_t* prompt_lens, int32_t batch, int32_t* sel,
+                                      int32_t kmax, int32_t* nsel, void* out, void* workspace,
+                                      size_t workspace_bytes, int32_t* error_flags,
+                                      srkv_stream stream);
 
 /*
  * Number of kernels one srkv_retrieval_decode call with these arguments launches on the
