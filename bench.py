@@ -71,6 +71,19 @@ WORKLOADS["offload-65536"] = (
     "pages in a pinned host pool, initial and window pages in HBM)",
     65536)
 OFFLOAD_WORKLOADS = ("offload-65536",)
+# Compressed pages: the same caches as E4M3 codes with one fp32 scale per row (vectors and
+# selection from the bf16 keys, at prefill).
+WORKLOADS["fp8-65536"] = (
+    WORKLOADS["llama8b-65536"][0],
+    "fp8-llama8b-layer-65536 (batch 1, 32/8 heads, d 128, top-k 0.2, 5% planted, shuffled "
+    "pages; K/V as E4M3 codes with fp32 row scales, bf16 q/out)",
+    65536)
+WORKLOADS["fp8-dense-vs-sparse-p0.2"] = (
+    WORKLOADS["dense-vs-sparse-p0.2"][0],
+    "fp8-dense-vs-sparse-4x131072 (batch 4, 32/8 heads, d 128, top-k 0.2, 3% planted, shuffled "
+    "pages; K/V as E4M3 codes with fp32 row scales, bf16 q/out)",
+    131072)
+FP8_WORKLOADS = ("fp8-65536", "fp8-dense-vs-sparse-p0.2")
 DEFAULT_WORKLOAD = "llama8b-65536"
 WORKLOAD = WORKLOADS[DEFAULT_WORKLOAD][1]
 FALLBACK_HBM = 6800.0
@@ -205,9 +218,9 @@ def attended_tokens(L: int, sel, INIT: int, LOCAL: int, S: int = 128) -> tuple[i
     return base + extra, len(blocks)
 
 
-def unique_kv_bytes(case, sel, nsel, S: int = 128) -> int:
+def unique_kv_bytes(case, sel, nsel, S: int = 128, row_bytes: int | None = None) -> int:
     """K/V bytes of the distinct (physical page, kv head, row) triples the step attends: a
-    page shared by several requests counts once."""
+    page shared by several requests counts once.  row_bytes: bytes of one K (or V) row."""
     cfg = case.cfg
     d, Hkv = cfg["head_dim"], cfg["num_kv_heads"]
     INIT, LOCAL = cfg["init_tokens"], cfg["local_tokens"]
@@ -232,7 +245,7 @@ def unique_kv_bytes(case, sel, nsel, S: int = 128) -> int:
                     masks[key] = masks.get(key, 0) | (((1 << (e - b * S)) - 1) ^ ((1 << (t - b * S)) - 1))
                     t = e
     rows = sum(bin(m).count("1") for m in masks.values())
-    return rows * 2 * d * case.k_cache.element_size()
+    return rows * 2 * (row_bytes if row_bytes is not None else d * case.k_cache.element_size())
 
 
 # ---- our arm --------------------------------------------------------------------------------
@@ -253,6 +266,20 @@ class Layer:
         self.buf = srkv.DecodeBuffers(c.cfg, c.batch, c.max_blocks, c.num_pages, device=device)
         self.srkv = srkv
         self.k_host = self.v_host = None  # the host pool of the offload workload
+        self.k_scale = self.v_scale = None  # row scales of compressed pages
+
+    def to_fp8(self):
+        """Compresses every page (srkv_quantize_kv_fp8) and drops the bf16 caches."""
+        c, b = self.case, self.buf
+        dev = c.k_cache.device
+        ids = torch.arange(c.num_pages, dtype=torch.int32, device=dev)
+        k8 = torch.empty(c.k_cache.shape, dtype=torch.uint8, device=dev)
+        v8 = torch.empty_like(k8)
+        self.k_scale = torch.empty(c.k_cache.shape[:3], dtype=torch.float32, device=dev)
+        self.v_scale = torch.empty_like(self.k_scale)
+        self.srkv.quantize_kv_fp8(c.cfg, c.k_cache, c.v_cache, ids, k8, v8, self.k_scale,
+                                  self.v_scale, b.error_flags)
+        c.k_cache, c.v_cache = k8, v8
 
     def to_host(self, dev_ids, host_ids, new_id):
         """Moves pages host_ids into a pinned host pool: the device pool keeps dev_ids (in that
@@ -277,6 +304,12 @@ class Layer:
         """One decode step: srkv_retrieval_decode (score + top-k, then split + combine), or
         srkv_retrieval_decode_tiered when pages live in a host pool."""
         c, b = self.case, self.buf
+        if self.k_scale is not None:
+            self.srkv.retrieval_decode_fp8(c.cfg, c.q, c.k_cache, c.v_cache, self.k_scale,
+                                           self.v_scale, b.reps, c.block_table, c.seq_lens,
+                                           c.prompt_lens, b.sel, b.nsel, b.out, b.workspace,
+                                           b.error_flags)
+            return
         if self.k_host is not None:
             self.srkv.retrieval_decode_tiered(c.cfg, c.q, c.k_cache, c.v_cache, self.k_host,
                                               self.v_host, b.reps, c.block_table, c.seq_lens,
@@ -295,13 +328,15 @@ class Layer:
         sel, nsel = b.sel.cpu().numpy(), b.nsel.cpu().numpy()
         L = c.seq_lens.cpu().numpy()
         from block_sparse_retrieval_gb300 import srkv
+        # bytes of one attended K (or V) row: bf16 values, or E4M3 codes and a fp32 scale
+        row = d * 2 if self.k_scale is None else d + 4
         kv = pages = n_cand = 0
         for r in range(c.batch):
             n_cand += srkv.num_candidates(cfg, int(L[r])) * Hkv
             for h in range(Hkv):
                 toks, pg = attended_tokens(int(L[r]), sel[r, h, :nsel[r, h]],
                                            cfg["init_tokens"], cfg["local_tokens"])
-                kv += toks * 2 * d * 2
+                kv += toks * 2 * row
                 pages += pg
         qo = c.batch * Hq * d * 2
         score = n_cand * (d * 4 + 4) + qo + int(nsel.sum()) * 4 + nsel.size * 4
@@ -315,7 +350,7 @@ class Layer:
                     blocks = sel[r, h, :nsel[r, h]]
                     host_kv += int((bt[r, blocks] >= P_dev).sum()) * 128 * d * 2 * 2
         return {"score": score, "decode": decode, "kv": kv, "total": score + decode,
-                "kv_unique": unique_kv_bytes(c, sel, nsel), "host_kv": host_kv}
+                "kv_unique": unique_kv_bytes(c, sel, nsel, row_bytes=row), "host_kv": host_kv}
 
 
 def capture(fn, stream):
@@ -357,6 +392,10 @@ def run_ours(args, world, rank, local):
     rep_ms = sum(ev[2 * i].elapsed_time(ev[2 * i + 1]) for i in range(len(layers)))
     if wl in OFFLOAD_WORKLOADS:
         offload_layers(layers)
+    if wl in FP8_WORKLOADS:
+        for ly in layers:
+            ly.to_fp8()
+        torch.cuda.synchronize()
 
     for ly in layers:                        # the step must run clean before it is timed
         ly.step()
@@ -430,7 +469,8 @@ def run_ours(args, world, rank, local):
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": "steps/s", "n_gpus": world,
         "steps": K, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5),
-        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "e4m3 K/V with fp32 row scales, bf16 q/out" if wl in FP8_WORKLOADS else "bf16",
         "data": "synthetic (seeded N(0,1) q/K/V, 5% planted blocks, shuffled pages)",
         "config": {"workload": WORKLOADS[wl][1], "global_batch": world * layers[0].case.batch,
                    "seq_len": WORKLOADS[wl][2], "parallelism": f"replicas x{world}",
