@@ -564,38 +564,61 @@ def time_append(dev, cfg, n: int = 200) -> dict:
 
 
 def run_e2e(layers, K, world, dev) -> dict:
-    """The same steps through the public entry point with host buffers: each step copies
-    its query and lengths from pinned host memory, runs srkv_retrieval_decode and reads the
-    output back."""
-    from block_sparse_retrieval_gb300 import srkv
-    host = []
+    """The same steps through the public entry point with host buffers, as a serving loop
+    runs them: each step copies its query and lengths from pinned host memory (one packed
+    copy), runs the decode and reads the output back into pinned memory, the three replayed
+    from a CUDA graph per layer, then waits for the result on the host."""
+    steps = []
     for ly in layers:
-        c = ly.case
-        host.append(dict(q=c.q.cpu().pin_memory(), L=c.seq_lens.cpu().pin_memory(),
-                         P=c.prompt_lens.cpu().pin_memory(),
-                         out=torch.empty_like(ly.buf.out, device="cpu").pin_memory()))
-    h2d = host[0]["q"].nbytes + host[0]["L"].nbytes + host[0]["P"].nbytes
-    d2h = host[0]["out"].nbytes
+        c, b = ly.case, ly.buf
+        qb = c.q.numel() * c.q.element_size()
+        nb = c.seq_lens.numel() * 4
+        host = torch.empty(qb + 2 * nb, dtype=torch.uint8).pin_memory()
+        host[:qb].copy_(c.q.cpu().contiguous().view(-1).view(torch.uint8))
+        host[qb:qb + nb].copy_(c.seq_lens.cpu().view(torch.uint8))
+        host[qb + nb:].copy_(c.prompt_lens.cpu().view(torch.uint8))
+        packed = torch.empty_like(host, device=dev)
+        # the layer reads its query and lengths from the packed device buffer
+        c.q = packed[:qb].view(c.q.dtype).view(c.q.shape)
+        c.seq_lens = packed[qb:qb + nb].view(torch.int32)
+        c.prompt_lens = packed[qb + nb:].view(torch.int32)
+        out = torch.empty_like(b.out, device="cpu").pin_memory()
+        steps.append(dict(ly=ly, host=host, packed=packed, out=out))
+    h2d = steps[0]["host"].nbytes
+    d2h = steps[0]["out"].nbytes
+    stream = torch.cuda.Stream(dev)
+    stream.wait_stream(torch.cuda.current_stream())
+    graphs = []
+    with torch.cuda.stream(stream):
+        for st in steps:
+            st["packed"].copy_(st["host"], non_blocking=True)
+            st["ly"].step()
+            st["out"].copy_(st["ly"].buf.out, non_blocking=True)
+        stream.synchronize()
+        for st in steps:
+            def one(st=st):
+                st["packed"].copy_(st["host"], non_blocking=True)
+                st["ly"].step()
+                st["out"].copy_(st["ly"].buf.out, non_blocking=True)
+            graphs.append(capture(one, stream))
+    torch.cuda.synchronize()
 
     def step(i):
-        ly, hb = layers[i % len(layers)], host[i % len(layers)]
-        c, b = ly.case, ly.buf
-        c.q.copy_(hb["q"], non_blocking=True)
-        c.seq_lens.copy_(hb["L"], non_blocking=True)
-        c.prompt_lens.copy_(hb["P"], non_blocking=True)
-        ly.step()
-        hb["out"].copy_(b.out, non_blocking=True)
-        torch.cuda.current_stream().synchronize()
+        graphs[i % len(graphs)].replay()
+        stream.synchronize()
 
-    for i in range(3):
-        step(i)
-    barrier(world)
-    t0 = time.perf_counter()
-    for i in range(K):
-        step(i)
-    dt = max_over_ranks(time.perf_counter() - t0, world, dev)
+    with torch.cuda.stream(stream):
+        for i in range(3):
+            step(i)
+        barrier(world)
+        t0 = time.perf_counter()
+        for i in range(K):
+            step(i)
+        dt = max_over_ranks(time.perf_counter() - t0, world, dev)
     return {"value": round(world * K / dt, 2), "unit": "steps/s", "h2d_bytes_per_step": h2d,
-            "d2h_bytes_per_step": d2h, "steps": K}
+            "d2h_bytes_per_step": d2h, "steps": K,
+            "how": "per step: packed pinned-host copy of q and lengths, the decode call, copy of "
+                   "the output to pinned host memory (one CUDA graph), host synchronize"}
 
 
 # ---- the oracle on the host --------------------------------------------------------------------
