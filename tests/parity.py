@@ -83,6 +83,22 @@ def check_selection(case, gpu_sel: np.ndarray, gpu_nsel: np.ndarray, ref: dict, 
     return exact
 
 
+# Two GPU decode paths over the same selection differ only in how the attended pages are
+# split into partials (fp32 sums in another order) and in the rounding of the output: a few
+# units in the last place of the output's dtype.  Much tighter than the method's tolerance
+# against the oracle, so that a lost or doubled partial (an error of the size of the output
+# itself, ~1e-2 here) cannot hide inside it.
+SAME_TOL = {synth.BF16: (1e-3, 1e-2), synth.F32: (1e-6, 1e-5)}
+
+
+def check_same(case, got: np.ndarray, want: np.ndarray):
+    atol, rtol = SAME_TOL[case.cfg["dtype"]]
+    err = np.abs(got - want)
+    bad = err > atol + rtol * np.abs(want)
+    assert not bad.any(), f"{bad.sum()} elements off between paths, max err {err.max():.3e}"
+    return float(err.max())
+
+
 def check_out(case, got: np.ndarray, want: np.ndarray, units=None):
     atol, rtol = TOL[case.cfg["dtype"]]
     G = case.cfg["num_q_heads"] // case.cfg["num_kv_heads"]

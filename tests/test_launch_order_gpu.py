@@ -6,7 +6,7 @@ import pytest
 import torch
 
 from block_sparse_retrieval_gb300 import srkv, synth
-from parity import check_out, gpu_select
+from parity import check_same, gpu_select
 
 pytestmark = pytest.mark.gpu
 
@@ -46,7 +46,7 @@ def test_inputs_written_just_before_the_call_are_read(name):
     assert int(got.error_flags.item()) == 0
     assert np.array_equal(got.sel.cpu().numpy(), want.sel.cpu().numpy())
     assert np.array_equal(got.nsel.cpu().numpy(), want.nsel.cpu().numpy())
-    check_out(case, got.out.float().cpu().numpy(), want.out.float().cpu().numpy())
+    check_same(case, got.out.float().cpu().numpy(), want.out.float().cpu().numpy())
     # and not the old query's result
     old = decode(case, reps, case.q, case.seq_lens)
     torch.cuda.synchronize()

@@ -10,7 +10,7 @@ import pytest
 import torch
 
 from block_sparse_retrieval_gb300 import srkv, synth
-from parity import check_out, check_selection, gpu_select, oracle_ref
+from parity import check_out, check_same, check_selection, gpu_select, oracle_ref
 
 pytestmark = pytest.mark.gpu
 
@@ -106,7 +106,7 @@ def test_offloaded_candidates_match_device_pages(name):
     else:
         # one kernel: CTAs take kept blocks from a shared pool, so the partials' split
         # depends on timing; equal up to rounding
-        check_out(case, got, want)
+        check_same(case, got, want)
     ref = oracle_ref(case, kmax=dev.kmax)
     exact = check_selection(case, tie.sel.cpu().numpy(), tie.nsel.cpu().numpy(), ref)
     if exact == units:
@@ -119,7 +119,7 @@ def test_random_pages_on_host_including_window():
     to_host = np.random.default_rng(3).random(case.num_pages) < 0.5
     dev, tie = run_both(case, to_host)
     assert np.array_equal(dev.sel.cpu().numpy(), tie.sel.cpu().numpy())
-    check_out(case, tie.out.float().cpu().numpy(), dev.out.float().cpu().numpy())
+    check_same(case, tie.out.float().cpu().numpy(), dev.out.float().cpu().numpy())
 
 
 def test_all_pages_on_host_split_path():
@@ -131,7 +131,7 @@ def test_all_pages_on_host_split_path():
     if srkv.retrieval_decode_launches(case.cfg, case.batch, case.max_blocks) == 3:
         assert np.array_equal(tie.out.float().cpu().numpy(), dev.out.float().cpu().numpy())
     else:
-        check_out(case, tie.out.float().cpu().numpy(), dev.out.float().cpu().numpy())
+        check_same(case, tie.out.float().cpu().numpy(), dev.out.float().cpu().numpy())
 
 
 def test_host_pool_arguments_are_checked():

@@ -9,7 +9,7 @@ import torch
 
 import oracle
 from block_sparse_retrieval_gb300 import srkv, synth
-from parity import check_out, check_selection, gpu_decode, gpu_select, oracle_ref
+from parity import check_out, check_same, check_selection, gpu_decode, gpu_select, oracle_ref
 
 pytestmark = pytest.mark.gpu
 
@@ -103,8 +103,7 @@ def check_fused_step(case, buf, ref, exact_score_topk, units=None):
     # spreads the initial and window pages over fewer CTAs (the scoring CTAs hold the other
     # SMs), so the partials split at other pages: equal up to rounding, not to the bit.
     again = gpu_decode(case, buf, fsel, fnsel)
-    if units is None:
-        check_out(case, got, again)
+    check_same(case, got, again)
     n_units = len(units) if units else case.batch * case.cfg["num_kv_heads"]
     if exact == n_units:
         check_out(case, got, ref["out"], units)
