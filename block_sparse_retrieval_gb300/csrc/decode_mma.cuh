@@ -287,23 +287,23 @@ __device__ __forceinline__ void store_partial(float* accp, float* mlp, const Sof
             make_float4(st.acc[k4][1], st.acc[k4][3], st.acc[k4 + 1][1], st.acc[k4 + 1][3]);
     }
   } else {
-  // values 4k..4k+3 of a lane sit at 4 consecutive d (d_of): 16-byte stores
+    // values 4k..4k+3 of a lane sit at 4 consecutive d (d_of): 16-byte stores
 #pragma unroll
-  for (int k4 = 0; k4 < C::MT; k4 += 4) {
-    const int da = d_of<D>(ln.g, k4), db = d_of<D>(ln.g, C::MT + k4);
-    if (h0 < G) {
-      *reinterpret_cast<float4*>(accp + h0 * D + da) = make_float4(
-          st.acc[k4][0], st.acc[k4 + 1][0], st.acc[k4 + 2][0], st.acc[k4 + 3][0]);
-      *reinterpret_cast<float4*>(accp + h0 * D + db) = make_float4(
-          st.acc[k4][2], st.acc[k4 + 1][2], st.acc[k4 + 2][2], st.acc[k4 + 3][2]);
+    for (int k4 = 0; k4 < C::MT; k4 += 4) {
+      const int da = d_of<D>(ln.g, k4), db = d_of<D>(ln.g, C::MT + k4);
+      if (h0 < G) {
+        *reinterpret_cast<float4*>(accp + h0 * D + da) = make_float4(
+            st.acc[k4][0], st.acc[k4 + 1][0], st.acc[k4 + 2][0], st.acc[k4 + 3][0]);
+        *reinterpret_cast<float4*>(accp + h0 * D + db) = make_float4(
+            st.acc[k4][2], st.acc[k4 + 1][2], st.acc[k4 + 2][2], st.acc[k4 + 3][2]);
+      }
+      if (h1 < G) {
+        *reinterpret_cast<float4*>(accp + h1 * D + da) = make_float4(
+            st.acc[k4][1], st.acc[k4 + 1][1], st.acc[k4 + 2][1], st.acc[k4 + 3][1]);
+        *reinterpret_cast<float4*>(accp + h1 * D + db) = make_float4(
+            st.acc[k4][3], st.acc[k4 + 1][3], st.acc[k4 + 2][3], st.acc[k4 + 3][3]);
+      }
     }
-    if (h1 < G) {
-      *reinterpret_cast<float4*>(accp + h1 * D + da) = make_float4(
-          st.acc[k4][1], st.acc[k4 + 1][1], st.acc[k4 + 2][1], st.acc[k4 + 3][1]);
-      *reinterpret_cast<float4*>(accp + h1 * D + db) = make_float4(
-          st.acc[k4][3], st.acc[k4 + 1][3], st.acc[k4 + 2][3], st.acc[k4 + 3][3]);
-    }
-  }
   }
   if (ln.g == 0) {
     if (h0 < G) {
@@ -407,17 +407,17 @@ __device__ __forceinline__ void consumer_loop(const DecodeArgs& a, unsigned char
         }
       } else {
 #pragma unroll
-      for (int j = 0; j < C::KJ; ++j) {
-        if (ln.g < a.G) {
-          const int4 v = lds128(q + ((size_t)ln.g * D + 32 * j + 8 * ln.t) * 2);
-          qb[j][0] = v.x;
-          qb[j][1] = v.y;
-          qb[j][2] = v.z;
-          qb[j][3] = v.w;
-        } else {
-          qb[j][0] = qb[j][1] = qb[j][2] = qb[j][3] = 0u;
+        for (int j = 0; j < C::KJ; ++j) {
+          if (ln.g < a.G) {
+            const int4 v = lds128(q + ((size_t)ln.g * D + 32 * j + 8 * ln.t) * 2);
+            qb[j][0] = v.x;
+            qb[j][1] = v.y;
+            qb[j][2] = v.z;
+            qb[j][3] = v.w;
+          } else {
+            qb[j][0] = qb[j][1] = qb[j][2] = qb[j][3] = 0u;
+          }
         }
-      }
       }
     }
     if (row0 < inf.hi && row0 + 16 > inf.lo) {
@@ -450,12 +450,12 @@ __device__ __forceinline__ void consumer_loop(const DecodeArgs& a, unsigned char
         sacc[3] *= kb;
       } else {
 #pragma unroll
-      for (int j = 0; j < C::KJ; ++j) {
-        const int4 k0 = lds128(k + swz(ra, 4 * j + ln.t));
-        const int4 k1 = lds128(k + swz(rb, 4 * j + ln.t));
-        mma_16816(sacc, k0.x, k1.x, k0.y, k1.y, qb[j][0], qb[j][1]);
-        mma_16816(sacc, k0.z, k1.z, k0.w, k1.w, qb[j][2], qb[j][3]);
-      }
+        for (int j = 0; j < C::KJ; ++j) {
+          const int4 k0 = lds128(k + swz(ra, 4 * j + ln.t));
+          const int4 k1 = lds128(k + swz(rb, 4 * j + ln.t));
+          mma_16816(sacc, k0.x, k1.x, k0.y, k1.y, qb[j][0], qb[j][1]);
+          mma_16816(sacc, k0.z, k1.z, k0.w, k1.w, qb[j][2], qb[j][3]);
+        }
       }
       // ---- mask, online softmax (log2 domain)
       const bool va = ra >= inf.lo && ra < inf.hi && (ra < inf.ie || ra >= inf.ws);
@@ -527,7 +527,8 @@ __device__ __forceinline__ void consumer_loop(const DecodeArgs& a, unsigned char
         for (int i = 0; i < C::MT; ++i) {
           const int wi = i >> 1, bo = 2 * (i & 1);
           // bytes (token a, d0), (token b, d0), (token a, d1), (token b, d1)
-          const uint32_t sel = (uint32_t)(bo | ((4 + bo) << 4) | ((bo + 1) << 8) | ((5 + bo) << 12));
+          const uint32_t sel =
+              (uint32_t)(bo | ((4 + bo) << 4) | ((bo + 1) << 8) | ((5 + bo) << 12));
           const uint32_t x01 = __byte_perm(word(vq[0], wi), word(vq[1], wi), sel);
           const uint32_t x23 = __byte_perm(word(vq[2], wi), word(vq[3], wi), sel);
           const uint32_t a0 = mul_f16x2(e4m3x2_to_f16x2(x01), sc01);
@@ -537,31 +538,30 @@ __device__ __forceinline__ void consumer_loop(const DecodeArgs& a, unsigned char
           mma_16816_f16(st.acc[i], a0, a1, a2, a3, b0, b1);
         }
       } else {
-      int4 vt[4][C::NCH];
-
+        int4 vt[4][C::NCH];
 #pragma unroll
-      for (int x = 0; x < 4; ++x) {
-        const bool in = trow[x] >= inf.lo && trow[x] < inf.hi;
+        for (int x = 0; x < 4; ++x) {
+          const bool in = trow[x] >= inf.lo && trow[x] < inf.hi;
 #pragma unroll
-        for (int c = 0; c < C::NCH; ++c)
-          vt[x][c] = in ? lds128(v + swz(trow[x], ln.g + 8 * c))
-                        : make_int4(0, 0, 0, 0);
-      }
+          for (int c = 0; c < C::NCH; ++c)
+            vt[x][c] = in ? lds128(v + swz(trow[x], ln.g + 8 * c))
+                          : make_int4(0, 0, 0, 0);
+        }
 #pragma unroll
-      for (int i = 0; i < C::MT; ++i) {
-        const int v0 = i, v1 = C::MT + i;  // value indices of rows g and g+8
-        const int c0 = v0 >> 3, e0 = v0 & 7, c1 = v1 >> 3, e1 = v1 & 7;
-        const uint32_t sel0 = (e0 & 1) ? 0x7632u : 0x5410u;
-        const uint32_t sel1 = (e1 & 1) ? 0x7632u : 0x5410u;
-        auto word = [](const int4& x, int w) -> uint32_t {
-          return (uint32_t)(w == 0 ? x.x : w == 1 ? x.y : w == 2 ? x.z : x.w);
-        };
-        const uint32_t a0 = __byte_perm(word(vt[0][c0], e0 >> 1), word(vt[1][c0], e0 >> 1), sel0);
-        const uint32_t a1 = __byte_perm(word(vt[0][c1], e1 >> 1), word(vt[1][c1], e1 >> 1), sel1);
-        const uint32_t a2 = __byte_perm(word(vt[2][c0], e0 >> 1), word(vt[3][c0], e0 >> 1), sel0);
-        const uint32_t a3 = __byte_perm(word(vt[2][c1], e1 >> 1), word(vt[3][c1], e1 >> 1), sel1);
-        mma_16816(st.acc[i], a0, a1, a2, a3, b0, b1);
-      }
+        for (int i = 0; i < C::MT; ++i) {
+          const int v0 = i, v1 = C::MT + i;  // value indices of rows g and g+8
+          const int c0 = v0 >> 3, e0 = v0 & 7, c1 = v1 >> 3, e1 = v1 & 7;
+          const uint32_t sel0 = (e0 & 1) ? 0x7632u : 0x5410u;
+          const uint32_t sel1 = (e1 & 1) ? 0x7632u : 0x5410u;
+          auto word = [](const int4& x, int w) -> uint32_t {
+            return (uint32_t)(w == 0 ? x.x : w == 1 ? x.y : w == 2 ? x.z : x.w);
+          };
+          const uint32_t a0 = __byte_perm(word(vt[0][c0], e0 >> 1), word(vt[1][c0], e0 >> 1), sel0);
+          const uint32_t a1 = __byte_perm(word(vt[0][c1], e1 >> 1), word(vt[1][c1], e1 >> 1), sel1);
+          const uint32_t a2 = __byte_perm(word(vt[2][c0], e0 >> 1), word(vt[3][c0], e0 >> 1), sel0);
+          const uint32_t a3 = __byte_perm(word(vt[2][c1], e1 >> 1), word(vt[3][c1], e1 >> 1), sel1);
+          mma_16816(st.acc[i], a0, a1, a2, a3, b0, b1);
+        }
       }
     }
     // release the stage

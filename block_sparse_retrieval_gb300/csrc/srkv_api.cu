@@ -395,7 +395,8 @@ srkv_status srkv_retrieval_decode_tiered(const srkv_config* cfg, const void* q,
         (void)cudaGetLastError();
         return SRKV_ERR_INVALID_ARG;
       }
-      if (at.type == cudaMemoryTypeUnregistered || !at.devicePointer) return SRKV_ERR_INVALID_ARG;
+      if (at.type == cudaMemoryTypeUnregistered || !at.devicePointer)
+        return SRKV_ERR_INVALID_ARG;
       hp[i] = at.devicePointer;
     }
     k_host = hp[0];
