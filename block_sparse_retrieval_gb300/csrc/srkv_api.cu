@@ -403,8 +403,8 @@ srkv_status srkv_retrieval_decode_tiered(const srkv_config* cfg, const void* q,
     v_host = hp[1];
   }
   return retrieval_decode(cfg, q, k_cache, v_cache, num_pages, k_host, v_host, num_host_pages,
-                          nullptr, nullptr, reps, block_table, max_blocks, seq_lens, prompt_lens, batch, sel, kmax,
-                          nsel, out, workspace, workspace_bytes, error_flags,
+                          nullptr, nullptr, reps, block_table, max_blocks, seq_lens, prompt_lens,
+                          batch, sel, kmax, nsel, out, workspace, workspace_bytes, error_flags,
                           (cudaStream_t)stream);
 }
 
