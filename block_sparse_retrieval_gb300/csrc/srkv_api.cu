@@ -427,6 +427,11 @@ srkv_status srkv_retrieval_decode_fp8(const srkv_config* cfg, const void* q, con
                           (cudaStream_t)stream);
 }
 
+srkv_status srkv_selftest_wait_timeout(int32_t* error_flags, srkv_stream stream) {
+  if (!error_flags) return SRKV_ERR_INVALID_ARG;
+  return cuda_status(launch_wait_timeout_selftest(error_flags, (cudaStream_t)stream));
+}
+
 // Scratch of srkv_sparse_paged_decode_noalloc: one array per device that loads the library.
 static __device__ __align__(256) unsigned char g_noalloc_workspace[SRKV_NOALLOC_WORKSPACE_BYTES];
 static std::atomic<void*> g_noalloc_address[128];

@@ -481,6 +481,7 @@ cudaError_t launch_block_reps(const srkv_config& cfg, const void* k_cache, int64
 // CTAs of the scoring grid (clusters of up to 8 per (request, kv head) unit).
 int64_t score_topk_ctas(const srkv_config& cfg, int32_t max_blocks, int32_t batch);
 
+cudaError_t launch_wait_timeout_selftest(int32_t* error_flags, cudaStream_t stream);
 cudaError_t launch_quantize_fp8(const srkv_config& cfg, const void* k_src, const void* v_src,
                                 int64_t num_pages, const int32_t* page_ids, int32_t n_pages,
                                 void* k8, void* v8, float* k_scale, float* v_scale,

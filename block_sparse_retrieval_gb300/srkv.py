@@ -30,7 +30,7 @@ EXPORTS = ("srkv_default_config", "srkv_status_string", "srkv_topk_count",
            "srkv_retrieval_decode", "srkv_sparse_paged_decode_noalloc",
            "srkv_retrieval_decode_launches", "srkv_append_kv",
            "srkv_retrieval_decode_tiered", "srkv_quantize_kv_fp8",
-           "srkv_retrieval_decode_fp8")
+           "srkv_retrieval_decode_fp8", "srkv_selftest_wait_timeout")
 NOALLOC_WORKSPACE_BYTES = 16 << 20
 
 
@@ -96,6 +96,8 @@ def load() -> ctypes.CDLL:
     lib.srkv_retrieval_decode_fp8.argtypes = [ctypes.POINTER(Config), _P, _P, _P, _P, _P, _P,
                                               _I64, _P, _I32, _P, _P, _I32, _P, _I32, _P, _P,
                                               _P, _SZ, _P, _P]
+    lib.srkv_selftest_wait_timeout.argtypes = [_P, _P]
+    lib.srkv_selftest_wait_timeout.restype = ctypes.c_int
     for name in ("srkv_build_block_reps", "srkv_score_topk", "srkv_sparse_paged_decode",
                  "srkv_retrieval_decode", "srkv_sparse_paged_decode_noalloc",
                  "srkv_retrieval_decode_tiered", "srkv_quantize_kv_fp8",
@@ -330,6 +332,13 @@ def retrieval_decode_fp8(cfg: Mapping, q: torch.Tensor, k_fp8: torch.Tensor,
         workspace.numel() * workspace.element_size(),
         _dev(error_flags, "error_flags", torch.int32), _stream(stream)),
         "srkv_retrieval_decode_fp8")
+
+
+def selftest_wait_timeout(error_flags: torch.Tensor, stream=None) -> None:
+    """srkv_selftest_wait_timeout: a kernel whose bounded waits never see an arrival; they
+    give up after their limit and set SRKV_EFLAG_TIMEOUT in error_flags."""
+    _check(load().srkv_selftest_wait_timeout(_dev(error_flags, "error_flags", torch.int32),
+                                             _stream(stream)), "srkv_selftest_wait_timeout")
 
 
 def sparse_paged_decode_noalloc(cfg: Mapping, q: torch.Tensor, k_cache: torch.Tensor,

@@ -323,6 +323,17 @@ srkv_status srkv_sparse_paged_decode_noalloc(const srkv_config* cfg, const void*
                                              const int32_t* nsel, void* out,
                                              int32_t* error_flags, srkv_stream stream);
 
+/*
+ * Self-test of the bounded on-chip waits (no counterpart on the pages; a service of this
+ * library).  Every wait of the decode kernels gives up after a limit of 2 s, sets
+ * SRKV_EFLAG_TIMEOUT and lets its kernel finish instead of hanging.  This call launches one
+ * kernel (a cluster of 2 CTAs) whose waits, one on a CTA-scope and one on a cluster-scope
+ * mbarrier, have no arrival at all: both run to their limit, OR SRKV_EFLAG_TIMEOUT into
+ * *error_flags (device memory) and return, about 4 s after the kernel starts.  Nothing else
+ * is read or written, nothing faults, and the context stays usable.
+ */
+srkv_status srkv_selftest_wait_timeout(int32_t* error_flags, srkv_stream stream);
+
 #ifdef __cplusplus
 }
 #endif
