@@ -232,7 +232,96 @@ __global__ void __launch_bounds__(kWarps * 32) combine_kernel(const DecodeArgs a
 
 }  // namespace
 
+// Batches with more units than split CTAs: a unit's positions meet few CTAs (a handful of
+// partials per head), so one CTA per unit with one warp per query head (G warps) merges them,
+// 16 partials per round of loads, with no cross-warp merge; the unit's offsets are found once
+// per CTA.  (The kernel above spends 4 warps per head, for heads with many partials.)
+template <typename TOut, int D>
+__global__ void __launch_bounds__(256) combine_unit_kernel(const DecodeArgs a) {
+  constexpr int V = D / 32;
+  const int lane = threadIdx.x & 31, j = threadIdx.x >> 5;  // warp j: query head j
+  const int32_t G = a.G;
+  const int32_t u = blockIdx.x;
+  const int32_t r = u / a.Hkv, h = u % a.Hkv;
+  griddep_wait();
+  const ListParts la = stored_parts(a, kListA, 0, u);
+  const ListParts lb = stored_parts(a, kListB, a.lay.bank, u);
+  if (j >= G) return;
+  const float* accw = reinterpret_cast<const float*>(a.ws + a.lay.acc);
+  const float* mlw = reinterpret_cast<const float*>(a.ws + a.lay.ml);
+  const int32_t total = la.parts + lb.parts;
+  float m_run = -INFINITY, l_run = 0.f, acc[V];
+#pragma unroll
+  for (int e = 0; e < V; ++e) acc[e] = 0.f;
+  for (int32_t p0 = 0; p0 < total; p0 += kPartsPerWarp) {
+    const int32_t p = p0 + lane;
+    int64_t slot = -1;
+    if (lane < kPartsPerWarp && p < total)
+      slot = p < la.parts ? part_slot(la, p) : part_slot(lb, p - la.parts);
+    float m = -INFINITY, l = 0.f;
+    if (slot >= 0) {
+      m = mlw[(slot * G + j) * 2];
+      l = mlw[(slot * G + j) * 2 + 1];
+    }
+    float xs[kPartsPerWarp][V];
+#pragma unroll
+    for (int t = 0; t < kPartsPerWarp; ++t) {
+      const int64_t st = __shfl_sync(0xffffffffu, slot, t);
+#pragma unroll
+      for (int e = 0; e < V; ++e) xs[t][e] = 0.f;
+      if (st >= 0) {
+        const float* src = accw + (st * G + j) * D + lane * V;
+        if constexpr (V == 4) {
+          const float4 v4 = *reinterpret_cast<const float4*>(src);
+          xs[t][0] = v4.x;
+          xs[t][1] = v4.y;
+          xs[t][2] = v4.z;
+          xs[t][3] = v4.w;
+        } else {
+          const float2 v2 = *reinterpret_cast<const float2*>(src);
+          xs[t][0] = v2.x;
+          xs[t][1] = v2.y;
+        }
+      }
+    }
+    float mx = m;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+    mx = fmaxf(mx, m_run);
+    if (mx == -INFINITY) continue;
+    const float f_run = fast_exp2(m_run - mx);
+    const float w = fast_exp2(m - mx);  // 0 for an absent part
+    float lw = w * l;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) lw += __shfl_xor_sync(0xffffffffu, lw, o);
+    l_run = l_run * f_run + lw;
+    m_run = mx;
+#pragma unroll
+    for (int e = 0; e < V; ++e) acc[e] *= f_run;
+#pragma unroll
+    for (int t = 0; t < kPartsPerWarp; ++t) {
+      const float wt = __shfl_sync(0xffffffffu, w, t);
+#pragma unroll
+      for (int e = 0; e < V; ++e) acc[e] += wt * xs[t][e];
+    }
+  }
+  float v[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+  for (int e = 0; e < V; ++e) v[e] = l_run > 0.f ? acc[e] / l_run : 0.f;
+  TOut* out = static_cast<TOut*>(a.out) + ((int64_t)r * a.Hq + (int64_t)h * G + j) * D + lane * V;
+  store_vec<TOut>(out, v, V);
+}
+
 cudaError_t launch_combine(const DecodeArgs& a, int32_t dtype, cudaStream_t stream) {
+  const int64_t units = (int64_t)a.batch * a.Hkv;
+  if (units > kDirectUnits && units >= a.ctas && a.G <= 8) {
+    const dim3 grid((unsigned)units), block((unsigned)(a.G * 32));
+    if (dtype == SRKV_BF16)
+      return a.d == 128 ? launch_pdl(combine_unit_kernel<__nv_bfloat16, 128>, grid, block, 0, stream, a)
+                        : launch_pdl(combine_unit_kernel<__nv_bfloat16, 64>, grid, block, 0, stream, a);
+    return a.d == 128 ? launch_pdl(combine_unit_kernel<float, 128>, grid, block, 0, stream, a)
+                      : launch_pdl(combine_unit_kernel<float, 64>, grid, block, 0, stream, a);
+  }
   const int64_t heads = (int64_t)a.batch * a.Hkv * a.G;
   if (heads == 0) return cudaSuccess;
   if (heads > INT32_MAX) return cudaErrorInvalidValue;

@@ -55,6 +55,11 @@ def small_cases():
                                      num_kv_heads=2, head_dim=128, init_tokens=1000,
                                      local_tokens=1500, topk_percent=0.3, dense_boundary=0,
                                      seed=18, device=DEV),
+        # more (request, kv head) units than split CTAs: the per-unit combine
+        "many-units": lambda: mk(seq_lens=[1500 + 97 * i for i in range(20)], num_q_heads=32,
+                                 num_kv_heads=8, head_dim=128, init_tokens=256,
+                                 local_tokens=512, topk_percent=0.2, dense_boundary=0, seed=20,
+                                 device=DEV),
         "dense-boundary": lambda: mk(seq_lens=[9000, 12000, 12000], prompt_lens=[9000, 11999, 12000],
                                      num_q_heads=8, num_kv_heads=2, head_dim=128,
                                      init_tokens=1024, local_tokens=2048, topk_percent=0.2,
