@@ -246,10 +246,22 @@ int32_t cluster_for(int64_t nmax) {
   return (int32_t)(c < 1 ? 1 : (c > 8 ? 8 : c));
 }
 
+// CTAs per unit for a batch of `units`: cluster_for, but when at least two CTAs per unit
+// still fit in half of a 152-SM GPU, no more than that, so that the other half of the SMs
+// streams the initial and window pages while the scoring runs (a scoring CTA keeps its SM
+// to itself); each CTA then scores more candidates, in more rounds of loads.
+int32_t cluster_for_batch(int64_t nmax, int64_t units) {
+  const int32_t c = cluster_for(nmax);
+  const int64_t fit = 76 / (units > 0 ? units : 1);
+  if (fit >= 2 && fit < c) return (int32_t)fit;
+  return c;
+}
+
 }  // namespace
 
 int64_t score_topk_ctas(const srkv_config& cfg, int32_t max_blocks, int32_t batch) {
-  return (int64_t)batch * cfg.num_kv_heads * cluster_for(max_candidates(cfg, max_blocks));
+  const int64_t units = (int64_t)batch * cfg.num_kv_heads;
+  return units * cluster_for_batch(max_candidates(cfg, max_blocks), units);
 }
 
 cudaError_t launch_score_topk(const srkv_config& cfg, const void* q, const float* reps,
@@ -282,7 +294,7 @@ cudaError_t launch_score_topk(const srkv_config& cfg, const void* q, const float
   const int64_t nmax = max_candidates(cfg, max_blocks);
   if (nmax > INT32_MAX) return cudaErrorInvalidValue;
   a.nmax = (int32_t)nmax;
-  const int32_t cluster = cluster_for(nmax);
+  const int32_t cluster = cluster_for_batch(nmax, units);
   if ((int64_t)units * cluster > INT32_MAX) return cudaErrorInvalidValue;
   if (cfg.dtype == SRKV_BF16)
     return cfg.head_dim == 128 ? launch<__nv_bfloat16, 128>(a, units, cluster, stream)
