@@ -252,8 +252,11 @@ int32_t cluster_for(int64_t nmax) {
 // to itself); each CTA then scores more candidates, in more rounds of loads.
 int32_t cluster_for_batch(int64_t nmax, int64_t units) {
   const int32_t c = cluster_for(nmax);
-  const int64_t fit = 76 / (units > 0 ? units : 1);
+  const int64_t u = units > 0 ? units : 1;
+  const int64_t fit = 76 / u;
   if (fit >= 2 && fit < c) return (int32_t)fit;
+  // larger batches: no more CTAs than one wave on 152 SMs needs (at least one per unit)
+  if (fit < 2 && u * c > 152) return (int32_t)(152 / u > 1 ? 152 / u : 1);
   return c;
 }
 
