@@ -194,8 +194,7 @@ srkv_status retrieval_decode(const srkv_config* cfg, const void* q, const void* 
   // The scoring kernel, then the decode, which streams list A while the scoring finishes
   // and knows the selection counts it will write from the lengths.  A scoring CTA keeps its
   // SM to itself, so list A goes to the decode CTAs that find an SM free at once (the grid
-  // is scheduled in block order), list B to those that start before the scoring ends (all
-  // but one SM per (request, kv head) cluster, whose leader selects last).
+  // is scheduled in block order); list B, read once the selection exists, to every CTA.
   a.prompt_lens = prompt_lens;
   a.reps = reps;
   a.sel_out = sel;
@@ -206,11 +205,7 @@ srkv_status retrieval_decode(const srkv_config* cfg, const void* q, const void* 
   if (cluster > 0) return cuda_status(launch_fused(a, cluster, s));
   const bool early = mma_split_supported(*cfg);
   const int64_t scoring = score_topk_ctas(*cfg, max_blocks, batch);
-  const int64_t leaders = (int64_t)batch * cfg->num_kv_heads;
-  if (early && 2 * scoring <= a.ctas) {
-    a.ctas_a = a.ctas - (int32_t)scoring;
-    a.ctas_b = a.ctas - (int32_t)leaders;
-  }
+  if (early && 2 * scoring <= a.ctas) a.ctas_a = a.ctas - (int32_t)scoring;
   if (launch_score_topk(*cfg, q, reps, num_pages + num_host_pages, block_table, max_blocks,
                         seq_lens, prompt_lens, batch, sel, kmax, nsel, error_flags, s) !=
       cudaSuccess)
