@@ -249,12 +249,14 @@ int32_t cluster_for(int64_t nmax) {
 // CTAs per unit for a batch of `units`: cluster_for, but when at least two CTAs per unit
 // still fit in half of a 152-SM GPU, no more than that, so that the other half of the SMs
 // streams the initial and window pages while the scoring runs (a scoring CTA keeps its SM
-// to itself); each CTA then scores more candidates, in more rounds of loads.
-int32_t cluster_for_batch(int64_t nmax, int64_t units) {
+// to itself); each CTA then scores more candidates, in more rounds of loads.  Not for
+// compressed (E4M3) pages: their consumers are bound by the code conversions rather than
+// by bytes, so half of the SMs cannot take all of list A, and the scoring keeps its grid.
+int32_t cluster_for_batch(int64_t nmax, int64_t units, bool compressed) {
   const int32_t c = cluster_for(nmax);
   const int64_t u = units > 0 ? units : 1;
   const int64_t fit = 76 / u;
-  if (fit >= 2 && fit < c) return (int32_t)fit;
+  if (fit >= 2 && fit < c) return compressed ? c : (int32_t)fit;
   // larger batches: no more CTAs than one wave on 152 SMs needs (at least one per unit)
   if (fit < 2 && u * c > 152) return (int32_t)(152 / u > 1 ? 152 / u : 1);
   return c;
@@ -262,9 +264,10 @@ int32_t cluster_for_batch(int64_t nmax, int64_t units) {
 
 }  // namespace
 
-int64_t score_topk_ctas(const srkv_config& cfg, int32_t max_blocks, int32_t batch) {
+int64_t score_topk_ctas(const srkv_config& cfg, int32_t max_blocks, int32_t batch,
+                        bool compressed) {
   const int64_t units = (int64_t)batch * cfg.num_kv_heads;
-  return units * cluster_for_batch(max_candidates(cfg, max_blocks), units);
+  return units * cluster_for_batch(max_candidates(cfg, max_blocks), units, compressed);
 }
 
 cudaError_t launch_score_topk(const srkv_config& cfg, const void* q, const float* reps,
@@ -272,7 +275,7 @@ cudaError_t launch_score_topk(const srkv_config& cfg, const void* q, const float
                               int32_t max_blocks, const int32_t* seq_lens,
                               const int32_t* prompt_lens, int32_t batch, int32_t* sel,
                               int32_t kmax, int32_t* nsel, int32_t* error_flags,
-                              cudaStream_t stream) {
+                              cudaStream_t stream, bool compressed) {
   ScoreArgs a;
   a.q = q;
   a.reps = reps;
@@ -297,7 +300,7 @@ cudaError_t launch_score_topk(const srkv_config& cfg, const void* q, const float
   const int64_t nmax = max_candidates(cfg, max_blocks);
   if (nmax > INT32_MAX) return cudaErrorInvalidValue;
   a.nmax = (int32_t)nmax;
-  const int32_t cluster = cluster_for_batch(nmax, units);
+  const int32_t cluster = cluster_for_batch(nmax, units, compressed);
   if ((int64_t)units * cluster > INT32_MAX) return cudaErrorInvalidValue;
   if (cfg.dtype == SRKV_BF16)
     return cfg.head_dim == 128 ? launch<__nv_bfloat16, 128>(a, units, cluster, stream)

@@ -199,16 +199,17 @@ srkv_status retrieval_decode(const srkv_config* cfg, const void* q, const void* 
   a.reps = reps;
   a.sel_out = sel;
   a.nsel_out = nsel;
+  const bool compressed = k_scale != nullptr;
   // A batch small enough for one cluster per unit to be resident: one kernel does it all.
   const int32_t cluster =
-      fused_cluster_size(*cfg, batch * cfg->num_kv_heads, max_blocks, k_scale != nullptr);
+      fused_cluster_size(*cfg, batch * cfg->num_kv_heads, max_blocks, compressed);
   if (cluster > 0) return cuda_status(launch_fused(a, cluster, s));
   const bool early = mma_split_supported(*cfg);
-  const int64_t scoring = score_topk_ctas(*cfg, max_blocks, batch);
+  const int64_t scoring = score_topk_ctas(*cfg, max_blocks, batch, compressed);
   if (early && 2 * scoring <= a.ctas) a.ctas_a = a.ctas - (int32_t)scoring;
   if (launch_score_topk(*cfg, q, reps, num_pages + num_host_pages, block_table, max_blocks,
-                        seq_lens, prompt_lens, batch, sel, kmax, nsel, error_flags, s) !=
-      cudaSuccess)
+                        seq_lens, prompt_lens, batch, sel, kmax, nsel, error_flags, s,
+                        compressed) != cudaSuccess)
     return SRKV_ERR_CUDA;
   return launch_decode(cfg, a, early ? 1 : 0, s);
 }

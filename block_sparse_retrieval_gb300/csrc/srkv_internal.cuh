@@ -478,8 +478,10 @@ cudaError_t launch_block_reps(const srkv_config& cfg, const void* k_cache, int64
                               const int32_t* page_ids, const int32_t* valid, int32_t n,
                               float* reps, int32_t* error_flags, cudaStream_t stream);
 
-// CTAs of the scoring grid (clusters of up to 8 per (request, kv head) unit).
-int64_t score_topk_ctas(const srkv_config& cfg, int32_t max_blocks, int32_t batch);
+// CTAs of the scoring grid (clusters of up to 8 per (request, kv head) unit); `compressed`:
+// the decode behind it reads E4M3 pages.
+int64_t score_topk_ctas(const srkv_config& cfg, int32_t max_blocks, int32_t batch,
+                        bool compressed = false);
 
 cudaError_t launch_wait_timeout_selftest(int32_t* error_flags, cudaStream_t stream);
 cudaError_t launch_quantize_fp8(const srkv_config& cfg, const void* k_src, const void* v_src,
@@ -497,7 +499,7 @@ cudaError_t launch_score_topk(const srkv_config& cfg, const void* q, const float
                               int32_t max_blocks, const int32_t* seq_lens,
                               const int32_t* prompt_lens, int32_t batch, int32_t* sel,
                               int32_t kmax, int32_t* nsel, int32_t* error_flags,
-                              cudaStream_t stream);
+                              cudaStream_t stream, bool compressed = false);
 
 // Split phase on tensor cores (bf16, G <= 8, d in {64, 128}); grid = SM count.
 bool mma_split_supported(const srkv_config& cfg);

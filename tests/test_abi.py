@@ -114,6 +114,10 @@ def test_score_topk_argument_checks(lib):
     assert call(191) == 1                    # below srkv_kmax_bound (192)
     assert call(192, q=None) == 1
     assert call(-1) == 1
+    # keys and pages of every candidate stay on chip: 25 600 blocks at most
+    wide = lambda mb: lib.srkv_score_topk(ctypes.byref(c), fake, fake, 10, fake, mb, fake,
+                                          None, 1, fake, 1 << 20, fake, None, None)
+    assert wide(25601) == 2
 
 
 def test_build_reps_argument_checks(lib):

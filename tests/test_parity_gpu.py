@@ -9,7 +9,7 @@ import torch
 
 import oracle
 from block_sparse_retrieval_gb300 import srkv, synth
-from parity import check_out, check_same, check_selection, gpu_decode, gpu_select, oracle_ref
+from parity import check_fused_step, check_out, check_selection, gpu_decode, gpu_select, oracle_ref
 
 pytestmark = pytest.mark.gpu
 
@@ -89,30 +89,6 @@ def test_small_case_parity(name):
     assert int(buf.error_flags.item()) == 0
     check_out(case, out, ref["out"])
     check_fused_step(case, buf, ref, exact)
-
-
-def check_fused_step(case, buf, ref, exact_score_topk, units=None):
-    """srkv_retrieval_decode (scoring, then the decode behind it) against the oracle."""
-    fused = srkv.DecodeBuffers(case.cfg, case.batch, case.max_blocks, case.num_pages,
-                               device=case.q.device)
-    fused.reps.copy_(buf.reps)
-    srkv.retrieval_decode(case.cfg, case.q, case.k_cache, case.v_cache, fused.reps,
-                          case.block_table, case.seq_lens, case.prompt_lens, fused.sel,
-                          fused.nsel, fused.out, fused.workspace, fused.error_flags)
-    torch.cuda.synchronize()
-    assert int(fused.error_flags.item()) == 0
-    fsel, fnsel = fused.sel.cpu().numpy(), fused.nsel.cpu().numpy()
-    exact = check_selection(case, fsel, fnsel, ref, units)
-    got = fused.out.float().cpu().numpy()
-    # The split decode fed the fused selection computes the same sums, but the fused call
-    # spreads the initial and window pages over fewer CTAs (the scoring CTAs hold the other
-    # SMs), so the partials split at other pages: equal up to rounding, not to the bit.
-    again = gpu_decode(case, buf, fsel, fnsel)
-    check_same(case, got, again)
-    n_units = len(units) if units else case.batch * case.cfg["num_kv_heads"]
-    if exact == n_units:
-        check_out(case, got, ref["out"], units)
-    return exact
 
 
 def test_empty_request_gives_zero_output():
