@@ -117,6 +117,19 @@ __global__ void __maxnreg__(128) fused_decode_kernel(const DecodeArgs a,
   griddep_wait();
   griddep_launch_dependents();
 
+  // The group's query values (thread e < D, a consumer: element e of its G heads), loaded
+  // ahead of the lengths: they do not depend on them, and the scoring waits for both
+  constexpr int kMaxG = 8;  // the MMA decode's largest group
+  static_assert(D <= kSelThreads, "one consumer thread per query element");
+  float qv[kMaxG] = {};
+  if (tid < D) {
+    const __nv_bfloat16* qp = static_cast<const __nv_bfloat16*>(a.q) +
+                              ((int64_t)r * a.Hq + (int64_t)h * a.G) * D + tid;
+#pragma unroll
+    for (int j = 0; j < kMaxG; ++j)
+      if (j < a.G) qv[j] = __bfloat162float(qp[(int64_t)j * D]);
+  }
+
   // The unit's sizes: candidates n, kept k (what the selection will write), list A length.
   const int32_t L_in = a.seq_lens[r];
   const int32_t prompt = a.prompt_lens ? a.prompt_lens[r] : L_in;
@@ -234,12 +247,12 @@ __global__ void __maxnreg__(128) fused_decode_kernel(const DecodeArgs a,
     const int32_t s_lo = share_begin((int32_t)crank, n, (int32_t)CS);
     const int32_t s_hi = share_begin((int32_t)crank + 1, n, (int32_t)CS);
     for (int32_t i = s_lo + tid; i < s_hi; i += kSelThreads) share[i - s_lo] = bt_r[b_lo + i];
-    const __nv_bfloat16* qp =
-        static_cast<const __nv_bfloat16*>(a.q) + ((int64_t)r * a.Hq + (int64_t)h * a.G) * D;
-    for (int e = tid; e < D; e += kSelThreads) {
+    if (tid < D) {  // the group query sum, in head order
       float s = 0.f;
-      for (int j = 0; j < a.G; ++j) s += __bfloat162float(qp[(int64_t)j * D + e]);
-      qbar[e] = s;
+#pragma unroll
+      for (int j = 0; j < kMaxG; ++j)
+        if (j < a.G) s += qv[j];
+      qbar[tid] = s;
     }
     bar();
     // 2. scores into the leader (keys, pages, top-8-bit histogram)
