@@ -38,7 +38,7 @@ template <int D, bool F8 = false>
 struct FusedCfg {
   using C = Cfg<D, F8>;
   // after the ring (every CTA)
-  // keys_ready, list_ready, parts_ready
+  // keys_ready, list_ready, parts_ready, scored
   static constexpr size_t kOffBars = (C::kSmem + 15) & ~size_t(15);
   static constexpr size_t kOffQbar = kOffBars + 4 * sizeof(uint64_t);
   static constexpr size_t kOffShare = kOffQbar + sizeof(float) * D;
@@ -60,6 +60,12 @@ struct FusedCfg {
   static_assert(kSelEnd <= C::kOffV, "selection state fits in the K ring");
   static_assert(kPartEnd <= C::kOffQ, "partials fit in the V ring");
   static_assert(kSmemAlloc <= 232448, "shared memory opt-in limit");
+  // Stages of list A a streaming CTA copies before its own scoring loads have returned.
+  // Those loads queue behind the copies already issued (a full ring is ~17 MB over the
+  // cluster's SMs), so the rest of the ring waits for them; two stages still keep the
+  // consumers fed once they turn to the pages.
+  static constexpr int kEarlyStages = 2;
+  static_assert(kEarlyStages < C::kStages, "the ring is never filled before the scoring");
 };
 
 // Share [q*n/S, (q+1)*n/S) of n items for part q of S (n * S < 2^31: n <= 1024 kept or
@@ -79,6 +85,7 @@ __global__ void __maxnreg__(128) fused_decode_kernel(const DecodeArgs a,
   uint64_t* keys_ready = reinterpret_cast<uint64_t*>(smem + F::kOffBars);
   uint64_t* list_ready = keys_ready + 1;
   uint64_t* parts_ready = keys_ready + 2;
+  uint64_t* scored = keys_ready + 3;
   float* qbar = reinterpret_cast<float*>(smem + F::kOffQbar);
   int32_t* share = reinterpret_cast<int32_t*>(smem + F::kOffShare);
   uint32_t* keys = reinterpret_cast<uint32_t*>(smem + F::kOffKeys);    // leader
@@ -103,6 +110,7 @@ __global__ void __maxnreg__(128) fused_decode_kernel(const DecodeArgs a,
     mbar_init(keys_ready, kMaxCand);            // one per candidate, the rest at once
     mbar_init(list_ready, 1);                   // the leader, once the pool is laid out
     mbar_init(parts_ready, 32u * (uint32_t)S);  // one per lane of a streaming CTA's warp 0
+    mbar_init(scored, kConsumerWarps);          // each consumer warp, its scores computed
     fence_mbar_init();
   }
   if (leader) {
@@ -151,11 +159,10 @@ __global__ void __maxnreg__(128) fused_decode_kernel(const DecodeArgs a,
       uint32_t eflags = 0;
       bool abort = false;
       int64_t it = 0, armed = 0;
-      // list A: 32 positions resolved at once, handed out in order, from the start: the
-      // streaming of list A, not the selection, is what the call waits for longest (the
-      // selection is ready ~2 µs before a CTA is through its list-A pages), so the copies are
-      // not held back for the scoring loads (that costs the scoring ~0.9 µs and gains the
-      // stream ~1.2 µs)
+      // list A: 32 positions resolved at once, handed out in order.  The first kEarlyStages
+      // copies go out at once; the rest of the ring waits for this CTA's scoring loads,
+      // which would otherwise return only after every copy ahead of them had landed (holding
+      // all of list A back costs the stream more than the scoring gains)
       for (int32_t j0 = a0; j0 < a1 && !abort; j0 += 32) {
         const int32_t cnt = min(32, a1 - j0);
         PageTask task;
@@ -169,6 +176,15 @@ __global__ void __maxnreg__(128) fused_decode_kernel(const DecodeArgs a,
           tl.hi = __shfl_sync(0xffffffffu, task.hi, l);
           tl.ie = __shfl_sync(0xffffffffu, task.ie, l);
           tl.ws = __shfl_sync(0xffffffffu, task.ws, l);
+          if (it == F::kEarlyStages) {  // the rest once this CTA's scores are in
+            bool ok = true;
+            if (lane == 0) ok = mbar_wait(scored, 0);
+            if (!__shfl_sync(0xffffffffu, ok, 0)) {
+              eflags |= SRKV_EFLAG_TIMEOUT;
+              abort = true;
+              break;
+            }
+          }
           issue_stage_warp<D, F8>(a, maps, smem, it, u, it == 0 ? kNewUnit : 0u, tl, armed, abort,
                               eflags, lane);
           ++it;
@@ -267,6 +283,7 @@ __global__ void __maxnreg__(128) fused_decode_kernel(const DecodeArgs a,
         },
         [&] { mbar_arrive_cluster(keys_ready, 0); });  // releases this lane's key, page, count
     if (!waited) cluster_wait();  // a warp without candidates
+    if (lane == 0) mbar_arrive(scored);
     if (lane == 0 && eflags) raise_flags(a.error_flags, eflags);
     // the arrivals the leader's barrier expects beyond the n candidates, at once
     if (leader && tid == 0 && n < kMaxCand)
