@@ -10,8 +10,8 @@
 //   * every CTA scores its share of the candidates (select.cuh: keys, page ids and the top-8-
 //     bit histogram go to the leader, CTA 0, through distributed shared memory);
 //   * meanwhile the other CTAs' producer warps stream their share of the initial and window
-//     pages (list A) into the stage ring (decode_mma.cuh): two stages at once, the rest once
-//     the CTA's own scores are in, then on through the selection;
+//     pages (list A) into the stage ring (decode_mma.cuh), through the scoring and the
+//     selection;
 //   * the leader selects (radix narrowing, ranked finish), writes sel / nsel, lays the kept
 //     blocks (page and block ids) out as a pool in its own shared memory and releases an
 //     mbarrier in every streaming CTA;
