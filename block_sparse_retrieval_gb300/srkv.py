@@ -174,11 +174,57 @@ def _check(status: int, where: str) -> None:
         raise SrkvError(status, where)
 
 
+def _shape(t: torch.Tensor | None, name: str, *dims) -> None:
+    """t (if given) has len(dims) dimensions of those sizes; None matches any size.  The
+    library sees only pointers, so a tensor of the wrong shape would be read or written out
+    of its bounds: the shapes are checked here, before anything is launched."""
+    if t is None:
+        return
+    if t.dim() != len(dims) or any(w is not None and g != w for g, w in zip(t.shape, dims)):
+        want = "[" + ", ".join("*" if w is None else str(w) for w in dims) + "]"
+        raise ValueError(f"{name} must have shape {want}, got {list(t.shape)}")
+
+
+def _rows(t: torch.Tensor, name: str, at_least: int) -> None:
+    if t.shape[0] < at_least:
+        raise ValueError(f"{name} needs at least {at_least} rows, got {t.shape[0]}")
+
+
+def _cache_dims(cfg: Mapping) -> tuple[int, int, int, int]:
+    return cfg["num_q_heads"], cfg["num_kv_heads"], cfg["block_size"], cfg["head_dim"]
+
+
+def _step_shapes(cfg: Mapping, q, k_cache, v_cache, block_table, seq_lens, prompt_lens, sel,
+                 nsel, out, reps=None, reps_rows: int = 0) -> tuple[int, int]:
+    """Shapes shared by the decode entry points; returns (batch, max_blocks)."""
+    Hq, Hkv, S, d = _cache_dims(cfg)
+    _shape(block_table, "block_table", None, None)
+    B, max_blocks = block_table.shape
+    _shape(q, "q", B, Hq, d)
+    _shape(k_cache, "k_cache", None, Hkv, S, d)
+    _shape(v_cache, "v_cache", k_cache.shape[0], Hkv, S, d)
+    _shape(seq_lens, "seq_lens", B)
+    _shape(prompt_lens, "prompt_lens", B)
+    _shape(sel, "sel", B, Hkv, None)
+    _shape(nsel, "nsel", B, Hkv)
+    _shape(out, "out", B, Hq, d)
+    if reps is not None:
+        _shape(reps, "reps", None, Hkv, d)
+        _rows(reps, "reps", reps_rows)
+    return B, max_blocks
+
+
 # ---- entry points --------------------------------------------------------------------------
 
 def build_block_reps(cfg: Mapping, k_cache: torch.Tensor, page_ids: torch.Tensor,
                      page_valid_tokens: torch.Tensor, reps: torch.Tensor,
                      error_flags: torch.Tensor | None = None, stream=None) -> None:
+    _, Hkv, S, d = _cache_dims(cfg)
+    _shape(k_cache, "k_cache", None, Hkv, S, d)
+    _shape(page_ids, "page_ids", None)
+    _shape(page_valid_tokens, "page_valid_tokens", page_ids.numel())
+    _shape(reps, "reps", None, Hkv, d)
+    _rows(reps, "reps", k_cache.shape[0])
     c = config(cfg)
     _check(load().srkv_build_block_reps(
         ctypes.byref(c), _dev(k_cache, "k_cache", _store_dtype(cfg)), k_cache.shape[0],
@@ -194,6 +240,16 @@ def append_kv(cfg: Mapping, k_new: torch.Tensor, v_new: torch.Tensor, k_cache: t
               stream=None) -> None:
     """Writes each request's new token (k_new, v_new: [B][Hkv][d]) at position seq_lens[r]
     and refreshes that page's representation vector; the caller then advances seq_lens."""
+    _, Hkv, S, d = _cache_dims(cfg)
+    _shape(block_table, "block_table", None, None)
+    B = block_table.shape[0]
+    _shape(k_new, "k_new", B, Hkv, d)
+    _shape(v_new, "v_new", B, Hkv, d)
+    _shape(k_cache, "k_cache", None, Hkv, S, d)
+    _shape(v_cache, "v_cache", k_cache.shape[0], Hkv, S, d)
+    _shape(seq_lens, "seq_lens", B)
+    _shape(reps, "reps", None, Hkv, d)
+    _rows(reps, "reps", k_cache.shape[0])
     c = config(cfg)
     st = _store_dtype(cfg)
     _check(load().srkv_append_kv(
@@ -209,8 +265,16 @@ def score_topk(cfg: Mapping, q: torch.Tensor, reps: torch.Tensor, block_table: t
                seq_lens: torch.Tensor, prompt_lens: torch.Tensor | None, sel: torch.Tensor,
                nsel: torch.Tensor, error_flags: torch.Tensor | None = None,
                stream=None) -> None:
-    c = config(cfg)
+    Hq, Hkv, _, d = _cache_dims(cfg)
+    _shape(block_table, "block_table", None, None)
     B, max_blocks = block_table.shape
+    _shape(q, "q", B, Hq, d)
+    _shape(reps, "reps", None, Hkv, d)
+    _shape(seq_lens, "seq_lens", B)
+    _shape(prompt_lens, "prompt_lens", B)
+    _shape(sel, "sel", B, Hkv, None)
+    _shape(nsel, "nsel", B, Hkv)
+    c = config(cfg)
     _check(load().srkv_score_topk(
         ctypes.byref(c), _dev(q, "q", _store_dtype(cfg)), _dev(reps, "reps", torch.float32),
         reps.shape[0], _dev(block_table, "block_table", torch.int32), max_blocks,
@@ -224,9 +288,10 @@ def sparse_paged_decode(cfg: Mapping, q: torch.Tensor, k_cache: torch.Tensor,
                         seq_lens: torch.Tensor, sel: torch.Tensor, nsel: torch.Tensor,
                         out: torch.Tensor, workspace: torch.Tensor,
                         error_flags: torch.Tensor | None = None, stream=None) -> None:
+    B, max_blocks = _step_shapes(cfg, q, k_cache, v_cache, block_table, seq_lens, None, sel,
+                                 nsel, out)
     c = config(cfg)
     dt = _store_dtype(cfg)
-    B, max_blocks = block_table.shape
     _check(load().srkv_sparse_paged_decode(
         ctypes.byref(c), _dev(q, "q", dt), _dev(k_cache, "k_cache", dt),
         _dev(v_cache, "v_cache", dt), k_cache.shape[0],
@@ -244,9 +309,10 @@ def retrieval_decode(cfg: Mapping, q: torch.Tensor, k_cache: torch.Tensor,
                      sel: torch.Tensor, nsel: torch.Tensor, out: torch.Tensor,
                      workspace: torch.Tensor, error_flags: torch.Tensor | None = None,
                      stream=None) -> None:
+    B, max_blocks = _step_shapes(cfg, q, k_cache, v_cache, block_table, seq_lens, prompt_lens,
+                                 sel, nsel, out, reps, k_cache.shape[0])
     c = config(cfg)
     dt = _store_dtype(cfg)
-    B, max_blocks = block_table.shape
     _check(load().srkv_retrieval_decode(
         ctypes.byref(c), _dev(q, "q", dt), _dev(k_cache, "k_cache", dt),
         _dev(v_cache, "v_cache", dt), _dev(reps, "reps", torch.float32), k_cache.shape[0],
@@ -279,10 +345,14 @@ def retrieval_decode_tiered(cfg: Mapping, q: torch.Tensor, k_cache: torch.Tensor
                             error_flags: torch.Tensor | None = None, stream=None) -> None:
     """srkv_retrieval_decode_tiered: page ids >= k_cache.shape[0] name pages of the pinned
     host pool k_host / v_host (page id - k_cache.shape[0])."""
+    _, Hkv, S, d = _cache_dims(cfg)
+    n_host = 0 if k_host is None else k_host.shape[0]
+    _shape(k_host, "k_host", None, Hkv, S, d)
+    _shape(v_host, "v_host", n_host, Hkv, S, d)
+    B, max_blocks = _step_shapes(cfg, q, k_cache, v_cache, block_table, seq_lens, prompt_lens,
+                                 sel, nsel, out, reps, k_cache.shape[0] + n_host)
     c = config(cfg)
     dt = _store_dtype(cfg)
-    B, max_blocks = block_table.shape
-    n_host = 0 if k_host is None else k_host.shape[0]
     _check(load().srkv_retrieval_decode_tiered(
         ctypes.byref(c), _dev(q, "q", dt), _dev(k_cache, "k_cache", dt),
         _dev(v_cache, "v_cache", dt), k_cache.shape[0], _host(k_host, "k_host", dt),
@@ -302,6 +372,15 @@ def quantize_kv_fp8(cfg: Mapping, k_cache: torch.Tensor, v_cache: torch.Tensor,
                     error_flags: torch.Tensor | None = None, stream=None) -> None:
     """srkv_quantize_kv_fp8: pages page_ids of the bf16 caches as E4M3 codes (uint8 tensors
     of the caches' shape) with one fp32 scale per (page, kv head, token) row."""
+    _, Hkv, S, d = _cache_dims(cfg)
+    _shape(k_cache, "k_cache", None, Hkv, S, d)
+    P = k_cache.shape[0]
+    _shape(v_cache, "v_cache", P, Hkv, S, d)
+    _shape(page_ids, "page_ids", None)
+    for t, name in ((k_fp8, "k_fp8"), (v_fp8, "v_fp8")):
+        _shape(t, name, P, Hkv, S, d)
+    for t, name in ((k_scale, "k_scale"), (v_scale, "v_scale")):
+        _shape(t, name, P, Hkv, S)
     c = config(cfg)
     _check(load().srkv_quantize_kv_fp8(
         ctypes.byref(c), _dev(k_cache, "k_cache", torch.bfloat16),
@@ -319,8 +398,12 @@ def retrieval_decode_fp8(cfg: Mapping, q: torch.Tensor, k_fp8: torch.Tensor,
                          out: torch.Tensor, workspace: torch.Tensor,
                          error_flags: torch.Tensor | None = None, stream=None) -> None:
     """srkv_retrieval_decode_fp8: the decode step over E4M3 pages (bf16 query and output)."""
+    _, Hkv, S, _ = _cache_dims(cfg)
+    B, max_blocks = _step_shapes(cfg, q, k_fp8, v_fp8, block_table, seq_lens, prompt_lens,
+                                 sel, nsel, out, reps, k_fp8.shape[0])
+    for t, name in ((k_scale, "k_scale"), (v_scale, "v_scale")):
+        _shape(t, name, k_fp8.shape[0], Hkv, S)
     c = config(cfg)
-    B, max_blocks = block_table.shape
     _check(load().srkv_retrieval_decode_fp8(
         ctypes.byref(c), _dev(q, "q", torch.bfloat16), _dev(k_fp8, "k_fp8", torch.uint8),
         _dev(v_fp8, "v_fp8", torch.uint8), _dev(k_scale, "k_scale", torch.float32),
@@ -347,9 +430,10 @@ def sparse_paged_decode_noalloc(cfg: Mapping, q: torch.Tensor, k_cache: torch.Te
                                 out: torch.Tensor, error_flags: torch.Tensor | None = None,
                                 stream=None) -> None:
     """srkv_sparse_paged_decode with the library's own static scratch (no workspace)."""
+    B, max_blocks = _step_shapes(cfg, q, k_cache, v_cache, block_table, seq_lens, None, sel,
+                                 nsel, out)
     c = config(cfg)
     dt = _store_dtype(cfg)
-    B, max_blocks = block_table.shape
     _check(load().srkv_sparse_paged_decode_noalloc(
         ctypes.byref(c), _dev(q, "q", dt), _dev(k_cache, "k_cache", dt),
         _dev(v_cache, "v_cache", dt), k_cache.shape[0],
