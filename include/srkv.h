@@ -178,7 +178,10 @@ srkv_status srkv_quantize_kv_fp8(const srkv_config* cfg, const void* k_cache,
  *   q: [B][Hq][d] (cfg dtype, 16-byte aligned); reps: [num_pages][Hkv][d] fp32 as written
  *   by srkv_build_block_reps for every page a candidate block maps to;
  *   prompt_lens may be NULL (then prompt = seq_len);
- *   kmax >= srkv_kmax_bound(cfg, max_blocks), else SRKV_ERR_INVALID_ARG.
+ *   kmax >= srkv_kmax_bound(cfg, max_blocks), else SRKV_ERR_INVALID_ARG;
+ *   max_blocks <= 25600 (3 276 800 tokens: the key and page of every candidate are held
+ *   on chip while a unit is selected), else SRKV_ERR_UNSUPPORTED.
+ * The selection is a function of the inputs alone: bitwise the same on every call.
  */
 srkv_status srkv_score_topk(const srkv_config* cfg, const void* q, const float* reps,
                             int64_t num_pages, const int32_t* block_table, int32_t max_blocks,
@@ -222,7 +225,11 @@ srkv_status srkv_sparse_paged_decode(const srkv_config* cfg, const void* q, cons
  *   group <= 8) runs as one kernel; otherwise the scoring kernel, the split decode (which
  *   streams the initial and window pages while the scoring runs) and the combine.  The first
  *   call for a configuration on a device queries the device (cluster residency); make it
- *   before any stream capture.
+ *   before any stream capture.  max_blocks <= 25600 as for srkv_score_topk.
+ *   Reproducibility: sel and nsel are bitwise the same on every call.  On the three-kernel
+ *   path (and in srkv_sparse_paged_decode) out is too; on the one-kernel path the CTAs of a
+ *   unit take kept blocks from a shared pool as their pages arrive, so the partial sums
+ *   split at pages that vary from call to call and out may differ in its last bits.
  */
 srkv_status srkv_retrieval_decode(const srkv_config* cfg, const void* q, const void* k_cache,
                                   const void* v_cache, const float* reps, int64_t num_pages,
