@@ -717,7 +717,7 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=8)
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--layers", type=int, default=None,
-                    help="rotated layer caches (default: enough to stream > 500 MB between uses)")
+                    help="rotated layer caches (default: 2 to 8, about 2 GB of K/V, far more than L2)")
     ap.add_argument("--workload", choices=list(WORKLOADS), default=DEFAULT_WORKLOAD)
     ap.add_argument("--e2e-steps", type=int, default=1000)
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
