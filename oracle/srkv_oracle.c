@@ -285,6 +285,9 @@ int oracle_unit(const oracle_cfg* c, const oracle_inputs* in, int32_t r, int32_t
       h >= Hkv)
     return ORACLE_BAD_ARG;
   if (c->dtype == 2 && (!in->k_scale || !in->v_scale)) return ORACLE_BAD_ARG;
+  /* R11: over compressed pages the selection comes from the full-precision keys' vectors,
+   * which this function does not have: the caller must pass it. */
+  if (c->dtype == 2 && !sel_in) return ORACLE_BAD_ARG;
   const int64_t G = Hq / Hkv;
   const int64_t L = in->seq_lens[r];
   const int64_t prompt = in->prompt_lens ? in->prompt_lens[r] : L;

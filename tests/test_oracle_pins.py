@@ -515,3 +515,24 @@ def test_e4m3_pages_accuracy_against_bf16():
             top = np.abs(o).max()
             assert e.max() <= 0.10 * top, (r, h, e.max(), top)
             assert e.mean() <= 0.025 * top, (r, h, e.mean(), top)
+
+
+def test_e4m3_decode_refuses_to_select_on_its_own():
+    """R11: over compressed pages the selection must come from the full-precision keys, which
+    the E4M3 decode does not see, so a call without a selection is refused instead of scoring
+    the dequantised keys."""
+    case = synth.make_case(seq_lens=[1500], num_q_heads=4, num_kv_heads=1, head_dim=128,
+                           init_tokens=256, local_tokens=512, topk_percent=0.2,
+                           dense_boundary=0, seed=24)
+    arr = synth.to_oracle_arrays(case)
+    kc, ks = oracle.quantize_e4m3(case.cfg, arr["k_cache"])
+    vc, vs = oracle.quantize_e4m3(case.cfg, arr["v_cache"])
+    with pytest.raises(ValueError):
+        oracle.decode(dict(case.cfg, dtype=2), arr["q"], kc, vc, arr["block_table"],
+                      arr["seq_lens"], arr["prompt_lens"], k_scale=ks, v_scale=vs)
+    ref = oracle.decode(case.cfg, arr["q"], arr["k_cache"], arr["v_cache"], arr["block_table"],
+                        arr["seq_lens"], arr["prompt_lens"])
+    got = oracle.decode(dict(case.cfg, dtype=2), arr["q"], kc, vc, arr["block_table"],
+                        arr["seq_lens"], arr["prompt_lens"], sel=ref["sel"], nsel=ref["nsel"],
+                        k_scale=ks, v_scale=vs)
+    assert np.isfinite(got["out"]).all()
