@@ -5,7 +5,7 @@
 #include <math.h>
 #include <stdint.h>
 
-#include <atomic>
+#include <mutex>
 
 #include "srkv_internal.cuh"
 
@@ -430,7 +430,66 @@ srkv_status srkv_selftest_wait_timeout(int32_t* error_flags, srkv_stream stream)
 
 // Scratch of srkv_sparse_paged_decode_noalloc: one array per device that loads the library.
 static __device__ __align__(256) unsigned char g_noalloc_workspace[SRKV_NOALLOC_WORKSPACE_BYTES];
-static std::atomic<void*> g_noalloc_address[128];
+
+// Where that array sits in the current context.  The address belongs to a context, not to a
+// device ordinal: after cudaDeviceReset (or under a context the caller created) the module is
+// loaded again and the array may move, so the cached address is keyed by the context's
+// process-unique id and looked up again whenever the current context differs.
+struct NoallocSlot {
+  unsigned long long ctx_id;
+  void* address;
+};
+static NoallocSlot g_noalloc_slot[128];
+static std::mutex g_noalloc_mu;
+
+using CtxGetCurrent = CUresult (*)(CUcontext*);
+using CtxGetId = CUresult (*)(CUcontext, unsigned long long*);
+
+// Process-unique id of the current context (false if there is none or it cannot be read).
+static bool current_ctx_id(unsigned long long* id) {
+  static CtxGetCurrent get_current = [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &q) !=
+            cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      p = nullptr;
+    return reinterpret_cast<CtxGetCurrent>(p);
+  }();
+  static CtxGetId get_id = [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &p, 12000, cudaEnableDefault, &q) !=
+            cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      p = nullptr;
+    return reinterpret_cast<CtxGetId>(p);
+  }();
+  CUcontext ctx = nullptr;
+  if (!get_current || !get_id || get_current(&ctx) != CUDA_SUCCESS || !ctx) return false;
+  return get_id(ctx, id) == CUDA_SUCCESS;
+}
+
+// The array's device address in the current context of device `dev`: cached, or looked up
+// with cudaGetSymbolAddress (which also brings up the device's primary context if no
+// context is current yet).  Null on failure.
+static void* noalloc_address(int dev) {
+  unsigned long long id = 0;
+  const bool have_id = current_ctx_id(&id);
+  std::lock_guard<std::mutex> lock(g_noalloc_mu);
+  NoallocSlot& slot = g_noalloc_slot[dev];
+  if (have_id && slot.address && slot.ctx_id == id) return slot.address;
+  void* ws = nullptr;
+  if (cudaGetSymbolAddress(&ws, g_noalloc_workspace) != cudaSuccess || !ws) {
+    (void)cudaGetLastError();
+    slot.address = nullptr;
+    return nullptr;
+  }
+  if (!current_ctx_id(&id)) return ws;  // no id to key it by: used for this call only
+  slot.ctx_id = id;
+  slot.address = ws;
+  return ws;
+}
 
 srkv_status srkv_sparse_paged_decode_noalloc(const srkv_config* cfg, const void* q,
                                              const void* k_cache, const void* v_cache,
@@ -441,12 +500,9 @@ srkv_status srkv_sparse_paged_decode_noalloc(const srkv_config* cfg, const void*
                                              int32_t* error_flags, srkv_stream stream) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 128) return SRKV_ERR_CUDA;
-  void* ws = g_noalloc_address[dev].load();
-  if (!ws) {  // once per device, with that device current: the array's device address
-    if (cudaGetSymbolAddress(&ws, g_noalloc_workspace) != cudaSuccess || !ws)
-      return SRKV_ERR_CUDA;
-    g_noalloc_address[dev].store(ws);
-  }
+  // once per context of the device, with it current: the array's device address
+  void* ws = noalloc_address(dev);
+  if (!ws) return SRKV_ERR_CUDA;
   DecodeArgs a;
   const srkv_status st = prepare_decode(cfg, q, k_cache, v_cache, num_pages, block_table,
                                         max_blocks, seq_lens, batch, sel, kmax, nsel, out, ws,

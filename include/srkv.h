@@ -313,7 +313,10 @@ int32_t srkv_retrieval_decode_launches(const srkv_config* cfg, int32_t batch, in
  *   - A batch whose decode needs more scratch than SRKV_NOALLOC_WORKSPACE_BYTES
  *     (srkv_decode_workspace_size) is rejected with SRKV_ERR_WORKSPACE before any launch.
  *   - The first call on a device looks up the array's device address (with that device
- *     current); make that first call before any stream capture.
+ *     current) and keeps it for the current CUDA context; a call made in another context of
+ *     the device (one the caller created, or the primary context brought up again after
+ *     cudaDeviceReset) looks it up again.  Make the first call in each context before any
+ *     stream capture.
  *   - Every call on a device shares the one array, and each call leaves its contents behind
  *     (nothing in it needs to start at zero: a call writes every value it reads).  Calls
  *     whose kernels overlap on the GPU (on different streams, without ordering between
