@@ -1,17 +1,23 @@
 """Benchmark of block-sparse retrieval decode on GB300.
 
 One step = one decode step of one layer through srkv_retrieval_decode: score + top-k of
-the offload blocks, then split-K sparse paged attention and its combine; one step of every
-rotated layer is captured in one CUDA graph, as a model's decode step would be.  The
-representation vectors are built once per page at prefill (as on the method's page: the
-store is written at prefill and read at decode) and reported separately under
-"prefill_reps".
+the offload blocks, then split-K sparse paged attention and its combine; steps of the rotated
+layers are captured in CUDA graphs, as a model's decode step would be.  The representation
+vectors are built once per page at prefill (as on the method's page: the store is written at
+prefill and read at decode) and reported separately under "prefill_reps".
 
 Workloads (--workload): the default, and the metric's, is one Llama-3-8B-shaped layer
 (batch 1, 32 q / 8 kv heads, d 128, bf16, 65536 cached tokens, init 1024, window 7192,
 top-k 20 %, 5 % planted blocks, shuffled 128-token pages); the others are a ragged batch of
 16 requests, batch 4 x 131072 at top-k 1.0 / 0.1 / 0.2 / 0.4, and 64 requests sharing a
-16384-token prefix.
+16384-token prefix.  The default run measures those too, under "workloads" (each over about
+--load-seconds of graph replays with its own clock record); --no-workloads skips them.
+
+Timing: exactly --steps steps (whole replays of a graph holding one step of every rotated
+layer, then a graph of the remaining steps) between barriers and device synchronizations,
+timed with CUDA events on the launching stream.  Around them, --load-seconds of replays
+before and after keep the GPU under the same load while nvidia-smi samples its clocks; their
+rate is reported as "sustained".
 
 L2: the step rotates over --layers layer caches (default: about 2 GB of K/V, 8 x 268 MB for
 the default workload; one block table and one set of lengths shared by all layers, as in a
@@ -377,104 +383,72 @@ def capture(fn, stream):
     return g
 
 
-def run_ours(args, world, rank, local):
-    dev = torch.device("cuda", local)
-    torch.cuda.set_device(dev)
-    peak, peak_kind = peaks()
-    # Same seed: the same page structure for every layer (one shared block table).  Enough
-    # layers for about 2 GB of K/V in the rotation (8 for the 65536-token layer).
-    wl = args.workload
+def build_layers(wl: str, n_layers, rank: int, dev):
+    """The rotated layer caches of a workload (prefill included): (layers, prefill record).
+    Same seed for every layer: one page structure and one block table shared by all."""
     first = Layer(1000 + 1000003 * rank, dev, workload=wl)
-    n_layers = args.layers
     if n_layers is None:
         layer_bytes = 2 * first.case.k_cache.numel() * first.case.k_cache.element_size()
         n_layers = max(2, min(8, -(-2_000_000_000 // layer_bytes)))
     layers = [first] + [Layer(1000 + 1000003 * rank, dev, shared=first.case, workload=wl)
                         for _ in range(n_layers - 1)]
-
-    # prefill: representation vectors of every page of every layer (timed separately)
-    ev = [torch.cuda.Event(enable_timing=True) for _ in range(2 * len(layers))]
+    # prefill: representation vectors of every page of every layer, one launch per layer,
+    # queued behind a short device sleep so that the events time the kernels, not the host
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
     for ly in layers:                        # warm the kernel once
         ly.prefill()
     torch.cuda.synchronize()
     rep_bytes = 0
-    for i, ly in enumerate(layers):
-        ev[2 * i].record()
+    torch.cuda._sleep(int(2e7))
+    ev[0].record()
+    for ly in layers:
         ly.prefill()
-        ev[2 * i + 1].record()
         c = ly.case
         rep_bytes += int(c.page_valid.sum()) * c.cfg["num_kv_heads"] * c.cfg["head_dim"] * 2 \
             + c.page_ids.numel() * c.cfg["num_kv_heads"] * c.cfg["head_dim"] * 4
+    ev[1].record()
     torch.cuda.synchronize()
-    rep_ms = sum(ev[2 * i].elapsed_time(ev[2 * i + 1]) for i in range(len(layers)))
+    rep_ms = ev[0].elapsed_time(ev[1])
     if wl in OFFLOAD_WORKLOADS:
         offload_layers(layers)
     if wl in FP8_WORKLOADS:
         for ly in layers:
             ly.to_fp8()
         torch.cuda.synchronize()
-
     for ly in layers:                        # the step must run clean before it is timed
         ly.step()
     torch.cuda.synchronize()
     flags = [int(ly.buf.error_flags.item()) for ly in layers]
     if any(flags):
         raise RuntimeError(f"device error flags {flags}")
-    step_bytes = [ly.step_bytes() for ly in layers]
+    prefill = {"kernel": "srkv_build_block_reps", "launches": len(layers),
+               "pages": sum(ly.case.page_ids.numel() for ly in layers),
+               "bytes": rep_bytes, "us": round(rep_ms * 1e3, 1),
+               "GB_s": round(rep_bytes / (rep_ms / 1e3) / 1e9, 1)}
+    return layers, prefill
 
-    # One CUDA graph holds one step of every layer, as a model's decode step would.
+
+def step_graphs(layers, K: int, stream):
+    """CUDA graphs that together run exactly K steps: `full` holds one step of every rotated
+    layer (replayed K // R times), `tail` the first K % R of them (None if K % R == 0)."""
     R = len(layers)
-    stream = torch.cuda.Stream(device=dev)
-    stream.wait_stream(torch.cuda.current_stream())
     with torch.cuda.stream(stream):
-        graph = capture(lambda: [ly.step() for ly in layers], stream)
+        full = capture(lambda: [ly.step() for ly in layers], stream)
+        tail = capture(lambda: [ly.step() for ly in layers[:K % R]], stream) if K % R else None
     torch.cuda.synchronize()
+    return full, tail
 
-    with torch.cuda.stream(stream):
-        for i in range(max(1, -(-args.warmup // R))):
-            graph.replay()
-    torch.cuda.synchronize()
 
-    K = -(-args.steps // R) * R               # whole replays of the R-layer graph
-    n_rep = K // R
-
-    def timed_region():
-        ev = [torch.cuda.Event(enable_timing=True) for _ in range(n_rep + 1)]
-        barrier(world)
-        torch.cuda.synchronize()
-        with ClockSampler(local) as clocks:
-            with torch.cuda.stream(stream):
-                torch.cuda._sleep(int(2e7))      # let the host queue ahead of the device
-                for i in range(n_rep):
-                    ev[i].record(stream)
-                    graph.replay()
-                ev[n_rep].record(stream)
-            torch.cuda.synchronize()
-        barrier(world)
-        return ev, clocks.summary()
-
-    ev, clk = timed_region()
-    # A region whose clocks disqualify it is measured once more; every rank takes the same
-    # path (the decision is the maximum over ranks), and the line keeps the first record.
-    why = clocks_rejected(clk)
-    remeasured = None
-    if max_over_ranks(1.0 if why else 0.0, world, dev) > 0:
-        remeasured = {"first_clocks": clk, "reason": why or "clocks of another rank"}
-        ev, clk = timed_region()
-    replay_ms = [ev[i].elapsed_time(ev[i + 1]) for i in range(n_rep)]
-    total_ms = max_over_ranks(ev[0].elapsed_time(ev[n_rep]), world, dev)
-    ms_per_step = total_ms / K
-    value = world * K / (total_ms / 1e3)
-
+def roofline_of(layers, step_bytes, call_ms: float, peak: float, peak_kind: str, wl: str,
+                dev) -> dict:
     avg_step_bytes = statistics.mean(sb["total"] for sb in step_bytes)
     avg_unique = statistics.mean(sb["total"] - sb["kv"] + sb["kv_unique"] for sb in step_bytes)
-    call_ms = statistics.mean(replay_ms) / R
     achieved = avg_step_bytes / (call_ms / 1e3) / 1e9
-    traffic = committed_traffic() if wl == DEFAULT_WORKLOAD else None
     roofline = {"kernel": None, "bound": "hbm", "achieved": round(achieved, 1), "peak": peak,
                 "unit": "GB/s", "frac": round(achieved / peak, 4), "peak_kind": peak_kind,
                 "bytes_per_launch": int(avg_step_bytes), "unique_bytes_per_launch": int(avg_unique),
-                "us_per_launch": round(call_ms * 1e3, 3), "traffic": traffic}
+                "unique_frac": round(avg_unique / (call_ms / 1e3) / 1e9 / peak, 4),
+                "us_per_launch": round(call_ms * 1e3, 3), "traffic": None}
     if wl in OFFLOAD_WORKLOADS:
         # bound by the host pool's reads over the chip-to-chip link
         host = statistics.mean(sb["host_kv"] for sb in step_bytes)
@@ -483,18 +457,96 @@ def run_ours(args, world, rank, local):
                          "peak": c2c, "frac": round(host / (call_ms / 1e3) / 1e9 / c2c, 4),
                          "peak_kind": "measured in this run: pinned host to device copy",
                          "bytes_per_launch": int(host),
-                         "unique_bytes_per_launch": int(host),
+                         "unique_bytes_per_launch": int(host), "unique_frac": None,
                          "device_bytes_per_launch": int(avg_step_bytes - host),
                          "device_GB_s": round((avg_step_bytes - host) / (call_ms / 1e3) / 1e9, 1)})
     c0 = layers[0].case
     launches = layers[0].srkv.retrieval_decode_launches(c0.cfg, c0.batch, c0.max_blocks)
-    kernel_desc = ("srkv_retrieval_decode call: one kernel (a thread-block cluster per "
-                   "(request, kv head) scores, selects and attends)" if launches == 1 else
-                   "srkv_retrieval_decode call: score_topk, split-K decode and combine kernels, "
-                   "overlapped by programmatic launch")
+    roofline["kernel"] = (
+        "srkv_retrieval_decode call: one kernel (a thread-block cluster per (request, kv head) "
+        "scores, selects and attends)" if launches == 1 else
+        "srkv_retrieval_decode call: score_topk, split-K decode and combine kernels, "
+        "overlapped by programmatic launch")
+    return roofline
 
-    e2e = run_e2e(layers, min(K, args.e2e_steps), world, dev)
+
+def replay_for(full, stream, seconds: float, est_ms: float) -> tuple[int, float]:
+    """Replays `full` for about `seconds` of device time; returns (replays, ms)."""
+    n = max(1, int(seconds * 1e3 / max(est_ms, 1e-3)))
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for _ in range(n):
+            full.replay()
+        e1.record(stream)
+    torch.cuda.synchronize()
+    return n, e0.elapsed_time(e1)
+
+
+def run_ours(args, world, rank, local):
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    peak, peak_kind = peaks()
+    wl = args.workload
+    layers, prefill = build_layers(wl, args.layers, rank, dev)
+    R = len(layers)
+    step_bytes = [ly.step_bytes() for ly in layers]
+    stream = torch.cuda.Stream(device=dev)
+    stream.wait_stream(torch.cuda.current_stream())
+    K = args.steps
+    full, tail = step_graphs(layers, K, stream)
+    with torch.cuda.stream(stream):           # W warm-up steps (whole replays, at least W)
+        for _ in range(max(1, -(-args.warmup // R))):
+            full.replay()
+    torch.cuda.synchronize()
+    _, probe_ms = replay_for(full, stream, 0.0, 1.0)
+    est_step_ms = probe_ms / R
+
+    def timed_region():
+        """Exactly K steps between barriers and synchronizations, inside a window of load
+        (about 0.15 s of replays before and after) over which nvidia-smi samples the clocks;
+        the window's replays give the sustained rate."""
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+        with ClockSampler(local) as clocks:
+            n0, ms0 = replay_for(full, stream, args.load_seconds, est_step_ms * R)
+            barrier(world)
+            torch.cuda.synchronize()
+            with torch.cuda.stream(stream):
+                torch.cuda._sleep(int(2e7))  # the host queues the K steps before they start
+                ev[0].record(stream)
+                for _ in range(K // R):
+                    full.replay()
+                if tail is not None:
+                    tail.replay()
+                ev[1].record(stream)
+            torch.cuda.synchronize()
+            barrier(world)
+            n1, ms1 = replay_for(full, stream, args.load_seconds, est_step_ms * R)
+        sustained = {"steps": (n0 + n1) * R, "ms": round(ms0 + ms1, 3),
+                     "us_per_step": round((ms0 + ms1) * 1e3 / ((n0 + n1) * R), 3)}
+        return ev[0].elapsed_time(ev[1]), clocks.summary(), sustained
+
+    region_ms, clk, sustained = timed_region()
+    # A region whose clocks disqualify it is measured once more; every rank takes the same
+    # path (the decision is the maximum over ranks), and the line keeps the first record.
+    why = clocks_rejected(clk)
+    remeasured = None
+    if max_over_ranks(1.0 if why else 0.0, world, dev) > 0:
+        remeasured = {"first_clocks": clk, "reason": why or "clocks of another rank"}
+        region_ms, clk, sustained = timed_region()
+    total_ms = max_over_ranks(region_ms, world, dev)
+    ms_per_step = total_ms / K
+    value = world * K / (total_ms / 1e3)
+    sustained["value"] = round(world * 1e3 / sustained["us_per_step"] * 1e3, 2)
+    roofline = roofline_of(layers, step_bytes, ms_per_step, peak, peak_kind, wl, dev)
+    roofline["traffic"] = committed_traffic() if wl == DEFAULT_WORKLOAD else None
+    roofline["us_per_launch_sustained"] = sustained["us_per_step"]
+    c0 = layers[0].case
+    launches = layers[0].srkv.retrieval_decode_launches(c0.cfg, c0.batch, c0.max_blocks)
+
+    e2e = run_e2e(layers, args.e2e_steps, world, dev) if args.e2e_steps > 0 else None
     append = time_append(dev, layers[0].case.cfg)
+    prefill["frac"] = round(prefill["GB_s"] / peak, 4)
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": "steps/s", "n_gpus": world,
         "steps": K, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5),
@@ -505,22 +557,72 @@ def run_ours(args, world, rank, local):
                    "seq_len": WORKLOADS[wl][2], "parallelism": f"replicas x{world}",
                    "layers_rotated": R,
                    "l2": f"inputs larger than L2: {R} layer caches rotated per step"},
-        "roofline": dict(roofline, kernel=kernel_desc),
-        "prefill_reps": {"kernel": "srkv_build_block_reps", "pages": sum(
-            ly.case.page_ids.numel() for ly in layers), "us": round(rep_ms * 1e3, 1),
-            "GB_s": round(rep_bytes / (rep_ms / 1e3) / 1e9, 1),
-            "frac": round(rep_bytes / (rep_ms / 1e3) / 1e9 / peak, 4)},
+        "roofline": roofline,
+        "sustained": sustained,
+        "prefill_reps": prefill,
         "clocks": clk,
-        "e2e": e2e,
+        "e2e": e2e["per_call"] if e2e else None,
+        "e2e_graph": e2e["graph"] if e2e else None,
         "append_kv": append,
         "gpu_launches": K * launches,  # kernels per srkv_retrieval_decode call x steps
     }
     if remeasured:
         line["remeasured"] = remeasured
+    base_case = base_arr = None
     if rank == 0 and not args.no_cpu_baseline and wl == DEFAULT_WORKLOAD:
-        line["cpu_baseline"] = cpu_baseline(layers[0], args.cpu_seconds)
+        from block_sparse_retrieval_gb300 import synth
+        base_case = layers[0].case
+        base_arr = synth.to_oracle_arrays(base_case)
+    del layers, full, tail
+    torch.cuda.empty_cache()
+    if wl == DEFAULT_WORKLOAD and not args.no_workloads:
+        line["workloads"] = {name: measure_workload(name, args, world, rank, dev, peak, peak_kind)
+                             for name in EXTRA_WORKLOADS}
+    if rank == 0 and not args.no_cpu_baseline and wl == DEFAULT_WORKLOAD:
+        line["cpu_baseline"] = cpu_baseline(base_case, base_arr, args.cpu_seconds)
     if rank == 0:
         print(json.dumps(line), flush=True)
+
+
+# The other configurations of the method's evaluation, measured in the default run beside the
+# metric's workload: the batch-4 x 131072 cache at four ratios, the ragged batch, the shared
+# prefix.
+EXTRA_WORKLOADS = ("dense-vs-sparse-p0.2", "dense-vs-sparse-p0.1", "dense-vs-sparse-p0.4",
+                   "dense-vs-sparse-p1.0", "ragged-16", "prefix-shared-64")
+
+
+def measure_workload(wl: str, args, world: int, rank: int, dev, peak: float,
+                     peak_kind: str) -> dict:
+    """One workload's decode step: about args.load_seconds of CUDA-graph replays over two
+    rotated layer caches (each larger than L2), timed with CUDA events, clocks sampled over
+    them.  Its prefill is one srkv_build_block_reps launch per layer over every page."""
+    layers, prefill = build_layers(wl, 2, rank, dev)
+    R = len(layers)
+    step_bytes = [ly.step_bytes() for ly in layers]
+    stream = torch.cuda.Stream(device=dev)
+    stream.wait_stream(torch.cuda.current_stream())
+    full, _ = step_graphs(layers, R, stream)
+    with torch.cuda.stream(stream):
+        for _ in range(3):
+            full.replay()
+    torch.cuda.synchronize()
+    _, probe_ms = replay_for(full, stream, 0.0, 1.0)
+    barrier(world)
+    with ClockSampler(dev.index or 0) as clocks:  # the rank's local GPU
+        n, ms = replay_for(full, stream, max(args.load_seconds, 0.1), probe_ms)
+    ms = max_over_ranks(ms, world, dev)
+    call_ms = ms / (n * R)
+    roofline = roofline_of(layers, step_bytes, call_ms, peak, peak_kind, wl, dev)
+    prefill["frac"] = round(prefill["GB_s"] / peak, 4)
+    c0 = layers[0].case
+    out = {"workload": WORKLOADS[wl][1], "steps": n * R, "us_per_launch": roofline["us_per_launch"],
+           "steps_per_s": round(world * 1e3 / call_ms, 2), "roofline": roofline,
+           "prefill_reps": prefill, "clocks": clocks.summary(),
+           "gpu_launches_per_step": layers[0].srkv.retrieval_decode_launches(
+               c0.cfg, c0.batch, c0.max_blocks)}
+    del layers, full
+    torch.cuda.empty_cache()
+    return out
 
 
 def offload_layers(layers):
@@ -595,10 +697,12 @@ def time_append(dev, cfg, n: int = 200) -> dict:
 
 
 def run_e2e(layers, K, world, dev) -> dict:
-    """The same steps through the public entry point with host buffers, as a serving loop
-    runs them: each step copies its query and lengths from pinned host memory (one packed
-    copy), runs the decode and reads the output back into pinned memory, the three replayed
-    from a CUDA graph per layer, then waits for the result on the host."""
+    """The same steps through the public entry point with host buffers, as a serving loop runs
+    them.  Per step: the step's query and lengths are copied from pinned host memory (one packed
+    copy), srkv_retrieval_decode is called through the binding (its argument checks and the
+    launch included), the output is copied back into pinned host memory, and the host waits
+    for it.  `per_call` issues those three from Python every step; `graph` replays them from one
+    CUDA graph per layer (what a serving loop that captures its step would see)."""
     steps = []
     for ly in layers:
         c, b = ly.case, ly.buf
@@ -619,63 +723,86 @@ def run_e2e(layers, K, world, dev) -> dict:
     d2h = steps[0]["out"].nbytes
     stream = torch.cuda.Stream(dev)
     stream.wait_stream(torch.cuda.current_stream())
+
+    def one(st):
+        st["packed"].copy_(st["host"], non_blocking=True)
+        st["ly"].step()
+        st["out"].copy_(st["ly"].buf.out, non_blocking=True)
+
     graphs = []
     with torch.cuda.stream(stream):
         for st in steps:
-            st["packed"].copy_(st["host"], non_blocking=True)
-            st["ly"].step()
-            st["out"].copy_(st["ly"].buf.out, non_blocking=True)
+            one(st)
         stream.synchronize()
         for st in steps:
-            def one(st=st):
-                st["packed"].copy_(st["host"], non_blocking=True)
-                st["ly"].step()
-                st["out"].copy_(st["ly"].buf.out, non_blocking=True)
-            graphs.append(capture(one, stream))
+            graphs.append(capture(lambda st=st: one(st), stream))
     torch.cuda.synchronize()
 
-    def step(i):
+    def timed(step) -> float:
+        with torch.cuda.stream(stream):
+            for i in range(3):
+                step(i)
+            barrier(world)
+            t0 = time.perf_counter()
+            for i in range(K):
+                step(i)
+            return max_over_ranks(time.perf_counter() - t0, world, dev)
+
+    def per_call(i):
+        one(steps[i % len(steps)])
+        stream.synchronize()
+
+    def replay(i):
         graphs[i % len(graphs)].replay()
         stream.synchronize()
 
-    with torch.cuda.stream(stream):
-        for i in range(3):
-            step(i)
-        barrier(world)
-        t0 = time.perf_counter()
-        for i in range(K):
-            step(i)
-        dt = max_over_ranks(time.perf_counter() - t0, world, dev)
-    return {"value": round(world * K / dt, 2), "unit": "steps/s", "h2d_bytes_per_step": h2d,
-            "d2h_bytes_per_step": d2h, "steps": K,
-            "how": "per step: packed pinned-host copy of q and lengths, the decode call, copy of "
-                   "the output to pinned host memory (one CUDA graph), host synchronize"}
+    dt_call, dt_graph = timed(per_call), timed(replay)
+    base = {"unit": "steps/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": K,
+            "copies_declared": True}
+    return {
+        "per_call": dict(base, value=round(world * K / dt_call, 2),
+                         how="per step from Python: packed pinned-host copy of q and lengths, "
+                             "srkv_retrieval_decode through the binding (checks and launch), "
+                             "copy of the output to pinned host memory, host synchronize"),
+        "graph": dict(base, value=round(world * K / dt_graph, 2),
+                      how="the same three per step replayed from one CUDA graph per layer, "
+                          "host synchronize"),
+    }
 
 
 # ---- the oracle on the host --------------------------------------------------------------------
 
-def oracle_step_fn(case, threads):
+def oracle_step_fn(case, threads, arr=None):
     import oracle
     from block_sparse_retrieval_gb300 import synth
-    arr = synth.to_oracle_arrays(case)
+    arr = arr or synth.to_oracle_arrays(case)
     args = [arr[k] for k in ("q", "k_cache", "v_cache", "block_table", "seq_lens",
                              "prompt_lens")]
     return lambda: oracle.decode(case.cfg, *args, threads=threads)
 
 
-def cpu_baseline(layer, seconds: float) -> dict:
-    units = layer.case.batch * layer.case.cfg["num_kv_heads"]
-    threads = max(1, min(os.cpu_count() or 1, units))
-    fn = oracle_step_fn(layer.case, threads)
+def time_oracle(fn, seconds: float) -> tuple[int, float]:
     fn()
     n, t0 = 0, time.perf_counter()
     while time.perf_counter() - t0 < seconds:
         fn()
         n += 1
-    dt = time.perf_counter() - t0
+    return n, time.perf_counter() - t0
+
+
+def cpu_baseline(case, arr, seconds: float) -> dict:
+    """The oracle as it stands on the host cores: all of them (one thread per kv-head unit,
+    at most the core count) and a single thread, full decode steps of the metric's layer."""
+    units = case.batch * case.cfg["num_kv_heads"]
+    threads = max(1, min(os.cpu_count() or 1, units))
+    n, dt = time_oracle(oracle_step_fn(case, threads, arr), seconds)
+    n1, dt1 = time_oracle(oracle_step_fn(case, 1, arr), seconds * 0.75)
     return {"value": round(n / dt, 3), "unit": "steps/s", "cores": threads, "kind": "oracle",
             "sample": f"{n} full decode steps of one 65536-token layer (all {units} kv-head "
-                      "units; the oracle recomputes block means from K as it scores)"}
+                      "units; the oracle recomputes block means from K as it scores)",
+            "host_cores": os.cpu_count(),
+            "single_thread": {"value": round(n1 / dt1, 3), "unit": "steps/s", "cores": 1,
+                              "sample": f"{n1} full decode steps, one thread"}}
 
 
 def run_reference(args, world, rank):
@@ -713,15 +840,20 @@ def run_reference(args, world, rank):
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=4000)
+    ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=8)
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--layers", type=int, default=None,
                     help="rotated layer caches (default: 2 to 8, about 2 GB of K/V, far more than L2)")
     ap.add_argument("--workload", choices=list(WORKLOADS), default=DEFAULT_WORKLOAD)
-    ap.add_argument("--e2e-steps", type=int, default=1000)
+    ap.add_argument("--e2e-steps", type=int, default=1000,
+                    help="steps of each end-to-end loop (0: skip)")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-workloads", action="store_true",
+                    help="measure only --workload (the default run adds the other configurations)")
+    ap.add_argument("--load-seconds", type=float, default=0.15,
+                    help="seconds of replays before and after the timed steps (clock sampling)")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")

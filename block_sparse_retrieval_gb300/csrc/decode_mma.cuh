@@ -11,7 +11,9 @@
 // of each product may be permuted consistently on both operands, so every fragment comes
 // from 16-byte shared loads; P^T -> P is one movmatrix.trans per 8x8 block.  Online softmax
 // in fp32, log2 domain; the sum uses the bf16-rounded weights the MMA sees.  Rows outside a
-// stage's loaded range are masked in the logits and zeroed in V.
+// stage's loaded range are masked in the logits and zeroed in V.  Over compressed pages (E4M3
+// codes with fp32 row scales) K's scale multiplies the logits and V's scale the weights, so
+// both products take the widened codes as they are.
 #pragma once
 
 #include "decode_plan.cuh"
@@ -22,6 +24,8 @@ constexpr int kConsumerWarps = 8;
 constexpr int kThreads = (kConsumerWarps + 1) * 32;
 constexpr int kProducerWarp = kConsumerWarps;
 constexpr uint32_t kNewUnit = 1, kSegEnd = 2, kBankB = 4, kLast = 8;
+// Compressed pages: factor on the V-scaled weights and on their sum (a power of two).
+constexpr float kPScale = 256.f;
 
 struct StageInfo {
   int32_t unit;
@@ -152,6 +156,8 @@ __device__ __forceinline__ void issue_stage(const DecodeArgs& a, const TmaMaps& 
   uint64_t* empty = full_v + C::kStages;
   const int s = (int)(it % C::kStages);
   if (it >= C::kStages && !mbar_wait(&empty[s], (uint32_t)((it / C::kStages - 1) & 1))) {
+    // Copies already armed may still be landing in the ring: every caller, on this path as
+    // on the normal one, waits (bounded) for the last kStages armed stages before its CTA ends.
     abort = true;
     eflags |= SRKV_EFLAG_TIMEOUT;
     return;
@@ -183,9 +189,11 @@ __device__ __forceinline__ void issue_stage(const DecodeArgs& a, const TmaMaps& 
     }
     return;
   }
-  mbar_arrive_expect_tx(&full[s], (rows ? (uint32_t)C::kSlab + kRowScales : 0u) +
+  // (compressed pages: both row-scale vectors complete `full`, since V's scales go into the
+  // weights, which are formed before V is read)
+  mbar_arrive_expect_tx(&full[s], (rows ? (uint32_t)C::kSlab + 2 * kRowScales : 0u) +
                                       ((fl & kNewUnit) ? qbytes : 0u));
-  mbar_arrive_expect_tx(&full_v[s], rows ? (uint32_t)C::kSlab + kRowScales : 0u);
+  mbar_arrive_expect_tx(&full_v[s], rows ? (uint32_t)C::kSlab : 0u);
   ++armed;
   if (u < 0) return;
   const int32_t h = u % a.Hkv, r = u / a.Hkv;
@@ -212,7 +220,7 @@ __device__ __forceinline__ void issue_stage(const DecodeArgs& a, const TmaMaps& 
     if constexpr (F8)
       bulk_load_hint(smem + C::kOffScale + (size_t)s * C::kScaleBytes + kRowScales,
                      a.v_scale + ((int64_t)t.page * a.Hkv + h) * kBlock, kRowScales,
-                     &full_v[s], once);
+                     &full[s], once);
   }
 }
 
@@ -479,10 +487,20 @@ __device__ __forceinline__ void consumer_loop(const DecodeArgs& a, unsigned char
       st.m[1] = mn1;
       uint32_t p01, p23;  // the weights as the second product's operand rounds them
       if constexpr (F8) {
-        p01 = pack_f16(fast_exp2(s0 - base0), fast_exp2(s1 - base1));
-        p23 = pack_f16(fast_exp2(s2 - base0), fast_exp2(s3 - base1));
-        st.l[0] = st.l[0] * alpha0 + f16_lo(p01) + f16_lo(p23);
-        st.l[1] = st.l[1] * alpha1 + f16_hi(p01) + f16_hi(p23);
+        // V's row scales go into the weights: O^T += codes^T . (P scale), one multiply per
+        // (token, head) instead of one per value.  kPScale (a power of two) keeps the scaled
+        // weights near the range of the weights themselves in fp16, and the sum carries the
+        // same factor, so it cancels in the output.  A row outside the loaded range gets
+        // scale 0 (its smem scale is not data).
+        const float* vsp = sScale + (size_t)s * (C::kScaleBytes / 4) + kBlock;
+        const float sa = (ra >= inf.lo && ra < inf.hi) ? vsp[ra] * kPScale : 0.f;
+        const float sb = (rb >= inf.lo && rb < inf.hi) ? vsp[rb] * kPScale : 0.f;
+        const float e0 = fast_exp2(s0 - base0), e1 = fast_exp2(s1 - base1);
+        const float e2 = fast_exp2(s2 - base0), e3 = fast_exp2(s3 - base1);
+        p01 = pack_f16(e0 * sa, e1 * sa);
+        p23 = pack_f16(e2 * sb, e3 * sb);
+        st.l[0] = st.l[0] * alpha0 + (e0 + e2) * kPScale;
+        st.l[1] = st.l[1] * alpha1 + (e1 + e3) * kPScale;
       } else {
         p01 = pack_bf16(fast_exp2(s0 - base0), fast_exp2(s1 - base1));
         p23 = pack_bf16(fast_exp2(s2 - base0), fast_exp2(s3 - base1));
@@ -506,20 +524,16 @@ __device__ __forceinline__ void consumer_loop(const DecodeArgs& a, unsigned char
       const int trow[4] = {row0 + tile_token(2 * ln.t), row0 + tile_token(2 * ln.t + 1),
                            row0 + tile_token(2 * ln.t + 8), row0 + tile_token(2 * ln.t + 9)};
       if constexpr (F8) {
-        // O^T += V^T . P: m-tile i takes d = 16 g + 2 i (row g) and 16 g + 2 i + 1 (row g + 8)
-        // from the lane's chunk g of the four token rows; a byte permute pairs the two tokens
-        // of each product row, widened to fp16 and multiplied by the tokens' V scales
-        // (masked rows load as zero codes with a zero scale)
-        const float* vsp = sScale + (size_t)s * (C::kScaleBytes / 4) + kBlock;
+        // O^T += codes^T . (P scale): m-tile i takes d = 16 g + 2 i (row g) and 16 g + 2 i + 1
+        // (row g + 8) from the lane's chunk g of the four token rows; a byte permute pairs the
+        // two tokens of each product row, widened to fp16 (exact).  Rows outside the loaded
+        // range load as zero codes (their smem bytes are not data).
         int4 vq[4];
-        float vsc[4];
 #pragma unroll
         for (int x = 0; x < 4; ++x) {
           const bool in = trow[x] >= inf.lo && trow[x] < inf.hi;
           vq[x] = in ? lds128(v + swz(trow[x], ln.g)) : make_int4(0, 0, 0, 0);
-          vsc[x] = in ? vsp[trow[x]] : 0.f;
         }
-        const uint32_t sc01 = pack_f16(vsc[0], vsc[1]), sc23 = pack_f16(vsc[2], vsc[3]);
         auto word = [](const int4& x, int w) -> uint32_t {
           return (uint32_t)(w == 0 ? x.x : w == 1 ? x.y : w == 2 ? x.z : x.w);
         };
@@ -531,11 +545,8 @@ __device__ __forceinline__ void consumer_loop(const DecodeArgs& a, unsigned char
               (uint32_t)(bo | ((4 + bo) << 4) | ((bo + 1) << 8) | ((5 + bo) << 12));
           const uint32_t x01 = __byte_perm(word(vq[0], wi), word(vq[1], wi), sel);
           const uint32_t x23 = __byte_perm(word(vq[2], wi), word(vq[3], wi), sel);
-          const uint32_t a0 = mul_f16x2(e4m3x2_to_f16x2(x01), sc01);
-          const uint32_t a1 = mul_f16x2(e4m3x2_to_f16x2(x01 >> 16), sc01);
-          const uint32_t a2 = mul_f16x2(e4m3x2_to_f16x2(x23), sc23);
-          const uint32_t a3 = mul_f16x2(e4m3x2_to_f16x2(x23 >> 16), sc23);
-          mma_16816_f16(st.acc[i], a0, a1, a2, a3, b0, b1);
+          mma_16816_f16(st.acc[i], e4m3x2_to_f16x2(x01), e4m3x2_to_f16x2(x01 >> 16),
+                        e4m3x2_to_f16x2(x23), e4m3x2_to_f16x2(x23 >> 16), b0, b1);
         }
       } else {
         int4 vt[4][C::NCH];

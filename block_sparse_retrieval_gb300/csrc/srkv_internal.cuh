@@ -249,12 +249,6 @@ __device__ __forceinline__ float f16_lo(uint32_t v) {
 __device__ __forceinline__ float f16_hi(uint32_t v) {
   return __half2float(__ushort_as_half((unsigned short)(v >> 16)));
 }
-// Lane-wise fp16 product of two fp16 pairs.
-__device__ __forceinline__ uint32_t mul_f16x2(uint32_t a, uint32_t b) {
-  const __half2 r = __hmul2(*reinterpret_cast<const __half2*>(&a),
-                            *reinterpret_cast<const __half2*>(&b));
-  return *reinterpret_cast<const uint32_t*>(&r);
-}
 
 __device__ __forceinline__ uint32_t movmatrix_trans(uint32_t x) {
   uint32_t y;
