@@ -61,9 +61,16 @@ WORKLOADS = {
         131072),
     "prefix-shared-64": (
         lambda seed, dev: __import__("block_sparse_retrieval_gb300.synth", fromlist=["x"]).prefix_shared(seed=seed, device=dev),
-        "prefix-shared-64 (64 requests, 64/8 heads, d 128, 16384-token shared prefix + U[2048, 8192], top-k 0.2, DENSE_BOUNDARY 0)",
+        "prefix-shared-64 (64 requests, 64/8 heads, d 128, 16384-token shared prefix + U[2048, 8192], top-k 0.2, DENSE_BOUNDARY 0; srkv_retrieval_decode_prefix: the shared pages attended once per kv head for all requests)",
         24576),
 }
+# The same shared-prefix batch through the plain call (every request attends its own view of
+# the shared pages).
+WORKLOADS["prefix-shared-64-plain"] = (
+    WORKLOADS["prefix-shared-64"][0],
+    "prefix-shared-64-plain (as prefix-shared-64, through srkv_retrieval_decode: no cascade)",
+    24576)
+PREFIX_WORKLOADS = ("prefix-shared-64",)
 for _p in (1.0, 0.1, 0.2, 0.4):
     WORKLOADS[f"dense-vs-sparse-p{_p}"] = (
         (lambda p: lambda seed, dev: __import__("block_sparse_retrieval_gb300.synth", fromlist=["x"]).dense_vs_sparse(p, seed=seed, device=dev))(_p),
@@ -273,6 +280,17 @@ def unique_kv_bytes(case, sel, nsel, S: int = 128, row_bytes: int | None = None)
 
 # ---- our arm --------------------------------------------------------------------------------
 
+def shared_prefix_blocks(case, S: int = 128) -> int:
+    """Leading logical blocks that every request maps to the same physical page and holds
+    whole."""
+    bt = case.block_table.cpu().numpy()
+    L = case.seq_lens.cpu().numpy()
+    n = 0
+    while n < bt.shape[1] and all(n < int(x) // S for x in L) and np.all(bt[:, n] == bt[0, n]):
+        n += 1
+    return n
+
+
 class Layer:
     """One attention layer's cache.  As in a model's paged cache, every layer has its own
     queries, K/V pages and representation vectors, while the block table and the sequence
@@ -286,7 +304,10 @@ class Layer:
                 assert torch.equal(getattr(self.case, name), getattr(shared, name))
                 setattr(self.case, name, getattr(shared, name))
         c = self.case
-        self.buf = srkv.DecodeBuffers(c.cfg, c.batch, c.max_blocks, c.num_pages, device=device)
+        # leading blocks every request maps to the same pages (the shared-prefix call)
+        self.prefix_blocks = shared_prefix_blocks(c) if workload in PREFIX_WORKLOADS else None
+        self.buf = srkv.DecodeBuffers(c.cfg, c.batch, c.max_blocks, c.num_pages, device=device,
+                                      prefix=self.prefix_blocks is not None)
         self.srkv = srkv
         self.k_host = self.v_host = None  # the host pool of the offload workload
         self.k_scale = self.v_scale = None  # row scales of compressed pages
@@ -333,6 +354,12 @@ class Layer:
                                            c.prompt_lens, b.sel, b.nsel, b.out, b.workspace,
                                            b.error_flags)
             return
+        if self.prefix_blocks is not None:
+            self.srkv.retrieval_decode_prefix(c.cfg, c.q, c.k_cache, c.v_cache, b.reps,
+                                              c.block_table, c.seq_lens, c.prompt_lens,
+                                              self.prefix_blocks, b.sel, b.nsel, b.out,
+                                              b.workspace, b.error_flags)
+            return
         if self.k_host is not None:
             self.srkv.retrieval_decode_tiered(c.cfg, c.q, c.k_cache, c.v_cache, self.k_host,
                                               self.v_host, b.reps, c.block_table, c.seq_lens,
@@ -376,6 +403,14 @@ class Layer:
                 "kv_unique": unique_kv_bytes(c, sel, nsel, row_bytes=row), "host_kv": host_kv}
 
 
+def launches_per_step(layer) -> int:
+    """Kernels one decode call of the layer launches (the shared-prefix call adds one)."""
+    c = layer.case
+    if layer.prefix_blocks:
+        return 4
+    return layer.srkv.retrieval_decode_launches(c.cfg, c.batch, c.max_blocks)
+
+
 def capture(fn, stream):
     g = torch.cuda.CUDAGraph()
     with torch.cuda.graph(g, stream=stream):
@@ -398,14 +433,15 @@ def build_layers(wl: str, n_layers, rank: int, dev):
     for ly in layers:                        # warm the kernel once
         ly.prefill()
     torch.cuda.synchronize()
-    rep_bytes = 0
+    rep_bytes = 0  # counted first: a read of a device tensor would wait for the queue
+    for ly in layers:
+        c = ly.case
+        rep_bytes += int(c.page_valid.sum()) * c.cfg["num_kv_heads"] * c.cfg["head_dim"] * 2 \
+            + c.page_ids.numel() * c.cfg["num_kv_heads"] * c.cfg["head_dim"] * 4
     torch.cuda._sleep(int(2e7))
     ev[0].record()
     for ly in layers:
         ly.prefill()
-        c = ly.case
-        rep_bytes += int(c.page_valid.sum()) * c.cfg["num_kv_heads"] * c.cfg["head_dim"] * 2 \
-            + c.page_ids.numel() * c.cfg["num_kv_heads"] * c.cfg["head_dim"] * 4
     ev[1].record()
     torch.cuda.synchronize()
     rep_ms = ev[0].elapsed_time(ev[1])
@@ -460,9 +496,9 @@ def roofline_of(layers, step_bytes, call_ms: float, peak: float, peak_kind: str,
                          "unique_bytes_per_launch": int(host), "unique_frac": None,
                          "device_bytes_per_launch": int(avg_step_bytes - host),
                          "device_GB_s": round((avg_step_bytes - host) / (call_ms / 1e3) / 1e9, 1)})
-    c0 = layers[0].case
-    launches = layers[0].srkv.retrieval_decode_launches(c0.cfg, c0.batch, c0.max_blocks)
-    roofline["kernel"] = (
+    launches = launches_per_step(layers[0])
+    roofline["kernel"] = "srkv_retrieval_decode_prefix call: score_topk, shared-prefix cascade, " \
+        "split-K decode and combine kernels, overlapped by programmatic launch" if launches == 4 else (
         "srkv_retrieval_decode call: one kernel (a thread-block cluster per (request, kv head) "
         "scores, selects and attends)" if launches == 1 else
         "srkv_retrieval_decode call: score_topk, split-K decode and combine kernels, "
@@ -541,8 +577,7 @@ def run_ours(args, world, rank, local):
     roofline = roofline_of(layers, step_bytes, ms_per_step, peak, peak_kind, wl, dev)
     roofline["traffic"] = committed_traffic() if wl == DEFAULT_WORKLOAD else None
     roofline["us_per_launch_sustained"] = sustained["us_per_step"]
-    c0 = layers[0].case
-    launches = layers[0].srkv.retrieval_decode_launches(c0.cfg, c0.batch, c0.max_blocks)
+    launches = launches_per_step(layers[0])
 
     e2e = run_e2e(layers, args.e2e_steps, world, dev) if args.e2e_steps > 0 else None
     append = time_append(dev, layers[0].case.cfg)
@@ -588,7 +623,8 @@ def run_ours(args, world, rank, local):
 # metric's workload: the batch-4 x 131072 cache at four ratios, the ragged batch, the shared
 # prefix.
 EXTRA_WORKLOADS = ("dense-vs-sparse-p0.2", "dense-vs-sparse-p0.1", "dense-vs-sparse-p0.4",
-                   "dense-vs-sparse-p1.0", "ragged-16", "prefix-shared-64")
+                   "dense-vs-sparse-p1.0", "ragged-16", "prefix-shared-64",
+                   "prefix-shared-64-plain")
 
 
 def measure_workload(wl: str, args, world: int, rank: int, dev, peak: float,
@@ -614,12 +650,10 @@ def measure_workload(wl: str, args, world: int, rank: int, dev, peak: float,
     call_ms = ms / (n * R)
     roofline = roofline_of(layers, step_bytes, call_ms, peak, peak_kind, wl, dev)
     prefill["frac"] = round(prefill["GB_s"] / peak, 4)
-    c0 = layers[0].case
     out = {"workload": WORKLOADS[wl][1], "steps": n * R, "us_per_launch": roofline["us_per_launch"],
            "steps_per_s": round(world * 1e3 / call_ms, 2), "roofline": roofline,
            "prefill_reps": prefill, "clocks": clocks.summary(),
-           "gpu_launches_per_step": layers[0].srkv.retrieval_decode_launches(
-               c0.cfg, c0.batch, c0.max_blocks)}
+           "gpu_launches_per_step": launches_per_step(layers[0])}
     del layers, full
     torch.cuda.empty_cache()
     return out

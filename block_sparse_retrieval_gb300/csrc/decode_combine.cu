@@ -91,6 +91,16 @@ __device__ __forceinline__ int64_t part_slot(const ListParts& lp, int32_t i) {
   return lp.slot0 + i;
 }
 
+// Slot of part p of unit u: list A's parts, then list B's, then the unit's shared-prefix
+// partials (one per block range of the cascade kernel), or -1 for a part that is absent.
+__device__ __forceinline__ int64_t unit_part_slot(const DecodeArgs& a, const ListParts& la,
+                                                  const ListParts& lb, int32_t u, int32_t p) {
+  if (p < la.parts) return part_slot(la, p);
+  p -= la.parts;
+  if (p < lb.parts) return part_slot(lb, p);
+  return a.lay.cascade + (int64_t)u * a.prefix_ranges + (p - lb.parts);
+}
+
 template <typename TOut>
 __device__ __forceinline__ void store_vec(TOut* p, const float (&v)[4], int n);
 template <>
@@ -142,7 +152,7 @@ __global__ void __launch_bounds__(kWarps * 32) combine_kernel(const DecodeArgs a
   }
   const float* accw = reinterpret_cast<const float*>(a.ws + a.lay.acc);
   const float* mlw = reinterpret_cast<const float*>(a.ws + a.lay.ml);
-  const int32_t total = la.parts + lb.parts;
+  const int32_t total = la.parts + lb.parts + a.prefix_ranges;
   float m_run = -INFINITY, l_run = 0.f, acc[V];
 #pragma unroll
   for (int e = 0; e < V; ++e) acc[e] = 0.f;
@@ -150,8 +160,7 @@ __global__ void __launch_bounds__(kWarps * 32) combine_kernel(const DecodeArgs a
     // every load of this warp's 16 parts is issued before any is used
     const int32_t p = p0 + lane;
     int64_t slot = -1;
-    if (lane < kPartsPerWarp && p < total)
-      slot = p < la.parts ? part_slot(la, p) : part_slot(lb, p - la.parts);
+    if (lane < kPartsPerWarp && p < total) slot = unit_part_slot(a, la, lb, u, p);
     float m = -INFINITY, l = 0.f;
     if (slot >= 0) {
       m = mlw[(slot * G + j) * 2];
@@ -249,15 +258,14 @@ __global__ void __launch_bounds__(256) combine_unit_kernel(const DecodeArgs a) {
   if (j >= G) return;
   const float* accw = reinterpret_cast<const float*>(a.ws + a.lay.acc);
   const float* mlw = reinterpret_cast<const float*>(a.ws + a.lay.ml);
-  const int32_t total = la.parts + lb.parts;
+  const int32_t total = la.parts + lb.parts + a.prefix_ranges;
   float m_run = -INFINITY, l_run = 0.f, acc[V];
 #pragma unroll
   for (int e = 0; e < V; ++e) acc[e] = 0.f;
   for (int32_t p0 = 0; p0 < total; p0 += kPartsPerWarp) {
     const int32_t p = p0 + lane;
     int64_t slot = -1;
-    if (lane < kPartsPerWarp && p < total)
-      slot = p < la.parts ? part_slot(la, p) : part_slot(lb, p - la.parts);
+    if (lane < kPartsPerWarp && p < total) slot = unit_part_slot(a, la, lb, u, p);
     float m = -INFINITY, l = 0.f;
     if (slot >= 0) {
       m = mlw[(slot * G + j) * 2];

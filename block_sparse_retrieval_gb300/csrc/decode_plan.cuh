@@ -25,7 +25,12 @@ namespace srkv {
 
 constexpr int kListA = 0, kListB = 1;
 
-__device__ __forceinline__ int32_t list_a_count(const Geom& g) { return g.a + (g.nb - g.wstart); }
+// Blocks below g.pb (a shared prefix, attended by the cascade kernel) are left out of list A:
+// its initial blocks are [pb, a), its window blocks [max(wstart, pb), nb).
+__device__ __forceinline__ int32_t list_a_count(const Geom& g) {
+  const int32_t ia = g.a > g.pb ? g.a - g.pb : 0;
+  return ia + (g.nb - (g.wstart > g.pb ? g.wstart : g.pb));
+}
 
 // Position j of list A: the page and the rows to read (init / window rows only).
 __device__ __forceinline__ PageTask resolve_a(const Geom& g, int32_t j, const int32_t* bt_r,
@@ -34,7 +39,8 @@ __device__ __forceinline__ PageTask resolve_a(const Geom& g, int32_t j, const in
   t.page = -1;
   t.block = -1;
   t.lo = t.hi = t.ie = t.ws = 0;
-  const int32_t b = j < g.a ? j : g.wstart + (j - g.a);
+  const int32_t ia = g.a > g.pb ? g.a - g.pb : 0;
+  const int32_t b = j < ia ? g.pb + j : (g.wstart > g.pb ? g.wstart : g.pb) + (j - ia);
   const int32_t base = b * kBlock;
   const int32_t cnt = min(kBlock, g.L - base);
   const int32_t ie = min(max(g.ie - base, 0), cnt);
@@ -70,6 +76,7 @@ __device__ __forceinline__ PageTask resolve_b(const Geom& g, int32_t i, const in
     eflags |= SRKV_EFLAG_SELECTION;
     return t;
   }
+  if (b < g.pb) return t;  // a shared-prefix block: the cascade kernel attends it
   const int32_t base = b * kBlock;
   const int32_t cnt = min(kBlock, g.L - base);
   const int32_t lo = max(INIT - base, 0);
@@ -102,14 +109,18 @@ __device__ __forceinline__ int32_t nsel_of(const DecodeArgs& a, int32_t u) {
 }
 
 __device__ __forceinline__ Geom unit_geom(const DecodeArgs& a, int32_t u, uint32_t& eflags) {
-  return make_geom(a.seq_lens[u / a.Hkv], nsel_of(a, u), a.max_blocks, a.kmax, a.init_tokens,
-                   a.local_tokens, eflags);
+  Geom g = make_geom(a.seq_lens[u / a.Hkv], nsel_of(a, u), a.max_blocks, a.kmax, a.init_tokens,
+                     a.local_tokens, eflags);
+  g.pb = prefix_of(g, a.prefix_blocks);
+  return g;
 }
 
 // Geometry without the selection count (list A, readable before the selection exists).
 __device__ __forceinline__ Geom unit_geom_a(const DecodeArgs& a, int32_t u, uint32_t& eflags) {
-  return make_geom(a.seq_lens[u / a.Hkv], 0, a.max_blocks, a.kmax, a.init_tokens,
-                   a.local_tokens, eflags);
+  Geom g = make_geom(a.seq_lens[u / a.Hkv], 0, a.max_blocks, a.kmax, a.init_tokens,
+                     a.local_tokens, eflags);
+  g.pb = prefix_of(g, a.prefix_blocks);
+  return g;
 }
 
 __device__ __forceinline__ int32_t list_count(const DecodeArgs& a, int list, int32_t u,

@@ -41,7 +41,7 @@ __global__ void __maxnreg__(128) split_mma_kernel(const DecodeArgs a,
   // The combine may be scheduled once every CTA has passed this point (it waits for this
   // grid before reading partials).  Without the early mode the inputs are only read after
   // the previous kernel in the stream has finished, and the combine reads them too.
-  if (!a.early) griddep_wait();
+  if (!a.early && !a.wait_late) griddep_wait();
   griddep_launch_dependents();
   if (tid == 0) init_ring<D, F8>(smem);
   __syncthreads();
@@ -65,7 +65,9 @@ __global__ void __maxnreg__(128) split_mma_kernel(const DecodeArgs a,
       rgs[list] = warp_plan(a, list, blockIdx.x, list_ctas(a, list), offsets, nullptr, eflags);
     }
     for (int list = kListA; list <= kListB && !abort; ++list) {
-      if (list == kListB && a.early) griddep_wait();  // the selection must exist from here on
+      // the selection (or, behind the shared-prefix kernel, that kernel's partials) must
+      // exist from here on
+      if (list == kListB && (a.early || a.wait_late)) griddep_wait();
       const ListRange rg = rgs[list];
       const int64_t npos = rg.end - rg.begin;
       if (npos <= 0) continue;
@@ -123,6 +125,9 @@ __global__ void __maxnreg__(128) split_mma_kernel(const DecodeArgs a,
           t.hi = __shfl_sync(0xffffffffu, task.hi, l);
           t.ie = __shfl_sync(0xffffffffu, task.ie, l);
           t.ws = __shfl_sync(0xffffffffu, task.ws, l);
+          // A selected shared-prefix block loads nothing here (the cascade kernel attends
+          // it); it takes a stage only when it opens or closes the unit's segment.
+          if (a.prefix_blocks > 0 && t.page < 0 && !(fl & (kNewUnit | kSegEnd))) continue;
           issue_stage_warp<D, F8>(a, maps, smem, it, u, fl, t, armed, abort, eflags, lane);
           ++it;
         }

@@ -65,12 +65,14 @@ int32_t host_kmax_bound(const srkv_config& c, int32_t max_blocks) {
   return (int32_t)(c.dense_boundary > 0 ? n : host_topk_count(n, c.topk_percent));
 }
 
-size_t workspace_size(const srkv_config* cfg, int32_t batch) {
+// ranges: partial slots per unit for a shared prefix (0: none).
+size_t workspace_size(const srkv_config* cfg, int32_t batch, int32_t ranges = 0) {
   if (!config_ok(cfg) || batch < 0) return 0;
   const int64_t units = (int64_t)batch * cfg->num_kv_heads;
   if (units > INT32_MAX - kMaxCtas) return 0;
+  if (units * (2 + ranges) > INT32_MAX / 2) return 0;
   const int32_t G = cfg->num_q_heads / cfg->num_kv_heads;
-  return ws_layout((int32_t)units, kMaxCtas, G, cfg->head_dim).total;
+  return ws_layout((int32_t)units, kMaxCtas, G, cfg->head_dim, ranges).total;
 }
 
 // Checks the decode arguments and fills `a`; SRKV_OK means there is work to launch.
@@ -79,7 +81,7 @@ srkv_status prepare_decode(const srkv_config* cfg, const void* q, const void* k_
                            int32_t max_blocks, const int32_t* seq_lens, int32_t batch,
                            const int32_t* sel, int32_t kmax, const int32_t* nsel, void* out,
                            void* workspace, size_t workspace_bytes, int32_t* error_flags,
-                           DecodeArgs& a) {
+                           DecodeArgs& a, int32_t ranges = 0) {
   if (!config_ok(cfg) || batch < 0 || max_blocks <= 0 || max_blocks > kMaxBlocks || kmax < 0 ||
       num_pages < 0)
     return SRKV_ERR_INVALID_ARG;
@@ -92,7 +94,7 @@ srkv_status prepare_decode(const srkv_config* cfg, const void* q, const void* k_
   const int32_t G = cfg->num_q_heads / cfg->num_kv_heads;
   const bool mma = mma_split_supported(*cfg);
   if (!mma && G > 16) return SRKV_ERR_UNSUPPORTED;
-  const size_t need = workspace_size(cfg, batch);
+  const size_t need = workspace_size(cfg, batch, ranges);
   if (need == 0) return SRKV_ERR_UNSUPPORTED;
   if (!workspace || workspace_bytes < need || !aligned(workspace, 256)) return SRKV_ERR_WORKSPACE;
   const int32_t sms = sm_count();
@@ -123,8 +125,12 @@ srkv_status prepare_decode(const srkv_config* cfg, const void* q, const void* k_
   if (a.ctas > kMaxCtas) a.ctas = kMaxCtas;
   a.ctas_a = a.ctas;
   a.ctas_b = a.ctas;
-  a.lay = ws_layout(batch * cfg->num_kv_heads, kMaxCtas, G, cfg->head_dim);
+  a.lay = ws_layout(batch * cfg->num_kv_heads, kMaxCtas, G, cfg->head_dim, ranges);
   a.early = 0;
+  a.wait_late = 0;
+  a.prefix_blocks = 0;
+  a.prefix_ranges = 0;
+  a.cascade_ctas = 0;
   a.prompt_lens = nullptr;
   a.reps = nullptr;
   a.sel_out = nullptr;
@@ -168,6 +174,39 @@ srkv_status check_score(const srkv_config* cfg, const void* q, const float* reps
   return SRKV_OK;
 }
 
+// Checks of a shared-prefix call beyond those of the plain one.
+srkv_status check_prefix(const srkv_config* cfg, int32_t prefix_blocks, int32_t max_blocks) {
+  if (!config_ok(cfg) || prefix_blocks < 0 || max_blocks <= 0) return SRKV_ERR_INVALID_ARG;
+  if (prefix_blocks > max_blocks) return SRKV_ERR_INVALID_ARG;
+  if (prefix_blocks > 0 && !cascade_supported(*cfg)) return SRKV_ERR_UNSUPPORTED;
+  if (prefix_blocks > kMaxPrefixRanges * kMaxRangeBlocks) return SRKV_ERR_UNSUPPORTED;
+  return SRKV_OK;
+}
+
+// How a shared prefix of prefix_blocks pages is split: the cascade kernel takes 3/8 of
+// the SMs, with about eight (kv head, request group, block range) items per CTA (ranges of at
+// most kMaxRangeBlocks blocks); the split decode keeps the other SMs, all resident at once.
+void prefix_plan(const srkv_config& cfg, DecodeArgs& a, int32_t prefix_blocks) {
+  const int32_t sms = sm_count();
+  const int32_t G = cfg.num_q_heads / cfg.num_kv_heads;
+  const int32_t groups = (a.batch + 128 / G - 1) / (128 / G);
+  const int32_t cas = cascade_ctas(sms);
+  const int64_t per = (int64_t)cfg.num_kv_heads * groups;
+  int64_t nr = (8 * (int64_t)cas + per - 1) / per;
+  const int32_t nr_min = (prefix_blocks + kMaxRangeBlocks - 1) / kMaxRangeBlocks;
+  if (nr > kMaxPrefixRanges) nr = kMaxPrefixRanges;
+  if (nr > prefix_blocks) nr = prefix_blocks;
+  if (nr < nr_min) nr = nr_min;
+  a.prefix_blocks = prefix_blocks;
+  a.prefix_ranges = (int32_t)nr;
+  const int64_t items = per * nr;
+  a.cascade_ctas = (int32_t)(items < cas ? items : cas);
+  a.ctas = sms - a.cascade_ctas;
+  if (a.ctas > kMaxCtas) a.ctas = kMaxCtas;
+  a.ctas_a = a.ctas;
+  a.ctas_b = a.ctas;
+}
+
 // srkv_retrieval_decode over a device pool [0, num_pages) and a host pool
 // [num_pages, num_pages + num_host_pages) of page ids (num_host_pages = 0: no host pool).
 srkv_status retrieval_decode(const srkv_config* cfg, const void* q, const void* k_cache,
@@ -178,14 +217,32 @@ srkv_status retrieval_decode(const srkv_config* cfg, const void* q, const void* 
                              const int32_t* seq_lens, const int32_t* prompt_lens, int32_t batch,
                              int32_t* sel, int32_t kmax, int32_t* nsel, void* out,
                              void* workspace, size_t workspace_bytes, int32_t* error_flags,
-                             cudaStream_t s) {
+                             cudaStream_t s, int32_t prefix_blocks = 0) {
   srkv_status st = check_score(cfg, q, reps, num_pages + num_host_pages, block_table, max_blocks,
                                seq_lens, batch, sel, kmax, nsel);
   if (st != SRKV_OK || batch == 0) return st;
   DecodeArgs a;
+  const int32_t ranges = prefix_blocks > 0 ? kMaxPrefixRanges : 0;
   st = prepare_decode(cfg, q, k_cache, v_cache, num_pages, block_table, max_blocks, seq_lens,
-                      batch, sel, kmax, nsel, out, workspace, workspace_bytes, error_flags, a);
+                      batch, sel, kmax, nsel, out, workspace, workspace_bytes, error_flags, a,
+                      ranges);
   if (st != SRKV_OK) return st;
+  if (prefix_blocks > 0) {
+    a.prompt_lens = prompt_lens;
+    a.reps = reps;
+    a.sel_out = sel;
+    a.nsel_out = nsel;
+    prefix_plan(*cfg, a, prefix_blocks);
+    const int64_t scoring = score_topk_ctas(*cfg, max_blocks, batch);
+    if (2 * scoring <= a.ctas) a.ctas_a = a.ctas - (int32_t)scoring;
+    // scoring, then the shared-prefix attention behind it (waiting for the selection), then
+    // the split decode, which streams the requests' own initial and window pages at once
+    if (launch_score_topk(*cfg, q, reps, num_pages, block_table, max_blocks, seq_lens,
+                          prompt_lens, batch, sel, kmax, nsel, error_flags, s) != cudaSuccess)
+      return SRKV_ERR_CUDA;
+    if (launch_cascade(a, true, s) != cudaSuccess) return SRKV_ERR_CUDA;
+    return launch_decode(cfg, a, 1, s);
+  }
   a.k_host = k_host;
   a.v_host = v_host;
   a.num_host_pages = num_host_pages;
@@ -352,6 +409,35 @@ srkv_status srkv_sparse_paged_decode(const srkv_config* cfg, const void* q, cons
   return launch_decode(cfg, a, 0, (cudaStream_t)stream);
 }
 
+size_t srkv_prefix_decode_workspace_size(const srkv_config* cfg, int32_t batch) {
+  return workspace_size(cfg, batch, kMaxPrefixRanges);
+}
+
+srkv_status srkv_sparse_paged_decode_prefix(const srkv_config* cfg, const void* q,
+                                            const void* k_cache, const void* v_cache,
+                                            int64_t num_pages, const int32_t* block_table,
+                                            int32_t max_blocks, const int32_t* seq_lens,
+                                            int32_t batch, int32_t prefix_blocks,
+                                            const int32_t* sel, int32_t kmax,
+                                            const int32_t* nsel, void* out, void* workspace,
+                                            size_t workspace_bytes, int32_t* error_flags,
+                                            srkv_stream stream) {
+  srkv_status st = check_prefix(cfg, prefix_blocks, max_blocks);
+  if (st != SRKV_OK) return st;
+  DecodeArgs a;
+  st = prepare_decode(cfg, q, k_cache, v_cache, num_pages, block_table, max_blocks, seq_lens,
+                      batch, sel, kmax, nsel, out, workspace, workspace_bytes, error_flags, a,
+                      kMaxPrefixRanges);
+  if (st != SRKV_OK || batch == 0) return st;
+  if (prefix_blocks == 0) return launch_decode(cfg, a, 0, (cudaStream_t)stream);
+  prefix_plan(*cfg, a, prefix_blocks);
+  // the shared-prefix attention first (a plain launch: every input is complete when it
+  // starts); the split decode behind it reads only inputs until list B, where it waits for it
+  if (launch_cascade(a, false, (cudaStream_t)stream) != cudaSuccess) return SRKV_ERR_CUDA;
+  a.wait_late = 1;
+  return launch_decode(cfg, a, 0, (cudaStream_t)stream);
+}
+
 srkv_status srkv_retrieval_decode(const srkv_config* cfg, const void* q, const void* k_cache,
                                   const void* v_cache, const float* reps, int64_t num_pages,
                                   const int32_t* block_table, int32_t max_blocks,
@@ -363,6 +449,23 @@ srkv_status srkv_retrieval_decode(const srkv_config* cfg, const void* q, const v
                           nullptr, reps,
                           block_table, max_blocks, seq_lens, prompt_lens, batch, sel, kmax, nsel,
                           out, workspace, workspace_bytes, error_flags, (cudaStream_t)stream);
+}
+
+srkv_status srkv_retrieval_decode_prefix(const srkv_config* cfg, const void* q,
+                                         const void* k_cache, const void* v_cache,
+                                         const float* reps, int64_t num_pages,
+                                         const int32_t* block_table, int32_t max_blocks,
+                                         const int32_t* seq_lens, const int32_t* prompt_lens,
+                                         int32_t batch, int32_t prefix_blocks, int32_t* sel,
+                                         int32_t kmax, int32_t* nsel, void* out, void* workspace,
+                                         size_t workspace_bytes, int32_t* error_flags,
+                                         srkv_stream stream) {
+  const srkv_status st = check_prefix(cfg, prefix_blocks, max_blocks);
+  if (st != SRKV_OK) return st;
+  return retrieval_decode(cfg, q, k_cache, v_cache, num_pages, nullptr, nullptr, 0, nullptr,
+                          nullptr, reps, block_table, max_blocks, seq_lens, prompt_lens, batch,
+                          sel, kmax, nsel, out, workspace, workspace_bytes, error_flags,
+                          (cudaStream_t)stream, prefix_blocks);
 }
 
 srkv_status srkv_retrieval_decode_tiered(const srkv_config* cfg, const void* q,

@@ -284,6 +284,7 @@ struct Geom {
   int32_t a;       // init blocks [0, a)
   int32_t wstart;  // window blocks [wstart, nb) that are not init blocks
   int32_t ns;      // clamped selection count
+  int32_t pb;      // blocks [0, pb) are attended elsewhere (a shared prefix), not listed
   __device__ __forceinline__ int32_t npos() const { return a + ns + (nb - wstart); }
 };
 
@@ -311,7 +312,15 @@ __device__ __forceinline__ Geom make_geom(int32_t seq_len, int32_t nsel, int32_t
   const int32_t wb = g.ws < L ? g.ws / kBlock : g.nb;
   g.wstart = wb > g.a ? wb : g.a;
   g.ns = ns;
+  g.pb = 0;
   return g;
+}
+
+// Blocks of a shared prefix of `prefix_blocks` pages that the cascade attends for this
+// request: the whole pages of the prefix its length covers.
+__device__ __forceinline__ int32_t prefix_of(const Geom& g, int32_t prefix_blocks) {
+  const int32_t full = g.L / kBlock;
+  return prefix_blocks < full ? prefix_blocks : full;
 }
 
 // Does logical block b meet the offload range [INIT, W)?
@@ -341,21 +350,30 @@ __device__ __forceinline__ int64_t cta_of(int64_t p, int64_t T, int64_t C) {
 // Workspace layout of the decode (all offsets 256-byte aligned).  Partials of list A use
 // slots [0, U + C), those of list B slots [U + C, 2 (U + C)).
 struct WsLayout {
-  size_t off_a;  // int64[U+1]: first list-A position of each unit; [U] = total
-  size_t off_b;  // int64[U+1]: the same for list B
-  size_t acc;    // float[slots][G][d]: unnormalised partial outputs
-  size_t ml;     // float[slots][G][2]: running max (log2 domain) and sum
+  size_t off_a;     // int64[U+1]: first list-A position of each unit; [U] = total
+  size_t off_b;     // int64[U+1]: the same for list B
+  size_t acc;       // float[slots][G][d]: unnormalised partial outputs
+  size_t ml;        // float[slots][G][2]: running max (log2 domain) and sum
   size_t total;
-  int32_t bank;  // U + C: slots per list
+  int32_t bank;     // U + C: slots per list
+  int64_t cascade;  // first slot of the shared-prefix partials: unit u, range r at
+                    // cascade + u * ranges + r
 };
 
 __host__ __device__ inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
+// Shared-prefix attention (decode_cascade.cu): at most kMaxPrefixRanges block ranges per
+// prefix (one partial per unit and range), each at most kMaxRangeBlocks blocks long.
+constexpr int32_t kMaxPrefixRanges = 8;
+constexpr int32_t kMaxRangeBlocks = 256;
+
+// `ranges`: partial slots per unit for a shared prefix (0 without one).
 __host__ __device__ inline WsLayout ws_layout(int32_t units, int32_t ctas, int32_t G,
-                                              int32_t d) {
+                                              int32_t d, int32_t ranges = 0) {
   WsLayout w;
   w.bank = units + ctas;
-  const size_t slots = 2 * (size_t)w.bank;
+  w.cascade = 2 * (int64_t)w.bank;
+  const size_t slots = 2 * (size_t)w.bank + (size_t)units * ranges;
   size_t off = 0;
   w.off_a = off;
   off = align256(off + sizeof(int64_t) * ((size_t)units + 1));
@@ -392,6 +410,14 @@ struct DecodeArgs {
   int32_t ctas;      // C, the split grid
   int32_t ctas_a;    // CTAs [0, ctas_a) share list A
   int32_t ctas_b;    // CTAs [0, ctas_b) share list B
+  int32_t wait_late;  // 1: the previous kernel writes nothing list A reads, so the split
+                      // waits for it only before list B (implied by early)
+  // Shared prefix: blocks [0, prefix_blocks) of every request map to the same pages and are
+  // attended by the cascade kernel (prefix_ranges ranges, cascade_ctas CTAs), not listed by
+  // the split kernel.  0: no shared prefix.
+  int32_t prefix_blocks;
+  int32_t prefix_ranges;
+  int32_t cascade_ctas;
   int32_t early;     // 1: the previous kernel is score_topk, so every input but sel and nsel
                      // may be read before it finishes (list A streams during the scoring)
   // early = 1 only: what score_topk derives its selection counts from, so that the
@@ -505,6 +531,13 @@ int32_t simt_split_ctas(int32_t sm_count);
 cudaError_t launch_split_simt(const DecodeArgs& a, int32_t dtype, cudaStream_t stream);
 
 cudaError_t launch_combine(const DecodeArgs& a, int32_t dtype, cudaStream_t stream);
+
+// Attention over a shared prefix for every request at once (bf16, d 128, group 1/2/4/8):
+// partials into the workspace's cascade slots.  pdl: launched behind the previous kernel of
+// the stream (it waits for that kernel before reading the selection).
+bool cascade_supported(const srkv_config& cfg);
+int32_t cascade_ctas(int32_t sm_count);
+cudaError_t launch_cascade(const DecodeArgs& a, bool pdl, cudaStream_t stream);
 
 // Scoring, selection and attention of a small batch in one kernel, one thread-block cluster
 // per (request, kv head) unit: the cluster size to use for `units` units (0 = not

@@ -21,7 +21,7 @@ from .build import LIB_PATH
 CFG_KEYS = ("num_q_heads", "num_kv_heads", "head_dim", "block_size", "init_tokens",
             "local_tokens", "topk_percent", "dense_boundary", "dtype")
 BF16, F32 = 0, 1
-EFLAG_PAGE_RANGE, EFLAG_SEQ_LEN, EFLAG_SELECTION, EFLAG_TIMEOUT = 1, 2, 4, 8
+EFLAG_PAGE_RANGE, EFLAG_SEQ_LEN, EFLAG_SELECTION, EFLAG_TIMEOUT, EFLAG_PREFIX = 1, 2, 4, 8, 16
 STATUS = {0: "ok", 1: "invalid argument", 2: "unsupported configuration",
           3: "workspace missing or too small", 4: "CUDA error"}
 EXPORTS = ("srkv_default_config", "srkv_status_string", "srkv_topk_count",
@@ -30,7 +30,9 @@ EXPORTS = ("srkv_default_config", "srkv_status_string", "srkv_topk_count",
            "srkv_retrieval_decode", "srkv_sparse_paged_decode_noalloc",
            "srkv_retrieval_decode_launches", "srkv_append_kv",
            "srkv_retrieval_decode_tiered", "srkv_quantize_kv_fp8",
-           "srkv_retrieval_decode_fp8", "srkv_selftest_wait_timeout")
+           "srkv_retrieval_decode_fp8", "srkv_selftest_wait_timeout",
+           "srkv_prefix_decode_workspace_size", "srkv_sparse_paged_decode_prefix",
+           "srkv_retrieval_decode_prefix")
 NOALLOC_WORKSPACE_BYTES = 16 << 20
 
 
@@ -96,12 +98,21 @@ def load() -> ctypes.CDLL:
     lib.srkv_retrieval_decode_fp8.argtypes = [ctypes.POINTER(Config), _P, _P, _P, _P, _P, _P,
                                               _I64, _P, _I32, _P, _P, _I32, _P, _I32, _P, _P,
                                               _P, _SZ, _P, _P]
+    lib.srkv_prefix_decode_workspace_size.argtypes = [ctypes.POINTER(Config), _I32]
+    lib.srkv_prefix_decode_workspace_size.restype = _SZ
+    lib.srkv_sparse_paged_decode_prefix.argtypes = [ctypes.POINTER(Config), _P, _P, _P, _I64, _P,
+                                                    _I32, _P, _I32, _I32, _P, _I32, _P, _P, _P,
+                                                    _SZ, _P, _P]
+    lib.srkv_retrieval_decode_prefix.argtypes = [ctypes.POINTER(Config), _P, _P, _P, _P, _I64,
+                                                 _P, _I32, _P, _P, _I32, _I32, _P, _I32, _P, _P,
+                                                 _P, _SZ, _P, _P]
     lib.srkv_selftest_wait_timeout.argtypes = [_P, _P]
     lib.srkv_selftest_wait_timeout.restype = ctypes.c_int
     for name in ("srkv_build_block_reps", "srkv_score_topk", "srkv_sparse_paged_decode",
                  "srkv_retrieval_decode", "srkv_sparse_paged_decode_noalloc",
                  "srkv_retrieval_decode_tiered", "srkv_quantize_kv_fp8",
-                 "srkv_retrieval_decode_fp8"):
+                 "srkv_retrieval_decode_fp8", "srkv_sparse_paged_decode_prefix",
+                 "srkv_retrieval_decode_prefix"):
         getattr(lib, name).restype = ctypes.c_int
     _lib = lib
     return lib
@@ -138,6 +149,12 @@ def kmax_bound(cfg: Mapping, max_blocks: int) -> int:
 def decode_workspace_size(cfg: Mapping, batch: int) -> int:
     c = config(cfg)
     return int(load().srkv_decode_workspace_size(ctypes.byref(c), batch))
+
+
+def prefix_decode_workspace_size(cfg: Mapping, batch: int) -> int:
+    """Workspace bytes of the shared-prefix calls for `batch` requests."""
+    c = config(cfg)
+    return int(load().srkv_prefix_decode_workspace_size(ctypes.byref(c), batch))
 
 
 def retrieval_decode_launches(cfg: Mapping, batch: int, max_blocks: int) -> int:
@@ -324,6 +341,53 @@ def retrieval_decode(cfg: Mapping, q: torch.Tensor, k_cache: torch.Tensor,
         _dev(error_flags, "error_flags", torch.int32), _stream(stream)), "srkv_retrieval_decode")
 
 
+def sparse_paged_decode_prefix(cfg: Mapping, q: torch.Tensor, k_cache: torch.Tensor,
+                               v_cache: torch.Tensor, block_table: torch.Tensor,
+                               seq_lens: torch.Tensor, prefix_blocks: int, sel: torch.Tensor,
+                               nsel: torch.Tensor, out: torch.Tensor, workspace: torch.Tensor,
+                               error_flags: torch.Tensor | None = None, stream=None) -> None:
+    """srkv_sparse_paged_decode_prefix: the first prefix_blocks logical blocks of every request
+    are the same pages, attended once per kv head for all requests."""
+    B, max_blocks = _step_shapes(cfg, q, k_cache, v_cache, block_table, seq_lens, None, sel,
+                                 nsel, out)
+    c = config(cfg)
+    dt = _store_dtype(cfg)
+    _check(load().srkv_sparse_paged_decode_prefix(
+        ctypes.byref(c), _dev(q, "q", dt), _dev(k_cache, "k_cache", dt),
+        _dev(v_cache, "v_cache", dt), k_cache.shape[0],
+        _dev(block_table, "block_table", torch.int32), max_blocks,
+        _dev(seq_lens, "seq_lens", torch.int32), B, prefix_blocks,
+        _dev(sel, "sel", torch.int32), sel.shape[-1], _dev(nsel, "nsel", torch.int32),
+        _dev(out, "out", dt), _dev(workspace, "workspace"),
+        workspace.numel() * workspace.element_size(),
+        _dev(error_flags, "error_flags", torch.int32), _stream(stream)),
+        "srkv_sparse_paged_decode_prefix")
+
+
+def retrieval_decode_prefix(cfg: Mapping, q: torch.Tensor, k_cache: torch.Tensor,
+                            v_cache: torch.Tensor, reps: torch.Tensor, block_table: torch.Tensor,
+                            seq_lens: torch.Tensor, prompt_lens: torch.Tensor | None,
+                            prefix_blocks: int, sel: torch.Tensor, nsel: torch.Tensor,
+                            out: torch.Tensor, workspace: torch.Tensor,
+                            error_flags: torch.Tensor | None = None, stream=None) -> None:
+    """srkv_retrieval_decode_prefix: scoring and selection, then the decode with the shared
+    prefix attended once per kv head for all requests."""
+    B, max_blocks = _step_shapes(cfg, q, k_cache, v_cache, block_table, seq_lens, prompt_lens,
+                                 sel, nsel, out, reps, k_cache.shape[0])
+    c = config(cfg)
+    dt = _store_dtype(cfg)
+    _check(load().srkv_retrieval_decode_prefix(
+        ctypes.byref(c), _dev(q, "q", dt), _dev(k_cache, "k_cache", dt),
+        _dev(v_cache, "v_cache", dt), _dev(reps, "reps", torch.float32), k_cache.shape[0],
+        _dev(block_table, "block_table", torch.int32), max_blocks,
+        _dev(seq_lens, "seq_lens", torch.int32), _dev(prompt_lens, "prompt_lens", torch.int32),
+        B, prefix_blocks, _dev(sel, "sel", torch.int32), sel.shape[-1],
+        _dev(nsel, "nsel", torch.int32), _dev(out, "out", dt), _dev(workspace, "workspace"),
+        workspace.numel() * workspace.element_size(),
+        _dev(error_flags, "error_flags", torch.int32), _stream(stream)),
+        "srkv_retrieval_decode_prefix")
+
+
 def _host(t: torch.Tensor | None, name: str, dtype: torch.dtype):
     if t is None:
         return None
@@ -451,13 +515,14 @@ class DecodeBuffers:
     workspace and the error word.  Allocated once by torch (the library allocates none)."""
 
     def __init__(self, cfg: Mapping, batch: int, max_blocks: int, num_pages: int,
-                 device="cuda"):
+                 device="cuda", prefix: bool = False):
         Hq, Hkv, d = cfg["num_q_heads"], cfg["num_kv_heads"], cfg["head_dim"]
         self.kmax = max(1, kmax_bound(cfg, max_blocks))
         self.reps = torch.zeros(num_pages, Hkv, d, dtype=torch.float32, device=device)
         self.sel = torch.full((batch, Hkv, self.kmax), -1, dtype=torch.int32, device=device)
         self.nsel = torch.zeros(batch, Hkv, dtype=torch.int32, device=device)
         self.out = torch.zeros(batch, Hq, d, dtype=_store_dtype(cfg), device=device)
-        nbytes = decode_workspace_size(cfg, batch)
+        # prefix: sized for the shared-prefix calls too
+        nbytes = (prefix_decode_workspace_size if prefix else decode_workspace_size)(cfg, batch)
         self.workspace = torch.empty(max(nbytes, 256), dtype=torch.uint8, device=device)
         self.error_flags = torch.zeros(1, dtype=torch.int32, device=device)

@@ -80,6 +80,9 @@ typedef enum { SRKV_BF16 = 0, SRKV_F32 = 1 } srkv_dtype;
 #define SRKV_EFLAG_SELECTION 4u  /* nsel outside [0, kmax], or a sel entry that is not a
                                     candidate or not ascending; such entries were skipped */
 #define SRKV_EFLAG_TIMEOUT 8u    /* a bounded on-chip wait ran out; the kernel returned early */
+#define SRKV_EFLAG_PREFIX 16u    /* a request maps a block of the declared shared prefix to
+                                    another page than the batch's other requests (the
+                                    shared-prefix calls read one page for all of them) */
 
 /* Configuration: the method's knobs ("Configuration Parameters") and the head layout. */
 typedef struct {
@@ -291,6 +294,50 @@ srkv_status srkv_retrieval_decode_fp8(const srkv_config* cfg, const void* q, con
                                       int32_t kmax, int32_t* nsel, void* out, void* workspace,
                                       size_t workspace_bytes, int32_t* error_flags,
                                       srkv_stream stream);
+
+/*
+ * Shared-prefix decode (KV-cache survey "大模型推理百倍加速之KV cache篇", section "Share--KV
+ * cache共享": FlashInfer's cascade inference and Hydragen attend a prefix shared by a batch's
+ * requests once, as a matrix-matrix product over all their queries, and merge it with each
+ * request's own part like Flash-Decoding partials; the ATB reuse article, §2.1 and §3.3, keeps
+ * such prefix pages once and references them from every request).  The results are those of
+ * srkv_sparse_paged_decode / srkv_retrieval_decode on the same inputs: only the way the work
+ * is split changes.  The first prefix_blocks logical blocks of EVERY request must map to the
+ * same physical pages (block_table[r][b] == block_table[0][b] for b < prefix_blocks); the
+ * whole pages of that prefix a request's length covers are attended for all requests at once,
+ * one (page, kv head) slab read per group of up to 128 query rows, with each request's own
+ * rows of it (initial tokens, window, its selected blocks) masked in; the rest of each request
+ * goes through the split decode.  A request whose table breaks the contract inside its
+ * prefix flags SRKV_EFLAG_PREFIX (its result is then not the definition's).
+ *   prefix_blocks: 0 <= prefix_blocks <= max_blocks, at most 2048 (else
+ *     SRKV_ERR_UNSUPPORTED); 0 gives the plain call.
+ *   cfg: bf16, head_dim 128, group 1, 2, 4 or 8 (else SRKV_ERR_UNSUPPORTED).
+ *   workspace: >= srkv_prefix_decode_workspace_size(cfg, batch) bytes, 256-byte aligned.
+ *   Other arguments, ownership and errors: srkv_sparse_paged_decode / srkv_retrieval_decode.
+ *   Both calls always take the kernels of the split path (no one-kernel path); their output
+ *   is bitwise the same on every call.
+ */
+size_t srkv_prefix_decode_workspace_size(const srkv_config* cfg, int32_t batch);
+
+srkv_status srkv_sparse_paged_decode_prefix(const srkv_config* cfg, const void* q,
+                                            const void* k_cache, const void* v_cache,
+                                            int64_t num_pages, const int32_t* block_table,
+                                            int32_t max_blocks, const int32_t* seq_lens,
+                                            int32_t batch, int32_t prefix_blocks,
+                                            const int32_t* sel, int32_t kmax,
+                                            const int32_t* nsel, void* out, void* workspace,
+                                            size_t workspace_bytes, int32_t* error_flags,
+                                            srkv_stream stream);
+
+srkv_status srkv_retrieval_decode_prefix(const srkv_config* cfg, const void* q,
+                                         const void* k_cache, const void* v_cache,
+                                         const float* reps, int64_t num_pages,
+                                         const int32_t* block_table, int32_t max_blocks,
+                                         const int32_t* seq_lens, const int32_t* prompt_lens,
+                                         int32_t batch, int32_t prefix_blocks, int32_t* sel,
+                                         int32_t kmax, int32_t* nsel, void* out, void* workspace,
+                                         size_t workspace_bytes, int32_t* error_flags,
+                                         srkv_stream stream);
 
 /*
  * Number of kernels one srkv_retrieval_decode call with these arguments launches on the

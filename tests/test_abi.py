@@ -105,6 +105,30 @@ def test_decode_argument_checks(lib):
     assert _call_decode(lib, dict(cfg, dtype=1, num_q_heads=8 * 17)) == 2
 
 
+def test_prefix_argument_checks(lib):
+    cfg = srkv.default_config()
+    c = srkv.config(cfg)
+    fake = ctypes.c_void_p(1 << 20)
+
+    def call(cfg_, prefix, max_blocks=8, ws=None, ws_bytes=0):
+        cc = srkv.config(cfg_)
+        return lib.srkv_sparse_paged_decode_prefix(
+            ctypes.byref(cc), fake, fake, fake, 10, fake, max_blocks, fake, 1, prefix, fake, 8,
+            fake, fake, ws, ws_bytes, None, None)
+    assert call(cfg, -1) == 1
+    assert call(cfg, 9) == 1                                    # longer than the block table
+    assert call(dict(cfg, head_dim=64), 2) == 2                 # the cascade takes d 128
+    assert call(dict(cfg, num_q_heads=8 * 3), 2) == 2           # group 3
+    assert call(cfg, 2049, max_blocks=4096) == 2                # at most 2048 shared blocks
+    assert call(cfg, 2) == 3                                    # no workspace
+    small = srkv.decode_workspace_size(cfg, 1)
+    assert srkv.prefix_decode_workspace_size(cfg, 1) > small
+    assert call(cfg, 2, ws=fake, ws_bytes=small) == 3           # the plain call's is too small
+    assert lib.srkv_retrieval_decode_prefix(ctypes.byref(c), fake, fake, fake, fake, 10, fake, 8,
+                                            fake, None, 1, -1, fake, 8, fake, fake, None, 0,
+                                            None, None) == 1
+
+
 def test_score_topk_argument_checks(lib):
     cfg = dict(srkv.default_config(), dense_boundary=0)
     c = srkv.config(cfg)

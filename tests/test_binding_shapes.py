@@ -92,7 +92,23 @@ def call_quantize(**over):
                          a["k_scale"], a["v_scale"])
 
 
+def call_sparse_prefix(**over):
+    a = {**step_args(), **over}
+    srkv.sparse_paged_decode_prefix(CFG, a["q"], a["k_cache"], a["v_cache"], a["block_table"],
+                                    a["seq_lens"], 2, a["sel"], a["nsel"], a["out"],
+                                    a["workspace"])
+
+
+def call_retrieval_prefix(**over):
+    a = {**step_args(), **over}
+    srkv.retrieval_decode_prefix(CFG, a["q"], a["k_cache"], a["v_cache"], a["reps"],
+                                 a["block_table"], a["seq_lens"], a["prompt_lens"], 2, a["sel"],
+                                 a["nsel"], a["out"], a["workspace"])
+
+
 CALLS = {"retrieval_decode": call_retrieval, "sparse_paged_decode": call_sparse,
+         "sparse_paged_decode_prefix": call_sparse_prefix,
+         "retrieval_decode_prefix": call_retrieval_prefix,
          "score_topk": call_score, "sparse_paged_decode_noalloc": call_noalloc,
          "retrieval_decode_tiered": call_tiered, "retrieval_decode_fp8": call_fp8,
          "build_block_reps": call_reps, "append_kv": call_append,
@@ -115,6 +131,8 @@ WRONG = [
     ("retrieval_decode", dict(k_cache=torch.zeros(P, 2, 64, 64, dtype=bf))),  # page size
     ("sparse_paged_decode", dict(nsel=torch.zeros(B * 2, dtype=i32))),       # flattened
     ("sparse_paged_decode", dict(block_table=torch.zeros(B * MAXB, dtype=i32))),
+    ("sparse_paged_decode_prefix", dict(sel=torch.zeros(B, 1, KMAX, dtype=i32))),
+    ("retrieval_decode_prefix", dict(reps=torch.zeros(P - 1, 2, 64, dtype=f32))),
     ("score_topk", dict(prompt_lens=torch.zeros(B, 1, dtype=i32))),
     ("score_topk", dict(reps=torch.zeros(P, 1, 64, dtype=f32))),
     ("sparse_paged_decode_noalloc", dict(q=torch.zeros(B, 8, 64, 1, dtype=bf))),
