@@ -7,22 +7,28 @@
 // results the Flash-Decoding way.  Here one thread-block cluster does all of it for one
 // (request, kv head) unit, so nothing crosses a kernel boundary or global memory between
 // the steps:
-//   * every CTA scores its share of the candidates (select.cuh: keys, page ids and the top-8-
-//     bit histogram go to the leader, CTA 0, through distributed shared memory);
+//   * every CTA scores its share of the candidates (select.cuh: keys, page ids and the
+//     histograms of the top 12 and top 8 key bits go to the leader, CTA 0, through
+//     distributed shared memory); the shares split the most candidates the block table
+//     allows, so the table entries load alongside the request's length;
 //   * meanwhile the other CTAs' producer warps stream their share of the initial and window
 //     pages (list A) into the stage ring (decode_mma.cuh), through the scoring and the
 //     selection;
-//   * the leader selects (radix narrowing, ranked finish), writes sel / nsel, lays the kept
-//     blocks (page and block ids) out as a pool in its own shared memory and releases an
-//     mbarrier in every streaming CTA;
-//   * each streaming CTA attends its share of list A, then takes kept blocks from the pool one
-//     at a time (an atomic counter in the leader's shared memory) until it is empty, so the
-//     CTAs whose pages arrive sooner take more and all finish within about one page of each
-//     other; the merged partial (max, sum, unnormalised output) of the whole segment goes into
-//     the leader's shared memory when the pool is empty;
+//   * the leader selects: one warp finds the 12-bit bin holding the k-th largest key, lays
+//     every key above it out as the pool of kept blocks (page and block ids) in its own
+//     shared memory, ranks the bin's few keys for the rest, and releases each streaming CTA
+//     with its first kStatic pool entries (written into that CTA's shared memory) and an
+//     mbarrier arrival; sel / nsel are written after that.  A bin too large to rank at once
+//     falls back to radix narrowing and the ordered finish;
+//   * each streaming CTA attends its share of list A, then its kStatic entries, then takes
+//     kept blocks from the rest of the pool one at a time (an atomic counter in the leader's
+//     shared memory) until it is empty, so the CTAs whose pages arrive sooner take more and
+//     all finish within about one page of each other; the merged partial (max, sum,
+//     unnormalised output) of the whole segment goes into the leader's shared memory;
 //   * the leader merges the partials and writes the output.
 // Every wait is bounded (SRKV_EFLAG_TIMEOUT); every thread ends at one cluster barrier, so no
-// CTA leaves while another may still reach its shared memory.
+// CTA leaves while another may still reach its shared memory (the leader's consumers arrive
+// on it right after the release, the last time they reach another CTA).
 #include "decode_mma.cuh"
 #include "select.cuh"
 
@@ -33,6 +39,18 @@ constexpr int kSelThreads = kConsumerWarps * 32;  // the consumer warps score an
 constexpr int32_t kMaxCand = kFastRounds * kSelThreads;  // candidates per unit (1024)
 constexpr int kMaxShare = 128;                             // candidates scored per CTA
 constexpr int kMaxCluster = 16;                            // CTAs per unit, at most
+// Kept blocks a streaming CTA gets with the release (pool entries q, q + S, ... of streaming
+// CTA q of S), before it takes the rest from the shared counter.
+constexpr int kStatic = 4;
+static_assert(kStatic == 4, "the release carries two 16-byte stores");
+// The scoring counts the top 12 bits of the keys besides the top 8: on score sets like the
+// method's (a few hundred candidates, scores spread over a few units) the 12-bit bin holding
+// the k-th largest key then holds a few keys, and one warp finishes the selection in one pass
+// over the keys and one rank of that bin, with no barrier.
+constexpr int kHistBits = 12;
+constexpr int kBins = 1 << kHistBits;
+constexpr int kBinRank = 32;  // boundary bins up to this size are ranked by one warp
+static_assert(kMaxCand <= 1024, "bin ranks pack a candidate index into 10 bits");
 
 template <int D, bool F8 = false>
 struct FusedCfg {
@@ -42,22 +60,30 @@ struct FusedCfg {
   static constexpr size_t kOffBars = (C::kSmem + 15) & ~size_t(15);
   static constexpr size_t kOffQbar = kOffBars + 4 * sizeof(uint64_t);
   static constexpr size_t kOffShare = kOffQbar + sizeof(float) * D;
-  static constexpr size_t kSmem = kOffShare + sizeof(int32_t) * kMaxShare;
+  static constexpr size_t kOffMail = kOffShare + sizeof(int32_t) * kMaxShare;  // kStatic int2
+  static constexpr size_t kSmem = kOffMail + sizeof(int2) * kStatic;
   static constexpr size_t kSmemAlloc = kSmem + 1024;
   // the leader streams no pages: its K ring holds the selection state ...
   static constexpr size_t kOffKeys = C::kOffK;
   static constexpr size_t kOffPages = kOffKeys + sizeof(uint32_t) * kMaxCand;
   static constexpr size_t kOffHist = kOffPages + sizeof(int32_t) * kMaxCand;
-  static constexpr size_t kOffFin = kOffHist + sizeof(int32_t) * 3 * 256;
+  static constexpr size_t kOffHist12 = kOffHist + sizeof(int32_t) * 3 * 256;  // 16-byte aligned
+  static constexpr size_t kOffFin = kOffHist12 + sizeof(int32_t) * kBins;
   static constexpr size_t kOffKept = (kOffFin + sizeof(FinishShared<kSelThreads>) + 15) & ~size_t(15);
   static constexpr size_t kOffPool = kOffKept + sizeof(int32_t) * kMaxCand;  // int2 (page, block)
   static constexpr size_t kOffTaken = kOffPool + sizeof(int2) * kMaxCand;    // pool counter
-  static constexpr size_t kSelEnd = kOffTaken + 16;
+  static constexpr size_t kOffBnd = kOffTaken + 16;  // boundary-bin candidates, their ranks' keys
+  static constexpr size_t kOffBinKey = kOffBnd + sizeof(int32_t) * kBinRank;
+  static constexpr size_t kOffKeepBits = kOffBinKey + sizeof(uint32_t) * kBinRank;  // a bit per candidate
+  static constexpr size_t kOffFast = kOffKeepBits + sizeof(uint32_t) * (kMaxCand / 32);
+  static constexpr size_t kSelEnd = kOffFast + 16;
   // ... and its V ring the streaming CTAs' partials: acc [15][8][D], then (m, l) [15][8][2]
   static constexpr size_t kOffPartAcc = C::kOffV;
   static constexpr size_t kOffPartMl = kOffPartAcc + sizeof(float) * (kMaxCluster - 1) * 8 * D;
   static constexpr size_t kPartEnd = kOffPartMl + sizeof(float) * (kMaxCluster - 1) * 8 * 2;
   static_assert(kSelEnd <= C::kOffV, "selection state fits in the K ring");
+  static_assert(kOffHist % 16 == 0 && kOffBinKey % 16 == 0 && kOffMail % 16 == 0,
+                "vector accesses");
   static_assert(kPartEnd <= C::kOffQ, "partials fit in the V ring");
   static_assert(kSmemAlloc <= 232448, "shared memory opt-in limit");
   // Stages of list A a streaming CTA copies before its own scoring loads have returned.
@@ -88,6 +114,7 @@ __global__ void __maxnreg__(128) fused_decode_kernel(const DecodeArgs a,
   uint64_t* scored = keys_ready + 3;
   float* qbar = reinterpret_cast<float*>(smem + F::kOffQbar);
   int32_t* share = reinterpret_cast<int32_t*>(smem + F::kOffShare);
+  int2* mail = reinterpret_cast<int2*>(smem + F::kOffMail);  // the release's pool entries
   uint32_t* keys = reinterpret_cast<uint32_t*>(smem + F::kOffKeys);    // leader
   int32_t* pages = reinterpret_cast<int32_t*>(smem + F::kOffPages);    // leader
   int32_t(*hist)[256] = reinterpret_cast<int32_t(*)[256]>(smem + F::kOffHist);  // leader
@@ -95,6 +122,11 @@ __global__ void __maxnreg__(128) fused_decode_kernel(const DecodeArgs a,
   int32_t* kept_list = reinterpret_cast<int32_t*>(smem + F::kOffKept);  // leader
   int2* pool = reinterpret_cast<int2*>(smem + F::kOffPool);              // leader
   uint32_t* taken = reinterpret_cast<uint32_t*>(smem + F::kOffTaken);    // leader
+  int32_t* hist12 = reinterpret_cast<int32_t*>(smem + F::kOffHist12);    // leader
+  int32_t* bnd = reinterpret_cast<int32_t*>(smem + F::kOffBnd);          // leader
+  uint32_t* bin_key = reinterpret_cast<uint32_t*>(smem + F::kOffBinKey);  // leader
+  uint32_t* keepbits = reinterpret_cast<uint32_t*>(smem + F::kOffKeepBits);  // leader
+  int32_t* fast_flag = reinterpret_cast<int32_t*>(smem + F::kOffFast);   // leader
   float* part_acc = reinterpret_cast<float*>(smem + F::kOffPartAcc);  // leader
   float* part_ml = reinterpret_cast<float*>(smem + F::kOffPartMl);    // leader
 
@@ -104,6 +136,7 @@ __global__ void __maxnreg__(128) fused_decode_kernel(const DecodeArgs a,
   const int32_t u = blockIdx.x / CS;
   const int32_t r = u / a.Hkv, h = u % a.Hkv;
   const bool leader = crank == 0;
+  bool arrived = false;  // on the closing cluster barrier (warp-uniform)
 
   if (tid == 0) {
     init_ring<D, F8>(smem);
@@ -113,9 +146,10 @@ __global__ void __maxnreg__(128) fused_decode_kernel(const DecodeArgs a,
     mbar_init(scored, kConsumerWarps);          // each consumer warp, its scores computed
     fence_mbar_init();
   }
-  if (leader) {
-    for (int i = tid; i < 3 * 256; i += blockDim.x) (&hist[0][0])[i] = 0;
-    if (tid == 0) *taken = 0u;
+  if (leader) {  // the histograms (contiguous) and the pool counter
+    int4* h4 = reinterpret_cast<int4*>(&hist[0][0]);
+    for (int i = tid; i < (3 * 256 + kBins) / 4; i += blockDim.x) h4[i] = make_int4(0, 0, 0, 0);
+    if (tid == 0) *taken = (uint32_t)(kStatic * S);  // entries below go with the release
   }
   __syncthreads();
   cluster_arrive();  // this CTA's barriers and the leader's histogram are ready (waited for
@@ -138,7 +172,19 @@ __global__ void __maxnreg__(128) fused_decode_kernel(const DecodeArgs a,
       if (j < a.G) qv[j] = __bfloat162float(qp[(int64_t)j * D]);
   }
 
-  // The unit's sizes: candidates n, kept k (what the selection will write), list A length.
+  // This CTA's page of each candidate of its scoring share.  The shares split the candidates
+  // a request of the table can have at most (nmax), not the request's own: the table entries
+  // then load alongside the request's length instead of after it.
+  const int32_t b_lo = a.init_tokens / kBlock;
+  const int32_t Wmax = a.max_blocks * kBlock - a.local_tokens;
+  const int32_t nmax = Wmax > a.init_tokens ? (Wmax + kBlock - 1) / kBlock - b_lo : 0;
+  const int32_t s_lo = share_begin((int32_t)crank, nmax, (int32_t)CS);
+  const int32_t s_hi = share_begin((int32_t)crank + 1, nmax, (int32_t)CS);  // <= kMaxShare apart
+  const int32_t* bt_r = a.block_table + (int64_t)r * a.max_blocks;
+  int32_t my_page = -1;  // b_lo + nmax <= max_blocks: inside the request's table row
+  if (tid < s_hi - s_lo) my_page = bt_r[b_lo + s_lo + tid];
+
+  // The unit's sizes: candidates n (<= nmax), kept k (what the selection will write), list A.
   const int32_t L_in = a.seq_lens[r];
   const int32_t prompt = a.prompt_lens ? a.prompt_lens[r] : L_in;
   const SelCount sc = selection_count(L_in, prompt, a.max_blocks, a.kmax, a.init_tokens,
@@ -147,8 +193,6 @@ __global__ void __maxnreg__(128) fused_decode_kernel(const DecodeArgs a,
   uint32_t geflags = 0;
   const Geom g = make_geom(L_in, k, a.max_blocks, a.kmax, a.init_tokens, a.local_tokens, geflags);
   const int32_t nA = list_a_count(g);
-  const int32_t b_lo = a.init_tokens / kBlock;
-  const int32_t* bt_r = a.block_table + (int64_t)r * a.max_blocks;
   const int32_t q = (int32_t)crank - 1;  // streaming rank
   const int32_t a0 = leader ? 0 : share_begin(q, nA, S), a1 = leader ? 0 : share_begin(q + 1, nA, S);
 
@@ -190,9 +234,11 @@ __global__ void __maxnreg__(128) fused_decode_kernel(const DecodeArgs a,
           ++it;
         }
       }
-      // list B: kept blocks from the leader's pool until it is empty.  Lane 0 takes the entries
-      // (a cluster atomic, then a cluster load) one ahead: the next entry is taken before the
-      // current one waits for a free stage, and read by the other lanes only after that wait.
+      // list B: the kStatic entries that came with the release, then kept blocks from the
+      // leader's pool until it is empty.  Lane 0 takes the entries (a cluster atomic, then a
+      // cluster load) one ahead: the first atomic goes out before the release's entries are
+      // issued, each next one before the current entry waits for a free stage; the other
+      // lanes read an entry only after that wait.
       if (k > 0 && !abort) {
         bool ok = true;
         if (lane == 0) ok = mbar_wait_cluster(list_ready, 0);
@@ -201,21 +247,9 @@ __global__ void __maxnreg__(128) fused_decode_kernel(const DecodeArgs a,
           abort = true;
         }
       }
-      auto take = [&](int2& e) -> bool {  // lane 0
-        const uint32_t i = atom_cluster_add(taken, 0, 1u);
-        if (i >= (uint32_t)k) return false;
-        e = ld_cluster_int2(pool + i, 0);
-        return true;
-      };
-      int2 e0 = make_int2(-1, 0);  // lane 0's entry
-      bool have = false;
-      if (k > 0 && !abort && lane == 0) have = take(e0);
-      have = __shfl_sync(0xffffffffu, have, 0);
-      while (have && !abort) {
-        const int2 e = make_int2(__shfl_sync(0xffffffffu, e0.x, 0), __shfl_sync(0xffffffffu, e0.y, 0));
-        int2 next0 = make_int2(-1, 0);
-        bool more = false;
-        if (lane == 0) more = take(next0);
+      uint32_t first = 0xffffffffu;  // lane 0: the first entry taken from the counter
+      if (k > 0 && !abort && lane == 0) first = atom_cluster_add(taken, 0, 1u);
+      auto issue_b = [&](const int2 e) {  // kept block (page, block id)
         PageTask t;
         t.page = -1;
         t.lo = t.hi = t.ie = t.ws = 0;
@@ -234,6 +268,34 @@ __global__ void __maxnreg__(128) fused_decode_kernel(const DecodeArgs a,
         issue_stage_warp<D, F8>(a, maps, smem, it, u, it == 0 ? kNewUnit : 0u, t, armed, abort,
                             eflags, lane);
         ++it;
+      };
+      if (k > 0 && !abort) {
+#pragma unroll 1
+        for (int j = 0; j < kStatic && !abort; ++j) {
+          const int2 e = mail[j];
+          if (e.y < 0) break;  // beyond the pool
+          issue_b(e);
+        }
+      }
+      auto take = [&](int2& e) -> bool {  // lane 0
+        const uint32_t i = atom_cluster_add(taken, 0, 1u);
+        if (i >= (uint32_t)k) return false;
+        e = ld_cluster_int2(pool + i, 0);
+        return true;
+      };
+      int2 e0 = make_int2(-1, 0);  // lane 0's entry
+      bool have = false;
+      if (lane == 0 && first < (uint32_t)k) {
+        e0 = ld_cluster_int2(pool + first, 0);
+        have = true;
+      }
+      have = __shfl_sync(0xffffffffu, have, 0) && !abort;
+      while (have && !abort) {
+        const int2 e = make_int2(__shfl_sync(0xffffffffu, e0.x, 0), __shfl_sync(0xffffffffu, e0.y, 0));
+        int2 next0 = make_int2(-1, 0);
+        bool more = false;
+        if (lane == 0) more = take(next0);
+        issue_b(e);
         e0 = next0;
         have = __shfl_sync(0xffffffffu, more, 0);
       }
@@ -260,9 +322,7 @@ __global__ void __maxnreg__(128) fused_decode_kernel(const DecodeArgs a,
     // ------------------------------------------------------------------ consumers
     auto bar = [] { named_bar_sync(1, kSelThreads); };
     // 1. this CTA's share of the candidates: table entries and the group query sum
-    const int32_t s_lo = share_begin((int32_t)crank, n, (int32_t)CS);
-    const int32_t s_hi = share_begin((int32_t)crank + 1, n, (int32_t)CS);
-    for (int32_t i = s_lo + tid; i < s_hi; i += kSelThreads) share[i - s_lo] = bt_r[b_lo + i];
+    if (tid < s_hi - s_lo) share[tid] = my_page;
     if (tid < D) {  // the group query sum, in head order
       float s = 0.f;
 #pragma unroll
@@ -271,12 +331,12 @@ __global__ void __maxnreg__(128) fused_decode_kernel(const DecodeArgs a,
       qbar[tid] = s;
     }
     bar();
-    // 2. scores into the leader (keys, pages, top-8-bit histogram)
+    // 2. scores into the leader (keys, pages, histograms of the top 12 and 8 key bits)
     // keys go to the leader once every CTA has passed its setup (cluster barrier)
     bool waited = false;
-    uint32_t eflags = score_share<D, kConsumerWarps>(
-        qbar, share, s_lo, s_hi, a.reps, total_pages(a), a.Hkv, h, keys, &hist[0][0], pages, warp,
-        lane,
+    uint32_t eflags = score_share<D, kConsumerWarps, kHistBits>(
+        qbar, share, s_lo, min(s_hi, n), a.reps, total_pages(a), a.Hkv, h, keys, hist12,
+        &hist[0][0], pages, warp, lane,
         [&] {
           cluster_wait();
           waited = true;
@@ -290,45 +350,160 @@ __global__ void __maxnreg__(128) fused_decode_kernel(const DecodeArgs a,
       mbar_arrive_cluster_n(keys_ready, 0, (uint32_t)(kMaxCand - n));
 
     if (leader) {
-      // 3. select the k kept blocks, write sel / nsel, lay out the pool of kept blocks
+      // 3. select the k kept blocks, lay them out as the pool of kept blocks (page, block),
+      // release the streaming CTAs, then write sel / nsel for the caller (nobody in the
+      // cluster reads them)
       if (!mbar_wait_cluster(keys_ready, 0)) {
         if (tid == 0) raise_flags(a.error_flags, SRKV_EFLAG_TIMEOUT);
       }
       int32_t kept = 0;
-      if (k == n) {
-        for (int32_t i = tid; i < n; i += kSelThreads) kept_list[i] = i;
-        kept = n;
-      } else if (k > 0) {
-        const RadixState rs = radix_narrow<kSelThreads>(keys, n, k, hist, tid, bar);
-        kept = finish_fast<kSelThreads>(keys, n, rs, fin, tid, bar,
-                                        [&](int32_t pos, int32_t i) { kept_list[pos] = i; });
+      int32_t* sel_u = a.sel_out + (int64_t)u * a.kmax;
+      const bool partial = k > 0 && k < n;
+      // Streaming CTA qq's release: its pool entries qq, qq + S, ... (up to kStatic; (-1, -1)
+      // beyond the pool) into its shared memory, then its list_ready (which orders them).
+      auto release = [&](int32_t qq) {
+        int2 e[kStatic];
+#pragma unroll
+        for (int j = 0; j < kStatic; ++j) {
+          const int32_t p = qq + j * S;
+          e[j] = p < k ? pool[p] : make_int2(-1, -1);
+        }
+        int4* m4 = reinterpret_cast<int4*>(mail);
+        st_cluster_int4(m4, (uint32_t)qq + 1, make_int4(e[0].x, e[0].y, e[1].x, e[1].y));
+        st_cluster_int4(m4 + 1, (uint32_t)qq + 1, make_int4(e[2].x, e[2].y, e[3].x, e[3].y));
+        mbar_arrive_cluster(list_ready, (uint32_t)qq + 1);
+      };
+      if (partial && warp == 0) {
+        // Warp 0: the 12-bit bin holding the k-th largest key.  Every key above it is kept:
+        // into the pool (the keys above, in block order) and the kept bits; the bin's keys
+        // (at most kBinRank) are ranked and the first k - (keys above) follow in the pool.
+        // (The count checks only matter if some scores never arrived: flagged.)
+        const Boundary bd = warp_boundary(&hist[0][0], hist12, k, lane);
+        const bool fast = bd.cnt <= kBinRank;
+        if (fast) {
+          const uint32_t lt = (1u << lane) - 1u;
+          const uint32_t dsel = (uint32_t)bd.digit;
+          int32_t na = 0, nb = 0;  // keys above the bin, in it, so far
+          // 8 rounds of 32 keys at a time: their loads first, then the stores
+#pragma unroll 1
+          for (int32_t g0 = 0; g0 < n; g0 += 8 * 32) {
+            uint32_t kk[8];
+            int32_t pg[8];
+#pragma unroll
+            for (int x = 0; x < 8; ++x) {
+              const int32_t i = g0 + 32 * x + lane;
+              kk[x] = i < n ? keys[i] : 0u;
+              pg[x] = i < n ? pages[i] : -1;
+            }
+            // the rounds' votes, then their counts (independent), then the stores
+            uint32_t ma[8], mb[8];
+#pragma unroll
+            for (int x = 0; x < 8; ++x) {
+              const int32_t i = g0 + 32 * x + lane;
+              const uint32_t dg = kk[x] >> (32 - kHistBits);
+              ma[x] = __ballot_sync(0xffffffffu, i < n && dg > dsel);
+              mb[x] = __ballot_sync(0xffffffffu, i < n && dg == dsel);
+            }
+#pragma unroll
+            for (int x = 0; x < 8; ++x) {
+              const int32_t i0 = g0 + 32 * x, i = i0 + lane;
+              if (i0 >= n) break;  // uniform
+              const int32_t sa = na + __popc(ma[x] & lt), sb = nb + __popc(mb[x] & lt);
+              if (((ma[x] >> lane) & 1u) && sa < k) pool[sa] = make_int2(pg[x], b_lo + i);
+              if (((mb[x] >> lane) & 1u) && sb < kBinRank) {
+                // rank key: the key's low bits (its top bits are the bin's), then the lower
+                // block; unique, larger = kept first
+                bnd[sb] = i;
+                bin_key[sb] = ((kk[x] & ((1u << (32 - kHistBits)) - 1u)) << 10) |
+                              (uint32_t)(kMaxCand - 1 - i);
+              }
+              if (lane == 0) keepbits[i0 >> 5] = ma[x];
+              na += __popc(ma[x]);
+              nb += __popc(mb[x]);
+            }
+          }
+          __syncwarp();
+          const int32_t nbin = min(nb, kBinRank), nab = min(na, k);
+          const uint32_t mine = lane < nbin ? bin_key[lane] : 0u;
+          int32_t rank = 0;
+#pragma unroll
+          for (int j = 0; j < kBinRank; j += 4) {
+            const uint4 v = *reinterpret_cast<const uint4*>(bin_key + j);
+            rank += (j < nbin && v.x > mine) + (j + 1 < nbin && v.y > mine) +
+                    (j + 2 < nbin && v.z > mine) + (j + 3 < nbin && v.w > mine);
+          }
+          const bool take = lane < nbin && rank < k - nab;
+          const uint32_t m = __ballot_sync(0xffffffffu, take);
+          if (take) {
+            const int32_t i = bnd[lane], slot = nab + __popc(m & lt);
+            if (slot < k) pool[slot] = make_int2(pages[i], b_lo + i);
+            atomicOr(&keepbits[i >> 5], 1u << (i & 31));
+          }
+          for (int32_t p = nab + __popc(m) + lane; p < k; p += 32) pool[p] = make_int2(-1, 0);
+          __syncwarp();  // the pool is complete
+          if (lane < S) release(lane);
+        }
+        if (lane == 0) *fast_flag = fast;
       }
       bar();
-      // the pool: k entries (an entry the selection did not fill has no page); the barrier
-      // orders every thread's entries before the releases below
-      for (int32_t p = tid; p < k; p += kSelThreads)
-        pool[p] = p < kept ? make_int2(pages[kept_list[p]], b_lo + kept_list[p]) : make_int2(-1, 0);
-      bar();
-      for (int32_t qq = tid; qq < S; qq += kSelThreads) mbar_arrive_cluster(list_ready, (uint32_t)qq + 1);
-      // the selection, for the caller (nobody in the cluster reads it)
-      int32_t* sel_u = a.sel_out + (int64_t)u * a.kmax;
-      for (int32_t p = tid; p < kept; p += kSelThreads) sel_u[p] = b_lo + kept_list[p];
+      if (partial && *fast_flag) {
+        // sel in block order: a kept candidate's slot = kept candidates of the earlier words
+        // of the kept bits + the earlier bits of its own word
+        const uint32_t lt = (1u << lane) - 1u;
+        const int32_t words = (n + 31) >> 5;
+        const int32_t wofs =
+            warp_exclusive_scan(lane < words ? __popc(keepbits[lane]) : 0, lane, &kept);
+        for (int32_t i0 = 0; i0 < n; i0 += kSelThreads) {
+          const int32_t i = i0 + tid, w = (i0 >> 5) + warp;
+          const uint32_t bits = i < n ? keepbits[w] : 0u;
+          const int32_t pos = __shfl_sync(0xffffffffu, wofs, w) + __popc(bits & lt);
+          if (((bits >> lane) & 1u) && pos < k) sel_u[pos] = b_lo + i;
+        }
+        kept = min(kept, k);
+      } else {
+        // k == n (every candidate), k == 0, or a boundary bin too large to rank at once:
+        // radix narrowing from the top-8-bit histogram, then the ordered finish
+        if (k == n) {
+          for (int32_t i = tid; i < n; i += kSelThreads) kept_list[i] = i;
+          kept = n;
+        } else if (k > 0) {
+          const RadixState rs = radix_narrow<kSelThreads>(keys, n, k, hist, tid, bar);
+          kept = finish_fast<kSelThreads>(keys, n, rs, fin, tid, bar,
+                                          [&](int32_t pos, int32_t i) { kept_list[pos] = i; });
+        }
+        bar();
+        // the pool: k entries (an entry the selection did not fill has no page); the barrier
+        // orders every thread's entries before the releases below
+        for (int32_t p = tid; p < k; p += kSelThreads)
+          pool[p] = p < kept ? make_int2(pages[kept_list[p]], b_lo + kept_list[p]) : make_int2(-1, 0);
+        bar();
+        for (int32_t qq = tid; qq < S; qq += kSelThreads) release(qq);
+        for (int32_t p = tid; p < kept; p += kSelThreads) sel_u[p] = b_lo + kept_list[p];
+      }
       if (tid == 0) {
         a.nsel_out[u] = kept;
         if (kept != k) raise_flags(a.error_flags, SRKV_EFLAG_SELECTION);
       }
-      // 4. merge the streaming CTAs' partials (warp w: query head w of the group)
+      // The leader reaches no other CTA's shared memory after the release: its consumers
+      // arrive on the closing cluster barrier now, while they would only wait (the arrival
+      // orders their earlier accesses), so the barrier is done by the time they have merged.
+      cluster_arrive();
+      arrived = true;
+      // 4. merge the streaming CTAs' partials: query head w % G, half w / G of d (G <= 4; with
+      // G = 8, both halves of head w)
       if (!mbar_wait_cluster(parts_ready, 0)) {
         if (tid == 0) raise_flags(a.error_flags, SRKV_EFLAG_TIMEOUT);
       }
-      if (warp < a.G) {
+      const int32_t hw = a.G <= 4 ? 2 : 1;  // warps per head
+      if (warp < a.G * hw) {
         // lane qq holds the (max, sum) of streaming CTA qq; weights by shuffles, then every
         // lane adds its d-slice of the weighted partials
-        constexpr int V = D / 32;
+        constexpr int V = D / 64;  // values per lane in half of d
+        const int32_t head = warp % a.G;
         float m = -INFINITY, l = 0.f;  // a CTA that attended nothing wrote (-inf, 0)
         if (lane < S) {
-          m = part_ml[(lane * a.G + warp) * 2];
-          l = part_ml[(lane * a.G + warp) * 2 + 1];
+          m = part_ml[(lane * a.G + head) * 2];
+          l = part_ml[(lane * a.G + head) * 2 + 1];
         }
         float mx = m;
 #pragma unroll
@@ -337,47 +512,47 @@ __global__ void __maxnreg__(128) fused_decode_kernel(const DecodeArgs a,
         float l_run = w * l;
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) l_run += __shfl_xor_sync(0xffffffffu, l_run, o);
-        // every streaming CTA wrote a partial (zeros if it attended nothing).  The loads and
-        // weight shuffles of a batch of 8 slots are unconditional, so they issue together
-        // (the partial area holds kMaxCluster - 1 slots, so every address is in it); a select
-        // drops the slots beyond S and those of weight 0
-        float acc[V];
+        for (int32_t half = warp / a.G; half < 2; half += hw) {
+          // every streaming CTA wrote a partial (zeros if it attended nothing).  The loads and
+          // weight shuffles of a batch of 8 slots are unconditional, so they issue together
+          // (the partial area holds kMaxCluster - 1 slots, so every address is in it); a
+          // select drops the slots beyond S and those of weight 0
+          const int32_t d0 = half * (D / 2) + lane * V;
+          float acc[V];
 #pragma unroll
-        for (int e = 0; e < V; ++e) acc[e] = 0.f;
+          for (int e = 0; e < V; ++e) acc[e] = 0.f;
 #pragma unroll
-        for (int b0 = 0; b0 < kMaxCluster - 1; b0 += 8) {
-          float x[8][V], wv[8];
+          for (int b0 = 0; b0 < kMaxCluster - 1; b0 += 8) {
+            float x[8][V], wv[8];
 #pragma unroll
-          for (int j = 0; j < 8; ++j) {
-            const int qq = b0 + j < kMaxCluster - 1 ? b0 + j : kMaxCluster - 2;
-            wv[j] = __shfl_sync(0xffffffffu, w, qq);
-            const float* src = part_acc + (qq * a.G + warp) * D + lane * V;
-            if constexpr (V == 4) {
-              const float4 v4 = *reinterpret_cast<const float4*>(src);
-              x[j][0] = v4.x;
-              x[j][1] = v4.y;
-              x[j][2] = v4.z;
-              x[j][3] = v4.w;
-            } else {
-              const float2 v2 = *reinterpret_cast<const float2*>(src);
-              x[j][0] = v2.x;
-              x[j][1] = v2.y;
+            for (int j = 0; j < 8; ++j) {
+              const int qq = b0 + j < kMaxCluster - 1 ? b0 + j : kMaxCluster - 2;
+              wv[j] = __shfl_sync(0xffffffffu, w, qq);
+              const float* src = part_acc + (qq * a.G + head) * D + d0;
+              if constexpr (V == 2) {
+                const float2 v2 = *reinterpret_cast<const float2*>(src);
+                x[j][0] = v2.x;
+                x[j][1] = v2.y;
+              } else {
+                x[j][0] = *src;
+              }
+            }
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+              const bool use = b0 + j < S && wv[j] != 0.f;
+#pragma unroll
+              for (int e = 0; e < V; ++e) acc[e] = use ? fmaf(wv[j], x[j][e], acc[e]) : acc[e];
             }
           }
-#pragma unroll
-          for (int j = 0; j < 8; ++j) {
-            const bool use = b0 + j < S && wv[j] != 0.f;
-#pragma unroll
-            for (int e = 0; e < V; ++e) acc[e] = use ? fmaf(wv[j], x[j][e], acc[e]) : acc[e];
+          __nv_bfloat16* o = static_cast<__nv_bfloat16*>(a.out) +
+                             ((int64_t)r * a.Hq + (int64_t)h * a.G + head) * D + d0;
+          if constexpr (V == 2) {
+            const float x0 = l_run > 0.f ? acc[0] / l_run : 0.f;
+            const float x1 = l_run > 0.f ? acc[1] / l_run : 0.f;
+            *reinterpret_cast<__nv_bfloat162*>(o) = __floats2bfloat162_rn(x0, x1);
+          } else {
+            *o = __float2bfloat16_rn(l_run > 0.f ? acc[0] / l_run : 0.f);
           }
-        }
-        __nv_bfloat16* o = static_cast<__nv_bfloat16*>(a.out) +
-                           ((int64_t)r * a.Hq + (int64_t)h * a.G + warp) * D + lane * V;
-#pragma unroll
-        for (int e = 0; e < V; e += 2) {
-          const float x0 = l_run > 0.f ? acc[e] / l_run : 0.f;
-          const float x1 = l_run > 0.f ? acc[e + 1] / l_run : 0.f;
-          *reinterpret_cast<__nv_bfloat162*>(o + e) = __floats2bfloat162_rn(x0, x1);
         }
       }
     } else {
@@ -395,8 +570,10 @@ __global__ void __maxnreg__(128) fused_decode_kernel(const DecodeArgs a,
       if (warp == 0) mbar_arrive_cluster(parts_ready, 0);
     }
   }
+  // nobody leaves while another CTA may still reach its shared memory
   __syncwarp();
-  cluster_sync();  // nobody leaves while another CTA may still reach its shared memory
+  if (!arrived) cluster_arrive();
+  cluster_wait();
 }
 
 }  // namespace

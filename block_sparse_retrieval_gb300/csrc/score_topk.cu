@@ -120,7 +120,8 @@ __global__ void __launch_bounds__(kThreads, 4) score_topk_kernel(ScoreArgs a) {
   // 2. scores of the share, one warp per candidate, into the leader's keys and histogram
   cluster_wait();
   eflags |= score_share<D, kWarps>(qbar, pages, s_lo, min(s_hi, n), a.reps, a.num_pages, a.Hkv,
-                                   h, keys, &hist[0][0], nullptr, warp, lane, [] {}, [] {});
+                                   h, keys, &hist[0][0], nullptr, nullptr, warp, lane, [] {},
+                                   [] {});
   if (lane == 0 && eflags) raise_flags(a.error_flags, eflags);
   cluster_sync();  // every key and the pass-0 histogram are in the leader
   if (crank != 0) return;

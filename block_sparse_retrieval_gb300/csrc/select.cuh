@@ -9,10 +9,13 @@
 //
 //   score_share: one warp per candidate, q_bar . rep in fp32 (fixed lane order); the key is
 //                stored into the leader CTA's shared memory and counted into the leader's
-//                histogram of the top 8 key bits, through distributed shared memory;
-//   radix_narrow: MSB-first radix passes of 8 bits (the first from that histogram) until the
-//                bin holding the k-th key has at most 32 keys (or four passes, when the k-th
-//                key is known exactly);
+//                histogram of the top 8 key bits (or of the top 12 and the top 8), through
+//                distributed shared memory;
+//   warp_boundary: from the 8- and 12-bit histograms, the 12-bit bin holding the k-th key
+//                (the fused decode ranks that bin with one warp when it is small);
+//   radix_narrow: MSB-first radix passes of 8 bits (the first from the 8-bit histogram)
+//                until the bin holding the k-th key has at most 32 keys (or four passes,
+//                when the k-th key is known exactly);
 //   finish_fast: one warp ranks that bin (score, then lower block); a kept key's output slot
 //                is the number of kept keys before it in block order, from ballot counts.
 #pragma once
@@ -55,6 +58,14 @@ __device__ __forceinline__ void st_cluster_u32(uint32_t* local, uint32_t rank, u
   uint32_t remote;
   asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(smem_u32(local)), "r"(rank));
   asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(remote), "r"(v) : "memory");
+}
+// 16-byte store to the same shared-memory offset in CTA `rank` (16-byte aligned).
+__device__ __forceinline__ void st_cluster_int4(int4* local, uint32_t rank, int4 v) {
+  uint32_t remote;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(smem_u32(local)), "r"(rank));
+  asm volatile("st.shared::cluster.v4.s32 [%0], {%1, %2, %3, %4};" ::"r"(remote), "r"(v.x), "r"(v.y),
+               "r"(v.z), "r"(v.w)
+               : "memory");
 }
 // Atomic add to the same shared-memory offset in CTA `rank` of this cluster.
 __device__ __forceinline__ void red_cluster_add(int32_t* local, uint32_t rank, int32_t v) {
@@ -162,7 +173,8 @@ __device__ __forceinline__ bool mbar_wait_cluster(uint64_t* bar, uint32_t parity
 
 // Scores candidates [s_lo, i_hi) of unit (r, h), one warp per candidate, 8 candidates of a
 // warp in one round of loads; lane x of the warp stores its x-th key into the leader's
-// keys[i] and counts it into the leader's hist0 (and, with pages_to_leader, the
+// keys[i] and counts it into the leader's histogram of the top kHistBits key bits, hist
+// (and, with leader_coarse, into that of the top 8 bits; with leader_pages, the
 // candidate's page into the leader's pages[i]).  `pages` holds the share's pages at
 // [i - s_lo].  issued() runs once, right after the warp's first round of vector loads has
 // been issued (before any of them is used; it may wait, e.g. for the cluster barrier that
@@ -170,12 +182,14 @@ __device__ __forceinline__ bool mbar_wait_cluster(uint64_t* bar, uint32_t parity
 // of range).
 //
 // stored() runs on every lane that wrote a key, after its writes (e.g. to release them).
-template <int D, int kWarps, typename Issued, typename Stored>
+// kHistBits: the histogram counts the top kHistBits bits of the keys (2^kHistBits bins).
+template <int D, int kWarps, int kHistBits = 8, typename Issued, typename Stored>
 __device__ __forceinline__ uint32_t score_share(const float* qbar, const int32_t* pages,
                                                 int32_t s_lo, int32_t i_hi, const float* reps,
                                                 int64_t num_pages, int32_t Hkv, int32_t h,
-                                                uint32_t* leader_keys, int32_t* leader_hist0,
-                                                int32_t* leader_pages, int warp, int lane,
+                                                uint32_t* leader_keys, int32_t* leader_hist,
+                                                int32_t* leader_coarse, int32_t* leader_pages,
+                                                int warp, int lane,
                                                 Issued issued, Stored stored) {
   constexpr int EPL = D / 32;  // elements per lane: 4 (d 128) or 2 (d 64)
   uint32_t eflags = 0;
@@ -240,9 +254,13 @@ __device__ __forceinline__ uint32_t score_share(const float* qbar, const int32_t
         st_cluster_u32(reinterpret_cast<uint32_t*>(&leader_pages[i]), 0,
                        (uint32_t)pages[i - s_lo]);
     }
-    const uint32_t digit = valid ? key >> 24 : 0xffffffffu;
+    const uint32_t digit = valid ? key >> (32 - kHistBits) : 0xffffffffu;
     const uint32_t peers = __match_any_sync(0xffffffffu, digit);
-    if (valid && lane == __ffs(peers) - 1) red_cluster_add(&leader_hist0[digit], 0, __popc(peers));
+    if (valid && lane == __ffs(peers) - 1) {
+      red_cluster_add(&leader_hist[digit], 0, __popc(peers));
+      if (kHistBits > 8 && leader_coarse)
+        red_cluster_add(&leader_coarse[digit >> (kHistBits - 8)], 0, __popc(peers));
+    }
     if (valid) stored();
   }
   return __reduce_or_sync(0xffffffffu, eflags);
@@ -297,6 +315,39 @@ __device__ __forceinline__ RadixState radix_narrow(const uint32_t* keys, int32_t
     }
   }
   return rs;
+}
+
+// Where the k-th largest key lies, from the histograms of the top 8 key bits (coarse, 256
+// bins) and of the top 12 (fine, 4096 bins) of the same keys: the fine bin (digit), the keys
+// in higher fine bins (above) and in the bin (cnt).  One warp; every lane gets the result.
+// 1 <= k <= the histograms' total (else the bin reported holds INT32_MAX keys).
+struct Boundary {
+  int32_t digit, above, cnt;
+};
+__device__ __forceinline__ Boundary warp_boundary(const int32_t* coarse, const int32_t* fine,
+                                                  int32_t k, int lane) {
+  Boundary bd;
+  bd.digit = 0;
+  bd.above = 0;
+  bd.cnt = INT32_MAX;
+  int32_t d8, rem, cnt8;
+  find_digit(coarse, lane, k, &d8, &rem, &cnt8);  // rem: keys to take from coarse bin d8
+  if (d8 < 0) return bd;
+  // lane j < 16 holds fine bin 16 d8 + 15 - j: the bins from the top down
+  const int32_t c = lane < 16 ? fine[16 * d8 + 15 - lane] : 0;
+  int32_t pre = c;  // keys in this lane's bin and the higher ones of the coarse bin
+#pragma unroll
+  for (int o = 1; o < 16; o <<= 1) {
+    const int32_t y = __shfl_up_sync(0xffffffffu, pre, o);
+    if (lane >= o) pre += y;
+  }
+  const uint32_t hit = __ballot_sync(0xffffffffu, lane < 16 && pre >= rem);
+  if (hit == 0u) return bd;
+  const int j = __ffs(hit) - 1;
+  bd.digit = 16 * d8 + 15 - j;
+  bd.cnt = __shfl_sync(0xffffffffu, c, j);
+  bd.above = k - rem + __shfl_sync(0xffffffffu, pre, j) - bd.cnt;
+  return bd;
 }
 
 // Scratch of finish_fast.

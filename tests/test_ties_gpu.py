@@ -2,8 +2,9 @@
 that are zero, every score is exactly 0 in any precision, so the selection is decided by the
 tie rule alone and must equal the oracle's bit for bit: the first k candidates when every
 key is zero; the blocks keyed along the group query (distinct positive scores) and then the
-lowest of the zero blocks when a few are.  This reaches the select's branch for a boundary
-bin that stays larger than 32 keys after every radix pass, which random scores do not.
+lowest of the zero blocks when a few are; or a group of equal positive scores that the k-th
+key falls in.  This reaches the select's branch for a boundary bin that stays larger than 32
+keys after every radix pass, which random scores do not, and a small bin of equal keys.
 Covered on the one-kernel path, on the scoring kernel's short (n <= 1024) and long lists."""
 import numpy as np
 import pytest
@@ -46,8 +47,7 @@ def expected(case, planted):
         n = srkv.num_candidates(cfg, int(L[r]))
         k = srkv.topk_count(n, cfg["topk_percent"])
         cands = range(b_lo, b_lo + n)
-        keep = [b for f, b in sorted(((f, b) for b, f in planted if b in cands),
-                                     reverse=True)][:k]
+        keep = [b for _, b in sorted((-f, b) for b, f in planted if b in cands)][:k]
         rest = [b for b in cands if b not in keep][:k - len(keep)]
         out.append(sorted(keep + rest))
     return out
@@ -66,7 +66,12 @@ CASES = {
                                           topk_percent=0.2, dense_boundary=0, seed=103,
                                           device=DEV),
 }
-PLANTED = {"all-zero": (), "three-keyed": ((13, 3.0), (9, 1.0), (40, 2.0))}
+PLANTED = {"all-zero": (), "three-keyed": ((13, 3.0), (9, 1.0), (40, 2.0)),
+           # 10 distinct scores above 6 equal ones; with 64 candidates (k = 13) the k-th
+           # key falls among the equal ones: a small boundary bin of equal keys, kept lowest
+           # blocks first
+           "tied-boundary": tuple((10 + j, 3.0 - 0.1 * j) for j in range(10)) +
+           tuple((b, 1.5) for b in (30, 22, 45, 60, 25, 50))}
 
 
 @pytest.mark.parametrize("pattern", list(PLANTED))
