@@ -26,9 +26,10 @@
 //     all finish within about one page of each other; the merged partial (max, sum,
 //     unnormalised output) of the whole segment goes into the leader's shared memory;
 //   * the leader merges the partials and writes the output.
-// Every wait is bounded (SRKV_EFLAG_TIMEOUT); every thread ends at one cluster barrier, so no
-// CTA leaves while another may still reach its shared memory (the leader's consumers arrive
-// on it right after the release, the last time they reach another CTA).
+// The partials land with asynchronous stores that count their bytes on one mbarrier of the
+// leader.  Every wait is bounded (SRKV_EFLAG_TIMEOUT); every thread ends at one cluster
+// barrier, so no CTA leaves while another may still reach its shared memory (the leader's
+// consumers arrive on it as soon as every partial has landed, before they merge).
 #include "decode_mma.cuh"
 #include "select.cuh"
 
@@ -142,9 +143,12 @@ __global__ void __maxnreg__(128) fused_decode_kernel(const DecodeArgs a,
     init_ring<D, F8>(smem);
     mbar_init(keys_ready, kMaxCand);            // one per candidate, the rest at once
     mbar_init(list_ready, 1);                   // the leader, once the pool is laid out
-    mbar_init(parts_ready, 32u * (uint32_t)S);  // one per lane of a streaming CTA's warp 0
+    mbar_init(parts_ready, 1);                  // the leader, expecting every partial's bytes
     mbar_init(scored, kConsumerWarps);          // each consumer warp, its scores computed
     fence_mbar_init();
+    // the streaming CTAs' partials land with asynchronous stores that count their bytes
+    if (leader)
+      mbar_arrive_expect_tx(parts_ready, (uint32_t)(S * a.G * (D + 2)) * (uint32_t)sizeof(float));
   }
   if (leader) {  // the histograms (contiguous) and the pool counter
     int4* h4 = reinterpret_cast<int4*>(&hist[0][0]);
@@ -238,8 +242,9 @@ __global__ void __maxnreg__(128) fused_decode_kernel(const DecodeArgs a,
       // leader's pool until it is empty.  Lane 0 takes the entries (a cluster atomic, then a
       // cluster load) one ahead: the first atomic goes out before the release's entries are
       // issued, each next one before the current entry waits for a free stage; the other
-      // lanes read an entry only after that wait.
-      if (k > 0 && !abort) {
+      // lanes read an entry only after that wait.  The release is waited for even with
+      // nothing to take: the leader's writes into this CTA are then all done before it ends.
+      if (!abort) {
         bool ok = true;
         if (lane == 0) ok = mbar_wait_cluster(list_ready, 0);
         if (!__shfl_sync(0xffffffffu, ok, 0)) {
@@ -484,16 +489,16 @@ __global__ void __maxnreg__(128) fused_decode_kernel(const DecodeArgs a,
         a.nsel_out[u] = kept;
         if (kept != k) raise_flags(a.error_flags, SRKV_EFLAG_SELECTION);
       }
-      // The leader reaches no other CTA's shared memory after the release: its consumers
-      // arrive on the closing cluster barrier now, while they would only wait (the arrival
-      // orders their earlier accesses), so the barrier is done by the time they have merged.
-      cluster_arrive();
-      arrived = true;
       // 4. merge the streaming CTAs' partials: query head w % G, half w / G of d (G <= 4; with
-      // G = 8, both halves of head w)
+      // G = 8, both halves of head w).  Once they are all in, no CTA reaches another's shared
+      // memory any more (each streaming CTA waited for its release, so the leader's writes
+      // into it are done): the leader's consumers arrive on the closing cluster barrier with
+      // nothing to order, and the barrier completes while they merge.
       if (!mbar_wait_cluster(parts_ready, 0)) {
         if (tid == 0) raise_flags(a.error_flags, SRKV_EFLAG_TIMEOUT);
       }
+      cluster_arrive_relaxed();
+      arrived = true;
       const int32_t hw = a.G <= 4 ? 2 : 1;  // warps per head
       if (warp < a.G * hw) {
         // lane qq holds the (max, sum) of streaming CTA qq; weights by shuffles, then every
@@ -560,14 +565,15 @@ __global__ void __maxnreg__(128) fused_decode_kernel(const DecodeArgs a,
       // merged partial goes to the leader's shared memory
       consumer_loop<D, F8>(a, smem, lane, warp,
                        [&](const SoftmaxState<D>& st, const StageInfo&, Lane ln) {
-                         float* acc_l = part_acc + (int64_t)q * a.G * D;
-                         float* ml_l = part_ml + (int64_t)q * a.G * 2;
-                         store_partial<D, F8>(static_cast<float*>(map_cluster_ptr(acc_l, 0)),
-                                          static_cast<float*>(map_cluster_ptr(ml_l, 0)), st, ln,
-                                          a.G);
+                         // asynchronous stores, each counted on the leader's parts_ready
+                         const uint32_t acc_r = cluster_addr(part_acc + (int64_t)q * a.G * D, 0);
+                         const uint32_t ml_r = cluster_addr(part_ml + (int64_t)q * a.G * 2, 0);
+                         const uint32_t bar_r = cluster_addr(parts_ready, 0);
+                         emit_partial<D, F8>(
+                             st, ln, a.G,
+                             [&](int i, float4 v) { st_async_f4(acc_r + 4u * i, v, bar_r); },
+                             [&](int j, float2 v) { st_async_f2(ml_r + 4u * j, v, bar_r); });
                        });
-      // each lane of warp 0 releases the part of the partial it wrote
-      if (warp == 0) mbar_arrive_cluster(parts_ready, 0);
     }
   }
   // nobody leaves while another CTA may still reach its shared memory

@@ -273,11 +273,11 @@ __device__ __forceinline__ void warp_arrive(uint64_t* bar) {
   if ((threadIdx.x & 31) == 0) mbar_arrive(bar);
 }
 
-// Writes a merged state (acc, m, l of the lane's two heads) as a partial: acc[G][D] and
-// ml[G][2] floats (generic pointers: global memory or another CTA's shared memory).
-template <int D, bool F8 = false>
-__device__ __forceinline__ void store_partial(float* accp, float* mlp, const SoftmaxState<D>& st,
-                                              Lane ln, int G) {
+// A merged state (acc, m, l of the lane's two heads) as a partial of acc[G][D] and ml[G][2]
+// floats: put4(i, v) for the 16-byte piece at acc[i], put2(j, v) for (m, l) at ml[j].
+template <int D, bool F8, typename Put4, typename Put2>
+__device__ __forceinline__ void emit_partial(const SoftmaxState<D>& st, Lane ln, int G,
+                                             Put4 put4, Put2 put2) {
   using C = Cfg<D>;
   const int h0 = 2 * ln.t, h1 = h0 + 1;
   if constexpr (F8) {
@@ -288,41 +288,48 @@ __device__ __forceinline__ void store_partial(float* accp, float* mlp, const Sof
     for (int k4 = 0; k4 < C::MT; k4 += 2) {
       const int dd = 16 * ln.g + 2 * k4;
       if (h0 < G)
-        *reinterpret_cast<float4*>(accp + h0 * D + dd) =
-            make_float4(st.acc[k4][0], st.acc[k4][2], st.acc[k4 + 1][0], st.acc[k4 + 1][2]);
+        put4(h0 * D + dd,
+             make_float4(st.acc[k4][0], st.acc[k4][2], st.acc[k4 + 1][0], st.acc[k4 + 1][2]));
       if (h1 < G)
-        *reinterpret_cast<float4*>(accp + h1 * D + dd) =
-            make_float4(st.acc[k4][1], st.acc[k4][3], st.acc[k4 + 1][1], st.acc[k4 + 1][3]);
+        put4(h1 * D + dd,
+             make_float4(st.acc[k4][1], st.acc[k4][3], st.acc[k4 + 1][1], st.acc[k4 + 1][3]));
     }
   } else {
-    // values 4k..4k+3 of a lane sit at 4 consecutive d (d_of): 16-byte stores
+    // values 4k..4k+3 of a lane sit at 4 consecutive d (d_of): 16-byte pieces
 #pragma unroll
     for (int k4 = 0; k4 < C::MT; k4 += 4) {
       const int da = d_of<D>(ln.g, k4), db = d_of<D>(ln.g, C::MT + k4);
       if (h0 < G) {
-        *reinterpret_cast<float4*>(accp + h0 * D + da) = make_float4(
-            st.acc[k4][0], st.acc[k4 + 1][0], st.acc[k4 + 2][0], st.acc[k4 + 3][0]);
-        *reinterpret_cast<float4*>(accp + h0 * D + db) = make_float4(
-            st.acc[k4][2], st.acc[k4 + 1][2], st.acc[k4 + 2][2], st.acc[k4 + 3][2]);
+        put4(h0 * D + da, make_float4(st.acc[k4][0], st.acc[k4 + 1][0], st.acc[k4 + 2][0],
+                                      st.acc[k4 + 3][0]));
+        put4(h0 * D + db, make_float4(st.acc[k4][2], st.acc[k4 + 1][2], st.acc[k4 + 2][2],
+                                      st.acc[k4 + 3][2]));
       }
       if (h1 < G) {
-        *reinterpret_cast<float4*>(accp + h1 * D + da) = make_float4(
-            st.acc[k4][1], st.acc[k4 + 1][1], st.acc[k4 + 2][1], st.acc[k4 + 3][1]);
-        *reinterpret_cast<float4*>(accp + h1 * D + db) = make_float4(
-            st.acc[k4][3], st.acc[k4 + 1][3], st.acc[k4 + 2][3], st.acc[k4 + 3][3]);
+        put4(h1 * D + da, make_float4(st.acc[k4][1], st.acc[k4 + 1][1], st.acc[k4 + 2][1],
+                                      st.acc[k4 + 3][1]));
+        put4(h1 * D + db, make_float4(st.acc[k4][3], st.acc[k4 + 1][3], st.acc[k4 + 2][3],
+                                      st.acc[k4 + 3][3]));
       }
     }
   }
   if (ln.g == 0) {
-    if (h0 < G) {
-      mlp[h0 * 2 + 0] = st.m[0];
-      mlp[h0 * 2 + 1] = st.l[0];
-    }
-    if (h1 < G) {
-      mlp[h1 * 2 + 0] = st.m[1];
-      mlp[h1 * 2 + 1] = st.l[1];
-    }
+    if (h0 < G) put2(h0 * 2, make_float2(st.m[0], st.l[0]));
+    if (h1 < G) put2(h1 * 2, make_float2(st.m[1], st.l[1]));
   }
+}
+
+// Writes a merged state as a partial through generic pointers (global memory or another
+// CTA's shared memory).
+template <int D, bool F8 = false>
+__device__ __forceinline__ void store_partial(float* accp, float* mlp, const SoftmaxState<D>& st,
+                                              Lane ln, int G) {
+  emit_partial<D, F8>(
+      st, ln, G, [&](int i, float4 v) { *reinterpret_cast<float4*>(accp + i) = v; },
+      [&](int j, float2 v) {
+        mlp[j] = v.x;
+        mlp[j + 1] = v.y;
+      });
 }
 
 // The 8 consumer warps' loop over the stages the producer hands out, until the sentinel.

@@ -67,6 +67,25 @@ __device__ __forceinline__ void st_cluster_int4(int4* local, uint32_t rank, int4
                "r"(v.z), "r"(v.w)
                : "memory");
 }
+// Address of the same shared-memory offset in CTA `rank`, for the shared::cluster forms.
+__device__ __forceinline__ uint32_t cluster_addr(const void* local, uint32_t rank) {
+  uint32_t remote;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(smem_u32(local)), "r"(rank));
+  return remote;
+}
+// Asynchronous 16- / 8-byte stores into another CTA's shared memory (shared::cluster
+// addresses) that count their bytes on an mbarrier of that CTA when they land.
+__device__ __forceinline__ void st_async_f4(uint32_t remote, float4 v, uint32_t remote_bar) {
+  asm volatile(
+      "st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.f32 [%0], {%1, %2, %3, %4}, [%5];"
+      ::"r"(remote), "f"(v.x), "f"(v.y), "f"(v.z), "f"(v.w), "r"(remote_bar)
+      : "memory");
+}
+__device__ __forceinline__ void st_async_f2(uint32_t remote, float2 v, uint32_t remote_bar) {
+  asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v2.f32 [%0], {%1, %2}, [%3];"
+               ::"r"(remote), "f"(v.x), "f"(v.y), "r"(remote_bar)
+               : "memory");
+}
 // Atomic add to the same shared-memory offset in CTA `rank` of this cluster.
 __device__ __forceinline__ void red_cluster_add(int32_t* local, uint32_t rank, int32_t v) {
   uint32_t remote;
@@ -90,6 +109,11 @@ __device__ __forceinline__ int2 ld_cluster_int2(const int2* local, uint32_t rank
 }
 __device__ __forceinline__ void cluster_arrive() {
   asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+}
+// Arrival that orders nothing: for a thread whose earlier accesses to other CTAs were all
+// observed already (through an mbarrier those CTAs waited on).
+__device__ __forceinline__ void cluster_arrive_relaxed() {
+  asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
 }
 __device__ __forceinline__ void cluster_wait() {
   asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
