@@ -9,9 +9,11 @@
 // the codes use the format's whole range; per row (not per page) so that a token appended
 // later needs no re-quantisation of its page.
 //
-// One warp per row: each lane loads d / 32 consecutive bf16 values (8 bytes for d = 128),
-// the warp reduces the maximum, and each lane writes its codes (4 bytes) and lane 0 the
-// scale.  Bytes per row: 2d read + d + 4 written.
+// A warp takes kRowsPerWarp consecutive rows of one (page, kv head) slab: d / 8 lanes per
+// row, each with 8 consecutive bf16 values (16 bytes), so every load of the warp is
+// contiguous and all of its rows' loads are in flight before the first is used.  The row's
+// maximum is reduced over its lanes; each lane writes 8 codes (8 bytes) and the row's first
+// lane the scale.  Bytes per row: 2d read + d + 4 written.
 #include <cuda_fp8.h>
 
 #include "srkv_internal.cuh"
@@ -20,6 +22,8 @@ namespace srkv {
 namespace {
 
 constexpr int kQuantWarps = 8;
+constexpr int kRowsPerWarp = 8;  // divides the 128 rows of a slab
+static_assert(kBlock % kRowsPerWarp == 0, "a warp's rows lie in one slab");
 
 template <int D>
 __global__ void __launch_bounds__(kQuantWarps * 32)
@@ -27,52 +31,61 @@ __global__ void __launch_bounds__(kQuantWarps * 32)
                         int64_t num_pages, const int32_t* page_ids, int32_t n_pages, int32_t Hkv,
                         uint8_t* k8, uint8_t* v8, float* k_scale, float* v_scale,
                         int32_t* error_flags) {
-  constexpr int V = D / 32;  // values per lane
+  constexpr int LPR = D / 8;              // lanes per row (16 bytes of bf16 each)
+  constexpr int RPL = 32 / LPR;           // rows per warp-wide load
+  constexpr int LOADS = kRowsPerWarp / RPL;
+  static_assert(LOADS * RPL == kRowsPerWarp, "whole loads per warp");
   const int lane = threadIdx.x & 31;
   const int64_t rows = (int64_t)n_pages * Hkv * kBlock;
   const int64_t gw = (int64_t)blockIdx.x * kQuantWarps + (threadIdx.x >> 5);
-  if (gw >= 2 * rows) return;
-  const int which = gw >= rows ? 1 : 0;  // 0: K, 1: V
-  const int64_t rr = gw - which * rows;
+  const int64_t r0 = gw * kRowsPerWarp;  // the warp's first row over K then V
+  if (r0 >= 2 * rows) return;
+  const int which = r0 >= rows ? 1 : 0;  // 0: K, 1: V (rows never straddle: rows % 8 == 0)
+  const int64_t rr = r0 - which * rows;
   const int64_t i = rr / (Hkv * kBlock), hr = rr % (Hkv * kBlock);
   const int32_t page = page_ids[i];
   if (page < 0 || (int64_t)page >= num_pages) {
     if (lane == 0 && hr == 0 && which == 0) raise_flags(error_flags, SRKV_EFLAG_PAGE_RANGE);
     return;
   }
-  const int64_t row = (int64_t)page * Hkv * kBlock + hr;  // the same row in the destination
-  const __nv_bfloat16* src = (which ? v_src : k_src) + row * D + lane * V;
-  float x[V];
-  if constexpr (V == 4) {
-    const uint2 w = *reinterpret_cast<const uint2*>(src);
-    x[0] = bf16_lo(w.x);
-    x[1] = bf16_hi(w.x);
-    x[2] = bf16_lo(w.y);
-    x[3] = bf16_hi(w.y);
-  } else {
-    const uint32_t w = *reinterpret_cast<const uint32_t*>(src);
-    x[0] = bf16_lo(w);
-    x[1] = bf16_hi(w);
+  const int64_t row0 = (int64_t)page * Hkv * kBlock + hr;  // the same rows in the destination
+  const int sub = lane / LPR, col = (lane % LPR) * 8;        // row within a load, first value
+  const __nv_bfloat16* src = (which ? v_src : k_src) + row0 * D;
+  int4 w[LOADS];
+#pragma unroll
+  for (int l = 0; l < LOADS; ++l)
+    w[l] = *reinterpret_cast<const int4*>(src + (int64_t)(l * RPL + sub) * D + col);
+  uint8_t* dst8 = (which ? v8 : k8) + row0 * D;
+  float* dscale = (which ? v_scale : k_scale) + row0;
+#pragma unroll
+  for (int l = 0; l < LOADS; ++l) {
+    const uint32_t u[4] = {(uint32_t)w[l].x, (uint32_t)w[l].y, (uint32_t)w[l].z,
+                           (uint32_t)w[l].w};
+    float x[8];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      x[2 * e] = bf16_lo(u[e]);
+      x[2 * e + 1] = bf16_hi(u[e]);
+    }
+    float amax = 0.f;
+#pragma unroll
+    for (int e = 0; e < 8; ++e) amax = fmaxf(amax, fabsf(x[e]));
+#pragma unroll
+    for (int o = LPR / 2; o > 0; o >>= 1)  // within the row's lanes
+      amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+    const float scale = amax > 0.f ? __fdiv_rn(amax, 448.f) : 1.f;
+    uint32_t packed[2] = {0u, 0u};
+#pragma unroll
+    for (int e = 0; e < 8; e += 2) {
+      const __nv_fp8x2_storage_t c = __nv_cvt_float2_to_fp8x2(
+          make_float2(__fdiv_rn(x[e], scale), __fdiv_rn(x[e + 1], scale)), __NV_SATFINITE,
+          __NV_E4M3);
+      packed[e / 4] |= (uint32_t)c << (8 * (e % 4));
+    }
+    const int row = l * RPL + sub;
+    *reinterpret_cast<uint2*>(dst8 + (int64_t)row * D + col) = make_uint2(packed[0], packed[1]);
+    if (lane % LPR == 0) dscale[row] = scale;
   }
-  float amax = 0.f;
-#pragma unroll
-  for (int e = 0; e < V; ++e) amax = fmaxf(amax, fabsf(x[e]));
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
-  const float scale = amax > 0.f ? __fdiv_rn(amax, 448.f) : 1.f;
-  uint32_t packed = 0;
-#pragma unroll
-  for (int e = 0; e < V; ++e) {
-    const __nv_fp8_storage_t c =
-        __nv_cvt_float_to_fp8(__fdiv_rn(x[e], scale), __NV_SATFINITE, __NV_E4M3);
-    packed |= (uint32_t)c << (8 * e);
-  }
-  uint8_t* dst = (which ? v8 : k8) + row * D + lane * V;
-  if constexpr (V == 4)
-    *reinterpret_cast<uint32_t*>(dst) = packed;
-  else
-    *reinterpret_cast<uint16_t*>(dst) = (uint16_t)packed;
-  if (lane == 0) (which ? v_scale : k_scale)[row] = scale;
 }
 
 }  // namespace
@@ -81,7 +94,7 @@ cudaError_t launch_quantize_fp8(const srkv_config& cfg, const void* k_src, const
                                 int64_t num_pages, const int32_t* page_ids, int32_t n_pages,
                                 void* k8, void* v8, float* k_scale, float* v_scale,
                                 int32_t* error_flags, cudaStream_t stream) {
-  const int64_t warps = 2 * (int64_t)n_pages * cfg.num_kv_heads * kBlock;
+  const int64_t warps = 2 * (int64_t)n_pages * cfg.num_kv_heads * kBlock / kRowsPerWarp;
   const int64_t grid = (warps + kQuantWarps - 1) / kQuantWarps;
   if (grid > INT32_MAX) return cudaErrorInvalidValue;
   const auto* ks = static_cast<const __nv_bfloat16*>(k_src);

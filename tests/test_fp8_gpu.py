@@ -39,6 +39,22 @@ def test_quantizer_matches_the_oracle_bit_for_bit():
         np.testing.assert_array_equal(got_s.cpu().numpy(), scales)
 
 
+def test_quantizer_d64_and_zero_rows_match_the_oracle():
+    case = synth.make_case(seq_lens=[3000, 1500], num_q_heads=4, num_kv_heads=2, head_dim=64,
+                           seed=73, device=DEV)
+    k = case.k_cache.clone()
+    k[0, 1, 5:9] = 0      # all-zero rows: scale 1, codes 0
+    k[1, 0, 100] *= 1e4   # a large row: the scale follows its maximum
+    case = synth.Case(**{**case.__dict__, "k_cache": k})
+    k8, v8, ks, vs = quantize(case)
+    arr = synth.to_oracle_arrays(case)
+    for got_c, got_s, src in ((k8, ks, arr["k_cache"]), (v8, vs, arr["v_cache"])):
+        codes, scales = oracle.quantize_e4m3(case.cfg, src)
+        np.testing.assert_array_equal(got_c.cpu().numpy(), codes)
+        np.testing.assert_array_equal(got_s.cpu().numpy(), scales)
+    assert (ks[0, 1, 5:9] == 1).all() and (k8[0, 1, 5:9] == 0).all()
+
+
 def test_quantizer_leaves_other_pages_and_flags_bad_ids():
     case = synth.llama8b_layer(seq_len=2048, device=DEV, seed=72)
     P = case.num_pages
