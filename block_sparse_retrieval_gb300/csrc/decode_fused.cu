@@ -38,7 +38,7 @@ namespace {
 
 constexpr int kSelThreads = kConsumerWarps * 32;  // the consumer warps score and select
 constexpr int32_t kMaxCand = kFastRounds * kSelThreads;  // candidates per unit (1024)
-constexpr int kMaxShare = 128;                             // candidates scored per CTA
+constexpr int kMaxShare = 256;                             // candidates scored per CTA
 constexpr int kMaxCluster = 16;                            // CTAs per unit, at most
 // Kept blocks a streaming CTA gets with the release (pool entries q, q + S, ... of streaming
 // CTA q of S), before it takes the rest from the shared counter.
@@ -338,15 +338,23 @@ __global__ void __maxnreg__(128) fused_decode_kernel(const DecodeArgs a,
     bar();
     // 2. scores into the leader (keys, pages, histograms of the top 12 and 8 key bits)
     // keys go to the leader once every CTA has passed its setup (cluster barrier)
+    // (a share of more than 8 per warp takes rounds of 16: fewer round trips, longer
+    // reductions per round)
     bool waited = false;
-    uint32_t eflags = score_share<D, kConsumerWarps, kHistBits>(
-        qbar, share, s_lo, min(s_hi, n), a.reps, total_pages(a), a.Hkv, h, keys, hist12,
-        &hist[0][0], pages, warp, lane,
-        [&] {
-          cluster_wait();
-          waited = true;
-        },
-        [&] { mbar_arrive_cluster(keys_ready, 0); });  // releases this lane's key, page, count
+    auto issued = [&] {
+      cluster_wait();
+      waited = true;
+    };
+    auto stored = [&] { mbar_arrive_cluster(keys_ready, 0); };  // releases this lane's key,
+                                                                 // page, count
+    const uint32_t eflags =
+        s_hi - s_lo <= kConsumerWarps * 8
+            ? score_share<D, kConsumerWarps, kHistBits, 8>(
+                  qbar, share, s_lo, min(s_hi, n), a.reps, total_pages(a), a.Hkv, h, keys,
+                  hist12, &hist[0][0], pages, warp, lane, issued, stored)
+            : score_share<D, kConsumerWarps, kHistBits, 16>(
+                  qbar, share, s_lo, min(s_hi, n), a.reps, total_pages(a), a.Hkv, h, keys,
+                  hist12, &hist[0][0], pages, warp, lane, issued, stored);
     if (!waited) cluster_wait();  // a warp without candidates
     if (lane == 0) mbar_arrive(scored);
     if (lane == 0 && eflags) raise_flags(a.error_flags, eflags);
@@ -612,7 +620,11 @@ int32_t max_active_clusters(int32_t cs) {
 }
 
 // Cluster size for `units` units (0 = the fused path does not apply): the largest of 16,
-// 12, 8 CTAs per unit such that every cluster is resident at once.  e4m3: compressed pages.
+// 12, 8, 4 CTAs per unit such that every cluster is resident at once.  e4m3: compressed pages.
+// Clusters of 4 (up to 36 units: 3 streaming CTAs each) only for bf16 pages, d 128, top-k
+// ratio <= 0.3: there the dynamic pool's balance beats the three kernels on every SM (batch 4
+// x 131072: 60.4 against 67.4 us at 0.1, 91.1 against 96.1 at 0.2), while at 0.4 and at 1.0
+// the three kernels' 152 streaming SMs win (151.3 against 152.6 us, 322 against 337).
 int32_t fused_cluster_size(const srkv_config& cfg, int32_t units, int32_t max_blocks,
                            bool e4m3) {
   if (!mma_split_supported(cfg) || units <= 0) return 0;
@@ -620,15 +632,16 @@ int32_t fused_cluster_size(const srkv_config& cfg, int32_t units, int32_t max_bl
   const int64_t W = (int64_t)max_blocks * kBlock - cfg.local_tokens;
   const int64_t nmax = W > cfg.init_tokens ? (W + kBlock - 1) / kBlock - cfg.init_tokens / kBlock : 0;
   if (nmax > kMaxCand) return 0;
-  // [device][d 64, d 128, d 128 compressed][cluster 16, 12, 8]: max active + 1
-  static int32_t cached[128][3][3];
+  // [device][d 64, d 128, d 128 compressed][cluster 16, 12, 8, 4]: max active + 1
+  static int32_t cached[128][3][4];
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 128) return 0;
   const int di = e4m3 ? 2 : cfg.head_dim == 128 ? 1 : 0;
-  const int32_t sizes[3] = {16, 12, 8};
-  for (int c = 0; c < 3; ++c) {
+  const int32_t sizes[4] = {16, 12, 8, 4};
+  for (int c = 0; c < 4; ++c) {
     const int32_t cs = sizes[c];
     if (nmax > (int64_t)kMaxShare * cs) continue;  // per-CTA scoring share
+    if (cs == 4 && (di != 1 || cfg.topk_percent > 0.3)) continue;
     if (cached[dev][di][c] == 0) {
       const int32_t n = di == 2   ? max_active_clusters<128, true>(cs)
                         : di == 1 ? max_active_clusters<128, false>(cs)

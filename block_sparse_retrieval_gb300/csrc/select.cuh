@@ -207,7 +207,8 @@ __device__ __forceinline__ bool mbar_wait_cluster(uint64_t* bar, uint32_t parity
 //
 // stored() runs on every lane that wrote a key, after its writes (e.g. to release them).
 // kHistBits: the histogram counts the top kHistBits bits of the keys (2^kHistBits bins).
-template <int D, int kWarps, int kHistBits = 8, typename Issued, typename Stored>
+template <int D, int kWarps, int kHistBits = 8, int UNROLL = 8, typename Issued,
+          typename Stored>
 __device__ __forceinline__ uint32_t score_share(const float* qbar, const int32_t* pages,
                                                 int32_t s_lo, int32_t i_hi, const float* reps,
                                                 int64_t num_pages, int32_t Hkv, int32_t h,
@@ -221,7 +222,7 @@ __device__ __forceinline__ uint32_t score_share(const float* qbar, const int32_t
 #pragma unroll
   for (int e = 0; e < EPL; ++e) qv[e] = qbar[lane * EPL + e];
   const uint64_t keep = l2_policy_evict_last();  // the vectors are read again every step
-  constexpr int UNROLL = 8;
+  static_assert(UNROLL <= 32, "lane x holds candidate x of the round");
   bool first = true;
   for (int32_t i0 = s_lo + warp; i0 < i_hi; i0 += kWarps * UNROLL) {
     float part[UNROLL];

@@ -224,8 +224,10 @@ srkv_status srkv_sparse_paged_decode(const srkv_config* cfg, const void* q, cons
  * and the window).  Arguments as for those two calls; prompt_lens may be NULL (the prompt
  * is then the sequence length).
  *   How: a batch small enough for one thread-block cluster per (request, kv head) unit to be
- *   resident (at most 15 units, <= 1024 candidate blocks per request, bf16, d 64 or 128,
- *   group <= 8) runs as one kernel; otherwise the scoring kernel, the split decode (which
+ *   resident (at most 15 units with clusters of 8 to 16 CTAs, or, for bf16 pages with d 128
+ *   and a top-k ratio <= 0.3, at most 36 units with clusters of 4; <= 1024 candidate blocks
+ *   per request, bf16, d 64 or 128, group <= 8) runs as one kernel; otherwise the scoring
+ *   kernel, the split decode (which
  *   streams the initial and window pages while the scoring runs) and the combine.  The first
  *   call for a configuration on a device queries the device (cluster residency); make it
  *   before any stream capture.  max_blocks <= 25600 as for srkv_score_topk.

@@ -27,7 +27,8 @@ def test_inputs_written_just_before_the_call_are_read(name):
     if name == "one-kernel":
         case = synth.llama8b_layer(seq_len=16384, device=DEV, seed=61)
     else:
-        case = synth.ragged_batch(n_requests=4, lo=9000, hi=20000, device=DEV, seed=62)
+        case = synth.ragged_batch(n_requests=5, lo=9000, hi=20000, device=DEV, seed=62)
+        assert srkv.retrieval_decode_launches(case.cfg, case.batch, case.max_blocks) == 3
     reps = gpu_select(case).reps
     g = torch.Generator(device=DEV).manual_seed(7)
     q_new = torch.randn(case.q.shape, generator=g, device=DEV).to(case.q.dtype)

@@ -123,7 +123,7 @@ def test_random_pages_on_host_including_window():
 
 
 def test_all_pages_on_host_split_path():
-    case = synth.ragged_batch(n_requests=3, lo=6000, hi=12000, device=DEV, seed=55)
+    case = synth.ragged_batch(n_requests=5, lo=6000, hi=12000, device=DEV, seed=55)  # 40 units
     to_host = np.ones(case.num_pages, bool)
     to_host[0] = False  # the device pool is never empty
     dev, tie = run_both(case, to_host)

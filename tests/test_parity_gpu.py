@@ -196,10 +196,15 @@ def test_full_size_sampled(name):
 
 
 def test_retrieval_decode_paths():
-    """One kernel for a batch whose clusters are all resident, three otherwise."""
+    """One kernel for a batch whose clusters are all resident (clusters of 4 for up to 36
+    units at a top-k ratio <= 0.3), three otherwise."""
     small = synth.llama8b_layer(seq_len=16384, device=DEV)
-    big = synth.ragged_batch(n_requests=4, lo=9000, hi=20000, device=DEV)
+    mid = synth.ragged_batch(n_requests=4, lo=9000, hi=20000, device=DEV)  # 32 units
+    big = synth.ragged_batch(n_requests=5, lo=9000, hi=20000, device=DEV)  # 40 units
     assert srkv.retrieval_decode_launches(small.cfg, small.batch, small.max_blocks) == 1
+    assert srkv.retrieval_decode_launches(mid.cfg, mid.batch, mid.max_blocks) == 1
+    wide = dict(mid.cfg, topk_percent=0.4)
+    assert srkv.retrieval_decode_launches(wide, mid.batch, mid.max_blocks) == 3
     assert srkv.retrieval_decode_launches(big.cfg, big.batch, big.max_blocks) == 3
     f32 = CASES["f32-d128"]()
     assert srkv.retrieval_decode_launches(f32.cfg, f32.batch, f32.max_blocks) == 3
