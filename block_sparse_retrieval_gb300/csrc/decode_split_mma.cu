@@ -194,8 +194,28 @@ EncodeTiled encode_tiled() {
 
 // [num_pages][Hkv * 128][d] of bf16 (boxes of 64 columns) or E4M3 bytes (boxes of 128
 // columns): 128-byte-wide boxes of 128 rows, 128-byte swizzle.
+// The maps of the last few caches this host thread encoded are kept (a map is a function of
+// these arguments alone), so a decode loop over the same caches encodes none per call.
 bool encode_cache_map(CUtensorMap* map, const void* base, int64_t num_pages, int32_t Hkv,
                       int32_t d, bool e4m3) {
+  struct Entry {
+    const void* base;
+    int64_t num_pages;
+    int32_t Hkv, d;
+    bool e4m3, used;
+    CUtensorMap map;
+  };
+  constexpr int kEntries = 8;
+  thread_local Entry cache[kEntries] = {};
+  thread_local int next = 0;
+  for (int i = 0; i < kEntries; ++i) {
+    const Entry& c = cache[i];
+    if (c.used && c.base == base && c.num_pages == num_pages && c.Hkv == Hkv && c.d == d &&
+        c.e4m3 == e4m3) {
+      *map = c.map;
+      return true;
+    }
+  }
   const EncodeTiled fn = encode_tiled();
   if (!fn || num_pages > INT32_MAX || (int64_t)Hkv * kBlock > INT32_MAX) return false;
   const cuuint64_t elem = e4m3 ? 1 : 2;
@@ -203,10 +223,15 @@ bool encode_cache_map(CUtensorMap* map, const void* base, int64_t num_pages, int
   const cuuint64_t strides[2] = {(cuuint64_t)d * elem, (cuuint64_t)Hkv * kBlock * d * elem};
   const cuuint32_t box[3] = {(cuuint32_t)(128 / elem), (cuuint32_t)kBlock, 1};
   const cuuint32_t estr[3] = {1, 1, 1};
-  return fn(map, e4m3 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3,
-            const_cast<void*>(base), dims, strides,
-            box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+  if (fn(map, e4m3 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3,
+         const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+         CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+    return false;
+  Entry& c = cache[next];
+  next = (next + 1) % kEntries;
+  c = Entry{base, num_pages, Hkv, d, e4m3, true, *map};
+  return true;
 }
 
 template <int D, bool F8>

@@ -181,9 +181,15 @@ def _store_dtype(cfg: Mapping) -> torch.dtype:
     return torch.bfloat16 if cfg["dtype"] == BF16 else torch.float32
 
 
+_raw_stream = getattr(torch._C, "_cuda_getCurrentRawStream", None)
+
+
 def _stream(stream) -> ctypes.c_void_p:
-    s = torch.cuda.current_stream() if stream is None else stream
-    return ctypes.c_void_p(s.cuda_stream if hasattr(s, "cuda_stream") else int(s))
+    if stream is None:
+        if _raw_stream is not None:  # the current stream's handle, without a Stream object
+            return ctypes.c_void_p(_raw_stream(torch.cuda.current_device()))
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream))
 
 
 def _check(status: int, where: str) -> None:
@@ -197,9 +203,15 @@ def _shape(t: torch.Tensor | None, name: str, *dims) -> None:
     of its bounds: the shapes are checked here, before anything is launched."""
     if t is None:
         return
-    if t.dim() != len(dims) or any(w is not None and g != w for g, w in zip(t.shape, dims)):
-        want = "[" + ", ".join("*" if w is None else str(w) for w in dims) + "]"
-        raise ValueError(f"{name} must have shape {want}, got {list(t.shape)}")
+    s = t.shape
+    if len(s) == len(dims):
+        for g, w in zip(s, dims):
+            if w is not None and g != w:
+                break
+        else:
+            return
+    want = "[" + ", ".join("*" if w is None else str(w) for w in dims) + "]"
+    raise ValueError(f"{name} must have shape {want}, got {list(s)}")
 
 
 def _rows(t: torch.Tensor, name: str, at_least: int) -> None:
