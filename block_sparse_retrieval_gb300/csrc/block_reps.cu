@@ -161,6 +161,10 @@ __global__ void __launch_bounds__(kRepKernelThreads, 1)
     fence_mbar_init();
   }
   __syncthreads();
+  // Launched behind the previous kernel of the stream (programmatic launch): the set-up above
+  // touches shared memory only; the inputs may be that kernel's outputs.
+  griddep_wait();
+  griddep_launch_dependents();
   const int64_t units = (int64_t)n * Hkv;
 
   if (warp == kRepWarps) {
@@ -283,6 +287,8 @@ __global__ void __launch_bounds__(kRepThreads)
   __shared__ float part[kRepWarps * D];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int32_t r = blockIdx.x / Hkv, h = blockIdx.x % Hkv;
+  griddep_wait();  // programmatic launch: the inputs may be the previous kernel's outputs
+  griddep_launch_dependents();
   const int32_t L = seq_lens[r];
   if (L < 0 || (int64_t)L >= (int64_t)max_blocks * kBlock) {
     if (threadIdx.x == 0) raise_flags(error_flags, SRKV_EFLAG_SEQ_LEN);
@@ -325,6 +331,24 @@ int32_t device_sms() {
   return cache[dev];
 }
 
+// Launch as a programmatic dependent of the previous kernel in the stream (the kernel waits
+// for it before reading its inputs), so that consecutive launches overlap their start-up.
+template <typename... Params, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(Params...), unsigned grid, unsigned block, size_t smem,
+                       cudaStream_t s, Args... args) {
+  cudaLaunchConfig_t lc = {};
+  lc.gridDim = dim3(grid);
+  lc.blockDim = dim3(block);
+  lc.dynamicSmemBytes = smem;
+  lc.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  lc.attrs = attr;
+  lc.numAttrs = 1;
+  return cudaLaunchKernelEx(&lc, kernel, static_cast<Params>(args)...);
+}
+
 template <typename T, int D>
 cudaError_t launch(const void* k, int64_t P, int32_t Hkv, const int32_t* ids,
                    const int32_t* valid, int32_t n, float* reps, int32_t* flags,
@@ -346,9 +370,8 @@ cudaError_t launch(const void* k, int64_t P, int32_t Hkv, const int32_t* ids,
     configured[dev] = true;
   }
   const int64_t grid = units < sms ? units : sms;
-  block_reps_kernel<T, D><<<(unsigned)grid, kRepKernelThreads, R::kSmemAlloc, s>>>(
-      static_cast<const T*>(k), P, Hkv, ids, valid, n, reps, flags);
-  return cudaGetLastError();
+  return launch_pdl(block_reps_kernel<T, D>, (unsigned)grid, kRepKernelThreads, R::kSmemAlloc,
+                    s, static_cast<const T*>(k), P, Hkv, ids, valid, n, reps, flags);
 }
 
 template <typename T, int D>
@@ -358,10 +381,9 @@ cudaError_t launch_append(const void* kn, const void* vn, void* k, void* v, int6
                           cudaStream_t s) {
   const int64_t grid = (int64_t)batch * Hkv;
   if (grid == 0) return cudaSuccess;
-  append_kv_kernel<T, D><<<(unsigned)grid, kRepThreads, 0, s>>>(
-      static_cast<const T*>(kn), static_cast<const T*>(vn), static_cast<T*>(k),
-      static_cast<T*>(v), P, bt, max_blocks, seq_lens, Hkv, reps, flags);
-  return cudaGetLastError();
+  return launch_pdl(append_kv_kernel<T, D>, (unsigned)grid, kRepThreads, 0, s,
+                    static_cast<const T*>(kn), static_cast<const T*>(vn), static_cast<T*>(k),
+                    static_cast<T*>(v), P, bt, max_blocks, seq_lens, Hkv, reps, flags);
 }
 
 }  // namespace
