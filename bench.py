@@ -70,7 +70,17 @@ WORKLOADS["prefix-shared-64-plain"] = (
     WORKLOADS["prefix-shared-64"][0],
     "prefix-shared-64-plain (as prefix-shared-64, through srkv_retrieval_decode: no cascade)",
     24576)
-PREFIX_WORKLOADS = ("prefix-shared-64",)
+# A shared prefix four times longer (65536 tokens, 512 pages: 256 MB of K/V per layer, more
+# than the L2), through both calls.
+WORKLOADS["prefix-shared-64-long"] = (
+    lambda seed, dev: __import__("block_sparse_retrieval_gb300.synth", fromlist=["x"]).prefix_shared(prefix=65536, seed=seed, device=dev),
+    "prefix-shared-64-long (64 requests, 64/8 heads, d 128, 65536-token shared prefix + U[2048, 8192], top-k 0.2, DENSE_BOUNDARY 0; srkv_retrieval_decode_prefix)",
+    73728)
+WORKLOADS["prefix-shared-64-long-plain"] = (
+    WORKLOADS["prefix-shared-64-long"][0],
+    "prefix-shared-64-long-plain (as prefix-shared-64-long, through srkv_retrieval_decode: no cascade)",
+    73728)
+PREFIX_WORKLOADS = ("prefix-shared-64", "prefix-shared-64-long")
 for _p in (1.0, 0.1, 0.2, 0.4):
     WORKLOADS[f"dense-vs-sparse-p{_p}"] = (
         (lambda p: lambda seed, dev: __import__("block_sparse_retrieval_gb300.synth", fromlist=["x"]).dense_vs_sparse(p, seed=seed, device=dev))(_p),
