@@ -41,9 +41,13 @@ constexpr int32_t kMaxCand = kFastRounds * kSelThreads;  // candidates per unit 
 constexpr int kMaxShare = 256;                             // candidates scored per CTA
 constexpr int kMaxCluster = 16;                            // CTAs per unit, at most
 // Kept blocks a streaming CTA gets with the release (pool entries q, q + S, ... of streaming
-// CTA q of S), before it takes the rest from the shared counter.
-constexpr int kStatic = 4;
-static_assert(kStatic == 4, "the release carries two 16-byte stores");
+// CTA q of S), before it takes the rest from the shared counter.  A pool of at most
+// kStatic * S entries (176 kept blocks with clusters of 12) goes out with the release whole:
+// every CTA's pages and the merge order are then fixed, so the output is bitwise
+// reproducible; longer pools are balanced through the counter (timing decides who takes
+// which of the rest).
+constexpr int kStatic = 16;
+static_assert(kStatic % 2 == 0, "the release carries kStatic / 2 16-byte stores");
 // The scoring counts the top 12 bits of the keys besides the top 8: on score sets like the
 // method's (a few hundred candidates, scores spread over a few units) the 12-bit bin holding
 // the k-th largest key then holds a few keys, and one warp finishes the selection in one pass
@@ -382,8 +386,10 @@ __global__ void __maxnreg__(128) fused_decode_kernel(const DecodeArgs a,
           e[j] = p < k ? pool[p] : make_int2(-1, -1);
         }
         int4* m4 = reinterpret_cast<int4*>(mail);
-        st_cluster_int4(m4, (uint32_t)qq + 1, make_int4(e[0].x, e[0].y, e[1].x, e[1].y));
-        st_cluster_int4(m4 + 1, (uint32_t)qq + 1, make_int4(e[2].x, e[2].y, e[3].x, e[3].y));
+#pragma unroll
+        for (int j = 0; j < kStatic; j += 2)
+          st_cluster_int4(m4 + j / 2, (uint32_t)qq + 1,
+                          make_int4(e[j].x, e[j].y, e[j + 1].x, e[j + 1].y));
         mbar_arrive_cluster(list_ready, (uint32_t)qq + 1);
       };
       if (partial && warp == 0) {

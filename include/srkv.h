@@ -232,9 +232,13 @@ srkv_status srkv_sparse_paged_decode(const srkv_config* cfg, const void* q, cons
  *   call for a configuration on a device queries the device (cluster residency); make it
  *   before any stream capture.  max_blocks <= 25600 as for srkv_score_topk.
  *   Reproducibility: sel and nsel are bitwise the same on every call.  On the three-kernel
- *   path (and in srkv_sparse_paged_decode) out is too; on the one-kernel path the CTAs of a
- *   unit take kept blocks from a shared pool as their pages arrive, so the partial sums
- *   split at pages that vary from call to call and out may differ in its last bits.
+ *   path (and in srkv_sparse_paged_decode) out is too.  On the one-kernel path each
+ *   streaming CTA of a unit's cluster gets its first 16 kept blocks assigned by the
+ *   selection (round robin); out is bitwise the same on every call when no unit keeps more
+ *   than 16 blocks per streaming CTA (with clusters of 12 CTAs, 11 streaming: up to 176 kept
+ *   blocks); beyond that the CTAs take the remaining kept blocks from a shared pool as their
+ *   pages arrive, the partial sums split at pages that vary from call to call, and out may
+ *   differ in its last bits.
  */
 srkv_status srkv_retrieval_decode(const srkv_config* cfg, const void* q, const void* k_cache,
                                   const void* v_cache, const float* reps, int64_t num_pages,

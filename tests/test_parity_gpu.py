@@ -124,6 +124,28 @@ def test_output_is_deterministic_and_page_order_invariant():
     assert np.array_equal(a, c)
 
 
+def test_one_kernel_output_is_reproducible_when_the_release_carries_every_kept_block():
+    """The one-kernel path assigns each streaming CTA's first 16 kept blocks with the release:
+    with k = 90 and 11 streaming CTAs per unit every kept block is assigned that way, so the
+    output is bitwise the same on every call."""
+    case = synth.llama8b_layer(device=DEV, seed=33)
+    assert srkv.retrieval_decode_launches(case.cfg, case.batch, case.max_blocks) == 1
+    reps = gpu_select(case).reps
+    outs = []
+    for _ in range(3):
+        b = srkv.DecodeBuffers(case.cfg, case.batch, case.max_blocks, case.num_pages,
+                               device=DEV)
+        b.reps.copy_(reps)
+        srkv.retrieval_decode(case.cfg, case.q, case.k_cache, case.v_cache, b.reps,
+                              case.block_table, case.seq_lens, case.prompt_lens, b.sel, b.nsel,
+                              b.out, b.workspace, b.error_flags)
+        torch.cuda.synchronize()
+        assert int(b.error_flags.item()) == 0
+        assert int(b.nsel.max().item()) <= 16 * 11
+        outs.append(b.out.clone())
+    assert torch.equal(outs[0], outs[1]) and torch.equal(outs[0], outs[2])
+
+
 # ---- device-side checks: bad inputs are skipped and flagged, never faulted -----------------
 
 def test_bad_page_ids_are_flagged():
