@@ -192,14 +192,19 @@ __global__ void __maxnreg__(128) fused_decode_kernel(const DecodeArgs a,
   int32_t my_page = -1;  // b_lo + nmax <= max_blocks: inside the request's table row
   if (tid < s_hi - s_lo) my_page = bt_r[b_lo + s_lo + tid];
 
-  // The unit's sizes: candidates n (<= nmax), kept k (what the selection will write), list A.
+  // The unit's sizes: list A and the candidates n (<= nmax) from the length alone; the kept
+  // count k (what the selection will write) takes a few double-precision steps, so each role
+  // computes it where it first needs it (the producer once list A is out).
   const int32_t L_in = a.seq_lens[r];
   const int32_t prompt = a.prompt_lens ? a.prompt_lens[r] : L_in;
-  const SelCount sc = selection_count(L_in, prompt, a.max_blocks, a.kmax, a.init_tokens,
-                                      a.local_tokens, a.dense_boundary, a.topk_percent);
-  const int32_t n = sc.n, k = sc.k;
   uint32_t geflags = 0;
-  const Geom g = make_geom(L_in, k, a.max_blocks, a.kmax, a.init_tokens, a.local_tokens, geflags);
+  const Geom g = make_geom(L_in, 0, a.max_blocks, a.kmax, a.init_tokens, a.local_tokens, geflags);
+  const int32_t n = candidate_count(g.L, a.local_tokens, a.init_tokens);
+  auto kept_count = [&] {
+    return selection_count(L_in, prompt, a.max_blocks, a.kmax, a.init_tokens, a.local_tokens,
+                           a.dense_boundary, a.topk_percent)
+        .k;
+  };
   const int32_t nA = list_a_count(g);
   const int32_t q = (int32_t)crank - 1;  // streaming rank
   const int32_t a0 = leader ? 0 : share_begin(q, nA, S), a1 = leader ? 0 : share_begin(q + 1, nA, S);
@@ -211,6 +216,7 @@ __global__ void __maxnreg__(128) fused_decode_kernel(const DecodeArgs a,
       uint32_t eflags = 0;
       bool abort = false;
       int64_t it = 0, armed = 0;
+      int32_t k = -1;  // the kept count, computed while the producer waits anyway
       // list A: 32 positions resolved at once, handed out in order.  The first kEarlyStages
       // copies go out at once; the rest of the ring waits for this CTA's scoring loads,
       // which would otherwise return only after every copy ahead of them had landed (holding
@@ -229,6 +235,7 @@ __global__ void __maxnreg__(128) fused_decode_kernel(const DecodeArgs a,
           tl.ie = __shfl_sync(0xffffffffu, task.ie, l);
           tl.ws = __shfl_sync(0xffffffffu, task.ws, l);
           if (it == F::kEarlyStages) {  // the rest once this CTA's scores are in
+            k = kept_count();             // (its steps overlap the wait)
             bool ok = true;
             if (lane == 0) ok = mbar_wait(scored, 0);
             if (!__shfl_sync(0xffffffffu, ok, 0)) {
@@ -242,6 +249,7 @@ __global__ void __maxnreg__(128) fused_decode_kernel(const DecodeArgs a,
           ++it;
         }
       }
+      if (k < 0) k = kept_count();
       // list B: the kStatic entries that came with the release, then kept blocks from the
       // leader's pool until it is empty.  Lane 0 takes the entries (a cluster atomic, then a
       // cluster load) one ahead: the first atomic goes out before the release's entries are
@@ -349,8 +357,9 @@ __global__ void __maxnreg__(128) fused_decode_kernel(const DecodeArgs a,
       cluster_wait();
       waited = true;
     };
-    auto stored = [&] { mbar_arrive_cluster(keys_ready, 0); };  // releases this lane's key,
-                                                                 // page, count
+    // one arrival for the round's keys, pages and counts of the warp (fewer remote arrivals
+    // on the leader's barrier than one per key)
+    auto stored = [&](uint32_t cnt) { mbar_arrive_cluster_n(keys_ready, 0, cnt); };
     const uint32_t eflags =
         s_hi - s_lo <= kConsumerWarps * 8
             ? score_share<D, kConsumerWarps, kHistBits, 8>(
@@ -370,6 +379,7 @@ __global__ void __maxnreg__(128) fused_decode_kernel(const DecodeArgs a,
       // 3. select the k kept blocks, lay them out as the pool of kept blocks (page, block),
       // release the streaming CTAs, then write sel / nsel for the caller (nobody in the
       // cluster reads them)
+      const int32_t k = kept_count();
       if (!mbar_wait_cluster(keys_ready, 0)) {
         if (tid == 0) raise_flags(a.error_flags, SRKV_EFLAG_TIMEOUT);
       }

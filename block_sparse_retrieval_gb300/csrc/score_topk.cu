@@ -121,7 +121,7 @@ __global__ void __launch_bounds__(kThreads, 4) score_topk_kernel(ScoreArgs a) {
   cluster_wait();
   eflags |= score_share<D, kWarps>(qbar, pages, s_lo, min(s_hi, n), a.reps, a.num_pages, a.Hkv,
                                    h, keys, &hist[0][0], nullptr, nullptr, warp, lane, [] {},
-                                   [] {});
+                                   [](uint32_t) {});
   if (lane == 0 && eflags) raise_flags(a.error_flags, eflags);
   cluster_sync();  // every key and the pass-0 histogram are in the leader
   if (crank != 0) return;

@@ -205,7 +205,9 @@ __device__ __forceinline__ bool mbar_wait_cluster(uint64_t* bar, uint32_t parity
 // makes the leader's shared memory safe to write).  Returns the error flags seen (pages out
 // of range).
 //
-// stored() runs on every lane that wrote a key, after its writes (e.g. to release them).
+// stored(n) runs on lane 0 of the warp once the warp's lanes have written the round's n >= 1
+// keys (after a warp barrier that orders their writes before it, e.g. to release them all
+// with one arrival).
 // kHistBits: the histogram counts the top kHistBits bits of the keys (2^kHistBits bins).
 template <int D, int kWarps, int kHistBits = 8, int UNROLL = 8, typename Issued,
           typename Stored>
@@ -286,7 +288,9 @@ __device__ __forceinline__ uint32_t score_share(const float* qbar, const int32_t
       if (kHistBits > 8 && leader_coarse)
         red_cluster_add(&leader_coarse[digit >> (kHistBits - 8)], 0, __popc(peers));
     }
-    if (valid) stored();
+    const uint32_t nvalid = __popc(__ballot_sync(0xffffffffu, valid));
+    __syncwarp();
+    if (lane == 0 && nvalid > 0) stored(nvalid);
   }
   return __reduce_or_sync(0xffffffffu, eflags);
 }

@@ -472,6 +472,13 @@ struct SelCount {
   uint32_t flags;
 };
 
+// Candidates of a request of (clamped) length L: blocks from INIT / 128 up to the one
+// holding token L - LOCAL - 1.
+__device__ __forceinline__ int32_t candidate_count(int32_t L, int32_t LOCAL, int32_t INIT) {
+  const int32_t W = L - LOCAL;
+  return W > INIT ? (W + kBlock - 1) / kBlock - INIT / kBlock : 0;
+}
+
 __device__ __forceinline__ SelCount selection_count(int32_t L, int32_t prompt, int32_t max_blocks,
                                                     int32_t kmax, int32_t INIT, int32_t LOCAL,
                                                     int32_t dense_boundary, double p) {
@@ -482,8 +489,7 @@ __device__ __forceinline__ SelCount selection_count(int32_t L, int32_t prompt, i
     c.flags |= SRKV_EFLAG_SEQ_LEN;
     L = L < 0 ? 0 : Lmax;
   }
-  const int32_t W = L - LOCAL;
-  c.n = W > INIT ? (W + kBlock - 1) / kBlock - INIT / kBlock : 0;
+  c.n = candidate_count(L, LOCAL, INIT);
   c.k = prompt < dense_boundary ? c.n : device_topk_count(c.n, p);
   if (c.k > kmax) {
     c.flags |= SRKV_EFLAG_SELECTION;
