@@ -14,12 +14,13 @@
 //   * meanwhile the other CTAs' producer warps stream their share of the initial and window
 //     pages (list A) into the stage ring (decode_mma.cuh), through the scoring and the
 //     selection;
-//   * the leader selects: one warp finds the 12-bit bin holding the k-th largest key, lays
-//     every key above it out as the pool of kept blocks (page and block ids) in its own
-//     shared memory, ranks the bin's few keys for the rest, and releases each streaming CTA
-//     with its first kStatic pool entries (written into that CTA's shared memory) and an
-//     mbarrier arrival; sel / nsel are written after that.  A bin too large to rank at once
-//     falls back to radix narrowing and the ordered finish;
+//   * the leader selects: one warp finds the 12-bit bin holding the k-th largest key; the 8
+//     warps lay every key above it out as the pool of kept blocks (page and block ids) in
+//     the leader's shared memory, a round of 32 keys each in turn; one warp ranks the bin's
+//     few keys for the rest; the warps release each streaming CTA with its first kStatic
+//     pool entries (written into that CTA's shared memory) and an mbarrier arrival; sel /
+//     nsel are written after that.  A bin too large to rank at once falls back to radix
+//     narrowing and the ordered finish;
 //   * each streaming CTA attends its share of list A, then its kStatic entries, then takes
 //     kept blocks from the rest of the pool one at a time (an atomic counter in the leader's
 //     shared memory) until it is empty, so the CTAs whose pages arrive sooner take more and
@@ -50,8 +51,8 @@ constexpr int kStatic = 16;
 static_assert(kStatic % 2 == 0, "the release carries kStatic / 2 16-byte stores");
 // The scoring counts the top 12 bits of the keys besides the top 8: on score sets like the
 // method's (a few hundred candidates, scores spread over a few units) the 12-bit bin holding
-// the k-th largest key then holds a few keys, and one warp finishes the selection in one pass
-// over the keys and one rank of that bin, with no barrier.
+// the k-th largest key then holds a few keys, and the selection finishes in one pass over the
+// keys and one rank of that bin.
 constexpr int kHistBits = 12;
 constexpr int kBins = 1 << kHistBits;
 constexpr int kBinRank = 32;  // boundary bins up to this size are ranked by one warp
@@ -81,7 +82,9 @@ struct FusedCfg {
   static constexpr size_t kOffBinKey = kOffBnd + sizeof(int32_t) * kBinRank;
   static constexpr size_t kOffKeepBits = kOffBinKey + sizeof(uint32_t) * kBinRank;  // a bit per candidate
   static constexpr size_t kOffFast = kOffKeepBits + sizeof(uint32_t) * (kMaxCand / 32);
-  static constexpr size_t kSelEnd = kOffFast + 16;
+  // per 32-key round: keys above the boundary bin, keys in it
+  static constexpr size_t kOffRounds = kOffFast + 16;
+  static constexpr size_t kSelEnd = kOffRounds + sizeof(int32_t) * 2 * (kMaxCand / 32);
   // ... and its V ring the streaming CTAs' partials: acc [15][8][D], then (m, l) [15][8][2]
   static constexpr size_t kOffPartAcc = C::kOffV;
   static constexpr size_t kOffPartMl = kOffPartAcc + sizeof(float) * (kMaxCluster - 1) * 8 * D;
@@ -131,7 +134,8 @@ __global__ void __maxnreg__(128) fused_decode_kernel(const DecodeArgs a,
   int32_t* bnd = reinterpret_cast<int32_t*>(smem + F::kOffBnd);          // leader
   uint32_t* bin_key = reinterpret_cast<uint32_t*>(smem + F::kOffBinKey);  // leader
   uint32_t* keepbits = reinterpret_cast<uint32_t*>(smem + F::kOffKeepBits);  // leader
-  int32_t* fast_flag = reinterpret_cast<int32_t*>(smem + F::kOffFast);   // leader
+  int32_t* fast_flag = reinterpret_cast<int32_t*>(smem + F::kOffFast);   // leader: flag, digit
+  int32_t* rounds = reinterpret_cast<int32_t*>(smem + F::kOffRounds);   // leader
   float* part_acc = reinterpret_cast<float*>(smem + F::kOffPartAcc);  // leader
   float* part_ml = reinterpret_cast<float*>(smem + F::kOffPartMl);    // leader
 
@@ -402,77 +406,100 @@ __global__ void __maxnreg__(128) fused_decode_kernel(const DecodeArgs a,
                           make_int4(e[j].x, e[j].y, e[j + 1].x, e[j + 1].y));
         mbar_arrive_cluster(list_ready, (uint32_t)qq + 1);
       };
-      if (partial && warp == 0) {
+      if (partial) {
         // Warp 0: the 12-bit bin holding the k-th largest key.  Every key above it is kept:
         // into the pool (the keys above, in block order) and the kept bits; the bin's keys
         // (at most kBinRank) are ranked and the first k - (keys above) follow in the pool.
+        // The pass over the keys is shared by the 8 warps, a round of 32 keys each in turn.
         // (The count checks only matter if some scores never arrived: flagged.)
-        const Boundary bd = warp_boundary(&hist[0][0], hist12, k, lane);
-        const bool fast = bd.cnt <= kBinRank;
-        if (fast) {
-          const uint32_t lt = (1u << lane) - 1u;
-          const uint32_t dsel = (uint32_t)bd.digit;
-          int32_t na = 0, nb = 0;  // keys above the bin, in it, so far
-          // 8 rounds of 32 keys at a time: their loads first, then the stores
-#pragma unroll 1
-          for (int32_t g0 = 0; g0 < n; g0 += 8 * 32) {
-            uint32_t kk[8];
-            int32_t pg[8];
-#pragma unroll
-            for (int x = 0; x < 8; ++x) {
-              const int32_t i = g0 + 32 * x + lane;
-              kk[x] = i < n ? keys[i] : 0u;
-              pg[x] = i < n ? pages[i] : -1;
-            }
-            // the rounds' votes, then their counts (independent), then the stores
-            uint32_t ma[8], mb[8];
-#pragma unroll
-            for (int x = 0; x < 8; ++x) {
-              const int32_t i = g0 + 32 * x + lane;
-              const uint32_t dg = kk[x] >> (32 - kHistBits);
-              ma[x] = __ballot_sync(0xffffffffu, i < n && dg > dsel);
-              mb[x] = __ballot_sync(0xffffffffu, i < n && dg == dsel);
-            }
-#pragma unroll
-            for (int x = 0; x < 8; ++x) {
-              const int32_t i0 = g0 + 32 * x, i = i0 + lane;
-              if (i0 >= n) break;  // uniform
-              const int32_t sa = na + __popc(ma[x] & lt), sb = nb + __popc(mb[x] & lt);
-              if (((ma[x] >> lane) & 1u) && sa < k) pool[sa] = make_int2(pg[x], b_lo + i);
-              if (((mb[x] >> lane) & 1u) && sb < kBinRank) {
-                // rank key: the key's low bits (its top bits are the bin's), then the lower
-                // block; unique, larger = kept first
-                bnd[sb] = i;
-                bin_key[sb] = ((kk[x] & ((1u << (32 - kHistBits)) - 1u)) << 10) |
-                              (uint32_t)(kMaxCand - 1 - i);
-              }
-              if (lane == 0) keepbits[i0 >> 5] = ma[x];
-              na += __popc(ma[x]);
-              nb += __popc(mb[x]);
-            }
+        if (warp == 0) {
+          const Boundary bd = warp_boundary(&hist[0][0], hist12, k, lane);
+          if (lane == 0) {
+            fast_flag[0] = bd.cnt <= kBinRank;
+            fast_flag[1] = bd.digit;
           }
-          __syncwarp();
-          const int32_t nbin = min(nb, kBinRank), nab = min(na, k);
-          const uint32_t mine = lane < nbin ? bin_key[lane] : 0u;
-          int32_t rank = 0;
-#pragma unroll
-          for (int j = 0; j < kBinRank; j += 4) {
-            const uint4 v = *reinterpret_cast<const uint4*>(bin_key + j);
-            rank += (j < nbin && v.x > mine) + (j + 1 < nbin && v.y > mine) +
-                    (j + 2 < nbin && v.z > mine) + (j + 3 < nbin && v.w > mine);
-          }
-          const bool take = lane < nbin && rank < k - nab;
-          const uint32_t m = __ballot_sync(0xffffffffu, take);
-          if (take) {
-            const int32_t i = bnd[lane], slot = nab + __popc(m & lt);
-            if (slot < k) pool[slot] = make_int2(pages[i], b_lo + i);
-            atomicOr(&keepbits[i >> 5], 1u << (i & 31));
-          }
-          for (int32_t p = nab + __popc(m) + lane; p < k; p += 32) pool[p] = make_int2(-1, 0);
-          __syncwarp();  // the pool is complete
-          if (lane < S) release(lane);
         }
-        if (lane == 0) *fast_flag = fast;
+        bar();
+        if (fast_flag[0]) {
+          constexpr int kRounds = kMaxCand / 32 / kConsumerWarps;  // a warp's rounds at most
+          const uint32_t lt = (1u << lane) - 1u;
+          const uint32_t dsel = (uint32_t)fast_flag[1];
+          uint32_t kk[kRounds], ma[kRounds], mb[kRounds];
+          int32_t pg[kRounds];
+#pragma unroll
+          for (int x = 0; x < kRounds; ++x) {  // round warp + 8 x: keys 32 (warp + 8 x) + lane
+            const int32_t rr = warp + kConsumerWarps * x, i = 32 * rr + lane;
+            kk[x] = i < n ? keys[i] : 0u;
+            pg[x] = i < n ? pages[i] : -1;
+          }
+#pragma unroll
+          for (int x = 0; x < kRounds; ++x) {
+            const int32_t rr = warp + kConsumerWarps * x, i = 32 * rr + lane;
+            const uint32_t dg = kk[x] >> (32 - kHistBits);
+            ma[x] = __ballot_sync(0xffffffffu, i < n && dg > dsel);
+            mb[x] = __ballot_sync(0xffffffffu, i < n && dg == dsel);
+            if (lane == 0 && 32 * rr < n) {
+              rounds[rr] = __popc(ma[x]);
+              rounds[kMaxCand / 32 + rr] = __popc(mb[x]);
+              keepbits[rr] = ma[x];
+            }
+          }
+          bar();
+          // every warp scans the rounds' counts; its own rounds' keys go to their places
+          const int32_t nr = (n + 31) >> 5;
+          int32_t na = 0, nb = 0;
+          const int32_t pa = warp_exclusive_scan(lane < nr ? rounds[lane] : 0, lane, &na);
+          const int32_t pb = warp_exclusive_scan(lane < nr ? rounds[kMaxCand / 32 + lane] : 0,
+                                                 lane, &nb);
+#pragma unroll
+          for (int x = 0; x < kRounds; ++x) {
+            const int32_t rr = warp + kConsumerWarps * x, i = 32 * rr + lane;
+            if (32 * rr >= n) break;  // uniform
+            const int32_t sa = __shfl_sync(0xffffffffu, pa, rr) + __popc(ma[x] & lt);
+            const int32_t sb = __shfl_sync(0xffffffffu, pb, rr) + __popc(mb[x] & lt);
+            if (((ma[x] >> lane) & 1u) && sa < k) pool[sa] = make_int2(pg[x], b_lo + i);
+            if (((mb[x] >> lane) & 1u) && sb < kBinRank) {
+              // rank key: the key's low bits (its top bits are the bin's), then the lower
+              // block; unique, larger = kept first
+              bnd[sb] = i;
+              bin_key[sb] = ((kk[x] & ((1u << (32 - kHistBits)) - 1u)) << 10) |
+                            (uint32_t)(kMaxCand - 1 - i);
+            }
+          }
+          bar();
+          if (warp == 0) {
+            const int32_t nbin = min(nb, kBinRank), nab = min(na, k);
+            const uint32_t mine = lane < nbin ? bin_key[lane] : 0u;
+            int32_t rank = 0;
+#pragma unroll
+            for (int j = 0; j < kBinRank; j += 4) {
+              const uint4 v = *reinterpret_cast<const uint4*>(bin_key + j);
+              rank += (j < nbin && v.x > mine) + (j + 1 < nbin && v.y > mine) +
+                      (j + 2 < nbin && v.z > mine) + (j + 3 < nbin && v.w > mine);
+            }
+            const bool take = lane < nbin && rank < k - nab;
+            const uint32_t m = __ballot_sync(0xffffffffu, take);
+            if (take) {
+              const int32_t i = bnd[lane], slot = nab + __popc(m & lt);
+              if (slot < k) pool[slot] = make_int2(pages[i], b_lo + i);
+              atomicOr(&keepbits[i >> 5], 1u << (i & 31));
+            }
+            for (int32_t p = nab + __popc(m) + lane; p < k; p += 32) pool[p] = make_int2(-1, 0);
+          }
+          bar();  // the pool is complete
+          // the releases: every entry store first (one 16-byte store per thread), then, once
+          // the barrier orders them all, one arrival per streaming CTA
+          for (int32_t x = tid; x < S * (kStatic / 2); x += kSelThreads) {
+            const int32_t qq = x / (kStatic / 2), j = 2 * (x % (kStatic / 2));
+            const int32_t p0 = qq + j * S, p1 = p0 + S;
+            const int2 e0 = p0 < k ? pool[p0] : make_int2(-1, -1);
+            const int2 e1 = p1 < k ? pool[p1] : make_int2(-1, -1);
+            st_cluster_int4(reinterpret_cast<int4*>(mail) + j / 2, (uint32_t)qq + 1,
+                            make_int4(e0.x, e0.y, e1.x, e1.y));
+          }
+          bar();
+          if (tid < S) mbar_arrive_cluster(list_ready, (uint32_t)tid + 1);
+        }
       }
       bar();
       if (partial && *fast_flag) {
