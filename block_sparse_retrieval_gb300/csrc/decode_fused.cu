@@ -662,12 +662,14 @@ int32_t max_active_clusters(int32_t cs) {
   return n;
 }
 
-// Cluster size for `units` units (0 = the fused path does not apply): the largest of 16,
-// 12, 8, 4 CTAs per unit such that every cluster is resident at once.  e4m3: compressed pages.
-// Clusters of 4 (up to 36 units: 3 streaming CTAs each) only for bf16 pages, d 128, top-k
+// Cluster size for `units` units (0 = the fused path does not apply): the largest of 16 down
+// to 4 CTAs per unit such that every cluster is resident at once (on a GB300: 16 CTAs for up
+// to 7 units, 12 for 8, 10 for up to 13, 9 for up to 15, 6 for up to 23, 5 for up to 28, 4
+// for up to 36).  e4m3: compressed pages.  Clusters of fewer than 8 only for bf16 pages, d 128, top-k
 // ratio <= 0.3: there the dynamic pool's balance beats the three kernels on every SM (batch 4
-// x 131072: 60.4 against 67.4 us at 0.1, 91.1 against 96.1 at 0.2), while at 0.4 and at 1.0
-// the three kernels' 152 streaming SMs win (151.3 against 152.6 us, 322 against 337).
+// x 131072 on clusters of 4: 60.4 against 67.4 us at 0.1, 91.1 against 96.1 at 0.2), while at
+// 0.4 and at 1.0 the three kernels' 152 streaming SMs win (151.3 against 152.6 us, 322
+// against 337).
 int32_t fused_cluster_size(const srkv_config& cfg, int32_t units, int32_t max_blocks,
                            bool e4m3) {
   if (!mma_split_supported(cfg) || units <= 0) return 0;
@@ -675,16 +677,16 @@ int32_t fused_cluster_size(const srkv_config& cfg, int32_t units, int32_t max_bl
   const int64_t W = (int64_t)max_blocks * kBlock - cfg.local_tokens;
   const int64_t nmax = W > cfg.init_tokens ? (W + kBlock - 1) / kBlock - cfg.init_tokens / kBlock : 0;
   if (nmax > kMaxCand) return 0;
-  // [device][d 64, d 128, d 128 compressed][cluster 16, 12, 8, 4]: max active + 1
-  static int32_t cached[128][3][4];
+  // [device][d 64, d 128, d 128 compressed][cluster 16 - c]: max active + 1
+  constexpr int kSizes = kMaxCluster - 3;  // 16 .. 4
+  static int32_t cached[128][3][kSizes];
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 128) return 0;
   const int di = e4m3 ? 2 : cfg.head_dim == 128 ? 1 : 0;
-  const int32_t sizes[4] = {16, 12, 8, 4};
-  for (int c = 0; c < 4; ++c) {
-    const int32_t cs = sizes[c];
+  for (int c = 0; c < kSizes; ++c) {
+    const int32_t cs = kMaxCluster - c;
     if (nmax > (int64_t)kMaxShare * cs) continue;  // per-CTA scoring share
-    if (cs == 4 && (di != 1 || cfg.topk_percent > 0.3)) continue;
+    if (cs < 8 && (di != 1 || cfg.topk_percent > 0.3)) continue;
     if (cached[dev][di][c] == 0) {
       const int32_t n = di == 2   ? max_active_clusters<128, true>(cs)
                         : di == 1 ? max_active_clusters<128, false>(cs)

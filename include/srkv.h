@@ -225,8 +225,9 @@ srkv_status srkv_sparse_paged_decode(const srkv_config* cfg, const void* q, cons
  * is then the sequence length).
  *   How: a batch small enough for one thread-block cluster per (request, kv head) unit to be
  *   resident (at most 15 units with clusters of 8 to 16 CTAs, or, for bf16 pages with d 128
- *   and a top-k ratio <= 0.3, at most 36 units with clusters of 4; <= 1024 candidate blocks
- *   per request, bf16, d 64 or 128, group <= 8) runs as one kernel; otherwise the scoring
+ *   and a top-k ratio <= 0.3, at most 36 units with clusters of 4 to 7; the largest cluster
+ *   size whose clusters are all resident is taken; <= 1024 candidate blocks per request,
+ *   bf16, d 64 or 128, group <= 8) runs as one kernel; otherwise the scoring
  *   kernel, the split decode (which
  *   streams the initial and window pages while the scoring runs) and the combine.  The first
  *   call for a configuration on a device queries the device (cluster residency); make it

@@ -22,6 +22,13 @@ def small_cases():
         "tiny": lambda: synth.tiny(device=DEV),
         "llama8b-16k": lambda: synth.llama8b_layer(seq_len=16384, device=DEV),
         "ragged-4": lambda: synth.ragged_batch(n_requests=4, lo=9000, hi=20000, device=DEV),
+        # 24 and 12 (request, kv head) units: one kernel on clusters of 5 and of 10 (the
+        # largest size whose clusters are all resident)
+        "ragged-3": lambda: synth.ragged_batch(n_requests=3, lo=9000, hi=20000, seed=21,
+                                               device=DEV),
+        "h4-3req": lambda: mk(seq_lens=[11000, 7000, 15000], num_q_heads=16, num_kv_heads=4,
+                              head_dim=128, init_tokens=1024, local_tokens=2048,
+                              topk_percent=0.2, dense_boundary=0, seed=22, device=DEV),
         "dense-p1.0": lambda: synth.dense_vs_sparse(1.0, batch=2, seq_len=24576, device=DEV),
         "sparse-p0.1": lambda: synth.dense_vs_sparse(0.1, batch=2, seq_len=24576, device=DEV),
         "sparse-p0.4": lambda: synth.dense_vs_sparse(0.4, batch=2, seq_len=24576, device=DEV),
@@ -219,11 +226,16 @@ def test_full_size_sampled(name):
 
 def test_retrieval_decode_paths():
     """One kernel for a batch whose clusters are all resident (clusters of 4 for up to 36
-    units at a top-k ratio <= 0.3), three otherwise."""
+    units at a top-k ratio <= 0.3; clusters of 8 or more for up to 15 units at any ratio),
+    three otherwise."""
     small = synth.llama8b_layer(seq_len=16384, device=DEV)
+    two = synth.ragged_batch(n_requests=2, lo=9000, hi=20000, device=DEV)  # 16 units
     mid = synth.ragged_batch(n_requests=4, lo=9000, hi=20000, device=DEV)  # 32 units
     big = synth.ragged_batch(n_requests=5, lo=9000, hi=20000, device=DEV)  # 40 units
     assert srkv.retrieval_decode_launches(small.cfg, small.batch, small.max_blocks) == 1
+    assert srkv.retrieval_decode_launches(two.cfg, two.batch, two.max_blocks) == 1
+    assert srkv.retrieval_decode_launches(dict(two.cfg, topk_percent=0.4), two.batch,
+                                          two.max_blocks) == 3
     assert srkv.retrieval_decode_launches(mid.cfg, mid.batch, mid.max_blocks) == 1
     wide = dict(mid.cfg, topk_percent=0.4)
     assert srkv.retrieval_decode_launches(wide, mid.batch, mid.max_blocks) == 3
