@@ -87,12 +87,13 @@ for _p in (1.0, 0.1, 0.2, 0.4):
         f"dense-vs-sparse-4x131072-bf16 (batch 4, 32/8 heads, d 128, top-k {_p}, 3% planted, shuffled pages)",
         131072)
 # Mid-size batches of the same cache shape: 2 and 3 requests (16 and 24 (request, kv head)
-# units), one kernel on clusters of 6 and 5.
+# units); at top-k 0.2 one kernel on clusters of 6 and 5.
 for _b in (2, 3):
-    WORKLOADS[f"dense-vs-sparse-b{_b}-p0.2"] = (
-        (lambda b: lambda seed, dev: __import__("block_sparse_retrieval_gb300.synth", fromlist=["x"]).dense_vs_sparse(0.2, batch=b, seed=seed, device=dev))(_b),
-        f"dense-vs-sparse-{_b}x131072-bf16 (batch {_b}, 32/8 heads, d 128, top-k 0.2, 3% planted, shuffled pages)",
-        131072)
+    for _p in (0.2, 0.4):
+        WORKLOADS[f"dense-vs-sparse-b{_b}-p{_p}"] = (
+            (lambda b, p: lambda seed, dev: __import__("block_sparse_retrieval_gb300.synth", fromlist=["x"]).dense_vs_sparse(p, batch=b, seed=seed, device=dev))(_b, _p),
+            f"dense-vs-sparse-{_b}x131072-bf16 (batch {_b}, 32/8 heads, d 128, top-k {_p}, 3% planted, shuffled pages)",
+            131072)
 # The offload tier: the same layer with every page that holds only offload-range tokens
 # ([INIT, L - LOCAL)) in a pinned host pool, read in place over NVLink-C2C.
 WORKLOADS["offload-65536"] = (
