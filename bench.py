@@ -749,12 +749,12 @@ def time_append(dev, cfg, n: int = 200) -> dict:
 
 
 def run_e2e(layers, K, world, dev) -> dict:
-    """The same steps through the public entry point with host buffers, as a serving loop runs
-    them.  Per step: the step's query and lengths are copied from pinned host memory (one packed
-    copy), srkv_retrieval_decode is called through the binding (its argument checks and the
-    launch included), the output is copied back into pinned host memory, and the host waits
-    for it.  `per_call` issues those three from Python every step; `graph` replays them from one
-    CUDA graph per layer (what a serving loop that captures its step would see)."""
+    """The same steps through the public entry points with host buffers, as a serving loop runs
+    them.  `per_call`: one srkv_retrieval_decode_host call per step through the binding (its
+    argument checks included): the step's query and lengths copied from pinned host memory,
+    the decode, the output copied back into pinned host memory, and the wait for it.  `graph`:
+    the same copies and srkv_retrieval_decode replayed from one CUDA graph per layer (what a
+    serving loop that captures its step would see), then the wait."""
     steps = []
     for ly in layers:
         c, b = ly.case, ly.buf
@@ -764,13 +764,20 @@ def run_e2e(layers, K, world, dev) -> dict:
         host[:qb].copy_(c.q.cpu().contiguous().view(-1).view(torch.uint8))
         host[qb:qb + nb].copy_(c.seq_lens.cpu().view(torch.uint8))
         host[qb + nb:].copy_(c.prompt_lens.cpu().view(torch.uint8))
+        # the host call's own buffers: page-locked inputs and output, device staging
+        hq = c.q.cpu().contiguous().pin_memory()
+        hlens = c.seq_lens.cpu().contiguous().pin_memory()
+        hprompt = c.prompt_lens.cpu().contiguous().pin_memory()
+        staging = torch.empty(ly.srkv.host_staging_size(c.cfg, c.batch), dtype=torch.uint8,
+                              device=dev)
         packed = torch.empty_like(host, device=dev)
         # the layer reads its query and lengths from the packed device buffer
         c.q = packed[:qb].view(c.q.dtype).view(c.q.shape)
         c.seq_lens = packed[qb:qb + nb].view(torch.int32)
         c.prompt_lens = packed[qb + nb:].view(torch.int32)
         out = torch.empty_like(b.out, device="cpu").pin_memory()
-        steps.append(dict(ly=ly, host=host, packed=packed, out=out))
+        steps.append(dict(ly=ly, host=host, packed=packed, out=out, hq=hq, hlens=hlens,
+                          hprompt=hprompt, staging=staging))
     h2d = steps[0]["host"].nbytes
     d2h = steps[0]["out"].nbytes
     stream = torch.cuda.Stream(dev)
@@ -801,8 +808,13 @@ def run_e2e(layers, K, world, dev) -> dict:
             return max_over_ranks(time.perf_counter() - t0, world, dev)
 
     def per_call(i):
-        one(steps[i % len(steps)])
-        stream.synchronize()
+        st = steps[i % len(steps)]
+        ly = st["ly"]
+        c, b = ly.case, ly.buf
+        ly.srkv.retrieval_decode_host(c.cfg, st["hq"], st["hlens"], st["hprompt"], st["out"],
+                                      st["staging"], c.k_cache, c.v_cache, b.reps,
+                                      c.block_table, b.sel, b.nsel, b.out, b.workspace,
+                                      b.error_flags, stream)
 
     def replay(i):
         graphs[i % len(graphs)].replay()
@@ -813,9 +825,10 @@ def run_e2e(layers, K, world, dev) -> dict:
             "copies_declared": True}
     return {
         "per_call": dict(base, value=round(world * K / dt_call, 2),
-                         how="per step from Python: packed pinned-host copy of q and lengths, "
-                             "srkv_retrieval_decode through the binding (checks and launch), "
-                             "copy of the output to pinned host memory, host synchronize"),
+                         how="per step from Python: one srkv_retrieval_decode_host call "
+                             "through the binding (argument checks; copies of q and lengths "
+                             "from pinned host memory, the decode, copy of the output to "
+                             "pinned host memory, stream synchronize)"),
         "graph": dict(base, value=round(world * K / dt_graph, 2),
                       how="the same three per step replayed from one CUDA graph per layer, "
                           "host synchronize"),

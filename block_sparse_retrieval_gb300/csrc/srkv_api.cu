@@ -451,6 +451,65 @@ srkv_status srkv_retrieval_decode(const srkv_config* cfg, const void* q, const v
                           out, workspace, workspace_bytes, error_flags, (cudaStream_t)stream);
 }
 
+// Staging of the host-buffer call: q, then the lengths, then the prompt lengths, each at a
+// 256-byte boundary.
+static size_t round256(size_t x) { return (x + 255) & ~size_t(255); }
+static size_t staging_q_bytes(const srkv_config* cfg, int32_t batch) {
+  return (size_t)batch * (size_t)cfg->num_q_heads * (size_t)cfg->head_dim *
+         (cfg->dtype == SRKV_F32 ? 4u : 2u);
+}
+
+size_t srkv_host_staging_size(const srkv_config* cfg, int32_t batch) {
+  if (!cfg || batch < 0 || cfg->num_q_heads <= 0 || cfg->head_dim <= 0) return 0;
+  return round256(staging_q_bytes(cfg, batch)) + 2 * round256((size_t)batch * 4);
+}
+
+srkv_status srkv_retrieval_decode_host(const srkv_config* cfg, const void* q_host,
+                                       const int32_t* seq_lens_host,
+                                       const int32_t* prompt_lens_host, void* out_host,
+                                       void* staging, size_t staging_bytes,
+                                       const void* k_cache, const void* v_cache,
+                                       const float* reps, int64_t num_pages,
+                                       const int32_t* block_table, int32_t max_blocks,
+                                       int32_t batch, int32_t* sel, int32_t kmax, int32_t* nsel,
+                                       void* out, void* workspace, size_t workspace_bytes,
+                                       int32_t* error_flags, srkv_stream stream) {
+  if (!cfg || batch < 0) return SRKV_ERR_INVALID_ARG;
+  if (batch > 0 && (!q_host || !seq_lens_host || !out_host || !staging))
+    return SRKV_ERR_INVALID_ARG;
+  const size_t need = srkv_host_staging_size(cfg, batch);
+  if (need == 0 || staging_bytes < need ||
+      (reinterpret_cast<uintptr_t>(staging) & 255u) != 0)
+    return SRKV_ERR_INVALID_ARG;
+  const cudaStream_t s = (cudaStream_t)stream;
+  const size_t qb = staging_q_bytes(cfg, batch), lb = (size_t)batch * 4;
+  unsigned char* q_dev = static_cast<unsigned char*>(staging);
+  int32_t* lens_dev = reinterpret_cast<int32_t*>(q_dev + round256(qb));
+  int32_t* prompt_dev = reinterpret_cast<int32_t*>(q_dev + round256(qb) + round256(lb));
+  if (batch > 0) {
+    if (cudaMemcpyAsync(q_dev, q_host, qb, cudaMemcpyHostToDevice, s) != cudaSuccess ||
+        cudaMemcpyAsync(lens_dev, seq_lens_host, lb, cudaMemcpyHostToDevice, s) != cudaSuccess ||
+        (prompt_lens_host &&
+         cudaMemcpyAsync(prompt_dev, prompt_lens_host, lb, cudaMemcpyHostToDevice, s) !=
+             cudaSuccess)) {
+      (void)cudaGetLastError();
+      return SRKV_ERR_CUDA;
+    }
+  }
+  const srkv_status st =
+      srkv_retrieval_decode(cfg, q_dev, k_cache, v_cache, reps, num_pages, block_table,
+                            max_blocks, lens_dev, prompt_lens_host ? prompt_dev : nullptr,
+                            batch, sel, kmax, nsel, out, workspace, workspace_bytes,
+                            error_flags, stream);
+  if (st != SRKV_OK) return st;
+  if ((batch > 0 && cudaMemcpyAsync(out_host, out, qb, cudaMemcpyDeviceToHost, s) != cudaSuccess) ||
+      cudaStreamSynchronize(s) != cudaSuccess) {
+    (void)cudaGetLastError();
+    return SRKV_ERR_CUDA;
+  }
+  return SRKV_OK;
+}
+
 srkv_status srkv_retrieval_decode_prefix(const srkv_config* cfg, const void* q,
                                          const void* k_cache, const void* v_cache,
                                          const float* reps, int64_t num_pages,

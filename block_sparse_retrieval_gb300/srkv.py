@@ -32,7 +32,8 @@ EXPORTS = ("srkv_default_config", "srkv_status_string", "srkv_topk_count",
            "srkv_retrieval_decode_tiered", "srkv_quantize_kv_fp8",
            "srkv_retrieval_decode_fp8", "srkv_selftest_wait_timeout",
            "srkv_prefix_decode_workspace_size", "srkv_sparse_paged_decode_prefix",
-           "srkv_retrieval_decode_prefix")
+           "srkv_retrieval_decode_prefix", "srkv_host_staging_size",
+           "srkv_retrieval_decode_host")
 NOALLOC_WORKSPACE_BYTES = 16 << 20
 
 
@@ -106,13 +107,18 @@ def load() -> ctypes.CDLL:
     lib.srkv_retrieval_decode_prefix.argtypes = [ctypes.POINTER(Config), _P, _P, _P, _P, _I64,
                                                  _P, _I32, _P, _P, _I32, _I32, _P, _I32, _P, _P,
                                                  _P, _SZ, _P, _P]
+    lib.srkv_host_staging_size.argtypes = [ctypes.POINTER(Config), _I32]
+    lib.srkv_host_staging_size.restype = _SZ
+    lib.srkv_retrieval_decode_host.argtypes = [ctypes.POINTER(Config), _P, _P, _P, _P, _P, _SZ,
+                                               _P, _P, _P, _I64, _P, _I32, _I32, _P, _I32, _P,
+                                               _P, _P, _SZ, _P, _P]
     lib.srkv_selftest_wait_timeout.argtypes = [_P, _P]
     lib.srkv_selftest_wait_timeout.restype = ctypes.c_int
     for name in ("srkv_build_block_reps", "srkv_score_topk", "srkv_sparse_paged_decode",
                  "srkv_retrieval_decode", "srkv_sparse_paged_decode_noalloc",
                  "srkv_retrieval_decode_tiered", "srkv_quantize_kv_fp8",
                  "srkv_retrieval_decode_fp8", "srkv_sparse_paged_decode_prefix",
-                 "srkv_retrieval_decode_prefix"):
+                 "srkv_retrieval_decode_prefix", "srkv_retrieval_decode_host"):
         getattr(lib, name).restype = ctypes.c_int
     _lib = lib
     return lib
@@ -170,6 +176,19 @@ def _dev(t: torch.Tensor | None, name: str, dtype: torch.dtype | None = None):
         return None
     if not t.is_cuda:
         raise ValueError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if dtype is not None and t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _host_buf(t: torch.Tensor | None, name: str, dtype: torch.dtype | None = None):
+    """A host tensor (page-locked or not) as a pointer."""
+    if t is None:
+        return None
+    if t.is_cuda:
+        raise ValueError(f"{name} must be a host tensor")
     if not t.is_contiguous():
         raise ValueError(f"{name} must be contiguous")
     if dtype is not None and t.dtype != dtype:
@@ -351,6 +370,40 @@ def retrieval_decode(cfg: Mapping, q: torch.Tensor, k_cache: torch.Tensor,
         _dev(out, "out", dt), _dev(workspace, "workspace"),
         workspace.numel() * workspace.element_size(),
         _dev(error_flags, "error_flags", torch.int32), _stream(stream)), "srkv_retrieval_decode")
+
+
+def host_staging_size(cfg: Mapping, batch: int) -> int:
+    """Bytes of device staging srkv_retrieval_decode_host needs for `batch` requests."""
+    c = config(cfg)
+    return int(load().srkv_host_staging_size(ctypes.byref(c), batch))
+
+
+def retrieval_decode_host(cfg: Mapping, q_host: torch.Tensor, seq_lens_host: torch.Tensor,
+                          prompt_lens_host: torch.Tensor | None, out_host: torch.Tensor,
+                          staging: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
+                          reps: torch.Tensor, block_table: torch.Tensor, sel: torch.Tensor,
+                          nsel: torch.Tensor, out: torch.Tensor, workspace: torch.Tensor,
+                          error_flags: torch.Tensor | None = None, stream=None) -> None:
+    """srkv_retrieval_decode_host: the query and lengths from host tensors (page-locked for
+    asynchronous copies), the output into a host tensor; returns once out_host holds it."""
+    B, max_blocks = _step_shapes(cfg, q_host, k_cache, v_cache, block_table, seq_lens_host,
+                                 prompt_lens_host, sel, nsel, out, reps, k_cache.shape[0])
+    _shape(out_host, "out_host", *out.shape)
+    c = config(cfg)
+    dt = _store_dtype(cfg)
+    _check(load().srkv_retrieval_decode_host(
+        ctypes.byref(c), _host_buf(q_host, "q_host", dt),
+        _host_buf(seq_lens_host, "seq_lens_host", torch.int32),
+        _host_buf(prompt_lens_host, "prompt_lens_host", torch.int32),
+        _host_buf(out_host, "out_host", dt), _dev(staging, "staging"),
+        staging.numel() * staging.element_size(), _dev(k_cache, "k_cache", dt),
+        _dev(v_cache, "v_cache", dt), _dev(reps, "reps", torch.float32), k_cache.shape[0],
+        _dev(block_table, "block_table", torch.int32), max_blocks, B,
+        _dev(sel, "sel", torch.int32), sel.shape[-1], _dev(nsel, "nsel", torch.int32),
+        _dev(out, "out", dt), _dev(workspace, "workspace"),
+        workspace.numel() * workspace.element_size(),
+        _dev(error_flags, "error_flags", torch.int32), _stream(stream)),
+        "srkv_retrieval_decode_host")
 
 
 def sparse_paged_decode_prefix(cfg: Mapping, q: torch.Tensor, k_cache: torch.Tensor,

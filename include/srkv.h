@@ -250,6 +250,32 @@ srkv_status srkv_retrieval_decode(const srkv_config* cfg, const void* q, const v
                                   int32_t* error_flags, srkv_stream stream);
 
 /*
+ * srkv_retrieval_decode with host buffers for the per-step inputs and the output, as a
+ * serving loop on the host calls it: q_host ([batch][Hq][d] in the cfg dtype), seq_lens_host
+ * and prompt_lens_host ([batch] int32; prompt_lens_host may be NULL) are copied into
+ * `staging`, the decode runs on them, out is copied into out_host ([batch][Hq][d] in the cfg
+ * dtype), and the call returns once out_host holds it (it synchronises `stream`).  Host
+ * buffers in page-locked memory copy asynchronously; pageable ones work too, more slowly.
+ *   staging: device memory of at least srkv_host_staging_size(cfg, batch) bytes, 256-byte
+ *     aligned, owned by the caller; its contents on entry do not matter.
+ *   Every other argument, its layout and its errors: srkv_retrieval_decode (out is still a
+ *   device buffer, the one the decode writes).  SRKV_ERR_INVALID_ARG for a NULL host
+ *   pointer or staging, a small or unaligned staging; SRKV_ERR_CUDA if a copy or the
+ *   synchronisation fails (out_host is then undefined).
+ */
+size_t srkv_host_staging_size(const srkv_config* cfg, int32_t batch);
+srkv_status srkv_retrieval_decode_host(const srkv_config* cfg, const void* q_host,
+                                       const int32_t* seq_lens_host,
+                                       const int32_t* prompt_lens_host, void* out_host,
+                                       void* staging, size_t staging_bytes,
+                                       const void* k_cache, const void* v_cache,
+                                       const float* reps, int64_t num_pages,
+                                       const int32_t* block_table, int32_t max_blocks,
+                                       int32_t batch, int32_t* sel, int32_t kmax, int32_t* nsel,
+                                       void* out, void* workspace, size_t workspace_bytes,
+                                       int32_t* error_flags, srkv_stream stream);
+
+/*
  * srkv_retrieval_decode with an offload tier (openGauss page, "Overall Solution" and
  * "Feature Description": KV blocks past the offload boundary live off the accelerator's
  * memory, their representation vectors stay resident, and only the topK blocks the query

@@ -129,6 +129,32 @@ def test_prefix_argument_checks(lib):
                                             None, None) == 1
 
 
+def test_host_call_staging_and_argument_checks(lib):
+    cfg = srkv.default_config()
+    c = srkv.config(cfg)
+    # q (batch x 32 heads x 128 x 2 bytes), then the lengths and the prompt lengths, each at a
+    # 256-byte boundary
+    assert srkv.host_staging_size(cfg, 1) == 8192 + 256 + 256
+    assert srkv.host_staging_size(cfg, 3) == 24576 + 256 + 256
+    assert srkv.host_staging_size(dict(cfg, dtype=1), 1) == 16384 + 512
+    assert lib.srkv_host_staging_size(None, 1) == 0
+    fake = ctypes.c_void_p(1 << 20)
+    host = ctypes.c_void_p(1 << 21)
+
+    def call(q=host, lens=host, out_host=host, staging=fake, staging_bytes=1 << 16, batch=1):
+        return lib.srkv_retrieval_decode_host(
+            ctypes.byref(c), q, lens, None, out_host, staging, staging_bytes, fake, fake, fake,
+            10, fake, 8, batch, fake, 8, fake, fake, None, 0, None, None)
+    # rejected before any copy or launch
+    assert call(q=None) == 1
+    assert call(lens=None) == 1
+    assert call(out_host=None) == 1
+    assert call(staging=None) == 1
+    assert call(staging_bytes=8192) == 1                        # smaller than the staging size
+    assert call(staging=ctypes.c_void_p((1 << 20) + 16)) == 1   # not 256-byte aligned
+    assert call(batch=-1) == 1
+
+
 def test_score_topk_argument_checks(lib):
     cfg = dict(srkv.default_config(), dense_boundary=0)
     c = srkv.config(cfg)
