@@ -764,10 +764,13 @@ def run_e2e(layers, K, world, dev) -> dict:
         host[:qb].copy_(c.q.cpu().contiguous().view(-1).view(torch.uint8))
         host[qb:qb + nb].copy_(c.seq_lens.cpu().view(torch.uint8))
         host[qb + nb:].copy_(c.prompt_lens.cpu().view(torch.uint8))
-        # the host call's own buffers: page-locked inputs and output, device staging
-        hq = c.q.cpu().contiguous().pin_memory()
-        hlens = c.seq_lens.cpu().contiguous().pin_memory()
-        hprompt = c.prompt_lens.cpu().contiguous().pin_memory()
+        # the host call's own buffers: page-locked inputs laid out like its staging (one
+        # copy), a page-locked output, the device staging
+        hin = ly.srkv.host_inputs(c.cfg, c.batch)
+        hq, hlens, hprompt = hin["q"], hin["seq_lens"], hin["prompt_lens"]
+        hq.copy_(c.q.cpu())
+        hlens.copy_(c.seq_lens.cpu())
+        hprompt.copy_(c.prompt_lens.cpu())
         staging = torch.empty(ly.srkv.host_staging_size(c.cfg, c.batch), dtype=torch.uint8,
                               device=dev)
         packed = torch.empty_like(host, device=dev)
@@ -826,9 +829,9 @@ def run_e2e(layers, K, world, dev) -> dict:
     return {
         "per_call": dict(base, value=round(world * K / dt_call, 2),
                          how="per step from Python: one srkv_retrieval_decode_host call "
-                             "through the binding (argument checks; copies of q and lengths "
-                             "from pinned host memory, the decode, copy of the output to "
-                             "pinned host memory, stream synchronize)"),
+                             "through the binding (argument checks; one copy of q and lengths "
+                             "from a pinned host buffer laid out like the staging, the decode, "
+                             "copy of the output to pinned host memory, stream synchronize)"),
         "graph": dict(base, value=round(world * K / dt_graph, 2),
                       how="the same three per step replayed from one CUDA graph per layer, "
                           "host synchronize"),

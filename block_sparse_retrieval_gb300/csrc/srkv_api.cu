@@ -487,11 +487,25 @@ srkv_status srkv_retrieval_decode_host(const srkv_config* cfg, const void* q_hos
   int32_t* lens_dev = reinterpret_cast<int32_t*>(q_dev + round256(qb));
   int32_t* prompt_dev = reinterpret_cast<int32_t*>(q_dev + round256(qb) + round256(lb));
   if (batch > 0) {
-    if (cudaMemcpyAsync(q_dev, q_host, qb, cudaMemcpyHostToDevice, s) != cudaSuccess ||
-        cudaMemcpyAsync(lens_dev, seq_lens_host, lb, cudaMemcpyHostToDevice, s) != cudaSuccess ||
-        (prompt_lens_host &&
-         cudaMemcpyAsync(prompt_dev, prompt_lens_host, lb, cudaMemcpyHostToDevice, s) !=
-             cudaSuccess)) {
+    // inputs laid out like the staging (one host buffer at the same offsets) go in one copy
+    const unsigned char* qh = static_cast<const unsigned char*>(q_host);
+    const bool packed =
+        reinterpret_cast<const unsigned char*>(seq_lens_host) == qh + round256(qb) &&
+        (!prompt_lens_host ||
+         reinterpret_cast<const unsigned char*>(prompt_lens_host) ==
+             qh + round256(qb) + round256(lb));
+    bool ok;
+    if (packed) {
+      const size_t bytes = prompt_lens_host ? round256(qb) + round256(lb) + lb : round256(qb) + lb;
+      ok = cudaMemcpyAsync(q_dev, q_host, bytes, cudaMemcpyHostToDevice, s) == cudaSuccess;
+    } else {
+      ok = cudaMemcpyAsync(q_dev, q_host, qb, cudaMemcpyHostToDevice, s) == cudaSuccess &&
+           cudaMemcpyAsync(lens_dev, seq_lens_host, lb, cudaMemcpyHostToDevice, s) ==
+               cudaSuccess &&
+           (!prompt_lens_host || cudaMemcpyAsync(prompt_dev, prompt_lens_host, lb,
+                                                 cudaMemcpyHostToDevice, s) == cudaSuccess);
+    }
+    if (!ok) {
       (void)cudaGetLastError();
       return SRKV_ERR_CUDA;
     }

@@ -378,6 +378,23 @@ def host_staging_size(cfg: Mapping, batch: int) -> int:
     return int(load().srkv_host_staging_size(ctypes.byref(c), batch))
 
 
+def host_inputs(cfg: Mapping, batch: int) -> dict:
+    """Page-locked host tensors for srkv_retrieval_decode_host laid out like its staging (q,
+    then seq_lens, then prompt_lens, each at a 256-byte boundary, in one buffer), so that the
+    call copies them in one go: {"q": [batch][Hq][d], "seq_lens": [batch], "prompt_lens":
+    [batch]} (views of one buffer)."""
+    Hq, _, _, d = _cache_dims(cfg)
+    dt = _store_dtype(cfg)
+    qb = batch * Hq * d * (2 if dt == torch.bfloat16 else 4)
+    r256 = lambda x: (x + 255) // 256 * 256
+    buf = torch.zeros(host_staging_size(cfg, batch), dtype=torch.uint8).pin_memory()
+    lo = r256(qb)
+    return {"q": buf[:qb].view(dt).view(batch, Hq, d),
+            "seq_lens": buf[lo:lo + 4 * batch].view(torch.int32),
+            "prompt_lens": buf[lo + r256(4 * batch):lo + r256(4 * batch) + 4 * batch].view(
+                torch.int32)}
+
+
 def retrieval_decode_host(cfg: Mapping, q_host: torch.Tensor, seq_lens_host: torch.Tensor,
                           prompt_lens_host: torch.Tensor | None, out_host: torch.Tensor,
                           staging: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,

@@ -257,7 +257,9 @@ srkv_status srkv_retrieval_decode(const srkv_config* cfg, const void* q, const v
  * dtype), and the call returns once out_host holds it (it synchronises `stream`).  Host
  * buffers in page-locked memory copy asynchronously; pageable ones work too, more slowly.
  *   staging: device memory of at least srkv_host_staging_size(cfg, batch) bytes, 256-byte
- *     aligned, owned by the caller; its contents on entry do not matter.
+ *     aligned, owned by the caller; its contents on entry do not matter.  It holds q, then
+ *     seq_lens, then prompt_lens, each at a 256-byte boundary; host inputs that sit in one
+ *     buffer at those same offsets go in one copy, others in one copy each.
  *   Every other argument, its layout and its errors: srkv_retrieval_decode (out is still a
  *   device buffer, the one the decode writes).  SRKV_ERR_INVALID_ARG for a NULL host
  *   pointer or staging, a small or unaligned staging; SRKV_ERR_CUDA if a copy or the

@@ -63,6 +63,34 @@ def test_host_call_matches_the_device_call(name, pinned, bitwise):
             assert np.array_equal(buf.sel[r, h, :k].cpu().numpy(), want_sel[r, h, :k].numpy())
 
 
+def test_host_call_with_inputs_in_one_buffer():
+    """Inputs laid out like the staging (srkv.host_inputs) go in one copy: same output."""
+    case = synth.ragged_batch(n_requests=3, lo=9000, hi=20000, seed=21, device=DEV)
+    buf = gpu_select(case)
+    want_out, _, want_nsel = _device_call(case, buf)
+    hin = srkv.host_inputs(case.cfg, case.batch)
+    hin["q"].copy_(case.q.cpu())
+    hin["seq_lens"].copy_(case.seq_lens.cpu())
+    hin["prompt_lens"].copy_(case.prompt_lens.cpu())
+    out_host = torch.zeros(buf.out.shape, dtype=buf.out.dtype).pin_memory()
+    staging = torch.full((srkv.host_staging_size(case.cfg, case.batch),), 0xFF,
+                         dtype=torch.uint8, device=DEV)
+    buf.nsel.fill_(-1)
+    srkv.retrieval_decode_host(case.cfg, hin["q"], hin["seq_lens"], hin["prompt_lens"],
+                               out_host, staging, case.k_cache, case.v_cache, buf.reps,
+                               case.block_table, buf.sel, buf.nsel, buf.out, buf.workspace,
+                               buf.error_flags)
+    assert int(buf.error_flags.item()) == 0
+    assert torch.equal(buf.nsel.cpu(), want_nsel)
+    check_same(case, out_host.float().numpy(), want_out.float().numpy())
+    # the staging now holds the query and lengths as the inputs had them
+    got = staging.cpu()
+    qb = case.q.numel() * 2
+    assert torch.equal(got[:qb], hin["q"].view(-1).view(torch.uint8))
+    lo = (qb + 255) // 256 * 256
+    assert torch.equal(got[lo:lo + 4 * case.batch].view(torch.int32), case.seq_lens.cpu())
+
+
 def test_host_call_rejects_a_device_query():
     case = synth.llama8b_layer(seq_len=16384, device=DEV)
     buf = gpu_select(case)
