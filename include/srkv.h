@@ -43,7 +43,8 @@
  *   sel             [B][Hkv][kmax]    int32 selected logical blocks, ascending
  *   nsel            [B][Hkv]          int32
  * Ownership: the caller owns every buffer.  The library allocates nothing, frees
- * nothing and never synchronises; every call is asynchronous on `stream` (a
+ * nothing and synchronises only in srkv_retrieval_decode_host (which returns its output in
+ * host memory); every other call is asynchronous on `stream` (a
  * cudaStream_t; NULL is the legacy default stream) and returns after launching.
  * Errors: the return value reports host-side argument checks and launch failures.
  * Problems only visible on the device (a page id outside [0, num_pages), a sequence
