@@ -26,9 +26,6 @@
 //     shared memory) until it is empty, so the CTAs whose pages arrive sooner take more and
 //     all finish within about one page of each other; the merged partial (max, sum,
 //     unnormalised output) of the whole segment goes into the leader's shared memory;
-//   * when the pool holds more than the releases carry, the leader takes kept blocks from it
-//     too, through the last stage of its ring (the other stages hold its selection state and
-//     the partials), and adds its own partial;
 //   * the leader merges the partials and writes the output.
 // The partials land with asynchronous stores that count their bytes on one mbarrier of the
 // leader.  Every wait is bounded (SRKV_EFLAG_TIMEOUT); every thread ends at one cluster
@@ -96,11 +93,6 @@ struct FusedCfg {
   static_assert(kOffHist % 16 == 0 && kOffBinKey % 16 == 0 && kOffMail % 16 == 0,
                 "vector accesses");
   static_assert(kPartEnd <= C::kOffQ, "partials fit in the V ring");
-  // A leader that streams kept blocks too uses the ring's last stage only, past both
-  static_assert(kSelEnd <= C::kOffK + (size_t)(C::kStages - 1) * C::kSlab,
-                "the selection state leaves the last K slab free");
-  static_assert(kPartEnd <= C::kOffV + (size_t)(C::kStages - 1) * C::kSlab,
-                "the partials leave the last V slab free");
   static_assert(kSmemAlloc <= 232448, "shared memory opt-in limit");
   // Stages of list A a streaming CTA copies before its own scoring loads have returned.
   // Those loads queue behind the copies already issued (a full ring is ~17 MB over the
@@ -114,22 +106,6 @@ struct FusedCfg {
 // candidate blocks, or list-A pages of one request, S < 16).
 __device__ __forceinline__ int32_t share_begin(int32_t q, int32_t n, int32_t S) {
   return n * q / S;
-}
-
-// The leader's consumers over the kept blocks it takes (its ring's last stage only), its
-// partial into acc_slot / ml_slot.  Out of line: the kernel's own registers stay with the
-// streaming CTAs' loop.
-template <int D, bool F8>
-__device__ __noinline__ void leader_stream_loop(const DecodeArgs& a, unsigned char* smem,
-                                                int lane, int warp, float* acc_slot,
-                                                float* ml_slot) {
-  using C = Cfg<D, F8>;
-  consumer_loop<D, F8>(
-      a, smem, lane, warp,
-      [&](const SoftmaxState<D>& st, const StageInfo&, Lane ln) {
-        store_partial<D, F8>(acc_slot, ml_slot, st, ln, a.G);
-      },
-      C::kStages - 1, C::kStages);
 }
 
 // Grid: one cluster of CS CTAs per unit; 8 consumer warps + 1 producer warp per CTA.
@@ -234,38 +210,17 @@ __global__ void __maxnreg__(128) fused_decode_kernel(const DecodeArgs a,
         .k;
   };
   const int32_t nA = list_a_count(g);
-  // The leader takes kept blocks from its pool too, into its ring's last stage (the rest of
-  // its ring holds the selection state and the partials), when the pool has more than the
-  // releases carry and a partial slot is left for it.
-  auto leader_streams = [&](int32_t kk) { return S <= kMaxCluster - 2 && kk > kStatic * S; };
   const int32_t q = (int32_t)crank - 1;  // streaming rank
   const int32_t a0 = leader ? 0 : share_begin(q, nA, S), a1 = leader ? 0 : share_begin(q + 1, nA, S);
 
   if (warp == kProducerWarp) {
     // ------------------------------------------------------------------ producer
     cluster_wait();
-    int32_t k = -1;  // the kept count (a streaming CTA computes it while it waits anyway)
-    bool run = !leader;
-    // The leader's consumers tell, with the pool, whether the leader streams (k, else -1).
-    // Its producer waits for that only when it may: the kept count is at most n, or, with a
-    // selection, within 1 of the single-precision p n.
-    const int32_t k_hi =
-        prompt < a.dense_boundary ? n : (int32_t)ceilf((float)a.topk_percent * (float)n) + 1;
-    if (leader && leader_streams(k_hi)) {
-      int32_t kk = -1;
-      if (lane == 0) {
-        if (mbar_wait_cluster(list_ready, 0)) kk = fast_flag[2];  // read after the acquire
-        else raise_flags(a.error_flags, SRKV_EFLAG_TIMEOUT);
-      }
-      k = __shfl_sync(0xffffffffu, kk, 0);
-      run = k >= 0;
-    }
-    if (run) {
+    if (!leader) {
       uint32_t eflags = 0;
       bool abort = false;
-      // the ring's iterations: all stages in turn, or (the leader) its last stage only
-      const int64_t it0 = leader ? C::kStages - 1 : 0, step = leader ? C::kStages : 1;
-      int64_t it = it0, armed = 0;
+      int64_t it = 0, armed = 0;
+      int32_t k = -1;  // the kept count, computed while the producer waits anyway
       // list A: 32 positions resolved at once, handed out in order.  The first kEarlyStages
       // copies go out at once; the rest of the ring waits for this CTA's scoring loads,
       // which would otherwise return only after every copy ahead of them had landed (holding
@@ -293,9 +248,9 @@ __global__ void __maxnreg__(128) fused_decode_kernel(const DecodeArgs a,
               break;
             }
           }
-          issue_stage_warp<D, F8>(a, maps, smem, it, u, it == it0 ? kNewUnit : 0u, tl, armed,
-                                  abort, eflags, lane);
-          it += step;
+          issue_stage_warp<D, F8>(a, maps, smem, it, u, it == 0 ? kNewUnit : 0u, tl, armed, abort,
+                              eflags, lane);
+          ++it;
         }
       }
       if (k < 0) k = kept_count();
@@ -331,11 +286,11 @@ __global__ void __maxnreg__(128) fused_decode_kernel(const DecodeArgs a,
         } else if (lo < hi) {
           eflags |= SRKV_EFLAG_PAGE_RANGE;
         }
-        issue_stage_warp<D, F8>(a, maps, smem, it, u, it == it0 ? kNewUnit : 0u, t, armed,
-                                abort, eflags, lane);
-        it += step;
+        issue_stage_warp<D, F8>(a, maps, smem, it, u, it == 0 ? kNewUnit : 0u, t, armed, abort,
+                            eflags, lane);
+        ++it;
       };
-      if (k > 0 && !abort && !leader) {  // (the leader gets no release)
+      if (k > 0 && !abort) {
 #pragma unroll 1
         for (int j = 0; j < kStatic && !abort; ++j) {
           const int2 e = mail[j];
@@ -373,16 +328,13 @@ __global__ void __maxnreg__(128) fused_decode_kernel(const DecodeArgs a,
         issue_stage<D, F8>(a, maps, smem, it, -1, kLast | kSegEnd, none, armed, abort, eflags);
         uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::kOffBar);
         uint64_t* full_v = full + C::kStages;
-        // every copy lands before the CTA ends: the last armed use of each stage in the ring
-        const int64_t n_last = armed < C::kStages / step ? armed : C::kStages / step;
-        for (int64_t j = armed - n_last; j < armed; ++j) {
-          const int64_t iv = it0 + step * j;
-          if (!mbar_wait(&full[iv % C::kStages], (uint32_t)((iv / C::kStages) & 1)) ||
-              !mbar_wait(&full_v[iv % C::kStages], (uint32_t)((iv / C::kStages) & 1))) {
+        const int64_t first = armed > C::kStages ? armed - C::kStages : 0;
+        for (int64_t i = first; i < armed; ++i)  // every copy lands before the CTA ends
+          if (!mbar_wait(&full[i % C::kStages], (uint32_t)((i / C::kStages) & 1)) ||
+              !mbar_wait(&full_v[i % C::kStages], (uint32_t)((i / C::kStages) & 1))) {
             eflags |= SRKV_EFLAG_TIMEOUT;
             break;
           }
-        }
       }
       eflags = __reduce_or_sync(0xffffffffu, eflags | geflags);
       if (lane == 0) raise_flags(a.error_flags, eflags);
@@ -584,21 +536,10 @@ __global__ void __maxnreg__(128) fused_decode_kernel(const DecodeArgs a,
         for (int32_t qq = tid; qq < S; qq += kSelThreads) release(qq);
         for (int32_t p = tid; p < kept; p += kSelThreads) sel_u[p] = b_lo + kept_list[p];
       }
-      const bool lead_stream = leader_streams(k);
       if (tid == 0) {
-        // the pool is complete: the leader's own producer learns whether it takes from it
-        fast_flag[2] = lead_stream ? k : -1;
-        mbar_arrive(list_ready);
         a.nsel_out[u] = kept;
         if (kept != k) raise_flags(a.error_flags, SRKV_EFLAG_SELECTION);
       }
-      if (lead_stream) {
-        // 3''. the leader's kept blocks, in its ring's last stage; its partial goes to slot S
-        leader_stream_loop<D, F8>(a, smem, lane, warp, part_acc + (int64_t)S * a.G * D,
-                                  part_ml + (int64_t)S * a.G * 2);
-        bar();  // the leader's own partial, before the merge reads it
-      }
-      const int32_t P = S + (lead_stream ? 1 : 0);  // partials to merge
       // 4. merge the streaming CTAs' partials: query head w % G, half w / G of d (G <= 4; with
       // G = 8, both halves of head w).  Once they are all in, no CTA reaches another's shared
       // memory any more (each streaming CTA waited for its release, so the leader's writes
@@ -616,7 +557,7 @@ __global__ void __maxnreg__(128) fused_decode_kernel(const DecodeArgs a,
         constexpr int V = D / 64;  // values per lane in half of d
         const int32_t head = warp % a.G;
         float m = -INFINITY, l = 0.f;  // a CTA that attended nothing wrote (-inf, 0)
-        if (lane < P) {
+        if (lane < S) {
           m = part_ml[(lane * a.G + head) * 2];
           l = part_ml[(lane * a.G + head) * 2 + 1];
         }
@@ -654,7 +595,7 @@ __global__ void __maxnreg__(128) fused_decode_kernel(const DecodeArgs a,
             }
 #pragma unroll
             for (int j = 0; j < 8; ++j) {
-              const bool use = b0 + j < P && wv[j] != 0.f;
+              const bool use = b0 + j < S && wv[j] != 0.f;
 #pragma unroll
               for (int e = 0; e < V; ++e) acc[e] = use ? fmaf(wv[j], x[j][e], acc[e]) : acc[e];
             }

@@ -336,12 +336,9 @@ __device__ __forceinline__ void store_partial(float* accp, float* mlp, const Sof
 // At the end of each segment (a stage flagged kSegEnd; the sentinel may carry the flag too,
 // closing a segment whose length the producer did not know in advance) the warps merge their
 // states and warp 0 calls write_partial(state, stage info, lane) with the merged state.
-// Iterations it0, it0 + step, ... (the producer's): step 1 from 0 walks the whole ring; step
-// kStages from kStages - 1 keeps to its last stage.
 template <int D, bool F8 = false, typename WritePartial>
 __device__ __forceinline__ void consumer_loop(const DecodeArgs& a, unsigned char* smem, int lane,
-                                              int warp, WritePartial&& write_partial,
-                                              int64_t it0 = 0, int64_t step = 1) {
+                                              int warp, WritePartial&& write_partial) {
   using C = Cfg<D, F8>;
   unsigned char* sK = smem + C::kOffK;
   unsigned char* sV = smem + C::kOffV;
@@ -391,7 +388,7 @@ __device__ __forceinline__ void consumer_loop(const DecodeArgs& a, unsigned char
     }
     ++merges;
   };
-  for (int64_t it = it0;; it += step) {
+  for (int64_t it = 0;; ++it) {
     const int s = (int)(it % C::kStages);
     if (!mbar_wait(&full[s], (uint32_t)((it / C::kStages) & 1))) {
       if (lane == 0) raise_flags(a.error_flags, SRKV_EFLAG_TIMEOUT);
