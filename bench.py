@@ -641,8 +641,8 @@ def run_ours(args, world, rank, local):
 # metric's workload: the batch-4 x 131072 cache at four ratios, the ragged batch, the shared
 # prefix.
 EXTRA_WORKLOADS = ("dense-vs-sparse-p0.2", "dense-vs-sparse-p0.1", "dense-vs-sparse-p0.4",
-                   "dense-vs-sparse-p1.0", "ragged-16", "prefix-shared-64",
-                   "prefix-shared-64-plain")
+                   "dense-vs-sparse-p1.0", "dense-vs-sparse-b2-p0.2", "dense-vs-sparse-b3-p0.2",
+                   "ragged-16", "prefix-shared-64", "prefix-shared-64-plain")
 
 
 def measure_workload(wl: str, args, world: int, rank: int, dev, peak: float,
