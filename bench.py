@@ -781,9 +781,16 @@ def run_e2e(layers, K, world, dev) -> dict:
         out = torch.empty_like(b.out, device="cpu").pin_memory()
         steps.append(dict(ly=ly, host=host, packed=packed, out=out, hq=hq, hlens=hlens,
                           hprompt=hprompt, staging=staging))
+    stream = torch.cuda.Stream(dev)
+    for st in steps:  # the host call over each layer's fixed buffers, marshalled once
+        ly = st["ly"]
+        c, b = ly.case, ly.buf
+        st["host_step"] = ly.srkv.HostDecodeStep(
+            c.cfg, st["hq"], st["hlens"], st["hprompt"], st["out"], st["staging"], c.k_cache,
+            c.v_cache, b.reps, c.block_table, b.sel, b.nsel, b.out, b.workspace, b.error_flags,
+            stream)
     h2d = steps[0]["host"].nbytes
     d2h = steps[0]["out"].nbytes
-    stream = torch.cuda.Stream(dev)
     stream.wait_stream(torch.cuda.current_stream())
 
     def one(st):
@@ -811,13 +818,7 @@ def run_e2e(layers, K, world, dev) -> dict:
             return max_over_ranks(time.perf_counter() - t0, world, dev)
 
     def per_call(i):
-        st = steps[i % len(steps)]
-        ly = st["ly"]
-        c, b = ly.case, ly.buf
-        ly.srkv.retrieval_decode_host(c.cfg, st["hq"], st["hlens"], st["hprompt"], st["out"],
-                                      st["staging"], c.k_cache, c.v_cache, b.reps,
-                                      c.block_table, b.sel, b.nsel, b.out, b.workspace,
-                                      b.error_flags, stream)
+        steps[i % len(steps)]["host_step"]()
 
     def replay(i):
         graphs[i % len(graphs)].replay()
@@ -829,9 +830,10 @@ def run_e2e(layers, K, world, dev) -> dict:
     return {
         "per_call": dict(base, value=round(world * K / dt_call, 2),
                          how="per step from Python: one srkv_retrieval_decode_host call "
-                             "through the binding (argument checks; one copy of q and lengths "
-                             "from a pinned host buffer laid out like the staging, the decode, "
-                             "copy of the output to pinned host memory, stream synchronize)"),
+                             "through the binding (srkv.HostDecodeStep: arguments checked and "
+                             "marshalled once per buffer set; one copy of q and lengths from a "
+                             "pinned host buffer laid out like the staging, the decode, copy of "
+                             "the output to pinned host memory, stream synchronize)"),
         "graph": dict(base, value=round(world * K / dt_graph, 2),
                       how="the same three per step replayed from one CUDA graph per layer, "
                           "host synchronize"),

@@ -423,6 +423,43 @@ def retrieval_decode_host(cfg: Mapping, q_host: torch.Tensor, seq_lens_host: tor
         "srkv_retrieval_decode_host")
 
 
+class HostDecodeStep:
+    """srkv_retrieval_decode_host over fixed buffers (a serving loop's): the arguments are
+    checked and marshalled once, here; each call runs one step with the buffers' current
+    contents and returns once out_host holds the output."""
+
+    def __init__(self, cfg: Mapping, q_host: torch.Tensor, seq_lens_host: torch.Tensor,
+                 prompt_lens_host: torch.Tensor | None, out_host: torch.Tensor,
+                 staging: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
+                 reps: torch.Tensor, block_table: torch.Tensor, sel: torch.Tensor,
+                 nsel: torch.Tensor, out: torch.Tensor, workspace: torch.Tensor,
+                 error_flags: torch.Tensor | None = None, stream=None):
+        B, max_blocks = _step_shapes(cfg, q_host, k_cache, v_cache, block_table, seq_lens_host,
+                                     prompt_lens_host, sel, nsel, out, reps, k_cache.shape[0])
+        _shape(out_host, "out_host", *out.shape)
+        dt = _store_dtype(cfg)
+        self._cfg = config(cfg)
+        # the tensors stay referenced as long as the step: their memory is what it reads
+        self._keep = (q_host, seq_lens_host, prompt_lens_host, out_host, staging, k_cache,
+                      v_cache, reps, block_table, sel, nsel, out, workspace, error_flags)
+        self._fn = load().srkv_retrieval_decode_host
+        self._args = (
+            ctypes.byref(self._cfg), _host_buf(q_host, "q_host", dt),
+            _host_buf(seq_lens_host, "seq_lens_host", torch.int32),
+            _host_buf(prompt_lens_host, "prompt_lens_host", torch.int32),
+            _host_buf(out_host, "out_host", dt), _dev(staging, "staging"),
+            staging.numel() * staging.element_size(), _dev(k_cache, "k_cache", dt),
+            _dev(v_cache, "v_cache", dt), _dev(reps, "reps", torch.float32), k_cache.shape[0],
+            _dev(block_table, "block_table", torch.int32), max_blocks, B,
+            _dev(sel, "sel", torch.int32), sel.shape[-1], _dev(nsel, "nsel", torch.int32),
+            _dev(out, "out", dt), _dev(workspace, "workspace"),
+            workspace.numel() * workspace.element_size(),
+            _dev(error_flags, "error_flags", torch.int32), _stream(stream))
+
+    def __call__(self) -> None:
+        _check(self._fn(*self._args), "srkv_retrieval_decode_host")
+
+
 def sparse_paged_decode_prefix(cfg: Mapping, q: torch.Tensor, k_cache: torch.Tensor,
                                v_cache: torch.Tensor, block_table: torch.Tensor,
                                seq_lens: torch.Tensor, prefix_blocks: int, sel: torch.Tensor,

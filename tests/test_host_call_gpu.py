@@ -91,6 +91,38 @@ def test_host_call_with_inputs_in_one_buffer():
     assert torch.equal(got[lo:lo + 4 * case.batch].view(torch.int32), case.seq_lens.cpu())
 
 
+def test_marshal_once_step_matches_the_call():
+    """srkv.HostDecodeStep (arguments checked and marshalled once) runs the same call: new
+    inputs written into the same host buffers give the new step's output."""
+    case = synth.llama8b_layer(seq_len=16384, device=DEV)
+    buf = gpu_select(case)
+    hin = srkv.host_inputs(case.cfg, case.batch)
+    out_host = torch.zeros(buf.out.shape, dtype=buf.out.dtype).pin_memory()
+    staging = torch.empty(srkv.host_staging_size(case.cfg, case.batch), dtype=torch.uint8,
+                          device=DEV)
+    step = srkv.HostDecodeStep(case.cfg, hin["q"], hin["seq_lens"], hin["prompt_lens"],
+                               out_host, staging, case.k_cache, case.v_cache, buf.reps,
+                               case.block_table, buf.sel, buf.nsel, buf.out, buf.workspace,
+                               buf.error_flags)
+    for scale in (1.0, -0.5):  # two steps: the second with another query, same buffers
+        q = (case.q.float() * scale).to(case.q.dtype)
+        hin["q"].copy_(q.cpu())
+        hin["seq_lens"].copy_(case.seq_lens.cpu())
+        hin["prompt_lens"].copy_(case.prompt_lens.cpu())
+        step()
+        got = out_host.clone()
+        ref = srkv.DecodeBuffers(case.cfg, case.batch, case.max_blocks, case.num_pages,
+                                 device=DEV)
+        ref.reps.copy_(buf.reps)
+        srkv.retrieval_decode(case.cfg, q, case.k_cache, case.v_cache, ref.reps,
+                              case.block_table, case.seq_lens, case.prompt_lens, ref.sel,
+                              ref.nsel, ref.out, ref.workspace, ref.error_flags)
+        torch.cuda.synchronize()
+        assert int(buf.error_flags.item()) == 0 and int(ref.error_flags.item()) == 0
+        # 8 units on clusters of 12, every kept block with the release: the same bits
+        assert torch.equal(got.view(torch.int16), ref.out.cpu().view(torch.int16))
+
+
 def test_host_call_rejects_a_device_query():
     case = synth.llama8b_layer(seq_len=16384, device=DEV)
     buf = gpu_select(case)
