@@ -5,9 +5,12 @@ the oracle under the rules of the method's statement:
     (s_(k) - s_(k+1)) / max_b |s_b| exceeds 1e-4; inside that band any selection that is a
     valid top-k within the band is accepted (scores are fp32 on the GPU, fp64 in the oracle);
   * attention outputs are compared with the oracle's own selection fed to the GPU decode:
-    |gpu - oracle| <= 2e-2 + 1e-2 |oracle| for bf16 inputs, 1e-5 + 1e-5 |oracle| for fp32.
+    |gpu - oracle| <= 2e-2 + 1e-2 |oracle| for bf16 inputs, 1e-5 + 1e-5 |oracle| for fp32;
+    bf16 outputs must also meet a tighter bound set by the GPU arithmetic (TIGHT_TOL).
 """
 from __future__ import annotations
+
+import os
 
 import numpy as np
 import torch
@@ -17,6 +20,15 @@ from block_sparse_retrieval_gb300 import srkv, synth
 
 GAP = 1e-4
 TOL = {synth.BF16: (2e-2, 1e-2), synth.F32: (1e-5, 1e-5)}
+# The method's bf16 tolerance is loose against the size of an attention output over many
+# tokens: on a 16384-token layer the outputs are ~1e-2, and dropping a whole kept block moves
+# them by ~3e-3, a sixth of it.  So bf16 outputs must also meet a bound set by the GPU's
+# arithmetic: fp32 sums, softmax weights entering the P.V products as 16-bit values (each
+# within 2^-8 relative, independent roundings that average out over the tokens) and one
+# rounding of the output to bf16 (within 2^-8 relative).  Emulating those roundings on the
+# parity cases gives errors of ~1e-4 to 2e-3, at most 0.4 of this bound, which a lost block
+# exceeds.
+TIGHT_TOL = {synth.BF16: (2e-3, 1e-2), synth.F32: (1e-5, 1e-5)}
 ORACLE_KEYS = ("q", "k_cache", "v_cache", "block_table", "seq_lens", "prompt_lens")
 
 
@@ -111,6 +123,12 @@ def check_out(case, got: np.ndarray, want: np.ndarray, units=None):
     err = np.abs(g - w)
     bad = err > atol + rtol * np.abs(w)
     assert not bad.any(), f"{bad.sum()} elements off, max err {err.max():.3e}"
+    tatol, trtol = TIGHT_TOL[case.cfg["dtype"]]
+    ratio = float((err / (tatol + trtol * np.abs(w))).max()) if err.size else 0.0
+    if os.environ.get("SRKV_PARITY_VERBOSE"):
+        print(f"[parity] {case.name}: max err {err.max() if err.size else 0.0:.3e}, "
+              f"{ratio:.3f} of the arithmetic bound")
+    assert ratio <= 1.0, f"max err {err.max():.3e} is {ratio:.2f} x the arithmetic bound"
     return float(err.max())
 
 
