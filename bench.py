@@ -388,6 +388,11 @@ class Layer:
                                    c.seq_lens, c.prompt_lens, b.sel, b.nsel, b.out,
                                    b.workspace, b.error_flags)
 
+    def plain(self) -> bool:
+        """True when the step is srkv_retrieval_decode over device pages (not compressed,
+        not tiered, no shared-prefix call): the step srkv_retrieval_decode_host runs."""
+        return self.k_scale is None and self.prefix_blocks is None and self.k_host is None
+
     def step_bytes(self) -> dict:
         """Algorithmic bytes of one step: what the method must read and write."""
         c, b = self.case, self.buf
@@ -752,9 +757,14 @@ def run_e2e(layers, K, world, dev) -> dict:
     """The same steps through the public entry points with host buffers, as a serving loop runs
     them.  `per_call`: one srkv_retrieval_decode_host call per step through the binding (its
     argument checks included): the step's query and lengths copied from pinned host memory,
-    the decode, the output copied back into pinned host memory, and the wait for it.  `graph`:
-    the same copies and srkv_retrieval_decode replayed from one CUDA graph per layer (what a
-    serving loop that captures its step would see), then the wait."""
+    the decode, the output copied back into pinned host memory, and the wait for it.  Steps
+    that srkv_retrieval_decode_host does not run (compressed or host-pool pages, the
+    shared-prefix call) are, per step from Python, one copy of the query and lengths from a
+    pinned host buffer, the layer's own entry point through the binding, the copy of the
+    output into pinned host memory and the wait.  `graph`: the same copies and decode call
+    replayed from one CUDA graph per layer (what a serving loop that captures its step would
+    see), then the wait."""
+    plain = all(ly.plain() for ly in layers)
     steps = []
     for ly in layers:
         c, b = ly.case, ly.buf
@@ -764,15 +774,17 @@ def run_e2e(layers, K, world, dev) -> dict:
         host[:qb].copy_(c.q.cpu().contiguous().view(-1).view(torch.uint8))
         host[qb:qb + nb].copy_(c.seq_lens.cpu().view(torch.uint8))
         host[qb + nb:].copy_(c.prompt_lens.cpu().view(torch.uint8))
-        # the host call's own buffers: page-locked inputs laid out like its staging (one
-        # copy), a page-locked output, the device staging
-        hin = ly.srkv.host_inputs(c.cfg, c.batch)
-        hq, hlens, hprompt = hin["q"], hin["seq_lens"], hin["prompt_lens"]
-        hq.copy_(c.q.cpu())
-        hlens.copy_(c.seq_lens.cpu())
-        hprompt.copy_(c.prompt_lens.cpu())
-        staging = torch.empty(ly.srkv.host_staging_size(c.cfg, c.batch), dtype=torch.uint8,
-                              device=dev)
+        hq = hlens = hprompt = staging = None
+        if plain:
+            # the host call's own buffers: page-locked inputs laid out like its staging (one
+            # copy), a page-locked output, the device staging
+            hin = ly.srkv.host_inputs(c.cfg, c.batch)
+            hq, hlens, hprompt = hin["q"], hin["seq_lens"], hin["prompt_lens"]
+            hq.copy_(c.q.cpu())
+            hlens.copy_(c.seq_lens.cpu())
+            hprompt.copy_(c.prompt_lens.cpu())
+            staging = torch.empty(ly.srkv.host_staging_size(c.cfg, c.batch), dtype=torch.uint8,
+                                  device=dev)
         packed = torch.empty_like(host, device=dev)
         # the layer reads its query and lengths from the packed device buffer
         c.q = packed[:qb].view(c.q.dtype).view(c.q.shape)
@@ -783,6 +795,8 @@ def run_e2e(layers, K, world, dev) -> dict:
                           hprompt=hprompt, staging=staging))
     stream = torch.cuda.Stream(dev)
     for st in steps:  # the host call over each layer's fixed buffers, marshalled once
+        if not plain:
+            break
         ly = st["ly"]
         c, b = ly.case, ly.buf
         st["host_step"] = ly.srkv.HostDecodeStep(
@@ -818,7 +832,12 @@ def run_e2e(layers, K, world, dev) -> dict:
             return max_over_ranks(time.perf_counter() - t0, world, dev)
 
     def per_call(i):
-        steps[i % len(steps)]["host_step"]()
+        st = steps[i % len(steps)]
+        if plain:
+            st["host_step"]()
+        else:
+            one(st)
+            stream.synchronize()
 
     def replay(i):
         graphs[i % len(graphs)].replay()
@@ -833,7 +852,10 @@ def run_e2e(layers, K, world, dev) -> dict:
                              "through the binding (srkv.HostDecodeStep: arguments checked and "
                              "marshalled once per buffer set; one copy of q and lengths from a "
                              "pinned host buffer laid out like the staging, the decode, copy of "
-                             "the output to pinned host memory, stream synchronize)"),
+                             "the output to pinned host memory, stream synchronize)" if plain
+                         else "per step from Python: copy of q and lengths from pinned host "
+                              "memory, the layer's decode entry point through the binding, "
+                              "copy of the output to pinned host memory, stream synchronize"),
         "graph": dict(base, value=round(world * K / dt_graph, 2),
                       how="the same three per step replayed from one CUDA graph per layer, "
                           "host synchronize"),
