@@ -106,7 +106,27 @@ def call_retrieval_prefix(**over):
                                  a["nsel"], a["out"], a["workspace"])
 
 
+def _host_args(over):
+    return {**step_args(), "out_host": torch.zeros(B, 8, 64, dtype=bf),
+            "staging": torch.zeros(4096, dtype=u8), **over}
+
+
+def call_host(**over):
+    a = _host_args(over)
+    srkv.retrieval_decode_host(CFG, a["q"], a["seq_lens"], a["prompt_lens"], a["out_host"],
+                               a["staging"], a["k_cache"], a["v_cache"], a["reps"],
+                               a["block_table"], a["sel"], a["nsel"], a["out"], a["workspace"])
+
+
+def call_host_step(**over):
+    a = _host_args(over)
+    srkv.HostDecodeStep(CFG, a["q"], a["seq_lens"], a["prompt_lens"], a["out_host"],
+                        a["staging"], a["k_cache"], a["v_cache"], a["reps"], a["block_table"],
+                        a["sel"], a["nsel"], a["out"], a["workspace"])
+
+
 CALLS = {"retrieval_decode": call_retrieval, "sparse_paged_decode": call_sparse,
+         "retrieval_decode_host": call_host, "HostDecodeStep": call_host_step,
          "sparse_paged_decode_prefix": call_sparse_prefix,
          "retrieval_decode_prefix": call_retrieval_prefix,
          "score_topk": call_score, "sparse_paged_decode_noalloc": call_noalloc,
@@ -145,6 +165,10 @@ WRONG = [
     ("append_kv", dict(k_new=torch.zeros(B, 8, 64, dtype=bf))),
     ("quantize_kv_fp8", dict(v_scale=torch.zeros(P, 2, 64, dtype=f32))),
     ("quantize_kv_fp8", dict(k_fp8=torch.zeros(P - 1, 2, 128, 64, dtype=u8))),
+    ("retrieval_decode_host", dict(out_host=torch.zeros(B, 8, 32, dtype=bf))),
+    ("retrieval_decode_host", dict(q=torch.zeros(B - 1, 8, 64, dtype=bf))),
+    ("HostDecodeStep", dict(out_host=torch.zeros(B + 1, 8, 64, dtype=bf))),
+    ("HostDecodeStep", dict(seq_lens=torch.zeros(B, 1, dtype=i32))),
 ]
 
 
@@ -152,3 +176,13 @@ WRONG = [
 def test_wrong_shapes_stop_before_the_library(name, over):
     with pytest.raises(ValueError, match="shape|rows"):
         CALLS[name](**over)
+
+
+def test_a_missing_library_fails_loudly(monkeypatch, tmp_path):
+    """No library, no answer: the binding has no other way to compute anything."""
+    monkeypatch.setattr(srkv, "_lib", None)
+    monkeypatch.setattr(srkv, "LIB_PATH", str(tmp_path / "libsrkv.so"))
+    with pytest.raises(RuntimeError, match="missing"):
+        srkv.load()
+    with pytest.raises(RuntimeError, match="missing"):
+        srkv.host_staging_size(CFG, B)
