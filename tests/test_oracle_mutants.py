@@ -63,6 +63,8 @@ MUTANTS = [
      "return (a->block < b->block) - (a->block > b->block);"),
     ("kept count rounded down",
      "double x = ceil(p * (double)n - 1e-9);", "double x = floor(p * (double)n + 1e-9);"),
+    ("kept count without the allowance for the binary error of p",
+     "double x = ceil(p * (double)n - 1e-9);", "double x = ceil(p * (double)n);"),
     ("dense at the boundary itself",
      "const int dense = prompt < (int64_t)c->dense_boundary;",
      "const int dense = prompt <= (int64_t)c->dense_boundary;"),
@@ -80,6 +82,11 @@ MUTANTS = [
      "(dist == bd && (code & 1u) == 0)", "(dist == bd && (code & 1u) == 1)"),
     ("row scale for a largest value of 240 (another 8-bit format's)",
      "amax / 448.0f", "amax / 240.0f"),
+    ("quotient x / scale taken in double, not fp32",
+     "const float y = (float)value_at(x, 0, e) / scale;",
+     "const double y = value_at(x, 0, e) / (double)scale;"),
+    ("NaN coded with the sign bit set",
+     "if (isnan(x)) return 0x7fu;", "if (isnan(x)) return 0xffu;"),
     ("row scale indexed by element",
      "sc[i / c->head_dim]", "sc[i % c->head_dim]"),
 ]

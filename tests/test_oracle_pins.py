@@ -104,13 +104,17 @@ def test_footprint_atb_example_and_its_printed_slip():
 
 @pytest.mark.parametrize("n,p,k", [(448, 0.2, 90), (445, 0.2, 89), (26, 0.2, 6), (960, 0.1, 96),
                                    (960, 0.2, 192), (960, 0.4, 384), (960, 1.0, 960),
-                                   (0, 0.2, 0), (100, 0.0, 0), (5, 0.01, 1), (1, 0.2, 1)])
+                                   (0, 0.2, 0), (100, 0.0, 0), (5, 0.01, 1), (1, 0.2, 1),
+                                   # p * n rounds to just above a whole number in binary
+                                   (100, 0.07, 7), (50, 0.14, 7), (25, 0.28, 7), (100, 0.55, 55)])
 def test_topk_count_worked_values(n, p, k):
     assert oracle.topk_count(n, p) == k
 
 
 def test_topk_count_equals_exact_rational_ceiling():
-    for p in (0.05, 0.1, 0.15, 0.2, 0.25, 0.3, 1 / 3, 0.4, 0.5, 0.7, 0.9, 1.0):
+    """Every ratio in hundredths (some of them, 0.07 or 0.55, give products p * n that round to
+    just above a whole number in binary), a third and 1."""
+    for p in [i / 100 for i in range(0, 101)] + [1 / 3]:
         for n in range(0, 2049):
             assert oracle.topk_count(n, p) == exact_k(n, p), (n, p)
 
@@ -193,6 +197,22 @@ def test_prompt_at_boundary_is_sparse():
                                      if k not in ("page_ids", "page_valid")})
     n = len(offload_blocks(700, 32, 64, 96))
     assert res["nsel"][0, 0] == exact_k(n, 0.2) < n
+
+
+def test_without_prompt_lengths_a_prompt_is_its_sequence():
+    """With no prompt lengths given, DENSE_BOUNDARY is compared with the sequence length: the
+    request below the boundary is attended densely, the other one is not."""
+    case = small_case(8, topk_percent=0.2, dense_boundary=800, seq_lens=[700, 900],
+                      prompt_lens=[700, 900])
+    arr = synth.to_oracle_arrays(case)
+    args = [arr[k] for k in ("q", "k_cache", "v_cache", "block_table", "seq_lens")]
+    given = oracle.decode(case.cfg, *args, arr["prompt_lens"])
+    absent = oracle.decode(case.cfg, *args, None)
+    for key in ("sel", "nsel", "out"):
+        np.testing.assert_array_equal(absent[key], given[key])
+    assert absent["nsel"][0, 0] == len(offload_blocks(700, 32, 64, 96))
+    n = len(offload_blocks(900, 32, 64, 96))
+    assert absent["nsel"][1, 0] == exact_k(n, 0.2) < n
 
 
 def test_ratio_zero_is_sinks_plus_window():
@@ -432,6 +452,9 @@ def test_e4m3_rounding_matches_the_library_and_ties_go_even():
     np.testing.assert_array_equal(oracle.e4m3_code(mids), want)
     # saturation past the largest finite value, both signs
     np.testing.assert_array_equal(oracle.e4m3_code([449.0, 1e9, -500.0]), [0x7E, 0x7E, 0xFE])
+    # a (positive) NaN gets the library's NaN code
+    nan = torch.tensor([float("nan")]).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    np.testing.assert_array_equal(oracle.e4m3_code([float("nan")]), nan)
 
 
 def test_e4m3_quantiser_scale_and_error_bound():
@@ -458,6 +481,34 @@ def test_e4m3_quantiser_scale_and_error_bound():
     ulp_half = np.where(y >= 2.0 ** -6, 2.0 ** (np.floor(np.log2(np.maximum(y, 2.0 ** -6))) - 4),
                         2.0 ** -10)
     assert np.all(np.abs(deq - xs) <= (ulp_half * 1.0001 + 1e-12) * scales[..., None])
+
+
+def test_e4m3_quantiser_matches_the_library_pipeline():
+    """R10 against PyTorch doing the same steps in fp32: the row's largest magnitude, the scale
+    max / 448, the quotient x / scale, its float8_e4m3fn code.  Besides random rows, rows
+    whose fp32 quotient lands exactly on the midpoint between two codes while the exact
+    quotient lies just above it (x = 4.875 in a row of largest magnitude 52: 42.0 in fp32,
+    42.0000012 exactly): the fp32 quotient goes to the even code, 40, not to 44."""
+    cfg = dict(num_q_heads=4, num_kv_heads=2, head_dim=64, block_size=128, init_tokens=0,
+               local_tokens=0, topk_percent=0.2, dense_boundary=0, dtype=0)
+    rng = np.random.default_rng(9)
+    x = (rng.normal(0, 1, (2, 2, 128, 64)) * rng.uniform(0.01, 50, (2, 2, 128, 1)))
+    pairs = [(52.0, 4.875), (9.25, -6.9375), (58.0, -10.875), (22.0, 4.125), (13.0, 9.75),
+             (5.625, 4.21875), (40.5, 30.375), (50.0, -37.5), (39.5, -7.40625), (25.0, -4.6875)]
+    for i, (amax, v) in enumerate(pairs):
+        row = x[0, 0, i]
+        row *= 0.5 * amax / np.abs(row).max()
+        row[0], row[1] = amax, v
+    t = torch.from_numpy(x.astype(np.float32)).to(torch.bfloat16)
+    bits = t.view(torch.int16).numpy().view(np.uint16)
+    codes, scales = oracle.quantize_e4m3(cfg, bits)
+    xf = t.float()
+    lib_scale = xf.abs().amax(-1) / 448.0
+    lib_scale = torch.where(lib_scale > 0, lib_scale, torch.ones_like(lib_scale))
+    lib_codes = (xf / lib_scale[..., None]).to(torch.float8_e4m3fn).view(torch.uint8)
+    np.testing.assert_array_equal(scales, lib_scale.numpy())
+    np.testing.assert_array_equal(codes, lib_codes.numpy())
+    assert codes[0, 0, 0, 1] == 0x62  # 4.875 in the row of 52: 40, the even neighbour of 42
 
 
 def test_e4m3_pages_decode_as_the_equivalent_bf16_cache():
