@@ -67,6 +67,14 @@ def small_cases():
                                  num_kv_heads=8, head_dim=128, init_tokens=256,
                                  local_tokens=512, topk_percent=0.2, dense_boundary=0, seed=20,
                                  device=DEV),
+        # p * n just above a whole number in binary (0.07 x 100 = 7.000000000000001): the
+        # kept count is 7 of 100 on both sides, and 55 of 100 at 0.55
+        "binary-ratio-0.07": lambda: mk(seq_lens=[21016, 21016 + 6400], num_q_heads=32,
+                                        num_kv_heads=8, head_dim=128, topk_percent=0.07,
+                                        dense_boundary=0, seed=23, device=DEV),
+        "binary-ratio-0.55": lambda: mk(seq_lens=[21016], num_q_heads=32, num_kv_heads=8,
+                                        head_dim=128, topk_percent=0.55, dense_boundary=0,
+                                        seed=24, device=DEV),
         "dense-boundary": lambda: mk(seq_lens=[9000, 12000, 12000], prompt_lens=[9000, 11999, 12000],
                                      num_q_heads=8, num_kv_heads=2, head_dim=128,
                                      init_tokens=1024, local_tokens=2048, topk_percent=0.2,
