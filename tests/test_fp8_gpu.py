@@ -55,6 +55,28 @@ def test_quantizer_d64_and_zero_rows_match_the_oracle():
     assert (ks[0, 1, 5:9] == 1).all() and (k8[0, 1, 5:9] == 0).all()
 
 
+def test_quantizer_rows_on_a_code_midpoint_match_the_oracle():
+    """Rows whose fp32 quotient x / scale lands exactly on the midpoint between two codes while
+    the exact quotient lies just above it (4.875 in a row of largest magnitude 52: 42.0 in
+    fp32): the fp32 quotient's tie goes to the even code on both sides."""
+    case = synth.make_case(seq_lens=[1024], num_q_heads=4, num_kv_heads=2, head_dim=64,
+                           seed=74, device=DEV)
+    pairs = [(52.0, 4.875), (9.25, -6.9375), (58.0, -10.875), (22.0, 4.125), (13.0, 9.75),
+             (5.625, 4.21875), (40.5, 30.375), (50.0, -37.5), (39.5, -7.40625), (25.0, -4.6875)]
+    k = case.k_cache.clone()
+    for i, (amax, v) in enumerate(pairs):
+        row = k[0, 0, i].float()
+        row = row * (0.5 * amax / row.abs().max())
+        row[0], row[1] = amax, v
+        k[0, 0, i] = row.to(torch.bfloat16)
+    case = synth.Case(**{**case.__dict__, "k_cache": k})
+    k8, _, ks, _ = quantize(case)
+    codes, scales = oracle.quantize_e4m3(case.cfg, synth.to_oracle_arrays(case)["k_cache"])
+    np.testing.assert_array_equal(k8.cpu().numpy(), codes)
+    np.testing.assert_array_equal(ks.cpu().numpy(), scales)
+    assert int(k8[0, 0, 0, 1]) == 0x62
+
+
 def test_quantizer_leaves_other_pages_and_flags_bad_ids():
     case = synth.llama8b_layer(seq_len=2048, device=DEV, seed=72)
     P = case.num_pages
