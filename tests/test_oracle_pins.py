@@ -199,6 +199,19 @@ def test_prompt_at_boundary_is_sparse():
     assert res["nsel"][0, 0] == exact_k(n, 0.2) < n
 
 
+def test_default_boundary_32k_is_strict():
+    """The pages' DENSE_BOUNDARY of 32K = 32768: a prompt of 32767 tokens is attended densely,
+    one of 32768 is not (the comparison is a strict "less than")."""
+    case = small_case(9, topk_percent=0.2, dense_boundary=32768, seq_lens=[33000, 33000],
+                      prompt_lens=[32767, 32768], head_dim=8)
+    arr = synth.to_oracle_arrays(case)
+    res = oracle.decode(case.cfg, *[arr[k] for k in ("q", "k_cache", "v_cache", "block_table",
+                                                      "seq_lens", "prompt_lens")], threads=4)
+    n = len(offload_blocks(33000, 32, 64, 96))
+    assert res["nsel"][0, 0] == n
+    assert res["nsel"][1, 0] == exact_k(n, 0.2) < n
+
+
 def test_without_prompt_lengths_a_prompt_is_its_sequence():
     """With no prompt lengths given, DENSE_BOUNDARY is compared with the sequence length: the
     request below the boundary is attended densely, the other one is not."""
