@@ -11,6 +11,7 @@ oracle under ``oracle/`` is never changed.
 import os
 import subprocess
 import sys
+from concurrent.futures import ThreadPoolExecutor
 
 import pytest
 
@@ -92,13 +93,14 @@ MUTANTS = [
 ]
 
 
-def _build(tmp_path, text: str) -> str:
-    src = tmp_path / "srkv_oracle.c"
-    so = tmp_path / "libsrkv_oracle.so"
-    src.write_text(text)
+def _build(folder, text: str) -> str:
+    src = os.path.join(folder, "srkv_oracle.c")
+    so = os.path.join(folder, "libsrkv_oracle.so")
+    with open(src, "w") as f:
+        f.write(text)
     subprocess.check_call(["gcc", "-O2", "-std=c11", "-ffp-contract=off", "-fPIC", "-shared",
-                           "-o", str(so), str(src), "-lm", "-lpthread"])
-    return str(so)
+                           "-o", so, src, "-lm", "-lpthread"])
+    return so
 
 
 def _pins(so: str) -> subprocess.CompletedProcess:
@@ -111,16 +113,32 @@ def _source() -> str:
         return f.read()
 
 
-def test_pins_pass_on_an_unchanged_copy(tmp_path):
-    run = _pins(_build(tmp_path, _source()))
+@pytest.fixture(scope="module")
+def runs(tmp_path_factory):
+    """Every copy (the unchanged one under None, then each planted mistake by name) built and
+    run against the pins, several child processes at a time."""
+    text = _source()
+    for name, old, _ in MUTANTS:
+        assert old in text, f"the text for {name!r} is not in the oracle's source"
+    jobs = [(None, text)] + [(name, text.replace(old, new)) for name, old, new in MUTANTS]
+    folders = [str(tmp_path_factory.mktemp(f"copy{i}")) for i in range(len(jobs))]
+
+    def run(i):
+        name, body = jobs[i]
+        return name, _pins(_build(folders[i], body))
+
+    with ThreadPoolExecutor(max_workers=max(1, min(8, os.cpu_count() or 1))) as pool:
+        return dict(pool.map(run, range(len(jobs))))
+
+
+def test_pins_pass_on_an_unchanged_copy(runs):
+    run = runs[None]
     assert run.returncode == 0, run.stdout[-2000:] + run.stderr[-2000:]
 
 
-@pytest.mark.parametrize("name,old,new", MUTANTS, ids=[m[0] for m in MUTANTS])
-def test_a_planted_mistake_fails_a_pin(tmp_path, name, old, new):
-    text = _source()
-    assert old in text, f"the text for {name!r} is not in the oracle's source"
-    run = _pins(_build(tmp_path, text.replace(old, new)))
+@pytest.mark.parametrize("name", [m[0] for m in MUTANTS])
+def test_a_planted_mistake_fails_a_pin(runs, name):
+    run = runs[name]
     # pytest's exit code 1: tests ran and at least one failed (not a collection or usage error).
     assert run.returncode == 1, (name, run.returncode, run.stdout[-2000:], run.stderr[-2000:])
     assert " failed" in run.stdout, (name, run.stdout[-2000:])
