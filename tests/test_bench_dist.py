@@ -41,4 +41,8 @@ def test_two_gloo_ranks(tmp_path):
     line = json.loads(lines[0])
     assert line["impl"] == "reference" and line["n_gpus"] == 2 and line["value"] > 0
     assert line["cpu_baseline"]["kind"] == "oracle"
+    # the same workload, data and metric as the library's arm prints by default
+    assert line["config"]["workload"] == bench.WORKLOAD and line["data"] == bench.DATA
+    assert line["metric"] == bench.METRIC and line["unit"] == "steps/s"
+    assert line["e2e"]["h2d_bytes_per_step"] == line["e2e"]["d2h_bytes_per_step"] == 0
     assert not [l for l in res[1]["stdout"].splitlines() if l.startswith("{")]
